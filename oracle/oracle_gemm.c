@@ -1,0 +1,213 @@
+/*
+ * CPU oracle for the tile-primitive matrix multiply  D = alpha*A*B + beta*C.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the plain, slow, obviously correct
+ * definition that the CUDA library is checked against. Only the test suite,
+ * the smoke check and the benchmark's CPU-baseline leg load it; the library
+ * never does, and it shares no code, header or constant with the library.
+ *
+ * What it computes (the TVM TIRx "gemm" tile primitive, as described on the
+ * page "TVM TIRx 同步 GEMM 深度解析：warp 级 mma.sync 的寄存器碎片排布与完整
+ * 下放链路", sections 语义定义 and 二 What it accepts):
+ *   - D = alpha*A*B + beta*C with alpha fixed at 1 and beta in {0, 1};
+ *   - A and B are both float16 or both bfloat16, C and D are float32;
+ *   - transpose_A / transpose_B only set the logical orientation: the operands
+ *     are normalised to A[M,K], B[K,N], C and D [M,N] (section 维度一致性);
+ *   - the accumulator is initialised from C when beta = 1 and from zero when
+ *     beta = 0, then accumulated over K (section 四 step 3).
+ *
+ * Precision: every 16-bit input is decoded exactly to double, each product is
+ * exact in double (at most 22 significant bits), the sum runs over k in
+ * increasing order in double, C is added when beta = 1, and the result is
+ * rounded once to float32 (round to nearest even, the C cast). The oracle
+ * accepts any positive shape; the divisibility rules belong to the library.
+ *
+ * Storage: dense row-major. A is [M,K], or [K,M] when transA. B is [K,N], or
+ * [N,K] when transB. C and D are [M,N].
+ *
+ * Alongside D it can return S[i,j] = sum_k |a(i,k) * b(k,j)| in double, the
+ * scale of the elementwise acceptance bound |D - D_ref| <= 2^-10 * S + 1e-6.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_F16 0
+#define ORACLE_BF16 1
+
+/* IEEE-754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Exponent field 0 encodes zero and subnormals (fraction * 2^-24); 31 encodes
+ * infinity (fraction 0) or NaN. */
+double oracle_decode_f16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24);
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25);
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper half of an IEEE-754 binary32. 1 sign bit, 8 exponent
+ * bits (bias 127), 7 fraction bits. Exponent 0 encodes zero and subnormals
+ * (fraction * 2^-133); 255 encodes infinity or NaN. */
+double oracle_decode_bf16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int m = h & 0x7f;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -133);
+    } else if (e == 255) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(128 + m), e - 134);
+    }
+    return sign ? -v : v;
+}
+
+static double decode(uint16_t h, int dtype) {
+    return dtype == ORACLE_BF16 ? oracle_decode_bf16(h) : oracle_decode_f16(h);
+}
+
+void oracle_decode(const uint16_t* src, double* dst, int64_t n, int dtype) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = decode(src[i], dtype);
+}
+
+/* Logical element a(i,k) of the M x K matrix A, whatever its storage. */
+static uint16_t a_bits(const uint16_t* A, int64_t i, int64_t k, int64_t M, int64_t K, int transA) {
+    return transA ? A[k * M + i] : A[i * K + k];
+}
+
+/* Logical element b(k,j) of the K x N matrix B, whatever its storage. */
+static uint16_t b_bits(const uint16_t* B, int64_t k, int64_t j, int64_t N, int64_t K, int transB) {
+    return transB ? B[j * K + k] : B[k * N + j];
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Full D. Returns 0 on success, -1 if the decode buffers cannot be allocated,
+ * -2 on a bad argument. sumabs may be NULL. C is read only when beta != 0. */
+int oracle_gemm(float* D, double* sumabs, const uint16_t* A, const uint16_t* B, const float* C,
+                int64_t M, int64_t N, int64_t K, int transA, int transB, int dtype, int beta) {
+    if (M <= 0 || N <= 0 || K <= 0 || !D || !A || !B || (beta && !C)) return -2;
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -2;
+    /* Decode once into the normalised orientation: a[i*K+k] = a(i,k) and
+     * bt[j*K+k] = b(k,j), so the sum over k walks both rows contiguously. */
+    double* a = (double*)malloc(sizeof(double) * (size_t)(M * K));
+    double* bt = (double*)malloc(sizeof(double) * (size_t)(N * K));
+    if (!a || !bt) {
+        free(a);
+        free(bt);
+        return -1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t k = 0; k < K; ++k) a[i * K + k] = decode(a_bits(A, i, k, M, K, transA), dtype);
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t k = 0; k < K; ++k) bt[j * K + k] = decode(b_bits(B, k, j, N, K, transB), dtype);
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        const double* ai = a + i * K;
+        for (int64_t j = 0; j < N; ++j) {
+            const double* bj = bt + j * K;
+            double s = 0.0, sa = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = ai[k] * bj[k];
+                s += p;
+                sa += fabs(p);
+            }
+            if (beta) s += (double)C[i * N + j];
+            D[i * N + j] = (float)s;
+            if (sumabs) sumabs[i * N + j] = sa;
+        }
+    }
+    free(a);
+    free(bt);
+    return 0;
+}
+
+/* Selected entries only: D_out[t] = D[rows[t], cols[t]] (and its sum of
+ * |products|), computed one by one straight from the 16-bit storage. This is
+ * how outputs of problems too large for the full triple loop are checked. */
+int oracle_gemm_entries(float* D_out, double* sumabs_out, const int64_t* rows, const int64_t* cols,
+                        int64_t count, const uint16_t* A, const uint16_t* B, const float* C,
+                        int64_t M, int64_t N, int64_t K, int transA, int transB, int dtype,
+                        int beta) {
+    if (M <= 0 || N <= 0 || K <= 0 || !D_out || !A || !B || (beta && !C) || count < 0) return -2;
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -2;
+    for (int64_t t = 0; t < count; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -2;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < count; ++t) {
+        int64_t i = rows[t], j = cols[t];
+        double s = 0.0, sa = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = decode(a_bits(A, i, k, M, K, transA), dtype) *
+                       decode(b_bits(B, k, j, N, K, transB), dtype);
+            s += p;
+            sa += fabs(p);
+        }
+        if (beta) s += (double)C[i * N + j];
+        D_out[t] = (float)s;
+        if (sumabs_out) sumabs_out[t] = sa;
+    }
+    return 0;
+}
+
+/* Rows [row_begin, row_end) of D only, written to D_rows[(i-row_begin)*N + j].
+ * Same arithmetic as oracle_gemm; used to time the oracle on a bounded sample
+ * of a large problem. */
+int oracle_gemm_rows(float* D_rows, const uint16_t* A, const uint16_t* B, const float* C,
+                     int64_t M, int64_t N, int64_t K, int64_t row_begin, int64_t row_end,
+                     int transA, int transB, int dtype, int beta) {
+    if (M <= 0 || N <= 0 || K <= 0 || !D_rows || !A || !B || (beta && !C)) return -2;
+    if (row_begin < 0 || row_end > M || row_begin >= row_end) return -2;
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -2;
+    int64_t R = row_end - row_begin;
+    double* a = (double*)malloc(sizeof(double) * (size_t)(R * K));
+    double* bt = (double*)malloc(sizeof(double) * (size_t)(N * K));
+    if (!a || !bt) {
+        free(a);
+        free(bt);
+        return -1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t k = 0; k < K; ++k)
+            a[r * K + k] = decode(a_bits(A, row_begin + r, k, M, K, transA), dtype);
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t k = 0; k < K; ++k) bt[j * K + k] = decode(b_bits(B, k, j, N, K, transB), dtype);
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t j = 0; j < N; ++j) {
+            const double* ai = a + r * K;
+            const double* bj = bt + j * K;
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += ai[k] * bj[k];
+            if (beta) s += (double)C[(row_begin + r) * N + j];
+            D_rows[r * N + j] = (float)s;
+        }
+    }
+    free(a);
+    free(bt);
+    return 0;
+}

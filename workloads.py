@@ -1,0 +1,148 @@
+"""Seeded synthetic inputs for the tile-primitive matrix multiply D = A.B + beta.C.
+
+This module only draws random operands. It holds none of the product's
+arithmetic, so both the CPU oracle and the CUDA library can be fed from it
+without sharing any code with each other.
+
+Storage conventions (dense, row-major, no leading dimensions):
+  A is [M, K], or [K, M] when transA is set (the logical A is its transpose);
+  B is [K, N], or [N, K] when transB is set;
+  C and D are [M, N] float32.
+A and B are float16 or bfloat16 (the same dtype). Values are drawn in float32
+and rounded to the 16-bit dtype with round-to-nearest-even (torch's cast), so
+both sides consume the very same 16-bit patterns.
+
+The five workloads are the shapes of the method's test matrix: a single
+m16n8k16 atom, a 256^3 transposed-B case with beta = 1, a 4096^3 square case
+(plus an integer-valued variant), an 8192^3 bf16 case, and a skinny ragged
+144 x 16392 x 4104 case that exercises tail tiles and the memory-bound regime.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+F16 = 0
+BF16 = 1
+_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
+_DTYPE_NAME = {F16: "f16", BF16: "bf16"}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic problem: shape, dtype, value distributions and flags."""
+
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype: int            # F16 or BF16
+    a_dist: tuple         # ("int", lo, hi) | ("uniform", lo, hi) | ("normal", mean, std)
+    b_dist: tuple
+    c_dist: Optional[tuple]  # None when beta == 0
+    beta: float
+    transA: bool
+    transB: bool
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Each operand read once, D written once; C only when beta = 1."""
+        e = 2
+        b = e * (self.M * self.K + self.K * self.N) + 4 * self.M * self.N
+        if self.beta != 0.0:
+            b += 4 * self.M * self.N
+        return b
+
+    @property
+    def integer_valued(self) -> bool:
+        return self.a_dist[0] == "int" and self.b_dist[0] == "int" and (
+            self.c_dist is None or self.c_dist[0] == "int")
+
+    def describe(self) -> dict:
+        return {
+            "workload": self.name, "M": self.M, "N": self.N, "K": self.K,
+            "dtype": _DTYPE_NAME[self.dtype], "beta": self.beta,
+            "transA": self.transA, "transB": self.transB, "seed": self.seed,
+        }
+
+    def with_shape(self, M: int, N: int, K: int, name: Optional[str] = None,
+                   seed: Optional[int] = None) -> "Workload":
+        return dataclasses.replace(self, M=M, N=N, K=K, name=name or f"{self.name}@{M}x{N}x{K}",
+                                   seed=self.seed if seed is None else seed)
+
+
+WORKLOADS = [
+    Workload("atom_16x8x16_f16_int", 16, 8, 16, F16, ("int", -2, 2), ("int", -2, 2), None,
+             0.0, False, False, 1000),
+    Workload("gemm_256_bf16_transB_beta1", 256, 256, 256, BF16, ("normal", 0.0, 1.0),
+             ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), 1.0, False, True, 1001),
+    Workload("gemm_4096_f16", 4096, 4096, 4096, F16, ("uniform", -1.0, 1.0),
+             ("uniform", -1.0, 1.0), None, 0.0, False, False, 1002),
+    Workload("gemm_8192_bf16_transB_beta1", 8192, 8192, 8192, BF16, ("normal", 0.0, 0.02),
+             ("normal", 0.0, 0.02), ("normal", 0.0, 1.0), 1.0, False, True, 1003),
+    Workload("skinny_144x16392x4104_f16_beta1", 144, 16392, 4104, F16, ("normal", 0.0, 1.0),
+             ("normal", 0.0, 0.02), ("normal", 0.0, 1.0), 1.0, False, False, 1004),
+]
+# Integer-valued variant of the 4096^3 case (values in [-3, 3]); every partial
+# sum is exactly representable in float32, so results must match bit for bit.
+WORKLOAD_4096_INT = Workload("gemm_4096_f16_int", 4096, 4096, 4096, F16, ("int", -3, 3),
+                             ("int", -3, 3), None, 0.0, False, False, 1031)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [WORKLOAD_4096_INT]}
+
+
+def _draw(shape, dist, gen: torch.Generator) -> torch.Tensor:
+    kind = dist[0]
+    if kind == "int":
+        lo, hi = dist[1], dist[2]
+        return torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int32).to(torch.float32)
+    if kind == "uniform":
+        lo, hi = dist[1], dist[2]
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * (hi - lo) + lo
+    if kind == "normal":
+        mean, std = dist[1], dist[2]
+        return torch.randn(shape, generator=gen, dtype=torch.float32) * std + mean
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def stored_shapes(w: Workload):
+    a = (w.K, w.M) if w.transA else (w.M, w.K)
+    b = (w.N, w.K) if w.transB else (w.K, w.N)
+    return a, b, (w.M, w.N)
+
+
+def make_inputs(w: Workload, c_fill: Optional[float] = None):
+    """Return CPU tensors (A, B, C) for a workload.
+
+    A and B are in the workload's 16-bit dtype and stored orientation; C is
+    float32 [M, N], or None when beta == 0 (unless c_fill is given, in which
+    case C is a constant-filled tensor, e.g. NaN to prove C is not read).
+    """
+    gen = torch.Generator("cpu").manual_seed(w.seed)
+    sa, sb, sc = stored_shapes(w)
+    td = _TORCH_DTYPE[w.dtype]
+    A = _draw(sa, w.a_dist, gen).to(td)
+    B = _draw(sb, w.b_dist, gen).to(td)
+    C = None
+    if w.c_dist is not None:
+        C = _draw(sc, w.c_dist, gen)
+    if c_fill is not None:
+        C = torch.full(sc, c_fill, dtype=torch.float32)
+    return A, B, C
+
+
+def bits(t: torch.Tensor):
+    """The raw 16-bit patterns of a float16/bfloat16 CPU tensor as numpy uint16."""
+    assert t.dtype in (torch.float16, torch.bfloat16)
+    return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def torch_dtype(dtype: int):
+    return _TORCH_DTYPE[dtype]
