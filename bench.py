@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Benchmark of the tile-primitive matrix multiply D = A.B + beta.C on GB300.
+
+One step is one call of the library's public C-ABI entry point (tpgemm_gemm)
+on one batch of seeded synthetic operands already resident in HBM: the whole
+hot path (TMA ring -> tcgen05.mma -> tensor-memory epilogue with beta.C) in
+one kernel launch. The default workload is the 8192^3 bf16 problem with B
+stored [N, K] and beta = 1, the shape the GEMM TFLOP/s metric is quoted on.
+
+Prints ONE JSON line (rank 0): metric, value (whole-job TFLOP/s), timing,
+clocks sampled during the timed region, the roofline of the kernel, an
+end-to-end number through host buffers, and the CPU oracle timed on a bounded
+sample of the same workload. ``--impl reference`` times that oracle alone, as
+the reference arm. With several GPUs (torchrun) every rank runs an independent
+replica: the method has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (fp16/bf16->fp32) at 4096^3/8192^3; % of tensor peak or HBM roof"
+DEFAULT_WORKLOAD = "gemm_8192_bf16_transB_beta1"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["tile_primitive_tensor_gb300/csrc/tc_gemm.cu",
+                  "tile_primitive_tensor_gb300/csrc/ptx.cuh",
+                  "tile_primitive_tensor_gb300/csrc/tpgemm_api.cu"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    return ap.parse_args()
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches this kernel."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("traffic_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons for one GPU."""
+
+    FIELDS = ("timestamp,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            bus = parts[1].lower()
+            if self.bus_id and not bus.endswith(self.bus_id[-12:]):
+                continue
+            try:
+                self.samples.append({
+                    "t": time.time(), "sm": float(parts[2]), "sm_max": float(parts[3]),
+                    "power": float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None,
+                    "hw_slowdown": parts[6] == "Active",
+                    "hw_thermal_slowdown": parts[7] == "Active",
+                    "sw_thermal_slowdown": parts[8] == "Active",
+                    "sw_power_cap": parts[9] == "Active",
+                })
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        s = [x for x in self.samples if t0 <= x["t"] <= t1]
+        if not s:
+            s = self.samples[-3:]
+        if not s:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = [r for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                               "sw_power_cap") if any(x[r] for x in s)]
+        pw = [x["power"] for x in s if x["power"] is not None]
+        return {"sm_mhz": statistics.median(x["sm"] for x in s),
+                "sm_max_mhz": max(x["sm_max"] for x in s), "reasons": reasons,
+                "samples": len(s), "power_w_max": max(pw) if pw else None}
+
+
+# -------------------------------------------------------------- CPU oracle
+def oracle_sample(w, A, B, C, seconds: float, seed: int = 0):
+    """Time the CPU oracle on a bounded sample of output entries of workload w.
+
+    Returns (tflops, entries, elapsed, threads). Each entry is one full
+    K-long dot product computed by the oracle from the 16-bit operands.
+    """
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    Ab, Bb = wl.bits(A), wl.bits(B)
+    Cn = None if C is None else C.numpy()
+    rng = np.random.default_rng(seed)
+
+    def run(n):
+        r = rng.integers(0, w.M, n)
+        c = rng.integers(0, w.N, n)
+        t = time.perf_counter()
+        oracle.gemm_entries(r, c, Ab, Bb, Cn, w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+        return time.perf_counter() - t
+
+    probe = max(16, oracle.num_threads() * 4)
+    tp = run(probe)
+    n = int(max(1, min(2_000_000, probe * seconds / max(tp, 1e-6))))
+    el = run(n)
+    return 2.0 * n * w.K / el / 1e12, n, el, oracle.num_threads()
+
+
+def sample_text(n, w):
+    return (f"{n} output entries of D at seeded uniform positions (of {w.M}x{w.N}), each a "
+            f"full {w.K}-long fp64 dot product from the 16-bit operands (oracle_gemm_entries)")
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import tile_primitive_tensor_gb300 as tp
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = wl.BY_NAME[args.workload]
+    A, B, C = wl.make_inputs(w)
+    Ad, Bd = A.to(dev), B.to(dev)
+    Cd = None if C is None else C.to(dev)
+    D = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    lib = tp.library()
+    plan = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)[1]
+    dp, ap_, bp = D.data_ptr(), Ad.data_ptr(), Bd.data_ptr()
+    cp = None if Cd is None else Cd.data_ptr()
+
+    def step():
+        st = lib.tpgemm_gemm(dp, ap_, bp, cp, w.M, w.N, w.K, int(w.transA), int(w.transB),
+                             w.dtype, float(w.beta), sh)
+        if st != 0:
+            raise RuntimeError(f"tpgemm_gemm: {st} {tp.tpgemm_last_error_detail()}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    tp.check(tp.tpgemm_last_device_error())
+
+    props = torch.cuda.get_device_properties(dev)
+    bus = None
+    if hasattr(props, "pci_bus_id"):
+        bus = f"{getattr(props, 'pci_domain_id', 0):08x}:{props.pci_bus_id:02x}:" \
+              f"{getattr(props, 'pci_device_id', 0):02x}.0"
+    sampler = ClockSampler(bus)
+    sampler.start()
+    time.sleep(0.4)  # let nvidia-smi start before the timed region
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    tp.check(tp.tpgemm_last_device_error())
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    launch_ms = statistics.mean(per_launch)
+    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # ---- end to end through host buffers: H2D of inputs + call + D2H of D
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    Ah, Bh = pin(A), pin(B)
+    Ch = None if C is None else pin(C)
+    Dh = torch.empty(w.M, w.N, dtype=torch.float32).pin_memory()
+    h2d = A.numel() * A.element_size() + B.numel() * B.element_size() + \
+        (0 if C is None else C.numel() * 4)
+    d2h = w.M * w.N * 4
+
+    def e2e_step():
+        Ad.copy_(Ah, non_blocking=True)
+        Bd.copy_(Bh, non_blocking=True)
+        if Ch is not None:
+            Cd.copy_(Ch, non_blocking=True)
+        step()
+        Dh.copy_(D, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    ne = max(1, min(args.e2e_steps, args.steps))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ne):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / ne
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * w.flops / (e2e_ms * 1e-3) / 1e12
+
+    # ---- roofline of the (single) kernel of a step
+    peaks, src = load_peaks()
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
+    tensor_bound = w.flops / w.algorithmic_bytes > ridge
+    if tensor_bound:
+        achieved = w.flops / (launch_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_kind": f"{src} bf16 dense burst",
+                "frac_of_sustained": round(achieved / peaks.get("bf16_tflops_sustained",
+                                                                 peaks["bf16_tflops"]), 4)}
+    else:
+        achieved = w.algorithmic_bytes / (launch_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_kind": f"{src} HBM copy bandwidth"}
+    roof["traffic"] = load_traffic(w.name)
+    roof["algorithmic"] = w.flops if tensor_bound else w.algorithmic_bytes
+    roof["kernel"] = plan
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
+            "bf16" if w.dtype == wl.BF16 else "f16",
+        "data": "synthetic (seeded, workloads.py)",
+        "config": {**w.describe(), "l2": "inputs larger than L2 (no flush needed)" if
+                   w.algorithmic_bytes > 2 * 129e6 else "L2 not flushed; working set fits L2",
+                   "parallelism": f"replicas x{world}"},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, el, cores = oracle_sample(w, A, B, C, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                               "sample": sample_text(n, w), "seconds": round(el, 2)}
+    return out
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    w = wl.BY_NAME[args.workload]
+    A, B, C = wl.make_inputs(w)
+    total = args.steps + args.warmup
+    budget = 150.0  # seconds for the whole run
+    per_step = max(0.02, budget / max(total, 1))
+    # calibrate the number of entries per step
+    _, n0, el0, _ = oracle_sample(w, A, B, C, 0.5, seed=1)
+    per_entry = el0 / n0
+    n_step = max(1, int(per_step / per_entry))
+    import numpy as np
+
+    import oracle
+    Ab, Bb = wl.bits(A), wl.bits(B)
+    Cn = None if C is None else C.numpy()
+    rng = np.random.default_rng(2)
+
+    def step():
+        r = rng.integers(0, w.M, n_step)
+        c = rng.integers(0, w.N, n_step)
+        oracle.gemm_entries(r, c, Ab, Bb, Cn, w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t
+    value = 2.0 * n_step * w.K * args.steps / el / 1e12
+    cores = oracle.num_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded, workloads.py)",
+        "config": {**w.describe(), "parallelism": "cpu oracle"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {sample_text(n_step, w)}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        out = run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

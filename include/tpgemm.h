@@ -1,0 +1,121 @@
+/*
+ * tpgemm — the tile-primitive matrix multiply  D = A·B + beta·C  on one GB300
+ * (sm_103a), as a C-ABI shared library (libtpgemm.so).
+ *
+ * The operation is the TVM TIRx "gemm" tile primitive as described on the page
+ * "TVM TIRx 同步 GEMM 深度解析：warp 级 mma.sync 的寄存器碎片排布与完整下放链路":
+ *   - section 语义定义: D = alpha·A·B + beta·C;
+ *   - section 二 (What it accepts): A and B are both float16 or both bfloat16,
+ *     C and D are float32, alpha = 1.0, beta ∈ {0.0, 1.0} (0 → D = A·B,
+ *     1 → D = A·B + C), M % 16 = 0, N % 8 = 0, K % 8 = 0;
+ *   - section 二 维度一致性: transpose_A / transpose_B only describe the logical
+ *     orientation; operands are normalised to A[M,K], B[K,N], C and D [M,N];
+ *   - section 三: the C position may be D itself (in-place accumulation).
+ * The library computes it with hand-written sm_103a kernels: TMA loads into
+ * 128-byte-swizzled shared memory, an mbarrier ring, single-thread-issued
+ * tcgen05.mma accumulating in tensor memory, and a warpgroup tcgen05.ld
+ * epilogue; small problems run a warp-level mma.sync.m16n8k16 kernel.
+ *
+ * Storage: dense row-major, no leading-dimension arguments.
+ *   A: [M,K] elements, or [K,M] when transA != 0 (the logical A is its transpose).
+ *   B: [K,N] elements, or [N,K] when transB != 0.
+ *   C: [M,N] float32 (read only when beta == 1; may be NULL when beta == 0).
+ *   D: [M,N] float32 (written).
+ * All four are device pointers owned by the caller. The library allocates no
+ * device memory per call and keeps no pointer after the call is enqueued.
+ *
+ * Errors: every function returns a status. Argument errors are detected on the
+ * host before anything is enqueued, and a readable reason is available from
+ * tpgemm_last_error_detail() on the calling thread.
+ */
+#ifndef TPGEMM_H
+#define TPGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of A and B (both the same). */
+typedef enum {
+    TPGEMM_F16 = 0,  /* IEEE binary16 */
+    TPGEMM_BF16 = 1  /* bfloat16 */
+} tpgemm_dtype;
+
+typedef enum {
+    TPGEMM_OK = 0,
+    TPGEMM_ERR_SHAPE = 1,   /* M, N, K not positive, or M%16, N%8, K%8 != 0 */
+    TPGEMM_ERR_DTYPE = 2,   /* dtype not TPGEMM_F16 / TPGEMM_BF16 */
+    TPGEMM_ERR_BETA = 3,    /* beta not exactly 0.0f or 1.0f */
+    TPGEMM_ERR_NULL = 4,    /* D, A or B NULL, or C NULL with beta == 1 */
+    TPGEMM_ERR_ALIGN = 5,   /* a pointer not 16-byte aligned */
+    TPGEMM_ERR_ALIAS = 6,   /* D overlaps A or B, or overlaps C without being equal to it */
+    TPGEMM_ERR_ARCH = 7,    /* current device is not compute capability 10.3 (sm_103) */
+    TPGEMM_ERR_LAUNCH = 8,  /* a CUDA call failed while enqueueing (detail has the CUDA error) */
+    TPGEMM_ERR_TIMEOUT = 9, /* a kernel's bounded wait expired (see tpgemm_last_device_error) */
+    TPGEMM_ERR_PATH = 10    /* the forced kernel path cannot run this problem */
+} tpgemm_status;
+
+/* Kernel path selection, for tests and measurement. AUTO is the default plan. */
+typedef enum {
+    TPGEMM_PATH_AUTO = 0,
+    TPGEMM_PATH_TCGEN05 = 1, /* TMA + tcgen05.mma + tensor-memory epilogue */
+    TPGEMM_PATH_MMA_SYNC = 2 /* warp-level mma.sync.m16n8k16 (k8 for a K%16 == 8 tail) */
+} tpgemm_path;
+
+/*
+ * D = A·B + beta·C  (alpha = 1).
+ *
+ * D, A, B, C: device pointers, 16-byte aligned, layouts as above. D == C is
+ *   allowed (in-place D += A·B when beta == 1); any other overlap of D with A,
+ *   B or C is rejected with TPGEMM_ERR_ALIAS.
+ * M, N, K: logical sizes, positive, M % 16 == 0, N % 8 == 0, K % 8 == 0.
+ * transA, transB: 0 or non-zero; select the stored orientation of A and B.
+ * dtype: TPGEMM_F16 or TPGEMM_BF16.
+ * beta: exactly 0.0f or 1.0f.
+ * stream: a cudaStream_t (0 for the legacy default stream) on the current
+ *   device; the call is asynchronous and returns once the work is enqueued.
+ *
+ * Returns TPGEMM_OK, or an error status with nothing enqueued (argument
+ * errors), or TPGEMM_ERR_LAUNCH if CUDA refused the launch.
+ */
+tpgemm_status tpgemm_gemm(float* D, const void* A, const void* B, const float* C, int64_t M,
+                          int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
+                          float beta, void* stream);
+
+/* As tpgemm_gemm, with an explicit kernel path (TPGEMM_ERR_PATH if the forced
+ * path cannot run the problem). Used by the tests to cover both kernels. */
+tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const float* C, int64_t M,
+                               int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
+                               float beta, void* stream, tpgemm_path path);
+
+/* Static English name of a status. Never NULL. */
+const char* tpgemm_status_string(tpgemm_status s);
+
+/* Readable reason for the last non-OK status returned on this thread
+ * (e.g. "N=12 is not a multiple of 8"). Thread-local; valid until the next
+ * call on the same thread. Empty string if the last call succeeded. */
+const char* tpgemm_last_error_detail(void);
+
+/* Device-side status of the kernels launched so far on the current device:
+ * TPGEMM_ERR_TIMEOUT if any bounded wait inside a kernel expired, else
+ * TPGEMM_OK. Synchronises the device first. Reading it resets it to OK. */
+tpgemm_status tpgemm_last_device_error(void);
+
+/* The plan tpgemm_gemm would use for this problem, written as text into buf
+ * (at most buflen bytes including the terminator): kernel path, tile shape,
+ * operand roles, grid. Returns the status the call itself would return for
+ * the arguments' shape, dtype and beta (pointers are not examined). */
+tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, int transB,
+                                   tpgemm_dtype dtype, float beta, tpgemm_path path, char* buf,
+                                   int buflen);
+
+/* Library version as "major.minor.patch". */
+const char* tpgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPGEMM_H */

@@ -1,0 +1,147 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every function
+that include/tpgemm.h declares, and rejects bad arguments on the host with a
+readable reason before anything is enqueued.
+
+The rejection cases mirror the acceptance table of the TVM TIRx synchronous
+gemm page ("TVM TIRx 同步 GEMM 深度解析", section 二 What it accepts, and its
+tests section: non-unit alpha, fractional beta, unsupported dtypes), restated
+for a fixed library entry point: M % 16, N % 8, K % 8; A/B float16 or
+bfloat16; beta in {0, 1}. Pointers here are fake addresses; the library never
+dereferences them on the rejection paths.
+"""
+import ctypes
+import os
+import subprocess
+import sys
+
+import pytest
+
+import tile_primitive_tensor_gb300 as tp
+from tile_primitive_tensor_gb300 import build as tpbuild
+
+BASE = 0x7F0000000000  # fake, 16-byte aligned device addresses
+MB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tpbuild.build()
+    return tp.library()
+
+
+def call(M=64, N=64, K=64, D=BASE, A=BASE + 64 * MB, B=BASE + 128 * MB, C=BASE + 192 * MB,
+         tA=0, tB=0, dtype=tp.TPGEMM_F16, beta=1.0, path=tp.TPGEMM_PATH_AUTO):
+    st = tp.tpgemm_gemm_path(D, A, B, C, M, N, K, tA, tB, dtype, beta, 0, path)
+    return st, tp.tpgemm_last_error_detail()
+
+
+def test_exports_every_declared_function(lib):
+    names = tp.header_functions()
+    assert "tpgemm_gemm" in names and len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in tpgemm.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", tp.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    for n in names:
+        assert f" T {n}" in out
+
+
+def test_status_strings(lib):
+    for s in range(0, 11):
+        assert tp.tpgemm_status_string(s) not in ("", "unknown status")
+    assert tp.tpgemm_status_string(99) == "unknown status"
+    assert tp.tpgemm_version().count(".") == 2
+
+
+@pytest.mark.parametrize("M,N,K,frag", [
+    (8, 64, 64, "M=8"), (64, 12, 64, "N=12"), (64, 64, 4, "K=4"), (0, 64, 64, "positive"),
+    (64, -8, 64, "positive"), (64, 64, 0, "positive"), (24, 64, 64, "M=24"),
+    (1 << 30, 64, 64, "2^30"),
+])
+def test_rejects_shape(lib, M, N, K, frag):
+    st, why = call(M=M, N=N, K=K)
+    assert st == tp.TPGEMM_ERR_SHAPE
+    assert frag in why
+
+
+@pytest.mark.parametrize("dtype", [2, 3, -1, 7])
+def test_rejects_dtype(lib, dtype):
+    # f16 accumulators, tf32, int8 and mixed types have no enumerator: any
+    # code other than TPGEMM_F16 / TPGEMM_BF16 is refused.
+    st, why = call(dtype=dtype)
+    assert st == tp.TPGEMM_ERR_DTYPE and "dtype" in why
+
+
+@pytest.mark.parametrize("beta", [0.5, 2.0, -1.0, float("nan"), 1e-30])
+def test_rejects_fractional_beta(lib, beta):
+    st, why = call(beta=beta)
+    assert st == tp.TPGEMM_ERR_BETA and "beta" in why
+
+
+def test_rejects_null_and_misaligned(lib):
+    assert call(D=None)[0] == tp.TPGEMM_ERR_NULL
+    assert call(A=None)[0] == tp.TPGEMM_ERR_NULL
+    assert call(B=None)[0] == tp.TPGEMM_ERR_NULL
+    assert call(C=None, beta=1.0)[0] == tp.TPGEMM_ERR_NULL
+    for kw in ({"D": BASE + 8}, {"A": BASE + 64 * MB + 2}, {"B": BASE + 128 * MB + 4},
+               {"C": BASE + 192 * MB + 12}):
+        st, why = call(**kw)
+        assert st == tp.TPGEMM_ERR_ALIGN and "16-byte" in why
+
+
+def test_rejects_aliasing(lib):
+    # D = 64x64 f32 = 16 KB at BASE; A starting inside it
+    st, why = call(A=BASE + 4096)
+    assert st == tp.TPGEMM_ERR_ALIAS and "A" in why
+    st, why = call(B=BASE + 16 * 1024 - 16)
+    assert st == tp.TPGEMM_ERR_ALIAS and "B" in why
+    st, why = call(C=BASE + 16)
+    assert st == tp.TPGEMM_ERR_ALIAS and "C" in why
+    # B just past the end of D is fine (the call then fails on the missing GPU only)
+    st, _ = call(B=BASE + 16 * 1024)
+    assert st not in (tp.TPGEMM_ERR_ALIAS,)
+
+
+def test_c_ignored_when_beta_zero(lib):
+    # With beta = 0, C may be NULL, misaligned or overlapping: it is never read.
+    for C in (None, BASE + 3, BASE + 16):
+        st, why = call(C=C, beta=0.0)
+        assert st not in (tp.TPGEMM_ERR_NULL, tp.TPGEMM_ERR_ALIGN, tp.TPGEMM_ERR_ALIAS), why
+
+
+def test_in_place_accepted(lib):
+    # D == C is the in-place form; validation passes (then no GPU here, or a launch).
+    st, why = call(C=BASE, beta=1.0)
+    assert st not in (tp.TPGEMM_ERR_ALIAS, tp.TPGEMM_ERR_NULL, tp.TPGEMM_ERR_ALIGN), why
+
+
+def test_plans_for_workloads(lib):
+    import workloads as wl
+    expect = {
+        "atom_16x8x16_f16_int": "path=mma_sync",
+        "gemm_256_bf16_transB_beta1": "path=mma_sync",
+        "gemm_4096_f16": "path=tcgen05 orientation=normal",
+        "gemm_8192_bf16_transB_beta1": "path=tcgen05 orientation=normal",
+        "skinny_144x16392x4104_f16_beta1": "path=tcgen05 orientation=swapped",
+    }
+    for w in wl.WORKLOADS:
+        st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+        assert st == tp.TPGEMM_OK, text
+        assert text.startswith(expect[w.name]), (w.name, text)
+    st, text = tp.tpgemm_describe_plan(256, 256, 256, 0, 1, tp.TPGEMM_BF16, 1.0,
+                                       tp.TPGEMM_PATH_TCGEN05)
+    assert st == tp.TPGEMM_OK and "tcgen05" in text
+    st, text = tp.tpgemm_describe_plan(64, 64, 64, 0, 0, 0, 1.0, 7)
+    assert st == tp.TPGEMM_ERR_PATH
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    """A fresh interpreter whose package copy has no built library raises."""
+    import shutil
+    pkg = os.path.dirname(tp.__file__)
+    dst = tmp_path / "tile_primitive_tensor_gb300"
+    shutil.copytree(pkg, dst, ignore=shutil.ignore_patterns("_lib", "_build", "__pycache__"))
+    code = ("import tile_primitive_tensor_gb300 as t\n"
+            "try:\n    t.tpgemm_version()\nexcept RuntimeError as e:\n    print('RAISED', e)\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
+    assert "RAISED" in r.stdout and "not built" in r.stdout

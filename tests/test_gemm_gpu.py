@@ -1,0 +1,258 @@
+"""Parity of the CUDA library with the CPU oracle, through the C-ABI (GPU only).
+
+Every case draws seeded inputs from ``workloads.py``, runs the library through
+``tpgemm_gemm`` / ``tpgemm_gemm_path`` and compares element by element with
+the oracle on the same 16-bit patterns. The bar (the synchronous gemm page,
+"TVM TIRx 同步 GEMM 深度解析", validates D = A.B within a tolerance; the bound
+used here is): bit-exact (by value) when every input is integer-valued, else
+|D - D_ref| <= 2^-10 * sum_k |a b| + 1e-6 elementwise.
+
+Coverage follows the page's test section: the single-atom demo, tilings x
+(dtype, beta) including ragged and 8-wide K tails, all four transpose combos
+x both dtypes, plus the in-place form (C position = D), beta = 0 ignoring C,
+guard bands around D, and the five workloads at their full sizes (sampled
+entries against the oracle, whole-output properties and an fp64 reference).
+"""
+import dataclasses
+import itertools
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tile_primitive_tensor_gb300 as tp
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+AUTO, TC, MMA = tp.TPGEMM_PATH_AUTO, tp.TPGEMM_PATH_TCGEN05, tp.TPGEMM_PATH_MMA_SYNC
+GUARD = 4096  # floats of NaN canary on each side of D
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tile_primitive_tensor_gb300 import build as tpbuild
+    tpbuild.build()
+    oracle.build()
+    yield
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+
+
+def device_inputs(w, c_fill=None):
+    A, B, C = wl.make_inputs(w, c_fill=c_fill)
+    return (A, B, C), (A.cuda(), B.cuda(), None if C is None else C.cuda())
+
+
+def run_gpu(w, Ad, Bd, Cd, path, D=None):
+    """Run the library; returns D on the host. D is carved from a canary buffer."""
+    n = w.M * w.N
+    if D is None:
+        buf = torch.full((n + 2 * GUARD,), float("nan"), dtype=torch.float32, device="cuda")
+        D = buf[GUARD:GUARD + n].view(w.M, w.N)
+    else:
+        buf = None
+    st = tp.tpgemm_gemm_path(D, Ad, Bd, Cd, w.M, w.N, w.K, w.transA, w.transB,
+                             w.dtype, w.beta, None, path)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    if buf is not None:
+        h = buf.cpu().numpy()
+        assert np.isnan(h[:GUARD]).all() and np.isnan(h[GUARD + n:]).all(), "write outside D"
+    return D.cpu().numpy()
+
+
+def oracle_full(w, A, B, C):
+    return oracle.gemm(wl.bits(A), wl.bits(B), None if C is None else C.numpy(), w.M, w.N, w.K,
+                       w.transA, w.transB, w.dtype, w.beta)
+
+
+def check_full(w, path, c_fill=None):
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w, c_fill=c_fill)
+    D = run_gpu(w, Ad, Bd, Cd, path)
+    Dref, S = oracle_full(w, A, B, C if w.beta else None)
+    ok, msg = oracle.compare(D, Dref, S, exact=w.integer_valued)
+    assert ok, f"{w.name} path={path}: {msg}"
+    return D
+
+
+# --------------------------------------------------------------- the atom
+@pytest.mark.parametrize("path", [AUTO, MMA, TC])
+def test_single_atom_bit_exact(path):
+    w = wl.WORKLOADS[0]
+    D = check_full(w, path)
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    import make_golden
+    g = make_golden.read_case(os.path.join(here, f"{w.name}.txt"))
+    assert np.array_equal(D, g["D_f32bits"])
+
+
+@pytest.mark.parametrize("path", [MMA, TC])
+def test_golden_ragged_fixture(path):
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    import make_golden
+    w = make_golden.CASES[1][0]
+    g = make_golden.read_case(os.path.join(here, f"{w.name}.txt"))
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+    D = run_gpu(w, Ad, Bd, Cd, path)
+    _, S = oracle_full(w, A, B, C)
+    ok, msg = oracle.compare(D, g["D_f32bits"], S)
+    assert ok, msg
+
+
+# ------------------------------------------------------- tilings x modes
+TILED_M = [16, 64, 144, 256]
+TILED_N = [8, 16, 264]
+TILED_K = [8, 24, 72]
+MODES = [(wl.F16, 0.0), (wl.F16, 1.0), (wl.BF16, 0.0), (wl.BF16, 1.0)]
+
+
+@pytest.mark.parametrize("path", [MMA, TC])
+@pytest.mark.parametrize("dtype,beta", MODES)
+def test_tiled_grid(path, dtype, beta):
+    base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
+    for i, (M, N, K) in enumerate(itertools.product(TILED_M, TILED_N, TILED_K)):
+        w = base.with_shape(M, N, K, seed=5000 + i)
+        w = dataclasses.replace(w, dtype=dtype, beta=beta, transB=False,
+                                c_dist=("normal", 0.0, 1.0) if beta else None)
+        check_full(w, path)
+
+
+@pytest.mark.parametrize("path", [MMA, TC])
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+@pytest.mark.parametrize("tA,tB", list(itertools.product([False, True], repeat=2)))
+def test_transpose_combos(path, dtype, tA, tB):
+    base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
+    w = base.with_shape(272, 392, 200, seed=6000 + 2 * tA + tB)
+    w = dataclasses.replace(w, dtype=dtype, transA=tA, transB=tB)
+    check_full(w, path)
+
+
+@pytest.mark.parametrize("tA,tB", list(itertools.product([False, True], repeat=2)))
+def test_transpose_combos_swapped_orientation(tA, tB):
+    # Small M with wide N runs the tcgen05 kernel in its swapped orientation.
+    base = wl.BY_NAME["skinny_144x16392x4104_f16_beta1"]
+    w = base.with_shape(48, 1544, 264, seed=6100 + 2 * tA + tB)
+    w = dataclasses.replace(w, transA=tA, transB=tB)
+    check_full(w, TC)
+
+
+def test_multi_tile_waves_tc():
+    # More tiles than SMs (several persistent waves), ragged in M, N and K.
+    base = wl.BY_NAME["gemm_8192_bf16_transB_beta1"]
+    w = base.with_shape(2320, 1800, 520, seed=6200)
+    check_full(w, TC)
+
+
+def test_integer_bit_exact_tc_multi_tile():
+    base = wl.WORKLOAD_4096_INT
+    w = base.with_shape(400, 520, 1032, seed=6300)
+    check_full(w, TC)
+    check_full(w, MMA)
+
+
+# ------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("path", [MMA, TC])
+def test_beta_zero_never_reads_c(path):
+    w = wl.BY_NAME["gemm_4096_f16"].with_shape(144, 264, 72, seed=6400)
+    (A, B, _), (Ad, Bd, _) = device_inputs(w)
+    Cnan = torch.full((w.M, w.N), float("nan"), device="cuda")
+    D = run_gpu(w, Ad, Bd, Cnan, path)
+    Dref, S = oracle_full(w, A, B, None)
+    ok, msg = oracle.compare(D, Dref, S)
+    assert ok, msg
+
+
+@pytest.mark.parametrize("path", [MMA, TC])
+def test_in_place_d_equals_c(path):
+    w = wl.BY_NAME["gemm_256_bf16_transB_beta1"].with_shape(272, 392, 200, seed=6500)
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+    D = run_gpu(w, Ad, Bd, Cd, path, D=Cd)
+    Dref, S = oracle_full(w, A, B, C)
+    ok, msg = oracle.compare(D, Dref, S)
+    assert ok, msg
+
+
+@pytest.mark.parametrize("path", [MMA, TC])
+def test_identity_bit_exact_real_data(path):
+    # A = I  =>  D = fp32(B) exactly, for any real B (the oracle pin, now on the GPU).
+    n, N = 208, 136
+    for dtype in (wl.F16, wl.BF16):
+        td = wl.torch_dtype(dtype)
+        g = torch.Generator().manual_seed(77)
+        Bh = torch.randn(n, N, generator=g).to(td)
+        I = torch.eye(n).to(td)
+        D = torch.empty(n, N, device="cuda")
+        st = tp.tpgemm_gemm_path(D, I.cuda(), Bh.cuda(), None, n, N, n, 0, 0, dtype, 0.0, None,
+                                 path)
+        assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+        assert torch.equal(D.cpu(), Bh.float())
+
+
+def test_rejects_misaligned_device_pointers():
+    A = torch.zeros(64 * 64 + 8, dtype=torch.float16, device="cuda")
+    B = torch.zeros(64 * 64, dtype=torch.float16, device="cuda")
+    D = torch.zeros(64 * 64, dtype=torch.float32, device="cuda")
+    st = tp.tpgemm_gemm(D, A.data_ptr() + 2, B, None, 64, 64, 64, 0, 0, 0, 0.0, None)
+    assert st == tp.TPGEMM_ERR_ALIGN
+
+
+# -------------------------------------------- the five workloads, full size
+def sample_positions(M, N, n, seed):
+    rng = np.random.default_rng(seed)
+    r = rng.integers(0, M, n)
+    c = rng.integers(0, N, n)
+    # always include the corners and the last row / column (ragged tails)
+    r = np.concatenate([r, [0, 0, M - 1, M - 1, M // 2]])
+    c = np.concatenate([c, [0, N - 1, 0, N - 1, N - 1]])
+    return r, c
+
+
+def fp64_reference(w, Ad, Bd, Cd):
+    a = Ad.double()
+    b = Bd.double()
+    a = a.t() if w.transA else a
+    b = b.t() if w.transB else b
+    ref = a @ b
+    if w.beta:
+        ref += Cd.double()
+    S = a.abs() @ b.abs()
+    return ref, S
+
+
+@pytest.mark.parametrize("name", [w.name for w in wl.WORKLOADS] + ["gemm_4096_f16_int"])
+def test_workload_full_size(name):
+    w = wl.BY_NAME[name]
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+    D = torch.empty(w.M, w.N, device="cuda")
+    st = tp.tpgemm_gemm(D, Ad, Bd, Cd, w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, None)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    Dh = D.cpu().numpy()
+    assert np.isfinite(Dh).all()
+    # 1) sampled entries against the oracle, computed one by one
+    r, c = sample_positions(w.M, w.N, 3000, w.seed)
+    Dref, S = oracle.gemm_entries(r, c, wl.bits(A), wl.bits(B), None if C is None else C.numpy(),
+                                  w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+    ok, msg = oracle.compare(Dh[r, c], Dref, S, exact=w.integer_valued)
+    assert ok, f"{name} sampled: {msg}"
+    # 2) every element: integer workloads are exact, so row sums must match
+    #    A . (B 1) exactly; real workloads are held to the bound against an
+    #    fp64 product computed by torch.
+    if w.integer_valued:
+        assert np.array_equal(Dh, np.round(Dh))
+        a = Ad.double().t() if w.transA else Ad.double()
+        b = Bd.double().t() if w.transB else Bd.double()
+        want = (a @ b.sum(dim=1, keepdim=True)).squeeze(1)
+        assert torch.equal(D.double().sum(dim=1), want)
+    else:
+        ref, Sd = fp64_reference(w, Ad, Bd, Cd)
+        bound = Sd * (2.0 ** -10) + 1e-6
+        err = (D.double() - ref).abs()
+        assert bool((err <= bound).all()), f"{name}: max err/bound {float((err / bound).max())}"

@@ -1,0 +1,399 @@
+// tcgen05 GEMM for sm_103a:  X = P . Q^T (+ C), f16/bf16 in, f32 accumulate and out.
+//
+// Persistent, warp-specialised CTA of 6 warps, one CTA per SM:
+//   warp 0      TMA producer: one thread fills a ring of shared-memory stages
+//               with 128-byte-swizzled P and Q tiles (cp.async.bulk.tensor).
+//   warp 1      owns tensor memory (tcgen05.alloc / dealloc, whole warp) and
+//               one thread issues tcgen05.mma for every 16-deep K step into a
+//               double-buffered accumulator, committing stage releases and
+//               "accumulator full" to mbarriers (tcgen05.commit).
+//   warps 2..5  epilogue warpgroup: tcgen05.ld 32x32b of its 32-lane quadrant,
+//               + beta.C (TMA-loaded into a swizzled staging tile), and a TMA
+//               store of D from the same staging tile.
+//
+// This follows the single-thread issue, commit-to-mbarrier and
+// alloc / relinquish / dealloc protocol of the tcgen05 copy page ("TVM
+// Blackwell tcgen05.cp 全解析", section 演示程序), the encode-once descriptor
+// with a patched 14-bit start address (same page, 调度算法四步 第3步/第4步), the
+// warpgroup .32x32b tensor-memory load of the tcgen05_ldst page (Algorithm,
+// Generated CUDA), and the gemm semantics of the synchronous gemm page
+// (语义定义, 二: D = A.B + beta.C, beta in {0,1}). Every mbarrier wait is bounded
+// in time; on expiry the kernel records a status word, stops every role, waits
+// for its own copies and MMAs in flight, frees tensor memory and returns.
+#include "ptx.cuh"
+#include "tpgemm_internal.h"
+
+namespace tpg {
+
+__device__ int g_tc_status;  // 0 = ok, kStatusTimeout after an expired wait
+
+namespace {
+
+constexpr int kBM = 128;           // P rows per tile (tensor-memory lanes)
+constexpr int kBK = 64;            // K elements per stage: one 128-byte swizzle row
+constexpr int kUmmaK = 16;         // K per tcgen05.mma (kind::f16)
+constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
+constexpr int kAccStride = 256;    // column offset of accumulator buffer 1
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBufFloats = 32 * 32;  // one 32 x 32 f32 staging tile (4 KB)
+constexpr int kAtomBytes = 8192;   // MN-major atom: 64 K rows x 128 bytes
+
+struct Smem {
+    uint8_t* stages;
+    float* epi;            // [4 warps][2 buffers][32*32]
+    uint64_t* full;        // [stages]
+    uint64_t* empty;       // [stages]
+    uint64_t* acc_full;    // [2]
+    uint64_t* acc_empty;   // [2]
+    uint64_t* cbar;        // [4 warps][2 buffers]
+    uint64_t* drain;       // [1]
+    uint32_t* tmem_base;
+    volatile int* abort;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw, const TcParams& p) {
+    Smem s;
+    uintptr_t a = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
+    uint8_t* b = reinterpret_cast<uint8_t*>(a);
+    s.stages = b;
+    b += size_t(p.stages) * (p.p_bytes + p.q_bytes);
+    s.epi = reinterpret_cast<float*>(b);
+    b += size_t(kEpiWarps) * 2 * kEpiBufFloats * sizeof(float);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(b);
+    s.full = bars;
+    s.empty = bars + p.stages;
+    s.acc_full = bars + 2 * p.stages;
+    s.acc_empty = s.acc_full + 2;
+    s.cbar = s.acc_empty + 2;
+    s.drain = s.cbar + 2 * kEpiWarps;
+    s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.abort = reinterpret_cast<volatile int*>(s.tmem_base + 1);
+    return s;
+}
+
+// Bounded wait on one mbarrier phase. False if the bound expired or (unless
+// draining) another role already gave up. A drain wait ignores the abort flag:
+// it is how a role lets its own copies or MMAs in flight finish before exit.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           uint64_t timeout_ns, bool drain = false) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (!drain && *abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            *abort = 1;
+            atomicExch(&g_tc_status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// Tile t -> (tile along P, tile along Q); groups of `group` P-tiles sweep all
+// Q-tiles so one wave of CTAs shares a few P and Q panels in L2.
+__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tp, int& tq) {
+    const int per_group = p.group * p.tiles_q;
+    const int g = t / per_group;
+    const int first = g * p.group;
+    const int gsz = min(p.tiles_p - first, p.group);
+    const int r = t - g * per_group;
+    tp = first + r % gsz;
+    tq = r / gsz;
+}
+
+template <bool SWAP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
+                   const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
+                   const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem s = carve(smem_raw, p);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---------------------------------------------------------------- set-up
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&mapP);
+        prefetch_tensormap(&mapQ);
+        if (p.beta) prefetch_tensormap(&mapC);
+        prefetch_tensormap(&mapD);
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.acc_full[i], 1);
+            mbar_init(&s.acc_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&s.cbar[i], 1);
+        mbar_init(s.drain, 1);
+        *s.abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(s.tmem_base, kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *s.tmem_base;
+    const uint64_t tmo = p.timeout_ns;
+    // In-flight bookkeeping kept to teardown, where an aborted CTA drains it.
+    uint32_t issued_parity = 0;  // producer: bit i = parity of the last fill of stage i
+    uint32_t issued_any = 0;     // producer: bit i = stage i was ever filled
+    uint32_t cphase = 0;         // epilogue: bit i = parity of the next C fill of buffer i
+    uint32_t cpend = 0;          // epilogue: bit i = a C fill into staging buffer i in flight
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                int tp, tq;
+                tile_coords(t, p, tp, tq);
+                const int p0 = tp * kBM;
+                const int q0 = tq * p.bn;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_phase(&s.empty[stage], phase ^ 1u, s.abort, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sp = s.stages + size_t(stage) * (p.p_bytes + p.q_bytes);
+                    uint8_t* sq = sp + p.p_bytes;
+                    mbar_arrive_expect_tx(&s.full[stage], p.tx_bytes);
+                    const int k0 = kb * kBK;
+                    if (p.p_mn) {
+                        tma_load_2d(sp, &mapP, &s.full[stage], p0, k0);
+                        tma_load_2d(sp + kAtomBytes, &mapP, &s.full[stage], p0 + 64, k0);
+                    } else {
+                        tma_load_2d(sp, &mapP, &s.full[stage], k0, p0);
+                    }
+                    if (p.q_mn) {
+                        for (uint32_t a = 0; a < p.q_boxes; ++a)
+                            tma_load_2d(sq + a * kAtomBytes, &mapQ, &s.full[stage], q0 + 64 * a, k0);
+                    } else {
+                        tma_load_2d(sq, &mapQ, &s.full[stage], k0, q0);
+                    }
+                    issued_any |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            // Descriptor templates, encoded once; each issue patches the start address.
+            const uint64_t dP = p.p_mn ? smem_desc_sw128_template(kAtomBytes, 1024)
+                                       : smem_desc_sw128_template(16, 1024);
+            const uint64_t dQ = p.q_mn ? smem_desc_sw128_template(kAtomBytes, 1024)
+                                       : smem_desc_sw128_template(16, 1024);
+            // Start-address step per 16-deep K slice: 32 bytes along a K-major
+            // swizzle row, 16 rows of 128 bytes for an MN-major tile.
+            const uint32_t stepP = p.p_mn ? kUmmaK * 128 : kUmmaK * 2;
+            const uint32_t stepQ = p.q_mn ? kUmmaK * 128 : kUmmaK * 2;
+            const uint32_t stage_base = smem_u32(s.stages);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!wait_phase(&s.acc_empty[b], acc_phase ^ 1u, s.abort, tmo)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem + uint32_t(b * kAccStride);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_phase(&s.full[stage], phase, s.abort, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t ap = stage_base + uint32_t(stage) * (p.p_bytes + p.q_bytes);
+                    const uint32_t aq = ap + p.p_bytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * stepP);
+                        const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * stepQ);
+                        tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (kb | kk) != 0);
+                    }
+                    tc_commit(&s.empty[stage]);  // stage free once these MMAs finish
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&s.acc_full[b]);  // accumulator ready for the epilogue
+            }
+            // Drain: every MMA this thread issued has completed before teardown.
+            tc_commit(s.drain);
+            wait_phase(s.drain, 0, s.abort, tmo, true);
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int ew = warp - 2;           // 0..3 staging slot
+        const int quad = warp & 3;         // tensor-memory lane quadrant of this warp
+        float* bufs = s.epi + size_t(ew) * 2 * kEpiBufFloats;
+        uint64_t* cb = s.cbar + 2 * ew;
+        const uint32_t lane_base = uint32_t(quad * 32) << 16;
+        const int nchunks = (p.bn + 31) / 32;
+        // Output extents in the kernel's (P, Q) frame, for skipping empty chunks.
+        const int lim_p = p.Mp;
+        const int lim_q = p.Nq;
+        int it = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+            int tp, tq;
+            tile_coords(t, p, tp, tq);
+            const int pw = tp * kBM + quad * 32;  // first P row of this warp's quadrant
+            const int q0 = tq * p.bn;
+            const bool warp_live = pw < lim_p;
+            int live_chunks = 0;
+            if (warp_live) live_chunks = min(nchunks, (lim_q - q0 + 31) / 32);
+            // D coordinates of chunk c's 32 x 32 box: (x = column, y = row).
+            auto box_x = [&](int c) { return SWAP ? pw : q0 + 32 * c; };
+            auto box_y = [&](int c) { return SWAP ? q0 + 32 * c : pw; };
+
+            // Both staging buffers free: every earlier store has read its source.
+            if (lane == 0) bulk_wait_group_read<0>();
+            // Prefetch C for the first two chunks while the MMAs still run.
+            if (p.beta) {
+                for (int c = 0; c < 2 && c < live_chunks; ++c) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&cb[c], kEpiBufFloats * 4);
+                        tma_load_2d(bufs + c * kEpiBufFloats, &mapC, &cb[c], box_x(c), box_y(c));
+                    }
+                    cpend |= 1u << c;
+                }
+            }
+            __syncwarp();
+            const int b = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            bool ok = wait_phase(&s.acc_full[b], acc_phase, s.abort, tmo);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t acc_col = uint32_t(b * kAccStride);
+            for (int c = 0; c < live_chunks && ok; ++c) {
+                const int bi = c & 1;
+                float* buf = bufs + bi * kEpiBufFloats;
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * c), r);
+                tmem_ld_wait(r);
+                if (p.beta) {
+                    ok = wait_phase(&cb[bi], (cphase >> bi) & 1u, s.abort, tmo);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    cphase ^= 1u << bi;
+                    cpend &= ~(1u << bi);
+                } else {
+                    if (lane == 0) bulk_wait_group_read<1>();  // the store of chunk c-2 read buf
+                    __syncwarp();
+                }
+                if (!SWAP) {
+                    // Lane = P row = D row; 8 16-byte chunks of its 32 columns,
+                    // placed by the 128-byte swizzle (chunk ^ row % 8).
+                    float* row = buf + lane * 32;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float4* dst = reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 2));
+                        float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                               __uint_as_float(r[4 * j + 2]),
+                                               __uint_as_float(r[4 * j + 3]));
+                        if (p.beta) {
+                            const float4 cv = *dst;
+                            v.x += cv.x;
+                            v.y += cv.y;
+                            v.z += cv.z;
+                            v.w += cv.w;
+                        }
+                        *dst = v;
+                    }
+                } else {
+                    // Lane = P row = D column; register i is D row 32c + i.
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int idx = i * 32 + ((((lane >> 2) ^ (i & 7))) << 2) + (lane & 3);
+                        float v = __uint_as_float(r[i]);
+                        if (p.beta) v += buf[idx];
+                        buf[idx] = v;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&mapD, buf, box_x(c), box_y(c));
+                    bulk_commit_group();
+                    if (p.beta && c + 2 < live_chunks) {
+                        bulk_wait_group_read<0>();  // the store just issued has read buf
+                        mbar_arrive_expect_tx(&cb[bi], kEpiBufFloats * 4);
+                        tma_load_2d(buf, &mapC, &cb[bi], box_x(c + 2), box_y(c + 2));
+                    }
+                }
+                if (p.beta && c + 2 < live_chunks) cpend |= 1u << bi;
+                __syncwarp();
+            }
+            // Accumulator buffer b may be overwritten by the next tile's MMAs.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.acc_empty[b]);
+            if (!ok) break;
+        }
+        if (lane == 0) bulk_wait_group<0>();
+    }
+
+    // --------------------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*s.abort) {
+        // An aborted CTA lets every TMA fill it issued land before it exits.
+        if (warp == 0 && lane == 0)
+            for (int i = 0; i < p.stages; ++i)
+                if (issued_any & (1u << i))
+                    wait_phase(&s.full[i], (issued_parity >> i) & 1u, s.abort, tmo, true);
+        if (warp >= 2)
+            for (int i = 0; i < 2; ++i)
+                if (cpend & (1u << i))
+                    wait_phase(&s.cbar[2 * (warp - 2) + i], (cphase >> i) & 1u, s.abort, tmo, true);
+        __syncthreads();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes) {
+    return 1024 + size_t(stages) * (p_bytes + q_bytes) +
+           size_t(kEpiWarps) * 2 * kEpiBufFloats * sizeof(float) +
+           sizeof(uint64_t) * (2 * size_t(stages) + 4 + 2 * kEpiWarps + 1) + 16;
+}
+
+cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
+    const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes);
+    if (smem > size_t(kTcMaxSmem)) return cudaErrorInvalidConfiguration;
+    auto kernel = p.swap ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kTcThreads, smem, stream>>>(maps.P, maps.Q, maps.C, maps.D, p);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_read_and_clear_device_status(int* status) {
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_tc_status, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(int));
+}
+
+}  // namespace tpg

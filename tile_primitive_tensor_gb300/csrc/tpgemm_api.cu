@@ -1,0 +1,408 @@
+// C-ABI entry points of libtpgemm.so: argument validation, kernel planning,
+// TMA tensor-map encoding and launch on the caller's stream.
+//
+// The acceptance rules are those of the TVM TIRx synchronous gemm page
+// ("TVM TIRx 同步 GEMM 深度解析", section 二 What it accepts and its
+// source-level conditions): M % 16 = 0, N % 8 = 0, K % 8 = 0; A and B both
+// float16 or both bfloat16; C and D float32; alpha = 1; beta in {0, 1};
+// transpose flags only select the stored orientation. As on that page, every
+// rejection carries a readable reason (there via DispatchFail / RuntimeError,
+// here via tpgemm_last_error_detail).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "ptx.cuh"
+#include "tpgemm.h"
+#include "tpgemm_internal.h"
+
+namespace {
+
+thread_local std::string g_detail;
+
+tpgemm_status fail(tpgemm_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_detail = buf;
+    return s;
+}
+
+// ------------------------------------------------------------ device cache
+struct DeviceInfo {
+    bool valid = false;
+    int major = 0, minor = 0, sms = 0;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+tpgemm_status device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(TPGEMM_ERR_ARCH, "no CUDA device available: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(TPGEMM_ERR_ARCH, "device index %d unsupported", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.valid) {
+        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return fail(TPGEMM_ERR_ARCH, "cannot query device %d", dev);
+        d.valid = true;
+    }
+    *out = d;
+    return TPGEMM_OK;
+}
+
+tpgemm_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+            return fail(TPGEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled not available from the driver");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    *fn = g_encode;
+    return TPGEMM_OK;
+}
+
+// ------------------------------------------------------------- validation
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+tpgemm_status check_shape(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype, float beta) {
+    if (M <= 0 || N <= 0 || K <= 0)
+        return fail(TPGEMM_ERR_SHAPE, "M=%lld N=%lld K=%lld must all be positive", (long long)M,
+                    (long long)N, (long long)K);
+    if (M % 16) return fail(TPGEMM_ERR_SHAPE, "M=%lld is not a multiple of 16", (long long)M);
+    if (N % 8) return fail(TPGEMM_ERR_SHAPE, "N=%lld is not a multiple of 8", (long long)N);
+    if (K % 8) return fail(TPGEMM_ERR_SHAPE, "K=%lld is not a multiple of 8", (long long)K);
+    // Coordinates and tile counts are 32-bit inside the kernels.
+    const int64_t lim = int64_t(1) << 30;
+    if (M >= lim || N >= lim || K >= lim)
+        return fail(TPGEMM_ERR_SHAPE, "M, N, K must each be below 2^30");
+    if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16)
+        return fail(TPGEMM_ERR_DTYPE, "dtype %d is neither TPGEMM_F16 (0) nor TPGEMM_BF16 (1)",
+                    int(dtype));
+    if (!(beta == 0.0f || beta == 1.0f))
+        return fail(TPGEMM_ERR_BETA, "beta=%g; only 0 and 1 are supported", double(beta));
+    return TPGEMM_OK;
+}
+
+tpgemm_status check_pointers(float* D, const void* A, const void* B, const float* C, int64_t M,
+                             int64_t N, int64_t K, float beta) {
+    if (!D) return fail(TPGEMM_ERR_NULL, "D is NULL");
+    if (!A) return fail(TPGEMM_ERR_NULL, "A is NULL");
+    if (!B) return fail(TPGEMM_ERR_NULL, "B is NULL");
+    if (beta == 1.0f && !C) return fail(TPGEMM_ERR_NULL, "C is NULL with beta = 1");
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(D)) return fail(TPGEMM_ERR_ALIGN, "D=%p is not 16-byte aligned", (void*)D);
+    if (misaligned(A)) return fail(TPGEMM_ERR_ALIGN, "A=%p is not 16-byte aligned", A);
+    if (misaligned(B)) return fail(TPGEMM_ERR_ALIGN, "B=%p is not 16-byte aligned", B);
+    if (beta == 1.0f && misaligned(C))
+        return fail(TPGEMM_ERR_ALIGN, "C=%p is not 16-byte aligned", (const void*)C);
+    const size_t dn = size_t(M) * size_t(N) * 4;
+    if (overlaps(D, dn, A, size_t(M) * size_t(K) * 2)) return fail(TPGEMM_ERR_ALIAS, "D overlaps A");
+    if (overlaps(D, dn, B, size_t(K) * size_t(N) * 2)) return fail(TPGEMM_ERR_ALIAS, "D overlaps B");
+    if (beta == 1.0f && static_cast<const void*>(C) != static_cast<const void*>(D) &&
+        overlaps(D, dn, C, dn))
+        return fail(TPGEMM_ERR_ALIAS, "D overlaps C without being equal to it");
+    return TPGEMM_OK;
+}
+
+// ----------------------------------------------------------------- planning
+enum class Kernel { MmaSync, Tc };
+
+struct Plan {
+    Kernel kernel = Kernel::Tc;
+    tpg::TcParams tc{};
+    int grid = 0;
+    bool swap = false;
+};
+
+uint64_t wait_timeout_ns() {
+    static uint64_t v = [] {
+        const char* s = getenv("TPGEMM_WAIT_TIMEOUT_MS");
+        long long ms = s ? atoll(s) : 0;
+        if (ms <= 0) ms = 2000;
+        return uint64_t(ms) * 1000000ull;
+    }();
+    return v;
+}
+
+// Shared bytes of one stage tile of an operand with `rows` rows along MN and
+// 64 K elements: K-contiguous tiles are rows x 128 bytes; MN-contiguous tiles
+// are whole 64-row atoms of 64 K rows x 128 bytes.
+uint32_t stage_tile_bytes(int rows, bool mn) {
+    return mn ? uint32_t((rows + 63) / 64) * 8192u : uint32_t(rows) * 128u;
+}
+
+tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB, bool bf16,
+                      float beta, int sms, Plan* out) {
+    tpg::TcParams p{};
+    // Small M: swap operands so N runs along the 128 tensor-memory lanes and
+    // all of M fits one accumulator (UMMA N = M <= 256, a multiple of 16).
+    const bool swap = M <= 256 && N > M;
+    const int64_t Mp = swap ? N : M;
+    const int64_t Nq = swap ? M : N;
+    const bool p_mn = swap ? !transB : transA;
+    const bool q_mn = swap ? transA : !transB;
+    int bn;
+    if (swap) {
+        bn = int(Nq);
+    } else {
+        // 128 x 256 tiles unless that leaves most SMs idle.
+        const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+        bn = (N <= 128 || tiles256 < sms) ? 128 : 256;
+        if (N <= 64) bn = int(((N + 15) / 16) * 16);
+    }
+    p.Mp = int(Mp);
+    p.Nq = int(Nq);
+    p.K = int(K);
+    p.bn = bn;
+    p.tiles_p = int((Mp + 127) / 128);
+    p.tiles_q = int((Nq + bn - 1) / bn);
+    p.num_tiles = p.tiles_p * p.tiles_q;
+    p.k_blocks = int((K + 63) / 64);
+    p.p_mn = p_mn;
+    p.q_mn = q_mn;
+    p.beta = beta == 1.0f;
+    p.idesc = tpg::idesc_f16_f32(bf16, p_mn, q_mn, 128, bn);
+    p.p_bytes = stage_tile_bytes(128, p_mn);
+    p.q_bytes = stage_tile_bytes(bn, q_mn);
+    p.q_boxes = q_mn ? uint32_t((bn + 63) / 64) : 1u;
+    p.tx_bytes = p.p_bytes + p.q_bytes;
+    p.timeout_ns = wait_timeout_ns();
+    p.swap = swap;
+    p.group = 16;
+    int stages = 8;
+    while (stages > 2 && tpg::tc_smem_bytes(stages, p.p_bytes, p.q_bytes) > size_t(tpg::kTcMaxSmem))
+        --stages;
+    if (tpg::tc_smem_bytes(stages, p.p_bytes, p.q_bytes) > size_t(tpg::kTcMaxSmem))
+        return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
+    // The epilogue stores 32-column boxes; a tile width that is not a multiple
+    // of 32 is only used when it is the only tile along Q (the box overhang is
+    // then past the end of the matrix and clipped by the TMA store).
+    if (bn % 32 != 0 && p.tiles_q != 1)
+        return fail(TPGEMM_ERR_PATH, "internal: tile width %d with %d tiles along Q", bn, p.tiles_q);
+    p.stages = stages;
+    out->kernel = Kernel::Tc;
+    out->tc = p;
+    out->grid = std::min(p.num_tiles, sms);
+    out->swap = swap;
+    return TPGEMM_OK;
+}
+
+tpgemm_status make_plan(int64_t M, int64_t N, int64_t K, bool transA, bool transB, bool bf16,
+                        float beta, tpgemm_path path, int sms, Plan* out) {
+    if (path == TPGEMM_PATH_MMA_SYNC) {
+        out->kernel = Kernel::MmaSync;
+        return TPGEMM_OK;
+    }
+    if (path == TPGEMM_PATH_AUTO) {
+        // Tiny problems finish faster on the mma.sync kernel (no TMA / TMEM
+        // set-up, more CTAs than 128-row tiles would give).
+        const double flops = 2.0 * double(M) * double(N) * double(K);
+        if (flops <= double(1 << 26)) {
+            out->kernel = Kernel::MmaSync;
+            return TPGEMM_OK;
+        }
+    } else if (path != TPGEMM_PATH_TCGEN05) {
+        return fail(TPGEMM_ERR_PATH, "unknown path %d", int(path));
+    }
+    return plan_tc(M, N, K, transA, transB, bf16, beta, sms, out);
+}
+
+// ---------------------------------------------------------- tensor maps
+tpgemm_status encode_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* base,
+                        CUtensorMapDataType type, int elem_bytes, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer, const char* what) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * uint64_t(elem_bytes)};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TPGEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
+                    int(r));
+    return TPGEMM_OK;
+}
+
+// Map of a K x rows operand: K-contiguous -> dims {K, rows}, box {64, box_rows};
+// MN-contiguous -> dims {rows, K}, box {64, 64}.
+tpgemm_status encode_operand(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map,
+                             const void* base, bool bf16, int64_t rows, int64_t K, bool mn,
+                             int box_rows, const char* what) {
+    const CUtensorMapDataType t =
+        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (mn) return encode_2d(enc, map, base, t, 2, uint64_t(rows), uint64_t(K), 64, 64, what);
+    return encode_2d(enc, map, base, t, 2, uint64_t(K), uint64_t(rows), 64, uint32_t(box_rows), what);
+}
+
+tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_t M, int64_t N,
+                  int64_t K, int transA, int transB, tpgemm_dtype dtype, float beta, void* stream,
+                  tpgemm_path path) {
+    g_detail.clear();
+    tpgemm_status s = check_shape(M, N, K, dtype, beta);
+    if (s != TPGEMM_OK) return s;
+    s = check_pointers(D, A, B, C, M, N, K, beta);
+    if (s != TPGEMM_OK) return s;
+    DeviceInfo dev;
+    s = device_info(&dev);
+    if (s != TPGEMM_OK) return s;
+    if (!(dev.major == 10 && dev.minor == 3))
+        return fail(TPGEMM_ERR_ARCH, "device is compute capability %d.%d; this build targets sm_103a",
+                    dev.major, dev.minor);
+    const bool bf16 = dtype == TPGEMM_BF16;
+    Plan plan;
+    s = make_plan(M, N, K, transA != 0, transB != 0, bf16, beta, path, dev.sms, &plan);
+    if (s != TPGEMM_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (plan.kernel == Kernel::MmaSync) {
+        tpg::MmaSyncArgs a{D, A, B, beta == 1.0f ? C : nullptr, int(M), int(N), int(K),
+                           transA != 0, transB != 0, bf16, beta == 1.0f};
+        cudaError_t e = tpg::launch_mma_sync(a, st);
+        if (e != cudaSuccess)
+            return fail(TPGEMM_ERR_LAUNCH, "mma.sync kernel launch: %s", cudaGetErrorString(e));
+        return TPGEMM_OK;
+    }
+
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    s = get_encoder(&enc);
+    if (s != TPGEMM_OK) return s;
+    const tpg::TcParams& p = plan.tc;
+    tpg::TcMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    // P / Q operands: normal P = A (rows M), Q = B^T (rows N); swapped P = B^T, Q = A.
+    const void* pp = plan.swap ? B : A;
+    const void* qq = plan.swap ? A : B;
+    s = encode_operand(enc, &maps.P, pp, bf16, p.Mp, K, p.p_mn, 128, "P operand");
+    if (s != TPGEMM_OK) return s;
+    s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.bn, "Q operand");
+    if (s != TPGEMM_OK) return s;
+    s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M), 32,
+                  32, "D");
+    if (s != TPGEMM_OK) return s;
+    if (p.beta) {
+        s = encode_2d(enc, &maps.C, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M),
+                      32, 32, "C");
+        if (s != TPGEMM_OK) return s;
+    }
+    cudaError_t e = tpg::launch_tc(maps, p, plan.grid, st);
+    if (e != cudaSuccess)
+        return fail(TPGEMM_ERR_LAUNCH, "tcgen05 kernel launch: %s", cudaGetErrorString(e));
+    return TPGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tpgemm_status tpgemm_gemm(float* D, const void* A, const void* B, const float* C, int64_t M,
+                          int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
+                          float beta, void* stream) {
+    return run(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream, TPGEMM_PATH_AUTO);
+}
+
+tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const float* C, int64_t M,
+                               int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
+                               float beta, void* stream, tpgemm_path path) {
+    return run(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream, path);
+}
+
+const char* tpgemm_status_string(tpgemm_status s) {
+    switch (s) {
+        case TPGEMM_OK: return "ok";
+        case TPGEMM_ERR_SHAPE: return "invalid shape";
+        case TPGEMM_ERR_DTYPE: return "unsupported dtype";
+        case TPGEMM_ERR_BETA: return "unsupported beta";
+        case TPGEMM_ERR_NULL: return "null pointer";
+        case TPGEMM_ERR_ALIGN: return "misaligned pointer";
+        case TPGEMM_ERR_ALIAS: return "overlapping operands";
+        case TPGEMM_ERR_ARCH: return "unsupported device";
+        case TPGEMM_ERR_LAUNCH: return "launch failed";
+        case TPGEMM_ERR_TIMEOUT: return "device wait timed out";
+        case TPGEMM_ERR_PATH: return "kernel path cannot run this problem";
+    }
+    return "unknown status";
+}
+
+const char* tpgemm_last_error_detail(void) { return g_detail.c_str(); }
+
+tpgemm_status tpgemm_last_device_error(void) {
+    g_detail.clear();
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return fail(TPGEMM_ERR_LAUNCH, "device synchronize: %s", cudaGetErrorString(e));
+    int st = 0;
+    e = tpg::tc_read_and_clear_device_status(&st);
+    if (e != cudaSuccess)
+        return fail(TPGEMM_ERR_LAUNCH, "reading device status: %s", cudaGetErrorString(e));
+    if (st == tpg::kStatusTimeout)
+        return fail(TPGEMM_ERR_TIMEOUT, "a tcgen05 kernel wait exceeded its bound");
+    return TPGEMM_OK;
+}
+
+tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, int transB,
+                                   tpgemm_dtype dtype, float beta, tpgemm_path path, char* buf,
+                                   int buflen) {
+    g_detail.clear();
+    tpgemm_status s = check_shape(M, N, K, dtype, beta);
+    if (s != TPGEMM_OK) return s;
+    int sms = 152;  // GB300; replaced by the live count when a device is present
+    int dev = 0;
+    int v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+        sms = v;
+    else
+        cudaGetLastError();
+    Plan plan;
+    s = make_plan(M, N, K, transA != 0, transB != 0, dtype == TPGEMM_BF16, beta, path, sms, &plan);
+    if (s != TPGEMM_OK) return s;
+    char text[512];
+    if (plan.kernel == Kernel::MmaSync) {
+        snprintf(text, sizeof(text),
+                 "path=mma_sync tile=%dx%dx32 grid=%lldx%lld warps=4 k_inst=%s",
+                 tpg::kMmaTileM, tpg::kMmaTileN, (long long)((N + 63) / 64),
+                 (long long)((M + 63) / 64), (K % 16) ? "m16n8k16+m16n8k8" : "m16n8k16");
+    } else {
+        const tpg::TcParams& p = plan.tc;
+        snprintf(text, sizeof(text),
+                 "path=tcgen05 orientation=%s tile=128x%dx64 umma=128x%dx16 stages=%d "
+                 "tiles=%dx%d grid=%d p_major=%s q_major=%s smem=%zu",
+                 plan.swap ? "swapped" : "normal", p.bn, p.bn, p.stages, p.tiles_p, p.tiles_q,
+                 plan.grid, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
+                 tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes));
+    }
+    if (buf && buflen > 0) {
+        strncpy(buf, text, size_t(buflen) - 1);
+        buf[buflen - 1] = '\0';
+    }
+    return TPGEMM_OK;
+}
+
+const char* tpgemm_version(void) { return "0.1.0"; }
+
+}  // extern "C"

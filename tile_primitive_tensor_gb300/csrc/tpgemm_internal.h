@@ -1,0 +1,63 @@
+// Host-side interfaces between the C-ABI entry points (tpgemm_api.cu) and the
+// two kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace tpg {
+
+constexpr int kStatusTimeout = 9;  // matches TPGEMM_ERR_TIMEOUT
+
+// ---- warp-level mma.sync kernel (small problems) ----
+struct MmaSyncArgs {
+    float* D;
+    const void* A;
+    const void* B;
+    const float* C;
+    int M, N, K;
+    bool transA, transB, bf16, beta;
+};
+constexpr int kMmaTileM = 64;
+constexpr int kMmaTileN = 64;
+cudaError_t launch_mma_sync(const MmaSyncArgs& a, cudaStream_t stream);
+
+// ---- tcgen05 kernel ----
+// The kernel computes a product X = P . Q^T over K with P rows mapped to the
+// 128 tensor-memory lanes of a tile and Q rows to its accumulator columns.
+// Normal orientation: P = A (rows m), Q = B^T (rows n), X = D.
+// Swapped orientation (small M): P = B^T (rows n), Q = A (rows m), X = D^T,
+// which the epilogue writes back transposed so that D stays [M, N].
+struct TcParams {
+    int Mp, Nq, K;          // rows of P, rows of Q, reduction length
+    int tiles_p, tiles_q;   // tile counts along P (128 rows) and Q (bn rows)
+    int num_tiles;
+    int k_blocks;           // ceil(K / 64)
+    int bn;                 // accumulator columns per tile = UMMA N (16..256, %16)
+    int stages;             // depth of the TMA ring
+    int p_mn, q_mn;         // operand stored MN-contiguous (1) or K-contiguous (0)
+    int beta;               // 0 or 1
+    int group;              // tiles along P per raster group (L2 reuse)
+    uint32_t idesc;         // tcgen05 instruction descriptor
+    uint32_t p_bytes;       // shared bytes of one P stage tile
+    uint32_t q_bytes;       // shared bytes of one Q stage tile
+    uint32_t q_boxes;       // TMA boxes per Q stage tile
+    uint32_t tx_bytes;      // bytes the TMA delivers per stage
+    uint64_t timeout_ns;    // bound on every mbarrier wait
+    int swap;               // orientation, for the epilogue's D coordinates
+};
+
+struct TcMaps {
+    CUtensorMap P, Q, C, D;
+};
+
+size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes);
+constexpr int kTcThreads = 192;
+constexpr int kTcMaxSmem = 232448;  // 227 KB opt-in per block on sm_100-class parts
+cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream);
+
+// Device status word written by the tcgen05 kernel's bounded waits.
+cudaError_t tc_read_and_clear_device_status(int* status);
+
+}  // namespace tpg
