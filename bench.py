@@ -46,7 +46,7 @@ def log(*a):
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="overwrite a buffer larger than L2 before every timed step (the GEMM "
+                         "alone is timed, with events around each launch)")
     return ap.parse_args()
 
 
@@ -231,30 +234,45 @@ def run_ours(args, rank, world, local_rank):
     sampler.start()
     time.sleep(0.4)  # let nvidia-smi start before the timed region
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    if args.flush_l2:
+        # Cold L2 for every step: a 512 MB write between launches, outside the
+        # per-launch events.
+        scrub = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            scrub.fill_(1.0)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    else:
+        # Events only around the whole timed loop: an event between two launches
+        # would stop the next launch's set-up from overlapping the previous one.
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        total_ms = ev0.elapsed_time(ev1)
     t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
     sampler.stop()
     tp.check(tp.tpgemm_last_device_error())
-    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = starts[0].elapsed_time(ends[-1])
     if world > 1:
         t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    launch_ms = statistics.mean(per_launch)
+    launch_ms = ms_per_step  # one launch of the kernel per step
     value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
     clocks = sampler.summary(t_wall0, t_wall1)
 
@@ -320,8 +338,9 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
             "bf16" if w.dtype == wl.BF16 else "f16",
         "data": "synthetic (seeded, workloads.py)",
-        "config": {**w.describe(), "l2": "inputs larger than L2 (no flush needed)" if
-                   w.algorithmic_bytes > 2 * 129e6 else "L2 not flushed; working set fits L2",
+        "config": {**w.describe(), "l2": "flushed before every step (512 MB write)" if
+                   args.flush_l2 else ("inputs larger than L2, no flush" if
+                                       w.algorithmic_bytes > 129e6 else "warm L2 (inputs fit)"),
                    "parallelism": f"replicas x{world}"},
         "clocks": clocks,
         "gpu_launches": args.steps,

@@ -146,7 +146,18 @@ def test_transpose_combos_swapped_orientation(tA, tB):
 def test_multi_tile_waves_tc():
     # More tiles than SMs (several persistent waves), ragged in M, N and K.
     base = wl.BY_NAME["gemm_8192_bf16_transB_beta1"]
-    w = base.with_shape(2320, 1800, 520, seed=6200)
+    w = base.with_shape(2320, 2600, 520, seed=6200)
+    check_full(w, TC)
+
+
+@pytest.mark.parametrize("bn", [32, 128, 160, 192, 224, 256])
+@pytest.mark.parametrize("tB", [False, True])
+def test_every_tile_width(bn, tB, monkeypatch):
+    # Each accumulator width the planner may choose, with B K- or MN-contiguous.
+    monkeypatch.setenv("TPGEMM_TC_BN", str(bn))
+    base = wl.BY_NAME["gemm_4096_f16"]
+    w = dataclasses.replace(base.with_shape(400, 1000, 264, seed=6250 + bn), transB=tB,
+                            beta=1.0, c_dist=("normal", 0.0, 1.0))
     check_full(w, TC)
 
 

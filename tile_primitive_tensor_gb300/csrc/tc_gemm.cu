@@ -40,12 +40,12 @@ constexpr int kAtomBytes = 8192;   // MN-major atom: 64 K rows x 128 bytes
 
 struct Smem {
     uint8_t* stages;
-    float* epi;            // [4 warps][2 buffers][32*32]
+    float* epi;            // [4 warps][epi_bufs][32*32]
     uint64_t* full;        // [stages]
     uint64_t* empty;       // [stages]
     uint64_t* acc_full;    // [2]
     uint64_t* acc_empty;   // [2]
-    uint64_t* cbar;        // [4 warps][2 buffers]
+    uint64_t* cbar;        // [4 warps][kTcMaxEpiBufs]
     uint64_t* drain;       // [1]
     uint32_t* tmem_base;
     volatile int* abort;
@@ -58,14 +58,14 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const TcParams& p) {
     s.stages = b;
     b += size_t(p.stages) * (p.p_bytes + p.q_bytes);
     s.epi = reinterpret_cast<float*>(b);
-    b += size_t(kEpiWarps) * 2 * kEpiBufFloats * sizeof(float);
+    b += size_t(kEpiWarps) * p.epi_bufs * kEpiBufFloats * sizeof(float);
     uint64_t* bars = reinterpret_cast<uint64_t*>(b);
     s.full = bars;
     s.empty = bars + p.stages;
     s.acc_full = bars + 2 * p.stages;
     s.acc_empty = s.acc_full + 2;
     s.cbar = s.acc_empty + 2;
-    s.drain = s.cbar + 2 * kEpiWarps;
+    s.drain = s.cbar + kTcMaxEpiBufs * kEpiWarps;
     s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.abort = reinterpret_cast<volatile int*>(s.tmem_base + 1);
     return s;
@@ -101,6 +101,17 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tp, i
     tq = r / gsz;
 }
 
+// First K block of tile t. With rotation, groups of k_rotate consecutive tiles
+// start at evenly spread blocks and wrap around, so CTAs that share an operand
+// tile (every CTA, when all of M fits one tile) do not all read the same K
+// slice of it at the same time.
+__device__ __forceinline__ int first_k_block(int t, const TcParams& p) {
+    if (!p.k_rotate) return 0;
+    const int g = t / p.k_rotate;
+    const int groups = (p.num_tiles + p.k_rotate - 1) / p.k_rotate;
+    return int((int64_t(g) * p.k_blocks) / groups) % p.k_blocks;
+}
+
 template <bool SWAP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
@@ -125,7 +136,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&s.acc_full[i], 1);
             mbar_init(&s.acc_empty[i], kEpiWarps);
         }
-        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&s.cbar[i], 1);
+        for (int i = 0; i < kTcMaxEpiBufs * kEpiWarps; ++i) mbar_init(&s.cbar[i], 1);
         mbar_init(s.drain, 1);
         *s.abort = 0;
         fence_mbarrier_init();
@@ -137,6 +148,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // Set-up above overlaps the previous grid's tail when launched with a
+    // programmatic dependency; global memory is touched only after this wait.
+    grid_launch_dependents();
+    grid_dependency_wait();
     const uint32_t tmem = *s.tmem_base;
     const uint64_t tmo = p.timeout_ns;
     // In-flight bookkeeping kept to teardown, where an aborted CTA drains it.
@@ -156,7 +171,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tile_coords(t, p, tp, tq);
                 const int p0 = tp * kBM;
                 const int q0 = tq * p.bn;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                int kb = first_k_block(t, p);
+                for (int i = 0; i < p.k_blocks; ++i, kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
                     if (!wait_phase(&s.empty[stage], phase ^ 1u, s.abort, tmo)) {
                         ok = false;
                         break;
@@ -209,7 +225,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!wait_phase(&s.acc_empty[b], acc_phase ^ 1u, s.abort, tmo)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem + uint32_t(b * kAccStride);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int i = 0; i < p.k_blocks; ++i) {
                     if (!wait_phase(&s.full[stage], phase, s.abort, tmo)) {
                         ok = false;
                         break;
@@ -221,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                         const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * stepP);
                         const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * stepQ);
-                        tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (kb | kk) != 0);
+                        tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (i | kk) != 0);
                     }
                     tc_commit(&s.empty[stage]);  // stage free once these MMAs finish
                     if (++stage == p.stages) {
@@ -240,8 +256,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // --------------------------------------------------------- epilogue
         const int ew = warp - 2;           // 0..3 staging slot
         const int quad = warp & 3;         // tensor-memory lane quadrant of this warp
-        float* bufs = s.epi + size_t(ew) * 2 * kEpiBufFloats;
-        uint64_t* cb = s.cbar + 2 * ew;
+        const int nbuf = p.epi_bufs;
+        float* bufs = s.epi + size_t(ew) * nbuf * kEpiBufFloats;
+        uint64_t* cb = s.cbar + kTcMaxEpiBufs * ew;
         const uint32_t lane_base = uint32_t(quad * 32) << 16;
         const int nchunks = (p.bn + 31) / 32;
         // Output extents in the kernel's (P, Q) frame, for skipping empty chunks.
@@ -260,11 +277,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             auto box_x = [&](int c) { return SWAP ? pw : q0 + 32 * c; };
             auto box_y = [&](int c) { return SWAP ? q0 + 32 * c : pw; };
 
-            // Both staging buffers free: every earlier store has read its source.
+            // All staging buffers free: every earlier store has read its source.
             if (lane == 0) bulk_wait_group_read<0>();
-            // Prefetch C for the first two chunks while the MMAs still run.
+            // Prefetch C for the first chunks (all of them when they fit the
+            // staging buffers) while the MMAs still run.
             if (p.beta) {
-                for (int c = 0; c < 2 && c < live_chunks; ++c) {
+                for (int c = 0; c < nbuf && c < live_chunks; ++c) {
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&cb[c], kEpiBufFloats * 4);
                         tma_load_2d(bufs + c * kEpiBufFloats, &mapC, &cb[c], box_x(c), box_y(c));
@@ -280,64 +298,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t acc_col = uint32_t(b * kAccStride);
-            for (int c = 0; c < live_chunks && ok; ++c) {
-                const int bi = c & 1;
+            // One 32-column chunk: its accumulator registers `cur` were loaded
+            // by the previous step; the next chunk's tcgen05.ld is issued into
+            // `nxt` before this one's shared-memory work so the two overlap.
+            auto chunk = [&](int c, uint32_t (&cur)[32], uint32_t (&nxt)[32]) -> bool {
+                const int bi = c % nbuf;
                 float* buf = bufs + bi * kEpiBufFloats;
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * c), r);
-                tmem_ld_wait(r);
+                tmem_ld_wait(cur);
+                if (c + 1 < live_chunks)
+                    tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * (c + 1)), nxt);
                 if (p.beta) {
-                    ok = wait_phase(&cb[bi], (cphase >> bi) & 1u, s.abort, tmo);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
+                    bool cok = wait_phase(&cb[bi], (cphase >> bi) & 1u, s.abort, tmo);
+                    cok = __all_sync(0xffffffffu, cok);
+                    if (!cok) {
+                        tmem_ld_wait_all();
+                        return false;
+                    }
                     cphase ^= 1u << bi;
                     cpend &= ~(1u << bi);
                 } else {
-                    if (lane == 0) bulk_wait_group_read<1>();  // the store of chunk c-2 read buf
+                    if (lane == 0) bulk_wait_group_read<1>();  // the store of chunk c-nbuf read buf
                     __syncwarp();
                 }
                 if (!SWAP) {
                     // Lane = P row = D row; 8 16-byte chunks of its 32 columns,
-                    // placed by the 128-byte swizzle (chunk ^ row % 8).
-                    float* row = buf + lane * 32;
+                    // placed by the 128-byte swizzle (chunk ^ row % 8). All C
+                    // reads are issued before any D write.
+                    float4* row = reinterpret_cast<float4*>(buf + lane * 32);
+                    float4 cv[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float4* dst = reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 2));
-                        float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                               __uint_as_float(r[4 * j + 2]),
-                                               __uint_as_float(r[4 * j + 3]));
-                        if (p.beta) {
-                            const float4 cv = *dst;
-                            v.x += cv.x;
-                            v.y += cv.y;
-                            v.z += cv.z;
-                            v.w += cv.w;
-                        }
-                        *dst = v;
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        cv[j] = p.beta ? row[j ^ (lane & 7)] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        row[j ^ (lane & 7)] = make_float4(__uint_as_float(cur[4 * j]) + cv[j].x,
+                                                          __uint_as_float(cur[4 * j + 1]) + cv[j].y,
+                                                          __uint_as_float(cur[4 * j + 2]) + cv[j].z,
+                                                          __uint_as_float(cur[4 * j + 3]) + cv[j].w);
                 } else {
                     // Lane = P row = D column; register i is D row 32c + i.
+                    float cv[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int idx = i * 32 + ((((lane >> 2) ^ (i & 7))) << 2) + (lane & 3);
-                        float v = __uint_as_float(r[i]);
-                        if (p.beta) v += buf[idx];
-                        buf[idx] = v;
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        cv[i] = p.beta ? buf[i * 32 + (((lane >> 2) ^ (i & 7)) << 2) + (lane & 3)]
+                                       : 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        buf[i * 32 + (((lane >> 2) ^ (i & 7)) << 2) + (lane & 3)] =
+                            __uint_as_float(cur[i]) + cv[i];
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     tma_store_2d(&mapD, buf, box_x(c), box_y(c));
                     bulk_commit_group();
-                    if (p.beta && c + 2 < live_chunks) {
+                    if (p.beta && c + nbuf < live_chunks) {
                         bulk_wait_group_read<0>();  // the store just issued has read buf
                         mbar_arrive_expect_tx(&cb[bi], kEpiBufFloats * 4);
-                        tma_load_2d(buf, &mapC, &cb[bi], box_x(c + 2), box_y(c + 2));
+                        tma_load_2d(buf, &mapC, &cb[bi], box_x(c + nbuf), box_y(c + nbuf));
                     }
                 }
-                if (p.beta && c + 2 < live_chunks) cpend |= 1u << bi;
+                if (p.beta && c + nbuf < live_chunks) cpend |= 1u << bi;
                 __syncwarp();
+                return true;
+            };
+            uint32_t ra[32], rb[32];
+            if (live_chunks > 0) tmem_ld_32x32b_x32(tmem + lane_base + acc_col, ra);
+            for (int c = 0; c < live_chunks && ok; c += 2) {
+                ok = chunk(c, ra, rb);
+                if (ok && c + 1 < live_chunks) ok = chunk(c + 1, rb, ra);
             }
             // Accumulator buffer b may be overwritten by the next tile's MMAs.
             tc_fence_before_sync();
@@ -345,7 +374,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive(&s.acc_empty[b]);
             if (!ok) break;
         }
-        if (lane == 0) bulk_wait_group<0>();
+        // Staging tiles must be read by their stores before shared memory is
+        // released; the stores' global writes complete with the grid.
+        if (lane == 0) bulk_wait_group_read<0>();
     }
 
     // --------------------------------------------------------------- teardown
@@ -358,9 +389,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (issued_any & (1u << i))
                     wait_phase(&s.full[i], (issued_parity >> i) & 1u, s.abort, tmo, true);
         if (warp >= 2)
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < p.epi_bufs; ++i)
                 if (cpend & (1u << i))
-                    wait_phase(&s.cbar[2 * (warp - 2) + i], (cphase >> i) & 1u, s.abort, tmo, true);
+                    wait_phase(&s.cbar[kTcMaxEpiBufs * (warp - 2) + i], (cphase >> i) & 1u, s.abort,
+                               tmo, true);
         __syncthreads();
     }
     if (warp == 1) {
@@ -372,21 +404,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace
 
-size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes) {
+size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs) {
     return 1024 + size_t(stages) * (p_bytes + q_bytes) +
-           size_t(kEpiWarps) * 2 * kEpiBufFloats * sizeof(float) +
-           sizeof(uint64_t) * (2 * size_t(stages) + 4 + 2 * kEpiWarps + 1) + 16;
+           size_t(kEpiWarps) * epi_bufs * kEpiBufFloats * sizeof(float) +
+           sizeof(uint64_t) * (2 * size_t(stages) + 4 + kTcMaxEpiBufs * kEpiWarps + 1) + 16;
 }
 
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
-    const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes);
+    if (p.epi_bufs < 2 || p.epi_bufs > kTcMaxEpiBufs || p.stages < 2 || p.stages > 32)
+        return cudaErrorInvalidValue;
+    const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs);
     if (smem > size_t(kTcMaxSmem)) return cudaErrorInvalidConfiguration;
     auto kernel = p.swap ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kTcThreads, smem, stream>>>(maps.P, maps.Q, maps.C, maps.D, p);
-    return cudaGetLastError();
+    // Programmatic dependent launch: this grid's set-up may overlap the tail of
+    // the previous kernel in the stream; the kernel waits (griddepcontrol.wait)
+    // before its first global-memory access.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, p);
 }
 
 cudaError_t tc_read_and_clear_device_status(int* status) {

@@ -155,6 +155,33 @@ uint32_t stage_tile_bytes(int rows, bool mn) {
     return mn ? uint32_t((rows + 63) / 64) * 8192u : uint32_t(rows) * 128u;
 }
 
+// Accumulator width (UMMA N) for the normal orientation: the multiple of 32
+// in [128, 256] that minimises (persistent waves) x (tile width + a fixed
+// per-tile cost), i.e. the least wave-quantisation loss; ties go to the wider
+// tile (fewer re-reads of A).
+int pick_bn(int64_t M, int64_t N, int sms) {
+    // TPGEMM_TC_BN (a multiple of 32 in [32, 256]) forces the width; the
+    // tests use it to cover every width the heuristic can choose.
+    if (const char* f = getenv("TPGEMM_TC_BN")) {
+        const int v = atoi(f);
+        if (v >= 32 && v <= 256 && v % 32 == 0) return v;
+    }
+    if (N <= 64) return int(((N + 15) / 16) * 16);
+    if (N <= 128) return 128;
+    int best = 256;
+    int64_t best_cost = -1;
+    for (int bn = 256; bn >= 128; bn -= 32) {
+        const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+        const int64_t waves = (tiles + sms - 1) / sms;
+        const int64_t cost = waves * (bn + 32);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
 tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB, bool bf16,
                       float beta, int sms, Plan* out) {
     tpg::TcParams p{};
@@ -165,15 +192,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     const int64_t Nq = swap ? M : N;
     const bool p_mn = swap ? !transB : transA;
     const bool q_mn = swap ? transA : !transB;
-    int bn;
-    if (swap) {
-        bn = int(Nq);
-    } else {
-        // 128 x 256 tiles unless that leaves most SMs idle.
-        const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
-        bn = (N <= 128 || tiles256 < sms) ? 128 : 256;
-        if (N <= 64) bn = int(((N + 15) / 16) * 16);
-    }
+    const int bn = swap ? int(Nq) : pick_bn(M, N, sms);
     p.Mp = int(Mp);
     p.Nq = int(Nq);
     p.K = int(K);
@@ -193,17 +212,52 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.timeout_ns = wait_timeout_ns();
     p.swap = swap;
     p.group = 16;
-    int stages = 8;
-    while (stages > 2 && tpg::tc_smem_bytes(stages, p.p_bytes, p.q_bytes) > size_t(tpg::kTcMaxSmem))
-        --stages;
-    if (tpg::tc_smem_bytes(stages, p.p_bytes, p.q_bytes) > size_t(tpg::kTcMaxSmem))
-        return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
+    // Every tile shares the one Q tile when all of Q fits it: spread the CTAs'
+    // starting K blocks so they do not contend for the same lines of it.
+    p.k_rotate = (p.tiles_q == 1 && p.tiles_p > 1) ? 1 : 0;
+    // Shared memory: the deepest TMA ring with two staging tiles per epilogue
+    // warp; with beta = 1, one staging tile per 32-column chunk instead (all of
+    // C prefetched at tile start) when that still leaves a 4-deep ring.
+    auto fits = [&](int st, int eb) {
+        return tpg::tc_smem_bytes(st, p.p_bytes, p.q_bytes, eb) <= size_t(tpg::kTcMaxSmem);
+    };
+    auto deepest = [&](int eb) {
+        int st = 8;
+        while (st > 2 && !fits(st, eb)) --st;
+        return fits(st, eb) ? st : 0;
+    };
+    int epi_bufs = 2;
+    int stages = deepest(2);
+    const int nchunks = (bn + 31) / 32;
+    if (p.beta && nchunks > 2 && nchunks <= tpg::kTcMaxEpiBufs) {
+        const int st = deepest(nchunks);
+        if (st >= 4) {
+            epi_bufs = nchunks;
+            stages = st;
+        }
+    }
+    // Tuning overrides (TPGEMM_TC_STAGES, TPGEMM_TC_EPI_BUFS, TPGEMM_TC_KROTATE),
+    // used to sweep the ring depth, staging and K rotation on real problems.
+    if (const char* f = getenv("TPGEMM_TC_EPI_BUFS")) {
+        const int v = atoi(f);
+        if (v >= 2 && v <= tpg::kTcMaxEpiBufs) {
+            epi_bufs = v;
+            stages = deepest(v);
+        }
+    }
+    if (const char* f = getenv("TPGEMM_TC_STAGES")) {
+        const int v = atoi(f);
+        if (v >= 2 && v <= 8 && fits(v, epi_bufs)) stages = v;
+    }
+    if (const char* f = getenv("TPGEMM_TC_KROTATE")) p.k_rotate = std::max(0, atoi(f));
+    if (stages == 0) return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
+    p.stages = stages;
+    p.epi_bufs = epi_bufs;
     // The epilogue stores 32-column boxes; a tile width that is not a multiple
     // of 32 is only used when it is the only tile along Q (the box overhang is
     // then past the end of the matrix and clipped by the TMA store).
     if (bn % 32 != 0 && p.tiles_q != 1)
         return fail(TPGEMM_ERR_PATH, "internal: tile width %d with %d tiles along Q", bn, p.tiles_q);
-    p.stages = stages;
     out->kernel = Kernel::Tc;
     out->tc = p;
     out->grid = std::min(p.num_tiles, sms);
@@ -391,10 +445,10 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
         const tpg::TcParams& p = plan.tc;
         snprintf(text, sizeof(text),
                  "path=tcgen05 orientation=%s tile=128x%dx64 umma=128x%dx16 stages=%d "
-                 "tiles=%dx%d grid=%d p_major=%s q_major=%s smem=%zu",
-                 plan.swap ? "swapped" : "normal", p.bn, p.bn, p.stages, p.tiles_p, p.tiles_q,
-                 plan.grid, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
-                 tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes));
+                 "epi_bufs=%d k_rotate=%d tiles=%dx%d grid=%d p_major=%s q_major=%s smem=%zu",
+                 plan.swap ? "swapped" : "normal", p.bn, p.bn, p.stages, p.epi_bufs, p.k_rotate,
+                 p.tiles_p, p.tiles_q, plan.grid, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
+                 tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));
     }
     if (buf && buflen > 0) {
         strncpy(buf, text, size_t(buflen) - 1);

@@ -46,13 +46,16 @@ struct TcParams {
     uint32_t tx_bytes;      // bytes the TMA delivers per stage
     uint64_t timeout_ns;    // bound on every mbarrier wait
     int swap;               // orientation, for the epilogue's D coordinates
+    int epi_bufs;           // 32 x 32 f32 staging tiles per epilogue warp (2..8)
+    int k_rotate;           // 0, or tiles per group sharing a rotated first K block
 };
 
 struct TcMaps {
     CUtensorMap P, Q, C, D;
 };
 
-size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes);
+constexpr int kTcMaxEpiBufs = 8;
+size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs);
 constexpr int kTcThreads = 192;
 constexpr int kTcMaxSmem = 232448;  // 227 KB opt-in per block on sm_100-class parts
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream);
