@@ -150,6 +150,21 @@ def test_multi_tile_waves_tc():
     check_full(w, TC)
 
 
+@pytest.mark.parametrize("mc", [1, 2, 4])
+@pytest.mark.parametrize("case", ["normal_kmajor", "normal_mnmajor", "swapped"])
+def test_cluster_sizes(mc, case, monkeypatch):
+    # 1, 2 or 4 CTAs per cluster sharing the Q tile through TMA multicast,
+    # including a P-tile count that is not a multiple of the cluster size.
+    monkeypatch.setenv("TPGEMM_TC_CLUSTER", str(mc))
+    if case == "swapped":
+        w = dataclasses.replace(wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(
+            128, 1416, 520, seed=6270 + mc))
+    else:
+        w = dataclasses.replace(wl.BY_NAME["gemm_8192_bf16_transB_beta1"].with_shape(
+            656, 536, 392, seed=6280 + mc), transB=(case == "normal_kmajor"))
+    check_full(w, TC)
+
+
 @pytest.mark.parametrize("bn", [32, 128, 160, 192, 224, 256])
 @pytest.mark.parametrize("tB", [False, True])
 def test_every_tile_width(bn, tB, monkeypatch):

@@ -89,15 +89,16 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
     }
 }
 
-// Tile t -> (tile along P, tile along Q); groups of `group` P-tiles sweep all
-// Q-tiles so one wave of CTAs shares a few P and Q panels in L2.
-__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tp, int& tq) {
+// Work item T of a cluster -> (group of mc P tiles, Q tile); runs of `group`
+// P groups sweep all Q tiles so one wave of clusters shares a few P and Q
+// panels in L2. The CTA of cluster rank r then owns P tile tps * mc + r.
+__device__ __forceinline__ void tile_coords(int T, const TcParams& p, int& tps, int& tq) {
     const int per_group = p.group * p.tiles_q;
-    const int g = t / per_group;
+    const int g = T / per_group;
     const int first = g * p.group;
-    const int gsz = min(p.tiles_p - first, p.group);
-    const int r = t - g * per_group;
-    tp = first + r % gsz;
+    const int gsz = min(p.tiles_ps - first, p.group);
+    const int r = T - g * per_group;
+    tps = first + r % gsz;
     tq = r / gsz;
 }
 
@@ -108,7 +109,7 @@ __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tp, i
 __device__ __forceinline__ int first_k_block(int t, const TcParams& p) {
     if (!p.k_rotate) return 0;
     const int g = t / p.k_rotate;
-    const int groups = (p.num_tiles + p.k_rotate - 1) / p.k_rotate;
+    const int groups = (p.num_super + p.k_rotate - 1) / p.k_rotate;
     return int((int64_t(g) * p.k_blocks) / groups) % p.k_blocks;
 }
 
@@ -121,6 +122,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const Smem s = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Cluster of p.mc CTAs sharing each Q tile: rank within it, which cluster,
+    // and how many clusters the persistent grid has.
+    const int rank = p.mc > 1 ? int(cluster_ctarank()) : 0;
+    const int cid = blockIdx.x / p.mc;
+    const int ncl = gridDim.x / p.mc;
+    const uint16_t mc_mask = uint16_t((1u << p.mc) - 1u);
 
     // ---------------------------------------------------------------- set-up
     if (warp == 0 && lane == 0) {
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&mapD);
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], 1);
+            mbar_init(&s.empty[i], p.mc);  // freed by the MMA thread of every CTA sharing it
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.acc_full[i], 1);
@@ -146,7 +153,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_relinquish_alloc_permit();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    // With a cluster, no CTA may multicast into a peer before the peer's
+    // barriers exist: the set-up sync spans the cluster.
+    if (p.mc > 1)
+        cluster_sync();
+    else
+        __syncthreads();
     tc_fence_after_sync();
     // Set-up above overlaps the previous grid's tail when launched with a
     // programmatic dependency; global memory is touched only after this wait.
@@ -166,12 +178,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-                int tp, tq;
-                tile_coords(t, p, tp, tq);
-                const int p0 = tp * kBM;
+            for (int T = cid; T < p.num_super && ok; T += ncl) {
+                int tps, tq;
+                tile_coords(T, p, tps, tq);
+                const int p0 = (tps * p.mc + rank) * kBM;
                 const int q0 = tq * p.bn;
-                int kb = first_k_block(t, p);
+                int kb = first_k_block(T, p);
                 for (int i = 0; i < p.k_blocks; ++i, kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
                     if (!wait_phase(&s.empty[stage], phase ^ 1u, s.abort, tmo)) {
                         ok = false;
@@ -187,11 +199,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     } else {
                         tma_load_2d(sp, &mapP, &s.full[stage], k0, p0);
                     }
-                    if (p.q_mn) {
-                        for (uint32_t a = 0; a < p.q_boxes; ++a)
-                            tma_load_2d(sq + a * kAtomBytes, &mapQ, &s.full[stage], q0 + 64 * a, k0);
+                    if (p.mc == 1) {
+                        if (p.q_mn) {
+                            for (uint32_t a = 0; a < p.q_boxes; ++a)
+                                tma_load_2d(sq + a * kAtomBytes, &mapQ, &s.full[stage], q0 + 64 * a,
+                                            k0);
+                        } else {
+                            tma_load_2d(sq, &mapQ, &s.full[stage], k0, q0);
+                        }
+                    } else if (p.q_mn) {
+                        // This CTA's share of the Q tile's 64-row atoms, to every CTA.
+                        const uint32_t per = p.q_boxes / p.mc;
+                        for (uint32_t a = rank * per; a < (rank + 1) * per; ++a)
+                            tma_load_2d_multicast(sq + a * kAtomBytes, &mapQ, &s.full[stage],
+                                                  q0 + 64 * int(a), k0, mc_mask);
                     } else {
-                        tma_load_2d(sq, &mapQ, &s.full[stage], k0, q0);
+                        // This CTA's bn / mc rows of the Q tile, to every CTA.
+                        const int rows = p.bn / p.mc;
+                        tma_load_2d_multicast(sq + size_t(rank) * rows * 128, &mapQ, &s.full[stage],
+                                              k0, q0 + rank * rows, mc_mask);
                     }
                     issued_any |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -219,7 +245,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+            for (int T = cid; T < p.num_super && ok; T += ncl, ++it) {
                 const int b = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_phase(&s.acc_empty[b], acc_phase ^ 1u, s.abort, tmo)) break;
@@ -239,7 +265,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * stepQ);
                         tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (i | kk) != 0);
                     }
-                    tc_commit(&s.empty[stage]);  // stage free once these MMAs finish
+                    // Stage free (in every CTA that multicast into it) once these
+                    // MMAs finish.
+                    if (p.mc > 1)
+                        tc_commit_multicast(&s.empty[stage], mc_mask);
+                    else
+                        tc_commit(&s.empty[stage]);
                     if (++stage == p.stages) {
                         stage = 0;
                         phase ^= 1u;
@@ -265,9 +296,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int lim_p = p.Mp;
         const int lim_q = p.Nq;
         int it = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
-            int tp, tq;
-            tile_coords(t, p, tp, tq);
+        for (int T = cid; T < p.num_super; T += ncl, ++it) {
+            int tps, tq;
+            tile_coords(T, p, tps, tq);
+            const int tp = tps * p.mc + rank;
             const int pw = tp * kBM + quad * 32;  // first P row of this warp's quadrant
             const int q0 = tq * p.bn;
             const bool warp_live = pw < lim_p;
@@ -395,6 +427,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                tmo, true);
         __syncthreads();
     }
+    // No CTA leaves while a peer may still multicast into it or arrive on it.
+    if (p.mc > 1) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
@@ -411,7 +445,8 @@ size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_buf
 }
 
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
-    if (p.epi_bufs < 2 || p.epi_bufs > kTcMaxEpiBufs || p.stages < 2 || p.stages > 32)
+    if (p.epi_bufs < 2 || p.epi_bufs > kTcMaxEpiBufs || p.stages < 2 || p.stages > 32 ||
+        !(p.mc == 1 || p.mc == 2 || p.mc == 4) || grid % p.mc != 0)
         return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs);
     if (smem > size_t(kTcMaxSmem)) return cudaErrorInvalidConfiguration;
@@ -427,12 +462,36 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(p.mc);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.mc > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, p);
+}
+
+cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters) {
+    const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs);
+    auto kernel = p.swap ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.mc));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(p.mc);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, p);
+    return cudaOccupancyMaxActiveClusters(clusters, kernel, &cfg);
 }
 
 cudaError_t tc_read_and_clear_device_status(int* status) {

@@ -250,6 +250,24 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         if (v >= 2 && v <= 8 && fits(v, epi_bufs)) stages = v;
     }
     if (const char* f = getenv("TPGEMM_TC_KROTATE")) p.k_rotate = std::max(0, atoi(f));
+    // Clusters: mc CTAs with consecutive P tiles share the Q tile, each TMA-
+    // loading 1/mc of it with multicast. A share must be whole 8-row swizzle
+    // groups (K-contiguous Q) or whole 64-row atoms (MN-contiguous Q). Used by
+    // default only when every tile shares the one Q tile (small M): there it
+    // halves the L2 reads of that tile; with many Q tiles the lock-step of
+    // the cluster's CTAs costs more than the traffic it saves (measured).
+    auto mc_ok = [&](int mc) {
+        if (mc == 1) return true;
+        if (p.tiles_p < mc) return false;
+        return p.q_mn ? (p.q_boxes % uint32_t(mc) == 0) : ((bn / mc) % 8 == 0 && bn % mc == 0);
+    };
+    p.mc = (p.tiles_q == 1 && mc_ok(2)) ? 2 : 1;
+    if (const char* f = getenv("TPGEMM_TC_CLUSTER")) {
+        const int v = atoi(f);
+        if ((v == 1 || v == 2 || v == 4) && mc_ok(v)) p.mc = v;
+    }
+    p.tiles_ps = (p.tiles_p + p.mc - 1) / p.mc;
+    p.num_super = p.tiles_ps * p.tiles_q;
     if (stages == 0) return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
     p.stages = stages;
     p.epi_bufs = epi_bufs;
@@ -260,8 +278,29 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         return fail(TPGEMM_ERR_PATH, "internal: tile width %d with %d tiles along Q", bn, p.tiles_q);
     out->kernel = Kernel::Tc;
     out->tc = p;
-    out->grid = std::min(p.num_tiles, sms);
+    out->grid = std::min(p.num_super, std::max(1, sms / p.mc)) * p.mc;
     out->swap = swap;
+    return TPGEMM_OK;
+}
+
+// Persistent grid: no more clusters than fit the device at once (clusters are
+// placed within GPCs, so with mc > 1 that can be fewer than SMs / mc).
+tpgemm_status fit_grid(Plan* plan) {
+    tpg::TcParams& p = plan->tc;
+    if (p.mc == 1) return TPGEMM_OK;
+    static std::mutex m;
+    static int cache[3][5] = {};  // [swap][mc]: 0 = unknown
+    std::lock_guard<std::mutex> lock(m);
+    int& n = cache[p.swap ? 1 : 0][p.mc];
+    if (n == 0) {
+        int v = 0;
+        cudaError_t e = tpg::tc_max_active_clusters(p, &v);
+        if (e != cudaSuccess || v <= 0)
+            return fail(TPGEMM_ERR_LAUNCH, "cluster occupancy query failed: %s",
+                        cudaGetErrorString(e));
+        n = v;
+    }
+    plan->grid = std::min(p.num_super, n) * p.mc;
     return TPGEMM_OK;
 }
 
@@ -353,7 +392,9 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     const void* qq = plan.swap ? A : B;
     s = encode_operand(enc, &maps.P, pp, bf16, p.Mp, K, p.p_mn, 128, "P operand");
     if (s != TPGEMM_OK) return s;
-    s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.bn, "Q operand");
+    s = fit_grid(&plan);
+    if (s != TPGEMM_OK) return s;
+    s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.bn / p.mc, "Q operand");
     if (s != TPGEMM_OK) return s;
     s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M), 32,
                   32, "D");
@@ -445,9 +486,10 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
         const tpg::TcParams& p = plan.tc;
         snprintf(text, sizeof(text),
                  "path=tcgen05 orientation=%s tile=128x%dx64 umma=128x%dx16 stages=%d "
-                 "epi_bufs=%d k_rotate=%d tiles=%dx%d grid=%d p_major=%s q_major=%s smem=%zu",
+                 "epi_bufs=%d k_rotate=%d cluster=%d tiles=%dx%d grid=%d p_major=%s q_major=%s "
+                 "smem=%zu",
                  plan.swap ? "swapped" : "normal", p.bn, p.bn, p.stages, p.epi_bufs, p.k_rotate,
-                 p.tiles_p, p.tiles_q, plan.grid, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
+                 p.mc, p.tiles_p, p.tiles_q, plan.grid, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
                  tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));
     }
     if (buf && buflen > 0) {

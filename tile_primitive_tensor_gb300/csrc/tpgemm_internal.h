@@ -48,6 +48,10 @@ struct TcParams {
     int swap;               // orientation, for the epilogue's D coordinates
     int epi_bufs;           // 32 x 32 f32 staging tiles per epilogue warp (2..8)
     int k_rotate;           // 0, or tiles per group sharing a rotated first K block
+    int mc;                 // CTAs per cluster sharing one Q tile (1, 2 or 4): each
+                            // loads 1/mc of it and multicasts it to the others
+    int tiles_ps;           // groups of mc consecutive P tiles: ceil(tiles_p / mc)
+    int num_super;          // tiles_ps * tiles_q: work items of one cluster
 };
 
 struct TcMaps {
@@ -59,6 +63,10 @@ size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_buf
 constexpr int kTcThreads = 192;
 constexpr int kTcMaxSmem = 232448;  // 227 KB opt-in per block on sm_100-class parts
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream);
+
+// Clusters of p.mc CTAs of this kernel that fit the device at once (the
+// persistent grid is this many clusters at most).
+cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters);
 
 // Device status word written by the tcgen05 kernel's bounded waits.
 cudaError_t tc_read_and_clear_device_status(int* status);
