@@ -165,6 +165,32 @@ def test_cluster_sizes(mc, case, monkeypatch):
     check_full(w, TC)
 
 
+@pytest.mark.parametrize("case", ["normal_kmajor", "normal_mnmajor", "normal_odd_tiles",
+                                  "swapped", "swapped_transA"])
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_cta_pair_mma(case, dtype, monkeypatch):
+    # CTA-pair MMA (cta_group::2, M = 256 per pair): each CTA loads its own 128
+    # P rows and half of the Q tile; the pair's leader issues the MMA.
+    monkeypatch.setenv("TPGEMM_TC_PAIR", "1")
+    monkeypatch.setenv("TPGEMM_TC_BN", "128")
+    base = wl.BY_NAME["gemm_8192_bf16_transB_beta1"]
+    if case == "normal_kmajor":
+        w = base.with_shape(512, 384, 328, seed=6300)
+    elif case == "normal_mnmajor":
+        w = dataclasses.replace(base.with_shape(512, 384, 328, seed=6301), transB=False)
+    elif case == "normal_odd_tiles":
+        w = dataclasses.replace(base.with_shape(656, 264, 200, seed=6302), transA=True)
+    elif case == "swapped":
+        w = base.with_shape(128, 1000, 264, seed=6303)
+    else:
+        w = dataclasses.replace(base.with_shape(128, 1000, 264, seed=6304), transA=True,
+                                transB=False)
+    w = dataclasses.replace(w, dtype=dtype)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert "pair=1" in text, text
+    check_full(w, TC)
+
+
 @pytest.mark.parametrize("bn", [32, 128, 160, 192, 224, 256])
 @pytest.mark.parametrize("tB", [False, True])
 def test_every_tile_width(bn, tB, monkeypatch):

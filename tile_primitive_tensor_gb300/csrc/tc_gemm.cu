@@ -32,8 +32,6 @@ namespace {
 constexpr int kBM = 128;           // P rows per tile (tensor-memory lanes)
 constexpr int kBK = 64;            // K elements per stage: one 128-byte swizzle row
 constexpr int kUmmaK = 16;         // K per tcgen05.mma (kind::f16)
-constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
-constexpr int kAccStride = 256;    // column offset of accumulator buffer 1
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBufFloats = 32 * 32;  // one 32 x 32 f32 staging tile (4 KB)
 constexpr int kAtomBytes = 8192;   // MN-major atom: 64 K rows x 128 bytes
@@ -113,7 +111,7 @@ __device__ __forceinline__ int first_k_block(int t, const TcParams& p) {
     return int((int64_t(g) * p.k_blocks) / groups) % p.k_blocks;
 }
 
-template <bool SWAP>
+template <bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
@@ -128,6 +126,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int cid = blockIdx.x / p.mc;
     const int ncl = gridDim.x / p.mc;
     const uint16_t mc_mask = uint16_t((1u << p.mc) - 1u);
+    constexpr int CG = PAIR ? 2 : 1;
+    // Accumulator buffer b starts at column b * acc_stride.
+    const int acc_stride = p.tmem_cols / 2;
 
     // ---------------------------------------------------------------- set-up
     if (warp == 0 && lane == 0) {
@@ -137,11 +138,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&mapD);
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], p.mc);  // freed by the MMA thread of every CTA sharing it
+            // Freed by the MMA thread of every CTA sharing the stage (one
+            // multicast commit from the pair's leader in pair mode).
+            mbar_init(&s.empty[i], PAIR ? 1 : p.mc);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.acc_full[i], 1);
-            mbar_init(&s.acc_empty[i], kEpiWarps);
+            // Pair mode: the leader's accumulator barrier collects the
+            // epilogue warps of both CTAs.
+            mbar_init(&s.acc_empty[i], PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
         for (int i = 0; i < kTcMaxEpiBufs * kEpiWarps; ++i) mbar_init(&s.cbar[i], 1);
         mbar_init(s.drain, 1);
@@ -149,8 +154,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_mbarrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(s.tmem_base, kTmemCols);
-        tmem_relinquish_alloc_permit();
+        tmem_alloc<CG>(s.tmem_base, uint32_t(p.tmem_cols));
+        tmem_relinquish_alloc_permit<CG>();
     }
     tc_fence_before_sync();
     // With a cluster, no CTA may multicast into a peer before the peer's
@@ -191,8 +196,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     uint8_t* sp = s.stages + size_t(stage) * (p.p_bytes + p.q_bytes);
                     uint8_t* sq = sp + p.p_bytes;
-                    mbar_arrive_expect_tx(&s.full[stage], p.tx_bytes);
                     const int k0 = kb * kBK;
+                    if (PAIR) {
+                        // Both CTAs' fills complete on the leader's full barrier;
+                        // the leader expects the bytes of both.
+                        const uint32_t fb = mapa_shared(smem_u32(&s.full[stage]), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * p.tx_bytes);
+                        if (p.p_mn) {
+                            tma_load_2d_pair(sp, &mapP, fb, p0, k0);
+                            tma_load_2d_pair(sp + kAtomBytes, &mapP, fb, p0 + 64, k0);
+                        } else {
+                            tma_load_2d_pair(sp, &mapP, fb, k0, p0);
+                        }
+                        const int qh = q0 + rank * (p.bn / 2);  // this CTA's half of the Q tile
+                        if (p.q_mn) {
+                            for (uint32_t a = 0; a < p.q_boxes; ++a)
+                                tma_load_2d_pair(sq + a * kAtomBytes, &mapQ, fb, qh + 64 * int(a), k0);
+                        } else {
+                            tma_load_2d_pair(sq, &mapQ, fb, k0, qh);
+                        }
+                        issued_any |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        if (++stage == p.stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(&s.full[stage], p.tx_bytes);
                     if (p.p_mn) {
                         tma_load_2d(sp, &mapP, &s.full[stage], p0, k0);
                         tma_load_2d(sp + kAtomBytes, &mapP, &s.full[stage], p0 + 64, k0);
@@ -230,7 +261,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // (in pair mode only the leader CTA issues, for both CTAs)
+        if (lane == 0 && (!PAIR || rank == 0)) {
             // Descriptor templates, encoded once; each issue patches the start address.
             const uint64_t dP = p.p_mn ? smem_desc_sw128_template(kAtomBytes, 1024)
                                        : smem_desc_sw128_template(16, 1024);
@@ -250,7 +282,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_phase(&s.acc_empty[b], acc_phase ^ 1u, s.abort, tmo)) break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem + uint32_t(b * kAccStride);
+                const uint32_t d_tmem = tmem + uint32_t(b * acc_stride);
                 for (int i = 0; i < p.k_blocks; ++i) {
                     if (!wait_phase(&s.full[stage], phase, s.abort, tmo)) {
                         ok = false;
@@ -263,11 +295,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                         const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * stepP);
                         const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * stepQ);
-                        tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (i | kk) != 0);
+                        if (PAIR)
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, p.idesc, (i | kk) != 0);
+                        else
+                            tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (i | kk) != 0);
                     }
-                    // Stage free (in every CTA that multicast into it) once these
-                    // MMAs finish.
-                    if (p.mc > 1)
+                    // Stage free (in every CTA that filled or multicast into it)
+                    // once these MMAs finish.
+                    if (PAIR)
+                        tc_commit_pair_multicast(&s.empty[stage], mc_mask);
+                    else if (p.mc > 1)
                         tc_commit_multicast(&s.empty[stage], mc_mask);
                     else
                         tc_commit(&s.empty[stage]);
@@ -277,10 +314,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 if (!ok) break;
-                tc_commit(&s.acc_full[b]);  // accumulator ready for the epilogue
+                // Accumulator ready for the epilogue (of both CTAs in pair mode).
+                if (PAIR)
+                    tc_commit_pair_multicast(&s.acc_full[b], mc_mask);
+                else
+                    tc_commit(&s.acc_full[b]);
             }
             // Drain: every MMA this thread issued has completed before teardown.
-            tc_commit(s.drain);
+            if (PAIR)
+                tc_commit_pair(s.drain);
+            else
+                tc_commit(s.drain);
             wait_phase(s.drain, 0, s.abort, tmo, true);
         }
     } else {
@@ -329,7 +373,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after_sync();
-            const uint32_t acc_col = uint32_t(b * kAccStride);
+            const uint32_t acc_col = uint32_t(b * acc_stride);
             // One 32-column chunk: its accumulator registers `cur` were loaded
             // by the previous step; the next chunk's tcgen05.ld is issued into
             // `nxt` before this one's shared-memory work so the two overlap.
@@ -400,10 +444,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = chunk(c, ra, rb);
                 if (ok && c + 1 < live_chunks) ok = chunk(c + 1, rb, ra);
             }
-            // Accumulator buffer b may be overwritten by the next tile's MMAs.
+            // Accumulator buffer b may be overwritten by the next tile's MMAs
+            // (issued by the pair's leader in pair mode).
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s.acc_empty[b]);
+            if (lane == 0) {
+                if (PAIR)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&s.acc_empty[b]), 0));
+                else
+                    mbar_arrive(&s.acc_empty[b]);
+            }
             if (!ok) break;
         }
         // Staging tiles must be read by their stores before shared memory is
@@ -416,7 +466,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     if (*s.abort) {
         // An aborted CTA lets every TMA fill it issued land before it exits.
-        if (warp == 0 && lane == 0)
+        // (In pair mode both CTAs' fills complete on the leader's barriers,
+        // so the leader drains for both before the final cluster sync.)
+        if (warp == 0 && lane == 0 && (!PAIR || rank == 0))
             for (int i = 0; i < p.stages; ++i)
                 if (issued_any & (1u << i))
                     wait_phase(&s.full[i], (issued_parity >> i) & 1u, s.abort, tmo, true);
@@ -432,11 +484,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc<CG>(tmem, uint32_t(p.tmem_cols));
     }
 }
 
 }  // namespace
+
+using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
+
+TcKernelFn pick_kernel(const TcParams& p) {
+    if (p.pair) return p.swap ? tc_gemm_kernel<true, true> : tc_gemm_kernel<false, true>;
+    return p.swap ? tc_gemm_kernel<true, false> : tc_gemm_kernel<false, false>;
+}
 
 size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs) {
     return 1024 + size_t(stages) * (p_bytes + q_bytes) +
@@ -446,11 +505,13 @@ size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_buf
 
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
     if (p.epi_bufs < 2 || p.epi_bufs > kTcMaxEpiBufs || p.stages < 2 || p.stages > 32 ||
-        !(p.mc == 1 || p.mc == 2 || p.mc == 4) || grid % p.mc != 0)
+        !(p.mc == 1 || p.mc == 2 || p.mc == 4) || grid % p.mc != 0 || (p.pair && p.mc != 2) ||
+        !(p.tmem_cols == 64 || p.tmem_cols == 128 || p.tmem_cols == 256 || p.tmem_cols == 512) ||
+        p.tmem_cols / 2 < 32 * ((p.bn + 31) / 32))
         return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs);
     if (smem > size_t(kTcMaxSmem)) return cudaErrorInvalidConfiguration;
-    auto kernel = p.swap ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    auto kernel = pick_kernel(p);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
@@ -476,7 +537,7 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
 
 cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters) {
     const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs);
-    auto kernel = p.swap ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    auto kernel = pick_kernel(p);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;

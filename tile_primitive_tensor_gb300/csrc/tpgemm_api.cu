@@ -204,10 +204,23 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.p_mn = p_mn;
     p.q_mn = q_mn;
     p.beta = beta == 1.0f;
-    p.idesc = tpg::idesc_f16_f32(bf16, p_mn, q_mn, 128, bn);
+    // Tensor memory: two accumulators, each a power-of-two >= 32 columns wide
+    // enough for the tile's 32-column epilogue chunks.
+    int acc_cols = 32;
+    while (acc_cols < 32 * ((bn + 31) / 32)) acc_cols *= 2;
+    p.tmem_cols = 2 * acc_cols;
+    // CTA-pair MMA: a pair of CTAs computes a 256 x bn tile with cta_group::2;
+    // each loads its own 128 P rows and half of the Q tile. The half must be
+    // whole 8-row swizzle groups (K-contiguous) or 64-row atoms (MN-contiguous).
+    const bool pair_ok = p.tiles_p >= 2 && (q_mn ? (bn % 128 == 0) : (bn % 16 == 0)) &&
+                         p.tmem_cols <= 256;
+    p.pair = 0;
+    if (const char* f = getenv("TPGEMM_TC_PAIR")) p.pair = (atoi(f) != 0 && pair_ok) ? 1 : 0;
+    const int q_rows = p.pair ? bn / 2 : bn;  // Q rows this CTA loads per stage
+    p.idesc = tpg::idesc_f16_f32(bf16, p_mn, q_mn, p.pair ? 256 : 128, bn);
     p.p_bytes = stage_tile_bytes(128, p_mn);
-    p.q_bytes = stage_tile_bytes(bn, q_mn);
-    p.q_boxes = q_mn ? uint32_t((bn + 63) / 64) : 1u;
+    p.q_bytes = stage_tile_bytes(q_rows, q_mn);
+    p.q_boxes = q_mn ? uint32_t((q_rows + 63) / 64) : 1u;
     p.tx_bytes = p.p_bytes + p.q_bytes;
     p.timeout_ns = wait_timeout_ns();
     p.swap = swap;
@@ -266,6 +279,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         const int v = atoi(f);
         if ((v == 1 || v == 2 || v == 4) && mc_ok(v)) p.mc = v;
     }
+    if (p.pair) p.mc = 2;  // the pair is a cluster of two
     p.tiles_ps = (p.tiles_p + p.mc - 1) / p.mc;
     p.num_super = p.tiles_ps * p.tiles_q;
     if (stages == 0) return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
@@ -289,9 +303,9 @@ tpgemm_status fit_grid(Plan* plan) {
     tpg::TcParams& p = plan->tc;
     if (p.mc == 1) return TPGEMM_OK;
     static std::mutex m;
-    static int cache[3][5] = {};  // [swap][mc]: 0 = unknown
+    static int cache[2][2][5] = {};  // [swap][pair][mc]: 0 = unknown
     std::lock_guard<std::mutex> lock(m);
-    int& n = cache[p.swap ? 1 : 0][p.mc];
+    int& n = cache[p.swap ? 1 : 0][p.pair ? 1 : 0][p.mc];
     if (n == 0) {
         int v = 0;
         cudaError_t e = tpg::tc_max_active_clusters(p, &v);
@@ -394,7 +408,8 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     if (s != TPGEMM_OK) return s;
     s = fit_grid(&plan);
     if (s != TPGEMM_OK) return s;
-    s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.bn / p.mc, "Q operand");
+    s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.pair ? p.bn / 2 : p.bn / p.mc,
+                       "Q operand");
     if (s != TPGEMM_OK) return s;
     s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M), 32,
                   32, "D");
@@ -485,11 +500,12 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     } else {
         const tpg::TcParams& p = plan.tc;
         snprintf(text, sizeof(text),
-                 "path=tcgen05 orientation=%s tile=128x%dx64 umma=128x%dx16 stages=%d "
-                 "epi_bufs=%d k_rotate=%d cluster=%d tiles=%dx%d grid=%d p_major=%s q_major=%s "
-                 "smem=%zu",
-                 plan.swap ? "swapped" : "normal", p.bn, p.bn, p.stages, p.epi_bufs, p.k_rotate,
-                 p.mc, p.tiles_p, p.tiles_q, plan.grid, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
+                 "path=tcgen05 orientation=%s tile=128x%dx64 umma=%dx%dx16 stages=%d "
+                 "epi_bufs=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d grid=%d "
+                 "p_major=%s q_major=%s smem=%zu",
+                 plan.swap ? "swapped" : "normal", p.bn, p.pair ? 256 : 128, p.bn, p.stages,
+                 p.epi_bufs, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid, p.p_mn ? "mn" : "k",
+                 p.q_mn ? "mn" : "k",
                  tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));
     }
     if (buf && buflen > 0) {

@@ -52,6 +52,9 @@ struct TcParams {
                             // loads 1/mc of it and multicasts it to the others
     int tiles_ps;           // groups of mc consecutive P tiles: ceil(tiles_p / mc)
     int num_super;          // tiles_ps * tiles_q: work items of one cluster
+    int pair;               // 1: CTA-pair MMA (cta_group::2, M = 256 per pair, mc = 2);
+                            // each CTA loads its 128 P rows and half of the Q tile
+    int tmem_cols;          // tensor-memory columns allocated (two accumulators)
 };
 
 struct TcMaps {
