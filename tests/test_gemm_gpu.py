@@ -134,6 +134,17 @@ def test_transpose_combos(path, dtype, tA, tB):
     check_full(w, path)
 
 
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+@pytest.mark.parametrize("tA,tB", list(itertools.product([False, True], repeat=2)))
+def test_transpose_combos_single_cta(dtype, tA, tB, monkeypatch):
+    # The one-CTA-per-tile tcgen05 path (the default uses CTA pairs here).
+    monkeypatch.setenv("TPGEMM_TC_PAIR", "0")
+    base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
+    w = base.with_shape(272, 392, 200, seed=6050 + 2 * tA + tB)
+    w = dataclasses.replace(w, dtype=dtype, transA=tA, transB=tB)
+    check_full(w, TC)
+
+
 @pytest.mark.parametrize("tA,tB", list(itertools.product([False, True], repeat=2)))
 def test_transpose_combos_swapped_orientation(tA, tB):
     # Small M with wide N runs the tcgen05 kernel in its swapped orientation.
@@ -156,6 +167,7 @@ def test_cluster_sizes(mc, case, monkeypatch):
     # 1, 2 or 4 CTAs per cluster sharing the Q tile through TMA multicast,
     # including a P-tile count that is not a multiple of the cluster size.
     monkeypatch.setenv("TPGEMM_TC_CLUSTER", str(mc))
+    monkeypatch.setenv("TPGEMM_TC_PAIR", "0")
     if case == "swapped":
         w = dataclasses.replace(wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(
             128, 1416, 520, seed=6270 + mc))
@@ -191,11 +203,36 @@ def test_cta_pair_mma(case, dtype, monkeypatch):
     check_full(w, TC)
 
 
+@pytest.mark.parametrize("bn,tB", [(256, True), (256, False), (224, False), (224, True),
+                                   (160, False)])
+def test_cta_pair_full_width(bn, tB, monkeypatch):
+    # Pair tiles up to 256 x 256 (two 256-column accumulators per CTA), with
+    # MN-contiguous Q halves that are not whole 64-row atoms (224, 160).
+    monkeypatch.setenv("TPGEMM_TC_PAIR", "1")
+    monkeypatch.setenv("TPGEMM_TC_BN", str(bn))
+    base = wl.BY_NAME["gemm_8192_bf16_transB_beta1"]
+    w = dataclasses.replace(base.with_shape(768, 1056, 456, seed=6310 + bn), transB=tB)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert "pair=1" in text, text
+    check_full(w, TC)
+
+
+def test_cta_pair_skinny_m144(monkeypatch):
+    monkeypatch.setenv("TPGEMM_TC_PAIR", "1")
+    w = wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(144, 2072, 520, seed=6320)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert "pair=1" in text, text
+    check_full(w, TC)
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("bn", [32, 128, 160, 192, 224, 256])
 @pytest.mark.parametrize("tB", [False, True])
-def test_every_tile_width(bn, tB, monkeypatch):
-    # Each accumulator width the planner may choose, with B K- or MN-contiguous.
+def test_every_tile_width(bn, tB, pair, monkeypatch):
+    # Each accumulator width the planner may choose, with B K- or MN-contiguous,
+    # on one CTA per tile and on CTA pairs.
     monkeypatch.setenv("TPGEMM_TC_BN", str(bn))
+    monkeypatch.setenv("TPGEMM_TC_PAIR", pair)
     base = wl.BY_NAME["gemm_4096_f16"]
     w = dataclasses.replace(base.with_shape(400, 1000, 264, seed=6250 + bn), transB=tB,
                             beta=1.0, c_dist=("normal", 0.0, 1.0))

@@ -155,11 +155,13 @@ uint32_t stage_tile_bytes(int rows, bool mn) {
     return mn ? uint32_t((rows + 63) / 64) * 8192u : uint32_t(rows) * 128u;
 }
 
-// Accumulator width (UMMA N) for the normal orientation: the multiple of 32
-// in [128, 256] that minimises (persistent waves) x (tile width + a fixed
-// per-tile cost), i.e. the least wave-quantisation loss; ties go to the wider
-// tile (fewer re-reads of A).
-int pick_bn(int64_t M, int64_t N, int sms) {
+// Accumulator width (UMMA N) for the normal orientation. With the CTA-pair
+// MMA, the widest tile (256, or N rounded up to 32 when narrower) measured
+// best at 4096^3 and 8192^3. A single CTA takes the multiple of 32 in
+// [128, 256] that minimises (persistent waves) x (tile width + a fixed
+// per-tile cost), i.e. the least wave-quantisation loss; ties go to the
+// wider tile (fewer re-reads of A).
+int pick_bn(int64_t M, int64_t N, int sms, bool pair) {
     // TPGEMM_TC_BN (a multiple of 32 in [32, 256]) forces the width; the
     // tests use it to cover every width the heuristic can choose.
     if (const char* f = getenv("TPGEMM_TC_BN")) {
@@ -168,6 +170,7 @@ int pick_bn(int64_t M, int64_t N, int sms) {
     }
     if (N <= 64) return int(((N + 15) / 16) * 16);
     if (N <= 128) return 128;
+    if (pair) return N >= 256 ? 256 : int(((N + 31) / 32) * 32);
     int best = 256;
     int64_t best_cost = -1;
     for (int bn = 256; bn >= 128; bn -= 32) {
@@ -192,7 +195,9 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     const int64_t Nq = swap ? M : N;
     const bool p_mn = swap ? !transB : transA;
     const bool q_mn = swap ? transA : !transB;
-    const int bn = swap ? int(Nq) : pick_bn(M, N, sms);
+    // The CTA-pair MMA needs at least two 128-row P tiles.
+    const bool pair_wanted = Mp > 128;
+    const int bn = swap ? int(Nq) : pick_bn(M, N, sms, pair_wanted);
     p.Mp = int(Mp);
     p.Nq = int(Nq);
     p.K = int(K);
@@ -210,11 +215,14 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     while (acc_cols < 32 * ((bn + 31) / 32)) acc_cols *= 2;
     p.tmem_cols = 2 * acc_cols;
     // CTA-pair MMA: a pair of CTAs computes a 256 x bn tile with cta_group::2;
-    // each loads its own 128 P rows and half of the Q tile. The half must be
-    // whole 8-row swizzle groups (K-contiguous) or 64-row atoms (MN-contiguous).
-    const bool pair_ok = p.tiles_p >= 2 && (q_mn ? (bn % 128 == 0) : (bn % 16 == 0)) &&
-                         p.tmem_cols <= 256;
-    p.pair = 0;
+    // each loads its own 128 P rows and half of the Q tile (the MMA splits N
+    // between the pair at bn / 2). A K-contiguous half must be whole 8-row
+    // swizzle groups; an MN-contiguous half starts on a 16-row boundary and is
+    // loaded as whole 64-row atoms (rows past the half are not read).
+    const bool pair_ok = p.tiles_p >= 2 && (q_mn ? (bn % 32 == 0) : (bn % 16 == 0));
+    // On by default where it applies (measured: 8192^3 1449 -> 1563 TFLOP/s,
+    // 4096^3 1105 -> 1383, skinny 36.1 -> 33.5 us); TPGEMM_TC_PAIR=0 turns it off.
+    p.pair = pair_ok ? 1 : 0;
     if (const char* f = getenv("TPGEMM_TC_PAIR")) p.pair = (atoi(f) != 0 && pair_ok) ? 1 : 0;
     const int q_rows = p.pair ? bn / 2 : bn;  // Q rows this CTA loads per stage
     p.idesc = tpg::idesc_f16_f32(bf16, p_mn, q_mn, p.pair ? 256 : 128, bn);
