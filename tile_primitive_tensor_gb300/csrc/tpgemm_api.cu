@@ -232,7 +232,10 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.tx_bytes = p.p_bytes + p.q_bytes;
     p.timeout_ns = wait_timeout_ns();
     p.swap = swap;
-    p.group = 16;
+    // Raster: runs of 8 P groups sweep all Q tiles (measured best at 8192^3:
+    // fewer panel re-reads from HBM than 16 or 32, less power, higher clock).
+    p.group = 8;
+    if (const char* f = getenv("TPGEMM_TC_GROUP")) p.group = std::max(1, atoi(f));
     // Every tile shares the one Q tile when all of Q fits it: spread the CTAs'
     // starting K blocks so they do not contend for the same lines of it.
     p.k_rotate = (p.tiles_q == 1 && p.tiles_p > 1) ? 1 : 0;
