@@ -276,7 +276,9 @@ def run_ours(args, rank, world, local_rank):
     value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
     clocks = sampler.summary(t_wall0, t_wall1)
 
-    # ---- end to end through host buffers: H2D of inputs + call + D2H of D
+    # ---- end to end through the host-buffer entry point: every step copies A,
+    # B (and C) in from page-locked host memory and D back out, pipelined by
+    # the library against the multiply of each row block.
     pin = lambda t: t.pin_memory()  # noqa: E731
     Ah, Bh = pin(A), pin(B)
     Ch = None if C is None else pin(C)
@@ -284,14 +286,17 @@ def run_ours(args, rank, world, local_rank):
     h2d = A.numel() * A.element_size() + B.numel() * B.element_size() + \
         (0 if C is None else C.numel() * 4)
     d2h = w.M * w.N * 4
+    del Ad, Bd, Cd, D
+    torch.cuda.empty_cache()
+    ws_bytes = lib.tpgemm_gemm_host_workspace_bytes(w.M, w.N, w.K, w.dtype, float(w.beta))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    hp = (Dh.data_ptr(), Ah.data_ptr(), Bh.data_ptr(), None if Ch is None else Ch.data_ptr())
 
     def e2e_step():
-        Ad.copy_(Ah, non_blocking=True)
-        Bd.copy_(Bh, non_blocking=True)
-        if Ch is not None:
-            Cd.copy_(Ch, non_blocking=True)
-        step()
-        Dh.copy_(D, non_blocking=True)
+        st = lib.tpgemm_gemm_host(*hp, w.M, w.N, w.K, int(w.transA), int(w.transB), w.dtype,
+                                  float(w.beta), ws.data_ptr(), ws_bytes, sh)
+        if st != 0:
+            raise RuntimeError(f"tpgemm_gemm_host: {st} {tp.tpgemm_last_error_detail()}")
 
     for _ in range(3):
         e2e_step()

@@ -21,8 +21,9 @@
  *   B: [K,N] elements, or [N,K] when transB != 0.
  *   C: [M,N] float32 (read only when beta == 1; may be NULL when beta == 0).
  *   D: [M,N] float32 (written).
- * All four are device pointers owned by the caller. The library allocates no
- * device memory per call and keeps no pointer after the call is enqueued.
+ * For tpgemm_gemm all four are device pointers owned by the caller (for
+ * tpgemm_gemm_host they are host pointers). The library allocates no device
+ * memory and keeps no pointer after a call is enqueued.
  *
  * Errors: every function returns a status. Argument errors are detected on the
  * host before anything is enqueued, and a readable reason is available from
@@ -31,6 +32,7 @@
 #ifndef TPGEMM_H
 #define TPGEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -89,6 +91,39 @@ tpgemm_status tpgemm_gemm(float* D, const void* A, const void* B, const float* C
 tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const float* C, int64_t M,
                                int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
                                float beta, void* stream, tpgemm_path path);
+
+/* Bytes of device workspace tpgemm_gemm_host needs for this problem: room for
+ * A, B, D and (beta == 1) C, each 256-byte aligned. Returns 0 for a shape,
+ * dtype or beta that tpgemm_gemm would reject. */
+size_t tpgemm_gemm_host_workspace_bytes(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype,
+                                        float beta);
+
+/*
+ * D = A·B + beta·C with A, B, C and D in HOST memory (layouts as for
+ * tpgemm_gemm). Page-locked host memory lets the copies run asynchronously and
+ * overlap; pageable memory works but serialises them.
+ *
+ * The call enqueues, ordered after the work already on `stream`: the copy of B
+ * to the device, then for each row block of M the copy-in of its A rows (and C
+ * rows), the multiply of that block by the tcgen05 / mma.sync kernels, and the
+ * copy-out of its D rows. Copies run on two library-owned helper streams so
+ * that block i+1's copy-in and block i-1's copy-out overlap block i's multiply;
+ * `stream` is ordered after the last copy-out, so synchronising `stream` (or
+ * an event recorded on it afterwards) makes D_host valid. The host buffers
+ * must stay valid and unmodified until then.
+ *
+ * workspace: device memory owned by the caller, at least
+ * tpgemm_gemm_host_workspace_bytes(M, N, K, dtype, beta) bytes, 256-byte
+ * aligned; its contents on entry do not matter. The library allocates nothing.
+ *
+ * Returns TPGEMM_OK once everything is enqueued; argument errors
+ * (TPGEMM_ERR_SHAPE / _DTYPE / _BETA / _NULL / _ALIGN) before anything is
+ * enqueued; TPGEMM_ERR_LAUNCH if CUDA refused a copy or a launch.
+ */
+tpgemm_status tpgemm_gemm_host(float* D_host, const void* A_host, const void* B_host,
+                               const float* C_host, int64_t M, int64_t N, int64_t K, int transA,
+                               int transB, tpgemm_dtype dtype, float beta, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /* Static English name of a status. Never NULL. */
 const char* tpgemm_status_string(tpgemm_status s);

@@ -145,3 +145,27 @@ def test_binding_fails_loudly_without_library(tmp_path):
             "try:\n    t.tpgemm_version()\nexcept RuntimeError as e:\n    print('RAISED', e)\n")
     r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
     assert "RAISED" in r.stdout and "not built" in r.stdout
+
+
+def test_host_path_workspace_and_rejections(lib):
+    # A (2MK) + B (2KN) + C (4MN, beta = 1) + D (4MN), each 256-byte aligned.
+    n = tp.tpgemm_gemm_host_workspace_bytes(64, 64, 64, tp.TPGEMM_F16, 1.0)
+    assert n == 8192 + 8192 + 16384 + 16384
+    assert tp.tpgemm_gemm_host_workspace_bytes(64, 64, 64, tp.TPGEMM_F16, 0.0) == 8192 + 8192 + 16384
+    assert tp.tpgemm_gemm_host_workspace_bytes(64, 12, 64, tp.TPGEMM_F16, 1.0) == 0
+    assert tp.tpgemm_gemm_host_workspace_bytes(64, 64, 64, 5, 1.0) == 0
+    H = 0x10000
+    args = dict(M=64, N=64, K=64, transA=0, transB=0, dtype=tp.TPGEMM_F16, beta=1.0)
+
+    def host(D=H, A=H, B=H, C=H, ws=BASE, wsb=n, **kw):
+        a = {**args, **kw}
+        return tp.tpgemm_gemm_host(D, A, B, C, a["M"], a["N"], a["K"], a["transA"], a["transB"],
+                                   a["dtype"], a["beta"], ws, wsb, 0)
+    assert host(M=8) == tp.TPGEMM_ERR_SHAPE
+    assert host(beta=0.5) == tp.TPGEMM_ERR_BETA
+    assert host(dtype=9) == tp.TPGEMM_ERR_DTYPE
+    assert host(A=None) == tp.TPGEMM_ERR_NULL
+    assert host(C=None) == tp.TPGEMM_ERR_NULL
+    assert host(ws=None) == tp.TPGEMM_ERR_NULL
+    assert host(ws=BASE + 64) == tp.TPGEMM_ERR_ALIGN
+    assert host(wsb=n - 1) == tp.TPGEMM_ERR_NULL and "needed" in tp.tpgemm_last_error_detail()

@@ -345,3 +345,28 @@ def test_workload_full_size(name):
         bound = Sd * (2.0 ** -10) + 1e-6
         err = (D.double() - ref).abs()
         assert bool((err <= bound).all()), f"{name}: max err/bound {float((err / bound).max())}"
+
+
+# ------------------------------------------------------ host-buffer entry point
+@pytest.mark.parametrize("M,N,K,tA,tB,beta", [
+    (16, 8, 16, False, False, 0.0),       # one block, mma.sync
+    (528, 392, 200, True, False, 1.0),    # 4 blocks of 144 (last 96), A column blocks
+    (2320, 1000, 264, False, True, 1.0),  # 8 blocks of 512 (last 272), tcgen05 per block
+    (4096, 520, 136, True, True, 0.0),
+])
+def test_gemm_host_buffers(M, N, K, tA, tB, beta):
+    base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
+    w = dataclasses.replace(base.with_shape(M, N, K, seed=6400 + M), transA=tA, transB=tB,
+                            beta=beta, c_dist=("normal", 0.0, 1.0) if beta else None)
+    A, B, C = wl.make_inputs(w)
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    Ch = None if C is None else C.pin_memory()
+    Dh = torch.full((M, N), float("nan")).pin_memory()
+    nbytes = tp.tpgemm_gemm_host_workspace_bytes(M, N, K, w.dtype, beta)
+    ws = torch.full((nbytes // 4,), float("nan"), device="cuda")
+    st = tp.tpgemm_gemm_host(Dh, Ah, Bh, Ch, M, N, K, tA, tB, w.dtype, beta, ws, nbytes, None)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.current_stream().synchronize()
+    Dref, S = oracle_full(w, A, B, C)
+    ok, msg = oracle.compare(Dh.numpy(), Dref, S)
+    assert ok, msg

@@ -68,6 +68,11 @@ def _load():
         lib.tpgemm_gemm.restype = ci
         lib.tpgemm_gemm_path.argtypes = gemm_args + [ci]
         lib.tpgemm_gemm_path.restype = ci
+        lib.tpgemm_gemm_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, cf, vp,
+                                         ctypes.c_size_t, vp]
+        lib.tpgemm_gemm_host.restype = ci
+        lib.tpgemm_gemm_host_workspace_bytes.argtypes = [i64, i64, i64, ci, cf]
+        lib.tpgemm_gemm_host_workspace_bytes.restype = ctypes.c_size_t
         lib.tpgemm_status_string.argtypes = [ci]
         lib.tpgemm_status_string.restype = ctypes.c_char_p
         lib.tpgemm_last_error_detail.argtypes = []
@@ -127,6 +132,20 @@ def tpgemm_gemm_path(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream=No
     return int(_load().tpgemm_gemm_path(_ptr(D), _ptr(A), _ptr(B), _ptr(C), int(M), int(N),
                                         int(K), int(bool(transA)), int(bool(transB)), int(dtype),
                                         float(beta), _stream(stream), int(path)))
+
+
+def tpgemm_gemm_host_workspace_bytes(M, N, K, dtype, beta) -> int:
+    return int(_load().tpgemm_gemm_host_workspace_bytes(int(M), int(N), int(K), int(dtype),
+                                                        float(beta)))
+
+
+def tpgemm_gemm_host(D_host, A_host, B_host, C_host, M, N, K, transA, transB, dtype, beta,
+                     workspace, workspace_bytes, stream=None) -> int:
+    """Enqueue D = A.B + beta.C on host buffers (copies pipelined with the multiply)."""
+    return int(_load().tpgemm_gemm_host(_ptr(D_host), _ptr(A_host), _ptr(B_host), _ptr(C_host),
+                                        int(M), int(N), int(K), int(bool(transA)),
+                                        int(bool(transB)), int(dtype), float(beta),
+                                        _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def tpgemm_status_string(status: int) -> str:

@@ -436,9 +436,171 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     return TPGEMM_OK;
 }
 
+// ------------------------------------------------------ host-buffer path
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct HostWsLayout {
+    size_t a, b, c, d, total;  // byte offsets in the workspace, and its size
+};
+
+HostWsLayout host_ws_layout(int64_t M, int64_t N, int64_t K, bool beta) {
+    HostWsLayout L;
+    size_t off = 0;
+    L.a = off;
+    off = align_up(off + size_t(M) * size_t(K) * 2, kWsAlign);
+    L.b = off;
+    off = align_up(off + size_t(K) * size_t(N) * 2, kWsAlign);
+    L.c = off;
+    if (beta) off = align_up(off + size_t(M) * size_t(N) * 4, kWsAlign);
+    L.d = off;
+    off = align_up(off + size_t(M) * size_t(N) * 4, kWsAlign);
+    L.total = off;
+    return L;
+}
+
+// Per-device helper streams and events of the host-buffer path (created once).
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    static constexpr int kEvents = 40;
+    cudaEvent_t ev[kEvents] = {};
+};
+HostPipe g_pipes[kMaxDevices];
+std::mutex g_pipe_mutex;
+
+tpgemm_status host_pipe(int dev, HostPipe** out) {
+    HostPipe& hp = g_pipes[dev];
+    if (!hp.ready) {
+        if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess)
+            return fail(TPGEMM_ERR_LAUNCH, "cannot create the copy streams");
+        for (int i = 0; i < HostPipe::kEvents; ++i)
+            if (cudaEventCreateWithFlags(&hp.ev[i], cudaEventDisableTiming) != cudaSuccess)
+                return fail(TPGEMM_ERR_LAUNCH, "cannot create the copy events");
+        hp.ready = true;
+    }
+    *out = &hp;
+    return TPGEMM_OK;
+}
+
+tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* Ch, int64_t M,
+                       int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
+                       float beta, void* ws, size_t ws_bytes, void* stream) {
+    g_detail.clear();
+    tpgemm_status s = check_shape(M, N, K, dtype, beta);
+    if (s != TPGEMM_OK) return s;
+    if (!Dh || !Ah || !Bh || (beta == 1.0f && !Ch))
+        return fail(TPGEMM_ERR_NULL, "a host operand is NULL");
+    if (!ws) return fail(TPGEMM_ERR_NULL, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) % kWsAlign)
+        return fail(TPGEMM_ERR_ALIGN, "workspace is not 256-byte aligned");
+    const bool use_c = beta == 1.0f;
+    const HostWsLayout L = host_ws_layout(M, N, K, use_c);
+    if (ws_bytes < L.total)
+        return fail(TPGEMM_ERR_NULL, "workspace of %zu bytes; %zu needed", ws_bytes, L.total);
+    DeviceInfo dev;
+    s = device_info(&dev);
+    if (s != TPGEMM_OK) return s;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    uint8_t* dA = w + L.a;
+    uint8_t* dB = w + L.b;
+    float* dC = reinterpret_cast<float*>(w + L.c);
+    float* dD = reinterpret_cast<float*>(w + L.d);
+    const uint8_t* hA = static_cast<const uint8_t*>(Ah);
+    const uint8_t* hB = static_cast<const uint8_t*>(Bh);
+
+    // Row blocks of M, multiples of 16 (of 256 when large), at most 8 of them.
+    int64_t blk = M;
+    if (M >= 2048) blk = ((M / 8 + 255) / 256) * 256;
+    else if (M >= 512) blk = ((M / 4 + 15) / 16) * 16;
+    const int nblk = int((M + blk - 1) / blk);
+
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe* hp = nullptr;
+    s = host_pipe(dev_id, &hp);
+    if (s != TPGEMM_OK) return s;
+    if (2 * nblk + 2 > HostPipe::kEvents) return fail(TPGEMM_ERR_LAUNCH, "too many row blocks");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaEvent_t start = hp->ev[0], done = hp->ev[1];
+    auto ev_in = [&](int i) { return hp->ev[2 + 2 * i]; };
+    auto ev_mm = [&](int i) { return hp->ev[3 + 2 * i]; };
+    auto ck = [&](cudaError_t e, const char* what) -> tpgemm_status {
+        if (e != cudaSuccess)
+            return fail(TPGEMM_ERR_LAUNCH, "%s: %s", what, cudaGetErrorString(e));
+        return TPGEMM_OK;
+    };
+#define TPG_CK(expr, what)                 \
+    do {                                   \
+        tpgemm_status r_ = ck((expr), what); \
+        if (r_ != TPGEMM_OK) return r_;    \
+    } while (0)
+    TPG_CK(cudaEventRecord(start, st), "event");
+    TPG_CK(cudaStreamWaitEvent(hp->in, start, 0), "stream wait");
+    TPG_CK(cudaStreamWaitEvent(hp->out, start, 0), "stream wait");
+    TPG_CK(cudaMemcpyAsync(dB, hB, size_t(K) * size_t(N) * 2, cudaMemcpyHostToDevice, hp->in),
+           "copy of B");
+    // A block i: rows [m0, m1) of the logical A, packed densely in the
+    // workspace (for transA a column block of the stored [K, M] matrix).
+    size_t a_off = 0;
+    for (int i = 0; i < nblk; ++i) {
+        const int64_t m0 = int64_t(i) * blk;
+        const int64_t mb = std::min(blk, M - m0);
+        uint8_t* dAi = dA + a_off;
+        if (!transA) {
+            TPG_CK(cudaMemcpyAsync(dAi, hA + size_t(m0) * size_t(K) * 2, size_t(mb) * size_t(K) * 2,
+                                   cudaMemcpyHostToDevice, hp->in),
+                   "copy of A");
+        } else {
+            TPG_CK(cudaMemcpy2DAsync(dAi, size_t(mb) * 2, hA + size_t(m0) * 2, size_t(M) * 2,
+                                     size_t(mb) * 2, size_t(K), cudaMemcpyHostToDevice, hp->in),
+                   "copy of A");
+        }
+        if (use_c)
+            TPG_CK(cudaMemcpyAsync(dC + size_t(m0) * size_t(N), Ch + size_t(m0) * size_t(N),
+                                   size_t(mb) * size_t(N) * 4, cudaMemcpyHostToDevice, hp->in),
+                   "copy of C");
+        TPG_CK(cudaEventRecord(ev_in(i), hp->in), "event");
+        TPG_CK(cudaStreamWaitEvent(st, ev_in(i), 0), "stream wait");
+        s = run(dD + size_t(m0) * size_t(N), dAi, dB, use_c ? dC + size_t(m0) * size_t(N) : nullptr,
+                mb, N, K, transA, transB, dtype, beta, st, TPGEMM_PATH_AUTO);
+        if (s != TPGEMM_OK) return s;
+        TPG_CK(cudaEventRecord(ev_mm(i), st), "event");
+        TPG_CK(cudaStreamWaitEvent(hp->out, ev_mm(i), 0), "stream wait");
+        TPG_CK(cudaMemcpyAsync(Dh + size_t(m0) * size_t(N), dD + size_t(m0) * size_t(N),
+                               size_t(mb) * size_t(N) * 4, cudaMemcpyDeviceToHost, hp->out),
+               "copy of D");
+        a_off += size_t(mb) * size_t(K) * 2;
+    }
+    TPG_CK(cudaEventRecord(done, hp->out), "event");
+    TPG_CK(cudaStreamWaitEvent(st, done, 0), "stream wait");
+#undef TPG_CK
+    return TPGEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t tpgemm_gemm_host_workspace_bytes(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype,
+                                        float beta) {
+    const std::string keep = g_detail;
+    const bool ok = check_shape(M, N, K, dtype, beta) == TPGEMM_OK;
+    g_detail = keep;
+    if (!ok) return 0;
+    return host_ws_layout(M, N, K, beta == 1.0f).total;
+}
+
+tpgemm_status tpgemm_gemm_host(float* D_host, const void* A_host, const void* B_host,
+                               const float* C_host, int64_t M, int64_t N, int64_t K, int transA,
+                               int transB, tpgemm_dtype dtype, float beta, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    return run_host(D_host, A_host, B_host, C_host, M, N, K, transA, transB, dtype, beta,
+                    workspace, workspace_bytes, stream);
+}
 
 tpgemm_status tpgemm_gemm(float* D, const void* A, const void* B, const float* C, int64_t M,
                           int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
