@@ -217,6 +217,20 @@ def test_cta_pair_full_width(bn, tB, monkeypatch):
     check_full(w, TC)
 
 
+@pytest.mark.parametrize("M,N,pair", [(2048, 2560, "1"), (2320, 2600, "1"), (2320, 2328, "0")])
+@pytest.mark.parametrize("tB", [False, True])
+def test_tail_wave_split(M, N, pair, tB, monkeypatch):
+    # More work items than clusters, so the last wave's tiles are split along
+    # N into 2 or 4 narrower units (the plan text shows "units=full+rem x split").
+    monkeypatch.setenv("TPGEMM_TC_PAIR", pair)
+    monkeypatch.setenv("TPGEMM_TC_BN", "256")
+    base = wl.BY_NAME["gemm_8192_bf16_transB_beta1"]
+    w = dataclasses.replace(base.with_shape(M, N, 136, seed=6330 + M), transB=tB)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert "x1 " not in text.split("units=")[1][:12], text
+    check_full(w, TC)
+
+
 def test_cta_pair_skinny_m144(monkeypatch):
     monkeypatch.setenv("TPGEMM_TC_PAIR", "1")
     w = wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(144, 2072, 520, seed=6320)

@@ -111,6 +111,18 @@ __device__ __forceinline__ int first_k_block(int t, const TcParams& p) {
     return int((int64_t(g) * p.k_blocks) / groups) % p.k_blocks;
 }
 
+// Work unit U -> work item T, offset of its Q columns inside the tile, width.
+struct Unit {
+    int T, q_off, width;
+};
+
+__device__ __forceinline__ Unit unit_of(int U, const TcParams& p) {
+    if (U < p.full_units) return {U, 0, p.bn};
+    const int r = U - p.full_units;
+    const int w = p.bn / p.tail_split;
+    return {p.full_units + r / p.tail_split, (r % p.tail_split) * w, w};
+}
+
 template <bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
@@ -183,12 +195,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int T = cid; T < p.num_super && ok; T += ncl) {
+            for (int U = cid; U < p.num_units && ok; U += ncl) {
+                const Unit u = unit_of(U, p);
                 int tps, tq;
-                tile_coords(T, p, tps, tq);
+                tile_coords(u.T, p, tps, tq);
                 const int p0 = (tps * p.mc + rank) * kBM;
-                const int q0 = tq * p.bn;
-                int kb = first_k_block(T, p);
+                const int q0 = tq * p.bn + u.q_off;
+                // Q rows this CTA loads per stage, and the bytes they fill.
+                const int q_rows = PAIR ? u.width / 2 : u.width;
+                const int q_atoms = (q_rows + 63) / 64;
+                const uint32_t tx = p.p_bytes + (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
+                                                        : uint32_t(q_rows) * 128u);
+                int kb = first_k_block(u.T, p);
                 for (int i = 0; i < p.k_blocks; ++i, kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
                     if (!wait_phase(&s.empty[stage], phase ^ 1u, s.abort, tmo)) {
                         ok = false;
@@ -201,19 +219,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // Both CTAs' fills complete on the leader's full barrier;
                         // the leader expects the bytes of both.
                         const uint32_t fb = mapa_shared(smem_u32(&s.full[stage]), 0);
-                        if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * p.tx_bytes);
+                        if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * tx);
                         if (p.p_mn) {
                             tma_load_2d_pair(sp, &mapP, fb, p0, k0);
                             tma_load_2d_pair(sp + kAtomBytes, &mapP, fb, p0 + 64, k0);
                         } else {
                             tma_load_2d_pair(sp, &mapP, fb, k0, p0);
                         }
-                        const int qh = q0 + rank * (p.bn / 2);  // this CTA's half of the Q tile
+                        const int qh = q0 + rank * q_rows;  // this CTA's half of the unit's Q
                         if (p.q_mn) {
-                            for (uint32_t a = 0; a < p.q_boxes; ++a)
-                                tma_load_2d_pair(sq + a * kAtomBytes, &mapQ, fb, qh + 64 * int(a), k0);
+                            for (int a = 0; a < q_atoms; ++a)
+                                tma_load_2d_pair(sq + a * kAtomBytes, &mapQ, fb, qh + 64 * a, k0);
                         } else {
-                            tma_load_2d_pair(sq, &mapQ, fb, k0, qh);
+                            for (int r = 0; r < q_rows; r += p.q_box_rows)
+                                tma_load_2d_pair(sq + size_t(r) * 128, &mapQ, fb, k0, qh + r);
                         }
                         issued_any |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -223,7 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         continue;
                     }
-                    mbar_arrive_expect_tx(&s.full[stage], p.tx_bytes);
+                    mbar_arrive_expect_tx(&s.full[stage], tx);
                     if (p.p_mn) {
                         tma_load_2d(sp, &mapP, &s.full[stage], p0, k0);
                         tma_load_2d(sp + kAtomBytes, &mapP, &s.full[stage], p0 + 64, k0);
@@ -232,11 +251,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     if (p.mc == 1) {
                         if (p.q_mn) {
-                            for (uint32_t a = 0; a < p.q_boxes; ++a)
+                            for (int a = 0; a < q_atoms; ++a)
                                 tma_load_2d(sq + a * kAtomBytes, &mapQ, &s.full[stage], q0 + 64 * a,
                                             k0);
                         } else {
-                            tma_load_2d(sq, &mapQ, &s.full[stage], k0, q0);
+                            for (int r = 0; r < q_rows; r += p.q_box_rows)
+                                tma_load_2d(sq + size_t(r) * 128, &mapQ, &s.full[stage], k0, q0 + r);
                         }
                     } else if (p.q_mn) {
                         // This CTA's share of the Q tile's 64-row atoms, to every CTA.
@@ -277,7 +297,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int T = cid; T < p.num_super && ok; T += ncl, ++it) {
+            for (int U = cid; U < p.num_units && ok; U += ncl, ++it) {
+                const uint32_t idesc = unit_of(U, p).width == p.bn ? p.idesc : p.idesc_tail;
                 const int b = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_phase(&s.acc_empty[b], acc_phase ^ 1u, s.abort, tmo)) break;
@@ -296,9 +317,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * stepP);
                         const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * stepQ);
                         if (PAIR)
-                            tc_mma_f16_pair(d_tmem, adesc, bdesc, p.idesc, (i | kk) != 0);
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (i | kk) != 0);
                         else
-                            tc_mma_f16(d_tmem, adesc, bdesc, p.idesc, (i | kk) != 0);
+                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, (i | kk) != 0);
                     }
                     // Stage free (in every CTA that filled or multicast into it)
                     // once these MMAs finish.
@@ -335,17 +356,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float* bufs = s.epi + size_t(ew) * nbuf * kEpiBufFloats;
         uint64_t* cb = s.cbar + kTcMaxEpiBufs * ew;
         const uint32_t lane_base = uint32_t(quad * 32) << 16;
-        const int nchunks = (p.bn + 31) / 32;
+
         // Output extents in the kernel's (P, Q) frame, for skipping empty chunks.
         const int lim_p = p.Mp;
         const int lim_q = p.Nq;
         int it = 0;
-        for (int T = cid; T < p.num_super; T += ncl, ++it) {
+        for (int U = cid; U < p.num_units; U += ncl, ++it) {
+            const Unit u = unit_of(U, p);
             int tps, tq;
-            tile_coords(T, p, tps, tq);
+            tile_coords(u.T, p, tps, tq);
             const int tp = tps * p.mc + rank;
             const int pw = tp * kBM + quad * 32;  // first P row of this warp's quadrant
-            const int q0 = tq * p.bn;
+            const int q0 = tq * p.bn + u.q_off;
+            const int nchunks = (u.width + 31) / 32;
             const bool warp_live = pw < lim_p;
             int live_chunks = 0;
             if (warp_live) live_chunks = min(nchunks, (lim_q - q0 + 31) / 32);

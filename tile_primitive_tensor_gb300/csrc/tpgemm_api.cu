@@ -293,6 +293,12 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     if (p.pair) p.mc = 2;  // the pair is a cluster of two
     p.tiles_ps = (p.tiles_p + p.mc - 1) / p.mc;
     p.num_super = p.tiles_ps * p.tiles_q;
+    // Work units before any tail split (set by apply_tail_split once the grid is known).
+    p.full_units = p.num_super;
+    p.tail_split = 1;
+    p.num_units = p.num_super;
+    p.idesc_tail = p.idesc;
+    p.q_box_rows = p.pair ? bn / 2 : bn / p.mc;
     if (stages == 0) return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
     p.stages = stages;
     p.epi_bufs = epi_bufs;
@@ -306,6 +312,37 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     out->grid = std::min(p.num_super, std::max(1, sms / p.mc)) * p.mc;
     out->swap = swap;
     return TPGEMM_OK;
+}
+
+// The last wave of the persistent grid is partial when the work items do not
+// divide evenly among the clusters. Its tiles are then split along Q into 2 or
+// 4 narrower units (as many as still fit one wave), so the wave takes half or
+// a quarter of the time. A unit stays a whole number of 32-column chunks and
+// each CTA's share of it whole 8-row groups (K-contiguous Q) or 16-row steps.
+void apply_tail_split(tpg::TcParams& p, int grid, bool bf16) {
+    const int ncl = std::max(1, grid / p.mc);
+    p.full_units = (p.num_super / ncl) * ncl;
+    const int rem = p.num_super - p.full_units;
+    int split = 1;
+    const bool allowed = !p.swap && (p.pair || p.mc == 1) && rem > 0;
+    if (allowed) {
+        for (int sp = 4; sp >= 2; sp /= 2) {
+            const int w = p.bn / sp;
+            const int share = p.pair ? w / 2 : w;
+            if (p.bn % sp == 0 && w % 32 == 0 && share % 16 == 0 && rem * sp <= ncl) {
+                split = sp;
+                break;
+            }
+        }
+    }
+    if (const char* f = getenv("TPGEMM_TC_TAIL"))
+        if (atoi(f) == 0) split = 1;
+    if (split == 1) p.full_units = p.num_super;
+    p.tail_split = split;
+    p.num_units = p.full_units + (p.num_super - p.full_units) * split;
+    p.idesc_tail = tpg::idesc_f16_f32(bf16, p.p_mn, p.q_mn, p.pair ? 256 : 128, p.bn / split);
+    const int share = (p.pair ? p.bn / 2 : p.bn / p.mc) / split;
+    p.q_box_rows = share;
 }
 
 // Persistent grid: no more clusters than fit the device at once (clusters are
@@ -419,8 +456,8 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     if (s != TPGEMM_OK) return s;
     s = fit_grid(&plan);
     if (s != TPGEMM_OK) return s;
-    s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.pair ? p.bn / 2 : p.bn / p.mc,
-                       "Q operand");
+    apply_tail_split(plan.tc, plan.grid, bf16);
+    s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
     if (s != TPGEMM_OK) return s;
     s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M), 32,
                   32, "D");
@@ -665,6 +702,7 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     s = make_plan(M, N, K, transA != 0, transB != 0, dtype == TPGEMM_BF16, beta, path, sms, &plan);
     if (s != TPGEMM_OK) return s;
     char text[512];
+    if (plan.kernel == Kernel::Tc) apply_tail_split(plan.tc, plan.grid, dtype == TPGEMM_BF16);
     if (plan.kernel == Kernel::MmaSync) {
         snprintf(text, sizeof(text),
                  "path=mma_sync tile=%dx%dx32 grid=%lldx%lld warps=4 k_inst=%s",
@@ -675,9 +713,10 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
         snprintf(text, sizeof(text),
                  "path=tcgen05 orientation=%s tile=128x%dx64 umma=%dx%dx16 stages=%d "
                  "epi_bufs=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d grid=%d "
-                 "p_major=%s q_major=%s smem=%zu",
+                 "units=%d+%dx%d p_major=%s q_major=%s smem=%zu",
                  plan.swap ? "swapped" : "normal", p.bn, p.pair ? 256 : 128, p.bn, p.stages,
-                 p.epi_bufs, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid, p.p_mn ? "mn" : "k",
+                 p.epi_bufs, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
+                 p.full_units, p.num_super - p.full_units, p.tail_split, p.p_mn ? "mn" : "k",
                  p.q_mn ? "mn" : "k",
                  tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));
     }

@@ -55,6 +55,14 @@ struct TcParams {
     int pair;               // 1: CTA-pair MMA (cta_group::2, M = 256 per pair, mc = 2);
                             // each CTA loads its 128 P rows and half of the Q tile
     int tmem_cols;          // tensor-memory columns allocated (two accumulators)
+    // Work units: the first full_units work items are whole tiles; the rest
+    // (the last, partial wave of the persistent grid) are each split along Q
+    // into tail_split narrower units so that wave finishes sooner.
+    int full_units;
+    int tail_split;         // 1, 2 or 4
+    int num_units;          // full_units + (num_super - full_units) * tail_split
+    uint32_t idesc_tail;    // instruction descriptor of a tail unit (N = bn / tail_split)
+    int q_box_rows;         // rows of one K-contiguous Q TMA box (the tail unit's share)
 };
 
 struct TcMaps {
