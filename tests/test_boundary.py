@@ -120,7 +120,7 @@ def test_plans_for_workloads(lib):
     expect = {
         "atom_16x8x16_f16_int": "path=mma_sync",
         "gemm_256_bf16_transB_beta1": "path=mma_sync",
-        "gemm_4096_f16": "path=tcgen05 orientation=normal",
+        "gemm_4096_f16": "path=tcgen05 orientation=swapped",  # B [K,N]: Q = A K-contiguous
         "gemm_8192_bf16_transB_beta1": "path=tcgen05 orientation=normal",
         "skinny_144x16392x4104_f16_beta1": "path=tcgen05 orientation=swapped",
     }

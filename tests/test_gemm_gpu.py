@@ -231,6 +231,35 @@ def test_tail_wave_split(M, N, pair, tB, monkeypatch):
     check_full(w, TC)
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("tA,tB", list(itertools.product([False, True], repeat=2)))
+def test_swapped_orientation_large(tA, tB, pair, monkeypatch):
+    # P = B^T, Q = A for a problem with many tiles along both, D written back
+    # transposed by the epilogue (the orientation used for B stored [K, N]).
+    monkeypatch.setenv("TPGEMM_TC_ORIENT", "swap")
+    monkeypatch.setenv("TPGEMM_TC_PAIR", pair)
+    base = wl.BY_NAME["gemm_4096_f16"]
+    w = dataclasses.replace(base.with_shape(784, 1320, 264, seed=6340 + 2 * tA + tB),
+                            transA=tA, transB=tB, beta=1.0, c_dist=("normal", 0.0, 1.0))
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert "orientation=swapped" in text, text
+    check_full(w, TC)
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_normal_orientation_mn_contiguous_q(pair, monkeypatch):
+    # A [M,K] and B [K,N] default to the swapped orientation; the normal one,
+    # with an MN-contiguous Q operand, stays correct when forced.
+    monkeypatch.setenv("TPGEMM_TC_ORIENT", "normal")
+    monkeypatch.setenv("TPGEMM_TC_PAIR", pair)
+    base = wl.BY_NAME["gemm_4096_f16"]
+    w = dataclasses.replace(base.with_shape(784, 1320, 264, seed=6350), beta=1.0,
+                            c_dist=("normal", 0.0, 1.0))
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert "orientation=normal" in text and "q_major=mn" in text, text
+    check_full(w, TC)
+
+
 def test_cta_pair_skinny_m144(monkeypatch):
     monkeypatch.setenv("TPGEMM_TC_PAIR", "1")
     w = wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(144, 2072, 520, seed=6320)

@@ -127,7 +127,7 @@ template <bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap mapQt, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&mapP);
         prefetch_tensormap(&mapQ);
+        if (p.tail_split > 1) prefetch_tensormap(&mapQt);
         if (p.beta) prefetch_tensormap(&mapC);
         prefetch_tensormap(&mapD);
         for (int i = 0; i < p.stages; ++i) {
@@ -204,6 +205,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // Q rows this CTA loads per stage, and the bytes they fill.
                 const int q_rows = PAIR ? u.width / 2 : u.width;
                 const int q_atoms = (q_rows + 63) / 64;
+                // K-contiguous Q: one box per stage, from the map whose box
+                // height is this unit's share (whole tile or tail unit).
+                const CUtensorMap* mq = u.width == p.bn ? &mapQ : &mapQt;
                 const uint32_t tx = p.p_bytes + (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
                                                         : uint32_t(q_rows) * 128u);
                 int kb = first_k_block(u.T, p);
@@ -231,8 +235,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             for (int a = 0; a < q_atoms; ++a)
                                 tma_load_2d_pair(sq + a * kAtomBytes, &mapQ, fb, qh + 64 * a, k0);
                         } else {
-                            for (int r = 0; r < q_rows; r += p.q_box_rows)
-                                tma_load_2d_pair(sq + size_t(r) * 128, &mapQ, fb, k0, qh + r);
+                            tma_load_2d_pair(sq, mq, fb, k0, qh);
                         }
                         issued_any |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -255,8 +258,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 tma_load_2d(sq + a * kAtomBytes, &mapQ, &s.full[stage], q0 + 64 * a,
                                             k0);
                         } else {
-                            for (int r = 0; r < q_rows; r += p.q_box_rows)
-                                tma_load_2d(sq + size_t(r) * 128, &mapQ, &s.full[stage], k0, q0 + r);
+                            tma_load_2d(sq, mq, &s.full[stage], k0, q0);
                         }
                     } else if (p.q_mn) {
                         // This CTA's share of the Q tile's 64-row atoms, to every CTA.
@@ -513,7 +515,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace
 
-using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
+using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                            TcParams);
 
 TcKernelFn pick_kernel(const TcParams& p) {
     if (p.pair) return p.swap ? tc_gemm_kernel<true, true> : tc_gemm_kernel<false, true>;
@@ -555,7 +558,7 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.mc > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, p);
+    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, maps.Qt, p);
 }
 
 cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters) {

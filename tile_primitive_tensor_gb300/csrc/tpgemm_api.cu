@@ -190,14 +190,25 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     tpg::TcParams p{};
     // Small M: swap operands so N runs along the 128 tensor-memory lanes and
     // all of M fits one accumulator (UMMA N = M <= 256, a multiple of 16).
-    const bool swap = M <= 256 && N > M;
+    // Small M: all of M fits one accumulator (swap_small). Otherwise the
+    // orientation is chosen so that the MMA's B operand (Q) is K-contiguous
+    // when one orientation allows it: with A stored [M,K] and B stored [K,N]
+    // the swapped orientation makes Q = A. Measured on GB300: an MN-contiguous
+    // B operand costs 7-11 %, an MN-contiguous A operand about 2 % (8192^3
+    // with B [K,N]: 726 -> 674 us). TPGEMM_TC_ORIENT=swap|normal overrides.
+    const bool swap_small = M <= 256 && N > M;
+    bool swap = swap_small || (!transA && !transB);
+    if (const char* f = getenv("TPGEMM_TC_ORIENT")) {
+        if (!strcmp(f, "swap")) swap = true;
+        if (!strcmp(f, "normal") && !swap_small) swap = false;
+    }
     const int64_t Mp = swap ? N : M;
     const int64_t Nq = swap ? M : N;
     const bool p_mn = swap ? !transB : transA;
     const bool q_mn = swap ? transA : !transB;
     // The CTA-pair MMA needs at least two 128-row P tiles.
     const bool pair_wanted = Mp > 128;
-    const int bn = swap ? int(Nq) : pick_bn(M, N, sms, pair_wanted);
+    const int bn = swap_small ? int(Nq) : pick_bn(Mp, Nq, sms, pair_wanted);
     p.Mp = int(Mp);
     p.Nq = int(Nq);
     p.K = int(K);
@@ -324,7 +335,7 @@ void apply_tail_split(tpg::TcParams& p, int grid, bool bf16) {
     p.full_units = (p.num_super / ncl) * ncl;
     const int rem = p.num_super - p.full_units;
     int split = 1;
-    const bool allowed = !p.swap && (p.pair || p.mc == 1) && rem > 0;
+    const bool allowed = p.tiles_q > 1 && (p.pair || p.mc == 1) && rem > 0;
     if (allowed) {
         for (int sp = 4; sp >= 2; sp /= 2) {
             const int w = p.bn / sp;
@@ -341,8 +352,7 @@ void apply_tail_split(tpg::TcParams& p, int grid, bool bf16) {
     p.tail_split = split;
     p.num_units = p.full_units + (p.num_super - p.full_units) * split;
     p.idesc_tail = tpg::idesc_f16_f32(bf16, p.p_mn, p.q_mn, p.pair ? 256 : 128, p.bn / split);
-    const int share = (p.pair ? p.bn / 2 : p.bn / p.mc) / split;
-    p.q_box_rows = share;
+    p.q_box_rows = p.pair ? p.bn / 2 : p.bn / p.mc;
 }
 
 // Persistent grid: no more clusters than fit the device at once (clusters are
@@ -459,6 +469,11 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     apply_tail_split(plan.tc, plan.grid, bf16);
     s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
     if (s != TPGEMM_OK) return s;
+    if (p.tail_split > 1) {
+        s = encode_operand(enc, &maps.Qt, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows / p.tail_split,
+                           "Q operand (tail units)");
+        if (s != TPGEMM_OK) return s;
+    }
     s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M), 32,
                   32, "D");
     if (s != TPGEMM_OK) return s;

@@ -62,11 +62,12 @@ struct TcParams {
     int tail_split;         // 1, 2 or 4
     int num_units;          // full_units + (num_super - full_units) * tail_split
     uint32_t idesc_tail;    // instruction descriptor of a tail unit (N = bn / tail_split)
-    int q_box_rows;         // rows of one K-contiguous Q TMA box (the tail unit's share)
+    int q_box_rows;         // rows of one K-contiguous Q TMA box of a whole tile
 };
 
 struct TcMaps {
     CUtensorMap P, Q, C, D;
+    CUtensorMap Qt;         // Q with the (narrower) box of a tail unit
 };
 
 constexpr int kTcMaxEpiBufs = 8;
