@@ -413,3 +413,35 @@ def test_gemm_host_buffers(M, N, K, tA, tB, beta):
     Dref, S = oracle_full(w, A, B, C)
     ok, msg = oracle.compare(Dh.numpy(), Dref, S)
     assert ok, msg
+
+
+# ------------------------------------------------------- failure detection
+@pytest.mark.parametrize("case", ["one_cta", "pair", "swapped_small"])
+def test_bounded_wait_reports_timeout_and_context_survives(case, monkeypatch):
+    # A stage fill that never arrives (no TMA is issued for it) must not hang
+    # the GPU: the kernel's bounded wait expires, the status word is set, every
+    # role stops, in-flight copies and MMAs drain, tensor memory is freed, and
+    # the next call on the same context computes the right answer.
+    if case == "one_cta":
+        monkeypatch.setenv("TPGEMM_TC_PAIR", "0")
+        w = wl.BY_NAME["gemm_8192_bf16_transB_beta1"].with_shape(512, 512, 256, seed=6360)
+    elif case == "pair":
+        w = wl.BY_NAME["gemm_8192_bf16_transB_beta1"].with_shape(512, 512, 256, seed=6361)
+    else:
+        w = wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(144, 1032, 264, seed=6362)
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+    D = torch.zeros(w.M, w.N, device="cuda")
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK
+    monkeypatch.setenv("TPGEMM_WAIT_TIMEOUT_MS", "200")
+    monkeypatch.setenv("TPGEMM_TEST_STALL", "1")
+    st = tp.tpgemm_gemm_path(D, Ad, Bd, Cd, w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta,
+                             None, TC)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_ERR_TIMEOUT
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK  # reading it cleared it
+    monkeypatch.delenv("TPGEMM_TEST_STALL")
+    Dh = run_gpu(w, Ad, Bd, Cd, TC)
+    Dref, S = oracle_full(w, A, B, C)
+    ok, msg = oracle.compare(Dh, Dref, S)
+    assert ok, msg
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK

@@ -219,6 +219,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint8_t* sp = s.stages + size_t(stage) * (p.p_bytes + p.q_bytes);
                     uint8_t* sq = sp + p.p_bytes;
                     const int k0 = kb * kBK;
+                    if (p.test_stall && blockIdx.x == 0 && U == cid && i == 0) {
+                        // Failure-detection test: expect the stage's bytes but
+                        // load nothing, so this stage never fills.
+                        mbar_arrive_expect_tx(&s.full[stage], PAIR ? 2 * tx : tx);
+                        if (++stage == p.stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     if (PAIR) {
                         // Both CTAs' fills complete on the leader's full barrier;
                         // the leader expects the bytes of both.

@@ -138,14 +138,13 @@ struct Plan {
     bool swap = false;
 };
 
+// Bound on every mbarrier wait inside the tcgen05 kernel: 2 s, or
+// TPGEMM_WAIT_TIMEOUT_MS (read at every call, so a test can shorten it).
 uint64_t wait_timeout_ns() {
-    static uint64_t v = [] {
-        const char* s = getenv("TPGEMM_WAIT_TIMEOUT_MS");
-        long long ms = s ? atoll(s) : 0;
-        if (ms <= 0) ms = 2000;
-        return uint64_t(ms) * 1000000ull;
-    }();
-    return v;
+    const char* s = getenv("TPGEMM_WAIT_TIMEOUT_MS");
+    long long ms = s ? atoll(s) : 0;
+    if (ms <= 0) ms = 2000;
+    return uint64_t(ms) * 1000000ull;
 }
 
 // Shared bytes of one stage tile of an operand with `rows` rows along MN and
@@ -242,6 +241,9 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.q_boxes = q_mn ? uint32_t((q_rows + 63) / 64) : 1u;
     p.tx_bytes = p.p_bytes + p.q_bytes;
     p.timeout_ns = wait_timeout_ns();
+    // Test only: TPGEMM_TEST_STALL=1 withholds CTA 0's first stage fill so the
+    // failure-detection path (bounded wait -> status word -> clean exit) runs.
+    if (const char* f = getenv("TPGEMM_TEST_STALL")) p.test_stall = atoi(f) != 0;
     p.swap = swap;
     // Raster: runs of 8 P groups sweep all Q tiles (measured best at 8192^3:
     // fewer panel re-reads from HBM than 16 or 32, less power, higher clock).

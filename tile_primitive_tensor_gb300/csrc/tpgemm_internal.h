@@ -63,6 +63,8 @@ struct TcParams {
     int num_units;          // full_units + (num_super - full_units) * tail_split
     uint32_t idesc_tail;    // instruction descriptor of a tail unit (N = bn / tail_split)
     int q_box_rows;         // rows of one K-contiguous Q TMA box of a whole tile
+    int test_stall;         // test only: CTA 0 never fills its first stage, so the
+                            // bounded waits expire and the kernel reports a timeout
 };
 
 struct TcMaps {
