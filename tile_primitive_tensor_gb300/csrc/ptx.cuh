@@ -119,6 +119,25 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------- cross-CTA publication (global)
+// Flag store with release semantics at GPU scope (orders this thread's prior
+// global writes, including completed bulk-async stores, before the flag).
+__device__ __forceinline__ void st_release_gpu(uint32_t* addr, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Orders generic-proxy accesses to global memory against async-proxy (TMA)
+// accesses of the same memory by this thread.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------- clusters
 // shared::cluster address of the same shared variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t smem_addr, uint32_t rank) {

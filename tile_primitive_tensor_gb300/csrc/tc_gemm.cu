@@ -123,11 +123,66 @@ __device__ __forceinline__ Unit unit_of(int U, const TcParams& p) {
     return {p.full_units + r / p.tail_split, (r % p.tail_split) * w, w};
 }
 
+// One cluster's piece of work: work item T (columns q_off .. q_off + width of
+// its Q tile) over K blocks [kb0, kb1). Whole tiles have owner = 1 and
+// has_next = 0. Stream-K segments: owner = the segment holds K block 0 (it
+// writes D); has_next = a later segment of the same tile exists, in the next
+// cluster, whose partial this segment adds.
+struct Seg {
+    int T, q_off, width, kb0, kb1, owner, has_next;
+};
+
+__device__ __forceinline__ int sk_begin(int c, int ncl, const TcParams& p) {
+    return int((int64_t(p.sk_total) * c) / ncl);
+}
+
+// This cluster's segments in order: its whole work units first (U = cid,
+// cid + ncl, ...), then its contiguous share of the stream-K K blocks.
+struct SegIter {
+    int U, u, ub;
+    __device__ __forceinline__ SegIter(int cid, int ncl, const TcParams& p)
+        : U(cid), u(p.sk ? sk_begin(cid, ncl, p) : 0), ub(p.sk ? sk_begin(cid + 1, ncl, p) : 0) {}
+    __device__ __forceinline__ bool next(int ncl, const TcParams& p, Seg& s) {
+        if (U < p.num_units) {
+            const Unit un = unit_of(U, p);
+            s = {un.T, un.q_off, un.width, 0, p.k_blocks, 1, 0};
+            U += ncl;
+            return true;
+        }
+        if (u < ub) {
+            const int t = u / p.k_blocks;
+            const int k0 = u - t * p.k_blocks;
+            const int k1 = min(p.k_blocks, k0 + (ub - u));
+            s = {p.full_units + t, 0, p.bn, k0, k1, k0 == 0, k1 < p.k_blocks};
+            u += k1 - k0;
+            return true;
+        }
+        return false;
+    }
+};
+
+// Bounded wait for a stream-K slot flag to reach this launch's epoch.
+__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t v, volatile int* abort,
+                                          uint64_t timeout_ns) {
+    if (ld_acquire_gpu(f) == v) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (ld_acquire_gpu(f) == v) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            *abort = 1;
+            atomicExch(&g_tc_status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
 template <bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
-                   const __grid_constant__ CUtensorMap mapQt, const TcParams p) {
+                   const __grid_constant__ CUtensorMap mapQt, const __grid_constant__ CUtensorMap mapW,
+                   const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
@@ -147,6 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&mapP);
         prefetch_tensormap(&mapQ);
         if (p.tail_split > 1) prefetch_tensormap(&mapQt);
+        if (p.sk) prefetch_tensormap(&mapW);
         if (p.beta) prefetch_tensormap(&mapC);
         prefetch_tensormap(&mapD);
         for (int i = 0; i < p.stages; ++i) {
@@ -196,8 +252,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int U = cid; U < p.num_units && ok; U += ncl) {
-                const Unit u = unit_of(U, p);
+            SegIter iter(cid, ncl, p);
+            Seg u;
+            bool first_seg = true;
+            for (; ok && iter.next(ncl, p, u); first_seg = false) {
                 int tps, tq;
                 tile_coords(u.T, p, tps, tq);
                 const int p0 = (tps * p.mc + rank) * kBM;
@@ -210,8 +268,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const CUtensorMap* mq = u.width == p.bn ? &mapQ : &mapQt;
                 const uint32_t tx = p.p_bytes + (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
                                                         : uint32_t(q_rows) * 128u);
-                int kb = first_k_block(u.T, p);
-                for (int i = 0; i < p.k_blocks; ++i, kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
+                const int nk = u.kb1 - u.kb0;
+                int kb = nk == p.k_blocks ? first_k_block(u.T, p) : u.kb0;
+                for (int i = 0; i < nk; ++i, kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
                     if (!wait_phase(&s.empty[stage], phase ^ 1u, s.abort, tmo)) {
                         ok = false;
                         break;
@@ -219,7 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint8_t* sp = s.stages + size_t(stage) * (p.p_bytes + p.q_bytes);
                     uint8_t* sq = sp + p.p_bytes;
                     const int k0 = kb * kBK;
-                    if (p.test_stall && blockIdx.x == 0 && U == cid && i == 0) {
+                    if (p.test_stall && blockIdx.x == 0 && first_seg && i == 0) {
                         // Failure-detection test: expect the stage's bytes but
                         // load nothing, so this stage never fills.
                         mbar_arrive_expect_tx(&s.full[stage], PAIR ? 2 * tx : tx);
@@ -309,14 +368,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int U = cid; U < p.num_units && ok; U += ncl, ++it) {
-                const uint32_t idesc = unit_of(U, p).width == p.bn ? p.idesc : p.idesc_tail;
+            SegIter iter(cid, ncl, p);
+            Seg u;
+            for (; ok && iter.next(ncl, p, u); ++it) {
+                const uint32_t idesc = u.width == p.bn ? p.idesc : p.idesc_tail;
+                const int nk = u.kb1 - u.kb0;
                 const int b = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_phase(&s.acc_empty[b], acc_phase ^ 1u, s.abort, tmo)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem + uint32_t(b * acc_stride);
-                for (int i = 0; i < p.k_blocks; ++i) {
+                for (int i = 0; i < nk; ++i) {
                     if (!wait_phase(&s.full[stage], phase, s.abort, tmo)) {
                         ok = false;
                         break;
@@ -373,8 +435,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int lim_p = p.Mp;
         const int lim_q = p.Nq;
         int it = 0;
-        for (int U = cid; U < p.num_units; U += ncl, ++it) {
-            const Unit u = unit_of(U, p);
+        SegIter iter(cid, ncl, p);
+        Seg u;
+        for (; iter.next(ncl, p, u); ++it) {
             int tps, tq;
             tile_coords(u.T, p, tps, tq);
             const int tp = tps * p.mc + rank;
@@ -384,19 +447,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool warp_live = pw < lim_p;
             int live_chunks = 0;
             if (warp_live) live_chunks = min(nchunks, (lim_q - q0 + 31) / 32);
-            // D coordinates of chunk c's 32 x 32 box: (x = column, y = row).
+            // Where chunk c's 32 x 32 box comes from (C, or the next stream-K
+            // segment's scratch slot) and goes to (D, or this CTA's slot).
+            // D / C boxes: (x = column, y = row) of D; slot boxes: the same
+            // tile layout, rows offset by the slot index.
+            const bool to_slot = !u.owner;
+            const bool from_slot = u.has_next;
+            const bool add_src = from_slot || p.beta;
+            const int src_slot = (cid + 1) * p.mc + rank;
+            const int dst_slot = int(blockIdx.x);
+            const int qw = quad * 32;
             auto box_x = [&](int c) { return SWAP ? pw : q0 + 32 * c; };
             auto box_y = [&](int c) { return SWAP ? q0 + 32 * c : pw; };
+            auto slot_x = [&](int c) { return SWAP ? qw : 32 * c; };
+            auto slot_y = [&](int slot, int c) {
+                return slot * p.sk_slot_rows + (SWAP ? 32 * c : qw);
+            };
+            const CUtensorMap* src_map = from_slot ? &mapW : &mapC;
+            const CUtensorMap* dst_map = to_slot ? &mapW : &mapD;
+            auto src_x = [&](int c) { return from_slot ? slot_x(c) : box_x(c); };
+            auto src_y = [&](int c) { return from_slot ? slot_y(src_slot, c) : box_y(c); };
+            auto dst_x = [&](int c) { return to_slot ? slot_x(c) : box_x(c); };
+            auto dst_y = [&](int c) { return to_slot ? slot_y(dst_slot, c) : box_y(c); };
 
             // All staging buffers free: every earlier store has read its source.
             if (lane == 0) bulk_wait_group_read<0>();
-            // Prefetch C for the first chunks (all of them when they fit the
-            // staging buffers) while the MMAs still run.
-            if (p.beta) {
+            // The next segment's partial must be published before it is read.
+            if (from_slot && live_chunks > 0) {
+                bool fok = true;
+                if (lane == 0) {
+                    fok = wait_flag(&p.sk_flags[src_slot * 4 + quad], p.sk_epoch, s.abort, tmo);
+                    fence_proxy_async_global();
+                }
+                fok = __shfl_sync(0xffffffffu, fok ? 1 : 0, 0) != 0;
+                if (!fok) break;
+            }
+            // Prefetch the source (C or the partial) for the first chunks (all
+            // of them when they fit the staging buffers) while the MMAs run.
+            if (add_src) {
                 for (int c = 0; c < nbuf && c < live_chunks; ++c) {
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&cb[c], kEpiBufFloats * 4);
-                        tma_load_2d(bufs + c * kEpiBufFloats, &mapC, &cb[c], box_x(c), box_y(c));
+                        tma_load_2d(bufs + c * kEpiBufFloats, src_map, &cb[c], src_x(c), src_y(c));
                     }
                     cpend |= 1u << c;
                 }
@@ -418,7 +510,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_ld_wait(cur);
                 if (c + 1 < live_chunks)
                     tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * (c + 1)), nxt);
-                if (p.beta) {
+                if (add_src) {
                     bool cok = wait_phase(&cb[bi], (cphase >> bi) & 1u, s.abort, tmo);
                     cok = __all_sync(0xffffffffu, cok);
                     if (!cok) {
@@ -439,7 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float4 cv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        cv[j] = p.beta ? row[j ^ (lane & 7)] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        cv[j] = add_src ? row[j ^ (lane & 7)] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         row[j ^ (lane & 7)] = make_float4(__uint_as_float(cur[4 * j]) + cv[j].x,
@@ -451,8 +543,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float cv[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        cv[i] = p.beta ? buf[i * 32 + (((lane >> 2) ^ (i & 7)) << 2) + (lane & 3)]
-                                       : 0.f;
+                        cv[i] = add_src ? buf[i * 32 + (((lane >> 2) ^ (i & 7)) << 2) + (lane & 3)]
+                                        : 0.f;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         buf[i * 32 + (((lane >> 2) ^ (i & 7)) << 2) + (lane & 3)] =
@@ -461,15 +553,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&mapD, buf, box_x(c), box_y(c));
+                    tma_store_2d(dst_map, buf, dst_x(c), dst_y(c));
                     bulk_commit_group();
-                    if (p.beta && c + nbuf < live_chunks) {
+                    if (add_src && c + nbuf < live_chunks) {
                         bulk_wait_group_read<0>();  // the store just issued has read buf
                         mbar_arrive_expect_tx(&cb[bi], kEpiBufFloats * 4);
-                        tma_load_2d(buf, &mapC, &cb[bi], box_x(c + nbuf), box_y(c + nbuf));
+                        tma_load_2d(buf, src_map, &cb[bi], src_x(c + nbuf), src_y(c + nbuf));
                     }
                 }
-                if (p.beta && c + nbuf < live_chunks) cpend |= 1u << bi;
+                if (add_src && c + nbuf < live_chunks) cpend |= 1u << bi;
                 __syncwarp();
                 return true;
             };
@@ -488,6 +580,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_cluster(mapa_shared(smem_u32(&s.acc_empty[b]), 0));
                 else
                     mbar_arrive(&s.acc_empty[b]);
+            }
+            // A partial written to this CTA's slot is published once its bulk
+            // stores have completed (not just read their shared source).
+            if (ok && to_slot && lane == 0) {
+                bulk_wait_group<0>();
+                fence_proxy_async_global();
+                st_release_gpu(&p.sk_flags[dst_slot * 4 + quad], p.sk_epoch);
             }
             if (!ok) break;
         }
@@ -526,12 +625,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }  // namespace
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
-                            TcParams);
+                            CUtensorMap, TcParams);
 
 TcKernelFn pick_kernel(const TcParams& p) {
     if (p.pair) return p.swap ? tc_gemm_kernel<true, true> : tc_gemm_kernel<false, true>;
     return p.swap ? tc_gemm_kernel<true, false> : tc_gemm_kernel<false, false>;
 }
+
 
 size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs) {
     return 1024 + size_t(stages) * (p_bytes + q_bytes) +
@@ -568,7 +668,7 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.mc > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, maps.Qt, p);
+    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, maps.Qt, maps.W, p);
 }
 
 cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters) {

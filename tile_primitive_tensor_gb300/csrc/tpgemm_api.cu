@@ -17,6 +17,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 
@@ -134,7 +135,9 @@ enum class Kernel { MmaSync, Tc };
 struct Plan {
     Kernel kernel = Kernel::Tc;
     tpg::TcParams tc{};
-    int grid = 0;
+    int grid = 0;      // persistent grid (CTAs)
+    int max_grid = 0;  // CTAs of every cluster the device holds at once
+    int sms = 0;
     bool swap = false;
 };
 
@@ -323,6 +326,8 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     out->kernel = Kernel::Tc;
     out->tc = p;
     out->grid = std::min(p.num_super, std::max(1, sms / p.mc)) * p.mc;
+    out->max_grid = std::max(1, sms / p.mc) * p.mc;
+    out->sms = sms;
     out->swap = swap;
     return TPGEMM_OK;
 }
@@ -332,8 +337,52 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
 // 4 narrower units (as many as still fit one wave), so the wave takes half or
 // a quarter of the time. A unit stays a whole number of 32-column chunks and
 // each CTA's share of it whole 8-row groups (K-contiguous Q) or 16-row steps.
-void apply_tail_split(tpg::TcParams& p, int grid, bool bf16) {
-    const int ncl = std::max(1, grid / p.mc);
+// Stream-K scratch: one partial-tile slot per CTA (128 x bn fp32, bn rounded
+// up to 32) and four epoch flags per CTA. Sized for the largest plan.
+constexpr int kSkMaxGrid = 256;
+constexpr size_t kSkSlotFloats = size_t(128) * 256;
+constexpr size_t kSkSlotBytes = kSkMaxGrid * kSkSlotFloats * sizeof(float);
+constexpr size_t kSkFlagBytes = kSkMaxGrid * 4 * sizeof(uint32_t);
+constexpr size_t kSkWorkspaceBytes = kSkSlotBytes + kSkFlagBytes;
+
+// Balance the last, partial wave of the persistent grid by splitting the
+// leftover tiles along Q into 2 or 4 narrower units (as many as still fit one
+// wave). A unit stays a whole number of 32-column chunks and each CTA's share
+// of it whole 8-row groups (K-contiguous Q) or 16-row steps.
+// Stream-K (TPGEMM_TC_SK=1) instead divides the leftover work items' K blocks
+// evenly among all clusters when each gets at least 4. It is correct and
+// tested but off by default: measured slower on GB300 for 4096^3 (108 vs 98
+// us), 8192^3 (696 vs 688 us) and the 144 x 16392 x 4104 shape (37.7 vs
+// 34.2 us), whose K loop already streams at ~91 % of the HBM copy rate; the
+// chained partials lengthen the epilogue and a full grid leaves no idle SMs
+// for the next launch's early start.
+// *grid is the persistent grid (at most one cluster per work item); max_grid
+// is every cluster the device holds at once. Stream-K runs on max_grid.
+void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool bf16) {
+    p.sk = 0;
+    p.sk_total = 0;
+    bool sk_on = false;
+    if (const char* f = getenv("TPGEMM_TC_SK")) sk_on = atoi(f) != 0;
+    {
+        const int ncl = std::max(1, max_grid / p.mc);
+        const int full = (p.num_super / ncl) * ncl;
+        const int rem = p.num_super - full;
+        if (sk_on && rem > 0 && (p.pair || p.mc == 1) && max_grid <= kSkMaxGrid &&
+            int64_t(rem) * p.k_blocks >= int64_t(4) * ncl) {
+            *grid = ncl * p.mc;
+            p.full_units = full;
+            p.sk = 1;
+            p.sk_total = rem * p.k_blocks;
+            p.k_rotate = 0;
+            p.tail_split = 1;
+            p.num_units = p.full_units;
+            p.idesc_tail = p.idesc;
+            p.q_box_rows = p.pair ? p.bn / 2 : p.bn / p.mc;
+            p.sk_slot_rows = p.swap ? 32 * ((p.bn + 31) / 32) : 128;
+            return;
+        }
+    }
+    const int ncl = std::max(1, *grid / p.mc);
     p.full_units = (p.num_super / ncl) * ncl;
     const int rem = p.num_super - p.full_units;
     int split = 1;
@@ -357,11 +406,47 @@ void apply_tail_split(tpg::TcParams& p, int grid, bool bf16) {
     p.q_box_rows = p.pair ? p.bn / 2 : p.bn / p.mc;
 }
 
+// Stream-K scratch per (device, stream): allocated on first use, kept until
+// exit, flags zeroed once; launches on one stream are ordered, so each takes
+// the next epoch and never sees an earlier launch's flags as its own.
+struct SkWorkspace {
+    void* base = nullptr;
+    uint32_t epoch = 0;
+};
+std::mutex g_sk_mutex;
+std::map<std::pair<int, cudaStream_t>, SkWorkspace> g_sk;
+
+tpgemm_status stream_k_workspace(cudaStream_t st, float** slots, uint32_t** flags,
+                                 uint32_t* epoch) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(g_sk_mutex);
+    SkWorkspace& w = g_sk[std::make_pair(dev, st)];
+    if (!w.base) {
+        void* b = nullptr;
+        cudaError_t e = cudaMalloc(&b, kSkWorkspaceBytes);
+        if (e != cudaSuccess)
+            return fail(TPGEMM_ERR_LAUNCH, "stream-K scratch allocation: %s", cudaGetErrorString(e));
+        e = cudaMemset(static_cast<uint8_t*>(b) + kSkSlotBytes, 0, kSkFlagBytes);
+        if (e != cudaSuccess)
+            return fail(TPGEMM_ERR_LAUNCH, "stream-K scratch init: %s", cudaGetErrorString(e));
+        w.base = b;
+    }
+    *slots = static_cast<float*>(w.base);
+    *flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(w.base) + kSkSlotBytes);
+    *epoch = ++w.epoch;
+    if (w.epoch == 0) *epoch = ++w.epoch;  // 0 is the flags' initial value
+    return TPGEMM_OK;
+}
+
 // Persistent grid: no more clusters than fit the device at once (clusters are
 // placed within GPCs, so with mc > 1 that can be fewer than SMs / mc).
 tpgemm_status fit_grid(Plan* plan) {
     tpg::TcParams& p = plan->tc;
-    if (p.mc == 1) return TPGEMM_OK;
+    if (p.mc == 1) {
+        plan->max_grid = plan->sms;
+        return TPGEMM_OK;
+    }
     static std::mutex m;
     static int cache[2][2][5] = {};  // [swap][pair][mc]: 0 = unknown
     std::lock_guard<std::mutex> lock(m);
@@ -375,6 +460,7 @@ tpgemm_status fit_grid(Plan* plan) {
         n = v;
     }
     plan->grid = std::min(p.num_super, n) * p.mc;
+    plan->max_grid = n * p.mc;
     return TPGEMM_OK;
 }
 
@@ -468,12 +554,24 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     if (s != TPGEMM_OK) return s;
     s = fit_grid(&plan);
     if (s != TPGEMM_OK) return s;
-    apply_tail_split(plan.tc, plan.grid, bf16);
+    apply_tail_split(plan.tc, &plan.grid, plan.max_grid, bf16);
     s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
     if (s != TPGEMM_OK) return s;
     if (p.tail_split > 1) {
         s = encode_operand(enc, &maps.Qt, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows / p.tail_split,
                            "Q operand (tail units)");
+        if (s != TPGEMM_OK) return s;
+    }
+    if (p.sk) {
+        // Slots laid out like D tiles: [128 rows][bn32 cols] (normal) or
+        // [bn32 rows][128 cols] (swapped), one per CTA, stacked along rows.
+        s = stream_k_workspace(st, &plan.tc.sk_ws, &plan.tc.sk_flags, &plan.tc.sk_epoch);
+        if (s != TPGEMM_OK) return s;
+        const uint64_t bn32 = uint64_t(32 * ((p.bn + 31) / 32));
+        const uint64_t cols = p.swap ? 128 : bn32;
+        const uint64_t rows = uint64_t(plan.grid) * uint64_t(p.sk_slot_rows);
+        s = encode_2d(enc, &maps.W, p.sk_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, 32, 32,
+                      "stream-K scratch");
         if (s != TPGEMM_OK) return s;
     }
     s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M), 32,
@@ -719,7 +817,8 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     s = make_plan(M, N, K, transA != 0, transB != 0, dtype == TPGEMM_BF16, beta, path, sms, &plan);
     if (s != TPGEMM_OK) return s;
     char text[512];
-    if (plan.kernel == Kernel::Tc) apply_tail_split(plan.tc, plan.grid, dtype == TPGEMM_BF16);
+    if (plan.kernel == Kernel::Tc)
+        apply_tail_split(plan.tc, &plan.grid, plan.max_grid, dtype == TPGEMM_BF16);
     if (plan.kernel == Kernel::MmaSync) {
         snprintf(text, sizeof(text),
                  "path=mma_sync tile=%dx%dx32 grid=%lldx%lld warps=4 k_inst=%s",
@@ -730,10 +829,10 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
         snprintf(text, sizeof(text),
                  "path=tcgen05 orientation=%s tile=128x%dx64 umma=%dx%dx16 stages=%d "
                  "epi_bufs=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d grid=%d "
-                 "units=%d+%dx%d p_major=%s q_major=%s smem=%zu",
+                 "units=%d+%dx%d stream_k=%d p_major=%s q_major=%s smem=%zu",
                  plan.swap ? "swapped" : "normal", p.bn, p.pair ? 256 : 128, p.bn, p.stages,
                  p.epi_bufs, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
-                 p.full_units, p.num_super - p.full_units, p.tail_split, p.p_mn ? "mn" : "k",
+                 p.full_units, p.num_super - p.full_units, p.tail_split, p.sk, p.p_mn ? "mn" : "k",
                  p.q_mn ? "mn" : "k",
                  tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));
     }

@@ -65,12 +65,27 @@ struct TcParams {
     int q_box_rows;         // rows of one K-contiguous Q TMA box of a whole tile
     int test_stall;         // test only: CTA 0 never fills its first stage, so the
                             // bounded waits expire and the kernel reports a timeout
+    // Stream-K: work items [full_units, num_super) are not given whole to one
+    // cluster; their K blocks (sk_total of them) are divided evenly among all
+    // clusters. A tile's segment holding its last K blocks adds C and writes a
+    // partial tile to its CTA's scratch slot; each earlier segment adds the
+    // next segment's partial to its accumulator; the segment holding K block 0
+    // writes D. Slots are published with per-quadrant epoch flags.
+    int sk;                 // 0 / 1
+    int sk_total;
+    float* sk_ws;           // partial tiles: slot = blockIdx.x (written through mapW)
+    uint32_t* sk_flags;     // [gridDim.x][4] epoch flags, one per epilogue quadrant
+    uint32_t sk_epoch;      // value of a flag once its slot holds this launch's data
+    int sk_slot_rows;       // rows of one slot in mapW's frame (128, or bn rounded to 32)
 };
 
 struct TcMaps {
     CUtensorMap P, Q, C, D;
     CUtensorMap Qt;         // Q with the (narrower) box of a tail unit
+    CUtensorMap W;          // stream-K scratch slots, laid out like D tiles
 };
+
+
 
 constexpr int kTcMaxEpiBufs = 8;
 size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs);
