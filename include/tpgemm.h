@@ -92,6 +92,39 @@ tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const flo
                                int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
                                float beta, void* stream, tpgemm_path path);
 
+/*
+ * tpgemm_gemm without any device-memory allocation. (The pages have no
+ * counterpart; this is a library convenience.)
+ *
+ * For callers that cannot or must not allocate device memory at the time of
+ * the call: code running under a fixed, pre-reserved device-memory budget
+ * (a long-running service that reserves everything at start-up), code inside
+ * another allocator's out-of-memory or reclaim path, or a process whose device
+ * memory is all held by another framework's pool. Such callers cannot use the
+ * stream-K scratch that the library would otherwise cudaMalloc per stream.
+ *
+ * Same arguments, layouts and results as tpgemm_gemm (within the same
+ * tolerance; the K-summation order differs). The tcgen05 kernel runs in its
+ * stream-K mode whenever the plan has a partial last wave, with its scratch
+ * (partial tiles and flags) in one file-scope static device array of
+ * TPGEMM_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds
+ * until exit. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The first call on a device takes the array's device address
+ * (cudaGetSymbolAddress) and zeroes its flag area, synchronising the device;
+ * make that first call before any stream capture. All calls on a device
+ * share the array and it keeps the last call's contents: calls that overlap
+ * on the GPU (e.g. on two streams at once) race, so serialise them.
+ *
+ * Returns TPGEMM_ERR_SHAPE, with the sizes in tpgemm_last_error_detail(), when
+ * the problem's stream-K scratch would exceed TPGEMM_NOALLOC_SCRATCH_BYTES;
+ * otherwise as tpgemm_gemm.
+ */
+#define TPGEMM_NOALLOC_SCRATCH_BYTES (20u << 20)
+tpgemm_status tpgemm_gemm_noalloc(float* D, const void* A, const void* B, const float* C,
+                                  int64_t M, int64_t N, int64_t K, int transA, int transB,
+                                  tpgemm_dtype dtype, float beta, void* stream);
+
 /* Bytes of device workspace tpgemm_gemm_host needs for this problem: room for
  * A, B, D and (beta == 1) C, each 256-byte aligned. Returns 0 for a shape,
  * dtype or beta that tpgemm_gemm would reject. */

@@ -68,6 +68,8 @@ def _load():
         lib.tpgemm_gemm.restype = ci
         lib.tpgemm_gemm_path.argtypes = gemm_args + [ci]
         lib.tpgemm_gemm_path.restype = ci
+        lib.tpgemm_gemm_noalloc.argtypes = gemm_args
+        lib.tpgemm_gemm_noalloc.restype = ci
         lib.tpgemm_gemm_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, cf, vp,
                                          ctypes.c_size_t, vp]
         lib.tpgemm_gemm_host.restype = ci
@@ -132,6 +134,13 @@ def tpgemm_gemm_path(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream=No
     return int(_load().tpgemm_gemm_path(_ptr(D), _ptr(A), _ptr(B), _ptr(C), int(M), int(N),
                                         int(K), int(bool(transA)), int(bool(transB)), int(dtype),
                                         float(beta), _stream(stream), int(path)))
+
+
+def tpgemm_gemm_noalloc(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream=None) -> int:
+    """tpgemm_gemm that allocates no device memory (static stream-K scratch)."""
+    return int(_load().tpgemm_gemm_noalloc(_ptr(D), _ptr(A), _ptr(B), _ptr(C), int(M), int(N),
+                                           int(K), int(bool(transA)), int(bool(transB)),
+                                           int(dtype), float(beta), _stream(stream)))
 
 
 def tpgemm_gemm_host_workspace_bytes(M, N, K, dtype, beta) -> int:

@@ -20,12 +20,19 @@
 // (语义定义, 二: D = A.B + beta.C, beta in {0,1}). Every mbarrier wait is bounded
 // in time; on expiry the kernel records a status word, stops every role, waits
 // for its own copies and MMAs in flight, frees tensor memory and returns.
+#include <mutex>
+
 #include "ptx.cuh"
 #include "tpgemm_internal.h"
 
 namespace tpg {
 
 __device__ int g_tc_status;  // 0 = ok, kStatusTimeout after an expired wait
+
+// Stream-K scratch of tpgemm_gemm_noalloc: partial-tile slots, then the epoch
+// flags in its last kStaticScratchFlagBytes. Every GPU that loads the library
+// holds it until exit; all calls of that entry point on a device share it.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 namespace {
 
@@ -689,6 +696,31 @@ cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaOccupancyMaxActiveClusters(clusters, kernel, &cfg);
+}
+
+cudaError_t tc_static_scratch(void** ptr) {
+    // Host code names g_static_scratch only through its device address, taken
+    // once per device with that device current; the flags start at zero.
+    static std::mutex m;
+    static void* addr[kMaxStaticScratchDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxStaticScratchDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(m);
+    if (!addr[dev]) {
+        void* a = nullptr;
+        e = cudaGetSymbolAddress(&a, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        e = cudaMemset(static_cast<unsigned char*>(a) + kStaticScratchBytes - kStaticScratchFlagBytes,
+                       0, kStaticScratchFlagBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return e;
+        addr[dev] = a;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t tc_read_and_clear_device_status(int* status) {

@@ -358,11 +358,13 @@ constexpr size_t kSkWorkspaceBytes = kSkSlotBytes + kSkFlagBytes;
 // for the next launch's early start.
 // *grid is the persistent grid (at most one cluster per work item); max_grid
 // is every cluster the device holds at once. Stream-K runs on max_grid.
-void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool bf16) {
+void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool bf16,
+                      bool force_sk = false) {
     p.sk = 0;
     p.sk_total = 0;
     bool sk_on = false;
     if (const char* f = getenv("TPGEMM_TC_SK")) sk_on = atoi(f) != 0;
+    if (force_sk) sk_on = true;
     {
         const int ncl = std::max(1, max_grid / p.mc);
         const int full = (p.num_super / ncl) * ncl;
@@ -512,9 +514,17 @@ tpgemm_status encode_operand(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap*
     return encode_2d(enc, map, base, t, 2, uint64_t(K), uint64_t(rows), 64, uint32_t(box_rows), what);
 }
 
+// Where a stream-K launch finds its scratch: a per-stream buffer the library
+// allocates on first use, or the static array of tpgemm_gemm_noalloc.
+enum class Scratch { Allocated, Static };
+
+// Per-device epoch counter of the static scratch (all its calls share it).
+std::mutex g_static_epoch_mutex;
+uint32_t g_static_epoch[tpg::kMaxStaticScratchDevices] = {};
+
 tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_t M, int64_t N,
                   int64_t K, int transA, int transB, tpgemm_dtype dtype, float beta, void* stream,
-                  tpgemm_path path) {
+                  tpgemm_path path, Scratch scratch = Scratch::Allocated) {
     g_detail.clear();
     tpgemm_status s = check_shape(M, N, K, dtype, beta);
     if (s != TPGEMM_OK) return s;
@@ -554,7 +564,7 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     if (s != TPGEMM_OK) return s;
     s = fit_grid(&plan);
     if (s != TPGEMM_OK) return s;
-    apply_tail_split(plan.tc, &plan.grid, plan.max_grid, bf16);
+    apply_tail_split(plan.tc, &plan.grid, plan.max_grid, bf16, scratch == Scratch::Static);
     s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
     if (s != TPGEMM_OK) return s;
     if (p.tail_split > 1) {
@@ -565,8 +575,37 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     if (p.sk) {
         // Slots laid out like D tiles: [128 rows][bn32 cols] (normal) or
         // [bn32 rows][128 cols] (swapped), one per CTA, stacked along rows.
-        s = stream_k_workspace(st, &plan.tc.sk_ws, &plan.tc.sk_flags, &plan.tc.sk_epoch);
-        if (s != TPGEMM_OK) return s;
+        if (scratch == Scratch::Static) {
+            // No allocation: slots at the start of the static array, flags at
+            // its end; the plan must fit, else the call is refused.
+            const size_t need = size_t(plan.grid) * size_t(p.sk_slot_rows) *
+                                    size_t(p.swap ? 128 : 32 * ((p.bn + 31) / 32)) * sizeof(float) +
+                                tpg::kStaticScratchFlagBytes;
+            if (need > tpg::kStaticScratchBytes || plan.grid > 256)
+                return fail(TPGEMM_ERR_SHAPE,
+                            "stream-K scratch for this problem needs %zu bytes; the static scratch "
+                            "holds %zu",
+                            need, tpg::kStaticScratchBytes);
+            void* base = nullptr;
+            cudaError_t e = tpg::tc_static_scratch(&base);
+            if (e != cudaSuccess)
+                return fail(TPGEMM_ERR_LAUNCH, "static scratch set-up: %s", cudaGetErrorString(e));
+            int dev = 0;
+            cudaGetDevice(&dev);
+            uint32_t epoch;
+            {
+                std::lock_guard<std::mutex> lock(g_static_epoch_mutex);
+                epoch = ++g_static_epoch[dev];
+                if (epoch == 0) epoch = ++g_static_epoch[dev];
+            }
+            plan.tc.sk_ws = static_cast<float*>(base);
+            plan.tc.sk_flags = reinterpret_cast<uint32_t*>(
+                static_cast<uint8_t*>(base) + tpg::kStaticScratchBytes - tpg::kStaticScratchFlagBytes);
+            plan.tc.sk_epoch = epoch;
+        } else {
+            s = stream_k_workspace(st, &plan.tc.sk_ws, &plan.tc.sk_flags, &plan.tc.sk_epoch);
+            if (s != TPGEMM_OK) return s;
+        }
         const uint64_t bn32 = uint64_t(32 * ((p.bn + 31) / 32));
         const uint64_t cols = p.swap ? 128 : bn32;
         const uint64_t rows = uint64_t(plan.grid) * uint64_t(p.sk_slot_rows);
@@ -764,6 +803,15 @@ tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const flo
                                int64_t N, int64_t K, int transA, int transB, tpgemm_dtype dtype,
                                float beta, void* stream, tpgemm_path path) {
     return run(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream, path);
+}
+
+// The stream-K variant for callers that must not allocate device memory: its
+// scratch is the static array in tc_gemm.cu, never cudaMalloc.
+tpgemm_status tpgemm_gemm_noalloc(float* D, const void* A, const void* B, const float* C,
+                                  int64_t M, int64_t N, int64_t K, int transA, int transB,
+                                  tpgemm_dtype dtype, float beta, void* stream) {
+    return run(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream, TPGEMM_PATH_AUTO,
+               Scratch::Static);
 }
 
 const char* tpgemm_status_string(tpgemm_status s) {

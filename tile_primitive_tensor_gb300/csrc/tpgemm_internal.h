@@ -97,6 +97,13 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
 // persistent grid is this many clusters at most).
 cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters);
 
+// Static stream-K scratch (no allocation): its size, the flag area at its end,
+// and its device address on the current device (taken on first use there).
+constexpr size_t kStaticScratchBytes = size_t(20) << 20;
+constexpr size_t kStaticScratchFlagBytes = size_t(256) * 4 * sizeof(uint32_t);
+constexpr int kMaxStaticScratchDevices = 64;
+cudaError_t tc_static_scratch(void** ptr);
+
 // Device status word written by the tcgen05 kernel's bounded waits.
 cudaError_t tc_read_and_clear_device_status(int* status);
 
