@@ -22,8 +22,11 @@
  *   C: [M,N] float32 (read only when beta == 1; may be NULL when beta == 0).
  *   D: [M,N] float32 (written).
  * For tpgemm_gemm all four are device pointers owned by the caller (for
- * tpgemm_gemm_host they are host pointers). The library allocates no device
- * memory and keeps no pointer after a call is enqueued.
+ * tpgemm_gemm_host they are host pointers). The library keeps no pointer to
+ * them after a call is enqueued. Its default plans allocate no device memory;
+ * the opt-in stream-K mode (environment TPGEMM_TC_SK=1) takes one scratch
+ * buffer per (device, stream) with cudaMalloc on first use and keeps it until
+ * exit, and tpgemm_gemm_noalloc runs that mode on a static array instead.
  *
  * Errors: every function returns a status. Argument errors are detected on the
  * host before anything is enqueued, and a readable reason is available from

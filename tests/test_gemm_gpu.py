@@ -286,6 +286,35 @@ def test_stream_k(case, monkeypatch):
     assert np.array_equal(D1.view(np.uint32), D2.view(np.uint32))
 
 
+@pytest.mark.parametrize("case", [
+    ("skinny_swap_pair", 144, 2072, 520, False, False, 1.0, {"TPGEMM_TC_PAIR": "1"}),
+    ("normal_beta1_one_buf", 1024, 1024, 2048, False, True, 1.0, {}),
+    ("normal_beta0_one_buf", 1024, 1024, 520, True, True, 0.0, {}),
+    ("swapped_beta0", 784, 1320, 264, False, False, 0.0, {"TPGEMM_TC_ORIENT": "swap"}),
+    ("odd_bufs_reload", 1024, 1024, 264, False, True, 1.0, {"TPGEMM_TC_EPI_BUFS": "3"}),
+    ("tail_split", 2048, 2560, 136, False, True, 1.0, {"TPGEMM_TC_BN": "256"}),
+    ("stream_k", 1024, 1024, 2048, False, True, 1.0, {"TPGEMM_TC_SK": "1"}),
+    ("one_cta", 784, 1320, 264, False, True, 1.0, {"TPGEMM_TC_PAIR": "0"}),
+], ids=lambda c: c[0])
+def test_epilogue_groups(case, monkeypatch):
+    # One or two epilogue warpgroups: the second splits each lane quadrant's
+    # 32-column chunks (and its staging tiles) with the first. The K order is
+    # the same, so both give the same bits; each is checked against the oracle.
+    name, M, N, K, tA, tB, beta, env = case
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
+    w = dataclasses.replace(base.with_shape(M, N, K, seed=6390 + M + K), transA=tA, transB=tB,
+                            beta=beta, c_dist=("normal", 0.0, 1.0) if beta else None)
+    out = []
+    for g in ("1", "2"):
+        monkeypatch.setenv("TPGEMM_TC_EPI_GROUPS", g)
+        st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+        assert f"epi_groups={g}" in text, text
+        out.append(check_full(w, TC))
+    assert np.array_equal(out[0].view(np.uint32), out[1].view(np.uint32))
+
+
 def test_cta_pair_skinny_m144(monkeypatch):
     monkeypatch.setenv("TPGEMM_TC_PAIR", "1")
     w = wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(144, 2072, 520, seed=6320)

@@ -1,15 +1,18 @@
 // tcgen05 GEMM for sm_103a:  X = P . Q^T (+ C), f16/bf16 in, f32 accumulate and out.
 //
-// Persistent, warp-specialised CTA of 6 warps, one CTA per SM:
+// Persistent, warp-specialised CTA of 10 warps, one CTA per SM:
 //   warp 0      TMA producer: one thread fills a ring of shared-memory stages
 //               with 128-byte-swizzled P and Q tiles (cp.async.bulk.tensor).
 //   warp 1      owns tensor memory (tcgen05.alloc / dealloc, whole warp) and
 //               one thread issues tcgen05.mma for every 16-deep K step into a
 //               double-buffered accumulator, committing stage releases and
 //               "accumulator full" to mbarriers (tcgen05.commit).
-//   warps 2..5  epilogue warpgroup: tcgen05.ld 32x32b of its 32-lane quadrant,
-//               + beta.C (TMA-loaded into a swizzled staging tile), and a TMA
-//               store of D from the same staging tile.
+//   warps 2..9  one or two epilogue warpgroups (the plan's epi_groups; the
+//               second sits idle when 1): tcgen05.ld 32x32b of the warp's
+//               32-lane quadrant (with two groups, warps w and w + 4 share
+//               one and take alternate 32-column chunks), + beta.C (TMA-loaded
+//               into a swizzled staging tile), and a TMA store of D from the
+//               same staging tile.
 //
 // This follows the single-thread issue, commit-to-mbarrier and
 // alloc / relinquish / dealloc protocol of the tcgen05 copy page ("TVM
@@ -39,18 +42,19 @@ namespace {
 constexpr int kBM = 128;           // P rows per tile (tensor-memory lanes)
 constexpr int kBK = 64;            // K elements per stage: one 128-byte swizzle row
 constexpr int kUmmaK = 16;         // K per tcgen05.mma (kind::f16)
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = kTcEpiWarps;  // two per lane quadrant
+constexpr int kEpiQuads = 4;
 constexpr int kEpiBufFloats = 32 * 32;  // one 32 x 32 f32 staging tile (4 KB)
 constexpr int kAtomBytes = 8192;   // MN-major atom: 64 K rows x 128 bytes
 
 struct Smem {
     uint8_t* stages;
-    float* epi;            // [4 warps][epi_bufs][32*32]
+    float* epi;            // [4 quadrants][epi_bufs][32*32]
     uint64_t* full;        // [stages]
     uint64_t* empty;       // [stages]
     uint64_t* acc_full;    // [2]
     uint64_t* acc_empty;   // [2]
-    uint64_t* cbar;        // [4 warps][kTcMaxEpiBufs]
+    uint64_t* cbar;        // [4 quadrants][kTcMaxEpiBufs]
     uint64_t* drain;       // [1]
     uint32_t* tmem_base;
     volatile int* abort;
@@ -63,17 +67,40 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const TcParams& p) {
     s.stages = b;
     b += size_t(p.stages) * (p.p_bytes + p.q_bytes);
     s.epi = reinterpret_cast<float*>(b);
-    b += size_t(kEpiWarps) * p.epi_bufs * kEpiBufFloats * sizeof(float);
+    b += size_t(kEpiQuads) * p.epi_bufs * kEpiBufFloats * sizeof(float);
     uint64_t* bars = reinterpret_cast<uint64_t*>(b);
     s.full = bars;
     s.empty = bars + p.stages;
     s.acc_full = bars + 2 * p.stages;
     s.acc_empty = s.acc_full + 2;
     s.cbar = s.acc_empty + 2;
-    s.drain = s.cbar + kTcMaxEpiBufs * kEpiWarps;
+    s.drain = s.cbar + kTcMaxEpiBufs * kEpiQuads;
     s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.abort = reinterpret_cast<volatile int*>(s.tmem_base + 1);
     return s;
+}
+
+// An epilogue warp's share of its quadrant's staging tiles: active epilogue
+// warp ew (0 .. 4 epi_groups - 1) reads lane quadrant (ew + 2) % 4 and, of the
+// quadrant's 32-column chunks, those with c % epi_groups == ew / 4. The
+// quadrant's epi_bufs staging tiles (and their C-fill barriers) are split
+// between its active warps, the first ones taking any remainder.
+struct EpiShare {
+    int g;          // this warp's group: it takes chunks c = groups * j + g
+    int nbw;        // staging tiles of this warp (>= 1)
+    float* bufs;    // its first staging tile
+    uint64_t* cb;   // its first C-fill barrier
+};
+
+__device__ __forceinline__ EpiShare epi_share(const Smem& s, const TcParams& p, int ew) {
+    const int qs = ew & 3;
+    const int g = ew >> 2;
+    const int base = p.epi_bufs / p.epi_groups;
+    const int extra = p.epi_bufs % p.epi_groups;
+    const int first = g * base + min(g, extra);
+    return {g, base + (g < extra ? 1 : 0),
+            s.epi + (size_t(qs) * p.epi_bufs + first) * kEpiBufFloats,
+            s.cbar + kTcMaxEpiBufs * qs + first};
 }
 
 // Bounded wait on one mbarrier phase. False if the bound expired or (unless
@@ -222,9 +249,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&s.acc_full[i], 1);
             // Pair mode: the leader's accumulator barrier collects the
             // epilogue warps of both CTAs.
-            mbar_init(&s.acc_empty[i], PAIR ? 2 * kEpiWarps : kEpiWarps);
+            mbar_init(&s.acc_empty[i], (PAIR ? 2 : 1) * kEpiQuads * p.epi_groups);
         }
-        for (int i = 0; i < kTcMaxEpiBufs * kEpiWarps; ++i) mbar_init(&s.cbar[i], 1);
+        for (int i = 0; i < kTcMaxEpiBufs * kEpiQuads; ++i) mbar_init(&s.cbar[i], 1);
         mbar_init(s.drain, 1);
         *s.abort = 0;
         fence_mbarrier_init();
@@ -429,13 +456,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_commit(s.drain);
             wait_phase(s.drain, 0, s.abort, tmo, true);
         }
-    } else {
+    } else if (warp < 2 + kEpiQuads * p.epi_groups) {
         // --------------------------------------------------------- epilogue
-        const int ew = warp - 2;           // 0..3 staging slot
+        const int ew = warp - 2;           // 0 .. 4 epi_groups - 1
         const int quad = warp & 3;         // tensor-memory lane quadrant of this warp
-        const int nbuf = p.epi_bufs;
-        float* bufs = s.epi + size_t(ew) * nbuf * kEpiBufFloats;
-        uint64_t* cb = s.cbar + kTcMaxEpiBufs * ew;
+        const EpiShare es = epi_share(s, p, ew);
+        const int ng = p.epi_groups;
+        const int half = es.g;
+        const int nbw = es.nbw;
+        float* bufs = es.bufs;
+        uint64_t* cb = es.cb;
         const uint32_t lane_base = uint32_t(quad * 32) << 16;
 
         // Output extents in the kernel's (P, Q) frame, for skipping empty chunks.
@@ -454,6 +484,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool warp_live = pw < lim_p;
             int live_chunks = 0;
             if (warp_live) live_chunks = min(nchunks, (lim_q - q0 + 31) / 32);
+            // This warp's chunks: c = ng j + half for j < my_chunks.
+            const int my_chunks = live_chunks > half ? (live_chunks - half + ng - 1) / ng : 0;
             // Where chunk c's 32 x 32 box comes from (C, or the next stream-K
             // segment's scratch slot) and goes to (D, or this CTA's slot).
             // D / C boxes: (x = column, y = row) of D; slot boxes: the same
@@ -480,10 +512,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // All staging buffers free: every earlier store has read its source.
             if (lane == 0) bulk_wait_group_read<0>();
             // The next segment's partial must be published before it is read.
-            if (from_slot && live_chunks > 0) {
+            if (from_slot && my_chunks > 0) {
                 bool fok = true;
                 if (lane == 0) {
-                    fok = wait_flag(&p.sk_flags[src_slot * 4 + quad], p.sk_epoch, s.abort, tmo);
+                    fok = wait_flag(&p.sk_flags[src_slot * kEpiWarps + ew], p.sk_epoch, s.abort, tmo);
                     fence_proxy_async_global();
                 }
                 fok = __shfl_sync(0xffffffffu, fok ? 1 : 0, 0) != 0;
@@ -492,12 +524,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Prefetch the source (C or the partial) for the first chunks (all
             // of them when they fit the staging buffers) while the MMAs run.
             if (add_src) {
-                for (int c = 0; c < nbuf && c < live_chunks; ++c) {
+                for (int j = 0; j < nbw && j < my_chunks; ++j) {
+                    const int c = ng * j + half;
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&cb[c], kEpiBufFloats * 4);
-                        tma_load_2d(bufs + c * kEpiBufFloats, src_map, &cb[c], src_x(c), src_y(c));
+                        mbar_arrive_expect_tx(&cb[j], kEpiBufFloats * 4);
+                        tma_load_2d(bufs + j * kEpiBufFloats, src_map, &cb[j], src_x(c), src_y(c));
                     }
-                    cpend |= 1u << c;
+                    cpend |= 1u << j;
                 }
             }
             __syncwarp();
@@ -508,15 +541,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t acc_col = uint32_t(b * acc_stride);
-            // One 32-column chunk: its accumulator registers `cur` were loaded
-            // by the previous step; the next chunk's tcgen05.ld is issued into
-            // `nxt` before this one's shared-memory work so the two overlap.
-            auto chunk = [&](int c, uint32_t (&cur)[32], uint32_t (&nxt)[32]) -> bool {
-                const int bi = c % nbuf;
+            // This warp's j-th chunk (column chunk c = ng j + half): its
+            // accumulator registers `cur` were loaded by the previous step; the
+            // next chunk's tcgen05.ld is issued into `nxt` before this one's
+            // shared-memory work so the two overlap.
+            auto chunk = [&](int j, uint32_t (&cur)[32], uint32_t (&nxt)[32]) -> bool {
+                const int c = ng * j + half;
+                const int bi = j % nbw;
                 float* buf = bufs + bi * kEpiBufFloats;
                 tmem_ld_wait(cur);
-                if (c + 1 < live_chunks)
-                    tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * (c + 1)), nxt);
+                if (j + 1 < my_chunks)
+                    tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * (c + ng)), nxt);
                 if (add_src) {
                     bool cok = wait_phase(&cb[bi], (cphase >> bi) & 1u, s.abort, tmo);
                     cok = __all_sync(0xffffffffu, cok);
@@ -527,7 +562,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     cphase ^= 1u << bi;
                     cpend &= ~(1u << bi);
                 } else {
-                    if (lane == 0) bulk_wait_group_read<1>();  // the store of chunk c-nbuf read buf
+                    // The store that last used buf (this warp's chunk j - nbw) has read it.
+                    if (lane == 0) {
+                        if (nbw == 1)
+                            bulk_wait_group_read<0>();
+                        else
+                            bulk_wait_group_read<1>();
+                    }
                     __syncwarp();
                 }
                 if (!SWAP) {
@@ -562,21 +603,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) {
                     tma_store_2d(dst_map, buf, dst_x(c), dst_y(c));
                     bulk_commit_group();
-                    if (add_src && c + nbuf < live_chunks) {
+                    if (add_src && j + nbw < my_chunks) {
+                        const int cn = c + ng * nbw;  // this warp's chunk j + nbw
                         bulk_wait_group_read<0>();  // the store just issued has read buf
                         mbar_arrive_expect_tx(&cb[bi], kEpiBufFloats * 4);
-                        tma_load_2d(buf, src_map, &cb[bi], src_x(c + nbuf), src_y(c + nbuf));
+                        tma_load_2d(buf, src_map, &cb[bi], src_x(cn), src_y(cn));
                     }
                 }
-                if (add_src && c + nbuf < live_chunks) cpend |= 1u << bi;
+                if (add_src && j + nbw < my_chunks) cpend |= 1u << bi;
                 __syncwarp();
                 return true;
             };
             uint32_t ra[32], rb[32];
-            if (live_chunks > 0) tmem_ld_32x32b_x32(tmem + lane_base + acc_col, ra);
-            for (int c = 0; c < live_chunks && ok; c += 2) {
-                ok = chunk(c, ra, rb);
-                if (ok && c + 1 < live_chunks) ok = chunk(c + 1, rb, ra);
+            if (my_chunks > 0)
+                tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * half), ra);
+            for (int j = 0; j < my_chunks && ok; j += 2) {
+                ok = chunk(j, ra, rb);
+                if (ok && j + 1 < my_chunks) ok = chunk(j + 1, rb, ra);
             }
             // Accumulator buffer b may be overwritten by the next tile's MMAs
             // (issued by the pair's leader in pair mode).
@@ -593,7 +636,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (ok && to_slot && lane == 0) {
                 bulk_wait_group<0>();
                 fence_proxy_async_global();
-                st_release_gpu(&p.sk_flags[dst_slot * 4 + quad], p.sk_epoch);
+                st_release_gpu(&p.sk_flags[dst_slot * kEpiWarps + ew], p.sk_epoch);
             }
             if (!ok) break;
         }
@@ -613,11 +656,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int i = 0; i < p.stages; ++i)
                 if (issued_any & (1u << i))
                     wait_phase(&s.full[i], (issued_parity >> i) & 1u, s.abort, tmo, true);
-        if (warp >= 2)
-            for (int i = 0; i < p.epi_bufs; ++i)
+        if (warp >= 2 && warp < 2 + kEpiQuads * p.epi_groups) {
+            const EpiShare es = epi_share(s, p, warp - 2);
+            for (int i = 0; i < es.nbw; ++i)
                 if (cpend & (1u << i))
-                    wait_phase(&s.cbar[kTcMaxEpiBufs * (warp - 2) + i], (cphase >> i) & 1u, s.abort,
-                               tmo, true);
+                    wait_phase(&es.cb[i], (cphase >> i) & 1u, s.abort, tmo, true);
+        }
         __syncthreads();
     }
     // No CTA leaves while a peer may still multicast into it or arrive on it.
@@ -642,12 +686,13 @@ TcKernelFn pick_kernel(const TcParams& p) {
 
 size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs) {
     return 1024 + size_t(stages) * (p_bytes + q_bytes) +
-           size_t(kEpiWarps) * epi_bufs * kEpiBufFloats * sizeof(float) +
-           sizeof(uint64_t) * (2 * size_t(stages) + 4 + kTcMaxEpiBufs * kEpiWarps + 1) + 16;
+           size_t(kEpiQuads) * epi_bufs * kEpiBufFloats * sizeof(float) +
+           sizeof(uint64_t) * (2 * size_t(stages) + 4 + kTcMaxEpiBufs * kEpiQuads + 1) + 16;
 }
 
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
     if (p.epi_bufs < 2 || p.epi_bufs > kTcMaxEpiBufs || p.stages < 2 || p.stages > 32 ||
+        !(p.epi_groups == 1 || p.epi_groups == 2) ||
         !(p.mc == 1 || p.mc == 2 || p.mc == 4) || grid % p.mc != 0 || (p.pair && p.mc != 2) ||
         !(p.tmem_cols == 64 || p.tmem_cols == 128 || p.tmem_cols == 256 || p.tmem_cols == 512) ||
         p.tmem_cols / 2 < 32 * ((p.bn + 31) / 32))

@@ -318,6 +318,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     if (stages == 0) return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
     p.stages = stages;
     p.epi_bufs = epi_bufs;
+    p.epi_groups = 1;  // set with the grid (choose_epi_groups)
     // The epilogue stores 32-column boxes; a tile width that is not a multiple
     // of 32 is only used when it is the only tile along Q (the box overhang is
     // then past the end of the matrix and clipped by the TMA store).
@@ -338,11 +339,12 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
 // a quarter of the time. A unit stays a whole number of 32-column chunks and
 // each CTA's share of it whole 8-row groups (K-contiguous Q) or 16-row steps.
 // Stream-K scratch: one partial-tile slot per CTA (128 x bn fp32, bn rounded
-// up to 32) and four epoch flags per CTA. Sized for the largest plan.
+// up to 32) and one epoch flag per epilogue warp of each CTA. Sized for the
+// largest plan.
 constexpr int kSkMaxGrid = 256;
 constexpr size_t kSkSlotFloats = size_t(128) * 256;
 constexpr size_t kSkSlotBytes = kSkMaxGrid * kSkSlotFloats * sizeof(float);
-constexpr size_t kSkFlagBytes = kSkMaxGrid * 4 * sizeof(uint32_t);
+constexpr size_t kSkFlagBytes = kSkMaxGrid * tpg::kTcEpiWarps * sizeof(uint32_t);
 constexpr size_t kSkWorkspaceBytes = kSkSlotBytes + kSkFlagBytes;
 
 // Balance the last, partial wave of the persistent grid by splitting the
@@ -406,6 +408,20 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool bf16,
     p.num_units = p.full_units + (p.num_super - p.full_units) * split;
     p.idesc_tail = tpg::idesc_f16_f32(bf16, p.p_mn, p.q_mn, p.pair ? 256 : 128, p.bn / split);
     p.q_box_rows = p.pair ? p.bn / 2 : p.bn / p.mc;
+}
+
+// Epilogue warpgroups. With at most one work unit per cluster (a single wave)
+// no later tile's MMAs run under the epilogue, so both warpgroups drain it;
+// with more, one group keeps up and the second only competes with the MMA and
+// producer warps for issue slots and shared memory. TPGEMM_TC_EPI_GROUPS
+// overrides.
+void choose_epi_groups(tpg::TcParams& p, int grid) {
+    const int ncl = std::max(1, grid / p.mc);
+    p.epi_groups = (!p.sk && p.num_units <= ncl) ? 2 : 1;
+    if (const char* f = getenv("TPGEMM_TC_EPI_GROUPS")) {
+        const int v = atoi(f);
+        if (v == 1 || v == 2) p.epi_groups = v;
+    }
 }
 
 // Stream-K scratch per (device, stream): allocated on first use, kept until
@@ -565,6 +581,7 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     s = fit_grid(&plan);
     if (s != TPGEMM_OK) return s;
     apply_tail_split(plan.tc, &plan.grid, plan.max_grid, bf16, scratch == Scratch::Static);
+    choose_epi_groups(plan.tc, plan.grid);
     s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
     if (s != TPGEMM_OK) return s;
     if (p.tail_split > 1) {
@@ -865,8 +882,10 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     s = make_plan(M, N, K, transA != 0, transB != 0, dtype == TPGEMM_BF16, beta, path, sms, &plan);
     if (s != TPGEMM_OK) return s;
     char text[512];
-    if (plan.kernel == Kernel::Tc)
+    if (plan.kernel == Kernel::Tc) {
         apply_tail_split(plan.tc, &plan.grid, plan.max_grid, dtype == TPGEMM_BF16);
+        choose_epi_groups(plan.tc, plan.grid);
+    }
     if (plan.kernel == Kernel::MmaSync) {
         snprintf(text, sizeof(text),
                  "path=mma_sync tile=%dx%dx32 grid=%lldx%lld warps=4 k_inst=%s",
@@ -876,10 +895,10 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
         const tpg::TcParams& p = plan.tc;
         snprintf(text, sizeof(text),
                  "path=tcgen05 orientation=%s tile=128x%dx64 umma=%dx%dx16 stages=%d "
-                 "epi_bufs=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d grid=%d "
-                 "units=%d+%dx%d stream_k=%d p_major=%s q_major=%s smem=%zu",
+                 "epi_bufs=%d epi_groups=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d "
+                 "grid=%d units=%d+%dx%d stream_k=%d p_major=%s q_major=%s smem=%zu",
                  plan.swap ? "swapped" : "normal", p.bn, p.pair ? 256 : 128, p.bn, p.stages,
-                 p.epi_bufs, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
+                 p.epi_bufs, p.epi_groups, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
                  p.full_units, p.num_super - p.full_units, p.tail_split, p.sk, p.p_mn ? "mn" : "k",
                  p.q_mn ? "mn" : "k",
                  tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));

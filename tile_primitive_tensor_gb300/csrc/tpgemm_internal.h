@@ -46,7 +46,10 @@ struct TcParams {
     uint32_t tx_bytes;      // bytes the TMA delivers per stage
     uint64_t timeout_ns;    // bound on every mbarrier wait
     int swap;               // orientation, for the epilogue's D coordinates
-    int epi_bufs;           // 32 x 32 f32 staging tiles per epilogue warp (2..8)
+    int epi_bufs;           // 32 x 32 f32 staging tiles per lane quadrant (2..8), split
+                            // between the quadrant's active epilogue warps
+    int epi_groups;         // active epilogue warpgroups (1 or 2); warp 2 + 4 g + i
+                            // reads lane quadrant (i + 2) % 4, chunks c % groups == g
     int k_rotate;           // 0, or tiles per group sharing a rotated first K block
     int mc;                 // CTAs per cluster sharing one Q tile (1, 2 or 4): each
                             // loads 1/mc of it and multicasts it to the others
@@ -74,7 +77,7 @@ struct TcParams {
     int sk;                 // 0 / 1
     int sk_total;
     float* sk_ws;           // partial tiles: slot = blockIdx.x (written through mapW)
-    uint32_t* sk_flags;     // [gridDim.x][4] epoch flags, one per epilogue quadrant
+    uint32_t* sk_flags;     // [gridDim.x][kTcEpiWarps] epoch flags, one per epilogue warp
     uint32_t sk_epoch;      // value of a flag once its slot holds this launch's data
     int sk_slot_rows;       // rows of one slot in mapW's frame (128, or bn rounded to 32)
 };
@@ -89,7 +92,11 @@ struct TcMaps {
 
 constexpr int kTcMaxEpiBufs = 8;
 size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs);
-constexpr int kTcThreads = 192;
+// Producer warp, MMA warp, then kTcEpiWarps epilogue warps: up to two per
+// tensor-memory lane quadrant (TcParams::epi_groups), splitting the
+// accumulator's 32-column chunks between them.
+constexpr int kTcEpiWarps = 8;
+constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);
 constexpr int kTcMaxSmem = 232448;  // 227 KB opt-in per block on sm_100-class parts
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream);
 
@@ -100,7 +107,7 @@ cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters);
 // Static stream-K scratch (no allocation): its size, the flag area at its end,
 // and its device address on the current device (taken on first use there).
 constexpr size_t kStaticScratchBytes = size_t(20) << 20;
-constexpr size_t kStaticScratchFlagBytes = size_t(256) * 4 * sizeof(uint32_t);
+constexpr size_t kStaticScratchFlagBytes = size_t(256) * kTcEpiWarps * sizeof(uint32_t);
 constexpr int kMaxStaticScratchDevices = 64;
 cudaError_t tc_static_scratch(void** ptr);
 
