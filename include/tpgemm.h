@@ -161,6 +161,126 @@ tpgemm_status tpgemm_gemm_host(float* D_host, const void* A_host, const void* B_
                                int transB, tpgemm_dtype dtype, float beta, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/*
+ * ------------------------------------------------------------------------
+ * Shared memory -> tensor memory copy (tcgen05.cp), as a standalone primitive.
+ *
+ * The operation is the smem-tmem variant of copy_async described on the page
+ * "TVM Blackwell tcgen05.cp 全解析": a matrix of `rows` rows x `row_bits` bits
+ * in shared memory, named by a 64-bit shared-memory matrix descriptor, is
+ * copied into tensor memory by single-thread tcgen05.cp instructions of one of
+ * six shape / multicast forms (section 形状选择), with the row -> lane and
+ * replica pattern of each form given in section 形状 → 行/复制模式映射表:
+ *
+ *   form                     rows  bits/row  row r goes to lane(s)
+ *   128x256b                  128    256      r
+ *   4x256b                      4    256      32 r            (rows 0..3)
+ *   128x128b                  128    128      r
+ *   64x128b.warpx2::02_13      64    128      r, r + 64
+ *   64x128b.warpx2::01_23      64    128      (r % 32) + 64 (r / 32), + 32
+ *   32x128b.warpx4             32    128      r, r + 32, r + 64, r + 96
+ *
+ * Bits [32 c, 32 c + 32) of a row go to tensor-memory column tmem_col + c.
+ * Wider regions are copied by several instructions along the row (one per
+ * 256 or 128 bits), and a 4x256b region of 4 j rows by j lane-tiled
+ * instructions: row 4 i + q goes to lane 32 q + i (the first j lanes of each
+ * warp's quadrant). The plan issues each instruction with the descriptor
+ * encoded once and only its 14-bit start address patched (section 调度算法四步,
+ * steps 3 and 4), and the caller-side completion is a tcgen05.commit to an
+ * mbarrier (section 演示程序).
+ *
+ * Shared-memory layout of the source (the K-major canonical layout of the
+ * matrix descriptor; byte offsets from a 1024-byte aligned buffer):
+ *   SWIZZLE_NONE: 16-byte unit u of row r at
+ *       smem_offset + (r / 8) sbo + (r % 8) 16 + u lbo
+ *   SWIZZLE_32B / _64B / _128B (S = 32, 64, 128 bytes per swizzle row, U =
+ *   S / 16 units each): unit u of row r at swz(smem_offset + (u / U) lbo +
+ *   (r / 8) sbo + (r % 8) S + 16 (u % U)), where swz XORs address bits
+ *   [4, 4 + log2 U) with bits [7, 7 + log2 U); a row wider than one swizzle row
+ *   continues in the next swizzle atom, lbo bytes on.
+ * The planner rejects strides under which two units would share bytes.
+ */
+typedef enum {
+    TPGEMM_CP_SWIZZLE_NONE = 0,
+    TPGEMM_CP_SWIZZLE_32B = 1,
+    TPGEMM_CP_SWIZZLE_64B = 2,
+    TPGEMM_CP_SWIZZLE_128B = 3
+} tpgemm_cp_swizzle;
+
+/* tcgen05.cp shape with its multicast qualifier. AUTO: the widest form whose
+ * pattern matches the destination lanes (the page's candidate order
+ * 128x256b, 4x256b, 128x128b, 64x128b.02_13, 64x128b.01_23, 32x128b.warpx4). */
+typedef enum {
+    TPGEMM_CP_AUTO = 0,
+    TPGEMM_CP_128x256b = 1,
+    TPGEMM_CP_4x256b = 2,
+    TPGEMM_CP_128x128b = 3,
+    TPGEMM_CP_64x128b_WARPX2_02_13 = 4,
+    TPGEMM_CP_64x128b_WARPX2_01_23 = 5,
+    TPGEMM_CP_32x128b_WARPX4 = 6
+} tpgemm_cp_shape;
+
+/* Where the region's rows go in tensor memory (lane_offset added to each). */
+typedef enum {
+    TPGEMM_CP_LANES_ROWS = 0,         /* row r -> lane r                        */
+    TPGEMM_CP_LANES_QUADRANTS = 1,    /* row 4 i + q -> lane 32 q + i           */
+    TPGEMM_CP_LANES_PAIRS_02_13 = 2,  /* row r -> lanes r, r + 64 (r < 64)      */
+    TPGEMM_CP_LANES_PAIRS_01_23 = 3,  /* row r -> lanes (r%32) + 64 (r/32) + {0, 32} */
+    TPGEMM_CP_LANES_ALL_QUADS = 4     /* row r -> lanes r + {0, 32, 64, 96}      */
+} tpgemm_cp_lanes;
+
+typedef struct {
+    int rows;                  /* rows of the region                               */
+    int row_bits;              /* bits per row: a positive multiple of 128         */
+    tpgemm_cp_swizzle swizzle; /* source layout                                    */
+    uint32_t lbo_bytes;        /* distance between a row's units (unswizzled) or
+                                  between swizzle atoms along the row (swizzled)  */
+    uint32_t sbo_bytes;        /* distance between 8-row groups (multiple of 16)   */
+    uint32_t smem_offset;      /* region start in the staging buffer               */
+    int tmem_col;              /* first tensor-memory column (multiple of 4)       */
+    int lane_offset;           /* added to every destination lane                  */
+    tpgemm_cp_lanes lanes;     /* destination row -> lane pattern                  */
+    tpgemm_cp_shape shape;     /* instruction form, or AUTO                        */
+    int cta_group;             /* 1, or 2 (the even CTA of a pair issues; each CTA
+                                  copies its own shared memory to its own tensor
+                                  memory)                                         */
+} tpgemm_cp_desc;
+
+/* Parse a form name ("128x256b", "4x256b", "128x128b", "64x128b.warpx2::02_13",
+ * "64x128b.warpx2::01_23", "32x128b.warpx4"; the multicast part may also be
+ * given alone after a '.'). TPGEMM_ERR_SHAPE with a readable reason for an
+ * unknown shape, a 64x128b without its multicast, or an illegal combination
+ * (e.g. "128x256b.warpx4"). */
+tpgemm_status tpgemm_cp_parse_shape(const char* name, tpgemm_cp_shape* out);
+
+/* The plan for a copy, as text into buf: the chosen form, the number of
+ * instructions, the descriptor fields (LBO, SBO, swizzle mode) and, per
+ * instruction, its shared-memory start offset and tensor-memory lane / column.
+ * Returns TPGEMM_OK, or TPGEMM_ERR_SHAPE with the reason in
+ * tpgemm_last_error_detail() (and in buf): form / lane-pattern mismatch,
+ * region larger than the 128 lanes, column offset not 128-bit aligned, SBO not
+ * a multiple of 16 bytes, a row wider than the swizzle row, a region that
+ * does not tile into the form's rows and bits. */
+tpgemm_status tpgemm_cp_plan(const tpgemm_cp_desc* d, char* buf, int buflen);
+
+/*
+ * Round trip through tensor memory, for tests and measurement: one CTA (two
+ * for cta_group 2) copies `image_bytes` bytes from `smem_image` (device memory)
+ * into a 1024-byte aligned shared-memory buffer, fills tensor-memory columns
+ * [0, ncols) of all 128 lanes with fill(lane, col) = fill_base + lane * 65536
+ * + col (tcgen05.st), issues the planned tcgen05.cp instructions, commits them
+ * to an mbarrier and waits, then reads the same columns back (tcgen05.ld
+ * 32x32b) into tmem_out[lane * ncols + col] (device memory, uint32). For
+ * cta_group 2, smem_image holds the two CTAs' images back to back and
+ * tmem_out the two CTAs' results. ncols: 32..512, a multiple of 32, covering
+ * the copied columns; image_bytes: a multiple of 16, at most 196608.
+ * Asynchronous on `stream`; argument errors as tpgemm_cp_plan, plus
+ * TPGEMM_ERR_NULL / _ALIGN for the pointers.
+ */
+tpgemm_status tpgemm_cp_roundtrip(uint32_t* tmem_out, const void* smem_image, size_t image_bytes,
+                                  const tpgemm_cp_desc* d, uint32_t fill_base, int ncols,
+                                  void* stream);
+
 /* Static English name of a status. Never NULL. */
 const char* tpgemm_status_string(tpgemm_status s);
 

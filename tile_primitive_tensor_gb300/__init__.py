@@ -39,6 +39,34 @@ TPGEMM_ERR_PATH = 10
 TPGEMM_PATH_AUTO = 0
 TPGEMM_PATH_TCGEN05 = 1
 TPGEMM_PATH_MMA_SYNC = 2
+# tpgemm_cp_swizzle
+TPGEMM_CP_SWIZZLE_NONE = 0
+TPGEMM_CP_SWIZZLE_32B = 1
+TPGEMM_CP_SWIZZLE_64B = 2
+TPGEMM_CP_SWIZZLE_128B = 3
+# tpgemm_cp_shape
+TPGEMM_CP_AUTO = 0
+TPGEMM_CP_128x256b = 1
+TPGEMM_CP_4x256b = 2
+TPGEMM_CP_128x128b = 3
+TPGEMM_CP_64x128b_WARPX2_02_13 = 4
+TPGEMM_CP_64x128b_WARPX2_01_23 = 5
+TPGEMM_CP_32x128b_WARPX4 = 6
+# tpgemm_cp_lanes
+TPGEMM_CP_LANES_ROWS = 0
+TPGEMM_CP_LANES_QUADRANTS = 1
+TPGEMM_CP_LANES_PAIRS_02_13 = 2
+TPGEMM_CP_LANES_PAIRS_01_23 = 3
+TPGEMM_CP_LANES_ALL_QUADS = 4
+
+
+class CpDesc(ctypes.Structure):
+    """tpgemm_cp_desc: a shared-memory region and where its rows go in tensor memory."""
+    _fields_ = [("rows", ctypes.c_int), ("row_bits", ctypes.c_int), ("swizzle", ctypes.c_int),
+                ("lbo_bytes", ctypes.c_uint32), ("sbo_bytes", ctypes.c_uint32),
+                ("smem_offset", ctypes.c_uint32), ("tmem_col", ctypes.c_int),
+                ("lane_offset", ctypes.c_int), ("lanes", ctypes.c_int), ("shape", ctypes.c_int),
+                ("cta_group", ctypes.c_int)]
 
 
 class TpgemmError(RuntimeError):
@@ -85,6 +113,13 @@ def _load():
         lib.tpgemm_describe_plan.restype = ci
         lib.tpgemm_version.argtypes = []
         lib.tpgemm_version.restype = ctypes.c_char_p
+        lib.tpgemm_cp_parse_shape.argtypes = [ctypes.c_char_p, ctypes.POINTER(ci)]
+        lib.tpgemm_cp_parse_shape.restype = ci
+        lib.tpgemm_cp_plan.argtypes = [ctypes.POINTER(CpDesc), ctypes.c_char_p, ci]
+        lib.tpgemm_cp_plan.restype = ci
+        lib.tpgemm_cp_roundtrip.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
+                                            ctypes.c_uint32, ci, vp]
+        lib.tpgemm_cp_roundtrip.restype = ci
         _lib = lib
         return lib
 
@@ -175,6 +210,35 @@ def tpgemm_describe_plan(M, N, K, transA, transB, dtype, beta, path=TPGEMM_PATH_
                                           int(bool(transB)), int(dtype), float(beta), int(path),
                                           buf, 512))
     return st, buf.value.decode()
+
+
+def cp_desc(rows, row_bits, *, swizzle=TPGEMM_CP_SWIZZLE_NONE, lbo=0, sbo=0, smem_offset=0,
+            tmem_col=0, lane_offset=0, lanes=TPGEMM_CP_LANES_ROWS, shape=TPGEMM_CP_AUTO,
+            cta_group=1) -> CpDesc:
+    return CpDesc(int(rows), int(row_bits), int(swizzle), int(lbo), int(sbo), int(smem_offset),
+                  int(tmem_col), int(lane_offset), int(lanes), int(shape), int(cta_group))
+
+
+def tpgemm_cp_parse_shape(name: str):
+    """(status, tpgemm_cp_shape) for a form name such as "64x128b.warpx2::02_13"."""
+    out = ctypes.c_int(0)
+    st = int(_load().tpgemm_cp_parse_shape(name.encode(), ctypes.byref(out)))
+    return st, out.value
+
+
+def tpgemm_cp_plan(desc: CpDesc):
+    """(status, text): the planned tcgen05.cp instructions, or the rejection reason."""
+    buf = ctypes.create_string_buffer(16384)
+    st = int(_load().tpgemm_cp_plan(ctypes.byref(desc), buf, 16384))
+    return st, buf.value.decode()
+
+
+def tpgemm_cp_roundtrip(tmem_out, smem_image, image_bytes, desc: CpDesc, fill_base, ncols,
+                        stream=None) -> int:
+    """Enqueue image -> shared memory -> tcgen05.cp -> tensor memory -> tmem_out."""
+    return int(_load().tpgemm_cp_roundtrip(_ptr(tmem_out), _ptr(smem_image), int(image_bytes),
+                                           ctypes.byref(desc), int(fill_base) & 0xFFFFFFFF,
+                                           int(ncols), _stream(stream)))
 
 
 def tpgemm_version() -> str:

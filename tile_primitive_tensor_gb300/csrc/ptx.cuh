@@ -316,6 +316,59 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
         : "memory");
 }
 
+// 32 lanes x 8 consecutive 32-bit columns, in both directions: thread t of
+// the warp owns lane (quadrant base + t), register j column col + j.
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::
+                     "r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Shared memory -> tensor memory copy, issued by one thread. The source is the
+// matrix named by the shared-memory descriptor; `form` selects the shape and
+// multicast qualifier (1 128x256b, 2 4x256b, 3 128x128b, 4 64x128b.warpx2::02_13,
+// 5 64x128b.warpx2::01_23, 6 32x128b.warpx4). CG = 2: issued by the even CTA
+// of a pair; each CTA copies from its own shared memory into its own tensor
+// memory.
+template <int CG>
+__device__ __forceinline__ void tc_cp(int form, uint32_t taddr, uint64_t sdesc) {
+#define TPG_CP(SHAPE)                                                                         \
+    do {                                                                                      \
+        if constexpr (CG == 2)                                                                \
+            asm volatile("tcgen05.cp.cta_group::2." SHAPE " [%0], %1;" ::"r"(taddr), "l"(sdesc) \
+                         : "memory");                                                         \
+        else                                                                                  \
+            asm volatile("tcgen05.cp.cta_group::1." SHAPE " [%0], %1;" ::"r"(taddr), "l"(sdesc) \
+                         : "memory");                                                         \
+    } while (0)
+    switch (form) {
+        case 1: TPG_CP("128x256b"); break;
+        case 2: TPG_CP("4x256b"); break;
+        case 3: TPG_CP("128x128b"); break;
+        case 4: TPG_CP("64x128b.warpx2::02_13"); break;
+        case 5: TPG_CP("64x128b.warpx2::01_23"); break;
+        case 6: TPG_CP("32x128b.warpx4"); break;
+        default: break;
+    }
+#undef TPG_CP
+}
+
 // -------------------------------------------------- descriptors (tcgen05)
 // Shared-memory matrix descriptor, SWIZZLE_128B, start address 0. Fields:
 // bits 0-13 start address >> 4, 16-29 leading-dimension byte offset >> 4,

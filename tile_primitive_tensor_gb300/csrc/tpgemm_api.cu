@@ -143,12 +143,7 @@ struct Plan {
 
 // Bound on every mbarrier wait inside the tcgen05 kernel: 2 s, or
 // TPGEMM_WAIT_TIMEOUT_MS (read at every call, so a test can shorten it).
-uint64_t wait_timeout_ns() {
-    const char* s = getenv("TPGEMM_WAIT_TIMEOUT_MS");
-    long long ms = s ? atoll(s) : 0;
-    if (ms <= 0) ms = 2000;
-    return uint64_t(ms) * 1000000ull;
-}
+using tpg::wait_timeout_ns;
 
 // Shared bytes of one stage tile of an operand with `rows` rows along MN and
 // 64 K elements: K-contiguous tiles are rows x 128 bytes; MN-contiguous tiles
@@ -801,6 +796,17 @@ tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* C
 
 }  // namespace
 
+namespace tpg {
+void set_error_detail(const char* text) { g_detail = text ? text : ""; }
+
+uint64_t wait_timeout_ns() {
+    const char* s = getenv("TPGEMM_WAIT_TIMEOUT_MS");
+    long long ms = s ? atoll(s) : 0;
+    if (ms <= 0) ms = 2000;
+    return uint64_t(ms) * 1000000ull;
+}
+}  // namespace tpg
+
 extern "C" {
 
 size_t tpgemm_gemm_host_workspace_bytes(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype,
@@ -865,12 +871,15 @@ tpgemm_status tpgemm_last_device_error(void) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
         return fail(TPGEMM_ERR_LAUNCH, "device synchronize: %s", cudaGetErrorString(e));
-    int st = 0;
+    int st = 0, st_cp = 0;
     e = tpg::tc_read_and_clear_device_status(&st);
+    if (e == cudaSuccess) e = tpg::cp_read_and_clear_device_status(&st_cp);
     if (e != cudaSuccess)
         return fail(TPGEMM_ERR_LAUNCH, "reading device status: %s", cudaGetErrorString(e));
     if (st == tpg::kStatusTimeout)
         return fail(TPGEMM_ERR_TIMEOUT, "a tcgen05 kernel wait exceeded its bound");
+    if (st_cp == tpg::kStatusTimeout)
+        return fail(TPGEMM_ERR_TIMEOUT, "a tensor-memory copy kernel wait exceeded its bound");
     return TPGEMM_OK;
 }
 

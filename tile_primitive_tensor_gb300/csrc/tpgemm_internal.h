@@ -10,6 +10,19 @@ namespace tpg {
 
 constexpr int kStatusTimeout = 9;  // matches TPGEMM_ERR_TIMEOUT
 
+// The calling thread's reason for its last non-OK status, as returned by
+// tpgemm_last_error_detail (empty after a success).
+void set_error_detail(const char* text);
+
+// Bound of every wait inside a kernel: TPGEMM_WAIT_TIMEOUT_MS (default 2 s),
+// read on each call.
+uint64_t wait_timeout_ns();
+
+// Device status words of the GEMM kernel and of the tensor-memory copy kernel
+// (0, or kStatusTimeout after an expired bounded wait); reading clears them.
+cudaError_t tc_read_and_clear_device_status(int* status);
+cudaError_t cp_read_and_clear_device_status(int* status);
+
 // ---- warp-level mma.sync kernel (small problems) ----
 struct MmaSyncArgs {
     float* D;
@@ -111,7 +124,5 @@ constexpr size_t kStaticScratchFlagBytes = size_t(256) * kTcEpiWarps * sizeof(ui
 constexpr int kMaxStaticScratchDevices = 64;
 cudaError_t tc_static_scratch(void** ptr);
 
-// Device status word written by the tcgen05 kernel's bounded waits.
-cudaError_t tc_read_and_clear_device_status(int* status);
 
 }  // namespace tpg
