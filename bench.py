@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--primitive", choices=["tcgen05_cp"], default=None,
+                    help="measure a standalone primitive instead of the GEMM step")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -360,6 +362,111 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
+# ------------------------------------------------------ tcgen05.cp primitive
+CP_REGIONS = [  # (form, lane pattern, rows, row bits): 16 KB or less per CTA per copy
+    ("128x256b", 1, 0, 128, 1024),
+    ("4x256b", 2, 1, 128, 256),
+    ("128x128b", 3, 0, 128, 1024),
+    ("64x128b.warpx2::02_13", 4, 2, 64, 1024),
+    ("64x128b.warpx2::01_23", 5, 3, 64, 1024),
+    ("32x128b.warpx4", 6, 4, 32, 1024),
+]
+
+
+def run_primitive_cp(args):
+    """Shared-memory -> tensor-memory copy throughput of every tcgen05.cp form.
+
+    One CTA per SM, each issuing its planned copy of a 128B-swizzled region
+    `repeat` times before one commit; bytes = shared-memory bytes read. The
+    derived peak is the shared-memory read port, 128 B per clock per SM, at the
+    SM clock sampled during the run."""
+    import torch
+
+    import tile_primitive_tensor_gb300 as tp
+
+    dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    repeat = 4096
+    sampler = ClockSampler(None)
+    sampler.start()
+    time.sleep(0.4)
+    t0 = time.time()
+    forms = {}
+    for name, shape, lanes, rows, bits in CP_REGIONS:
+        groups = (rows + 7) // 8
+        lbo, sbo = groups * 1024, 1024
+        atoms = (bits // 128 + 7) // 8
+        nbytes = atoms * lbo
+        image = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=dev)
+        ncols = max(32, bits // 32)
+        out = torch.empty(sms * 128 * ncols, dtype=torch.int32, device=dev)
+        d = tp.cp_desc(rows, bits, swizzle=tp.TPGEMM_CP_SWIZZLE_128B, lbo=lbo, sbo=sbo,
+                       lanes=lanes, shape=shape)
+
+        def go(r):
+            st = tp.tpgemm_cp_roundtrip_repeat(out, image, nbytes, d, 0, ncols, r, sms)
+            if st != 0:
+                raise RuntimeError(f"tpgemm_cp_roundtrip_repeat: {tp.tpgemm_last_error_detail()}")
+
+        for _ in range(3):
+            go(repeat)
+        torch.cuda.synchronize()
+        times = {}
+        for r in (1, repeat):  # the fixed cost of a launch (image, fill, read-back) subtracts
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                go(r)
+            e1.record()
+            torch.cuda.synchronize()
+            times[r] = e0.elapsed_time(e1) / args.steps
+        tp.check(tp.tpgemm_last_device_error())
+        per_copy_s = (times[repeat] - times[1]) * 1e-3 / (repeat - 1)
+        region = rows * bits // 8
+        gbs = sms * region / per_copy_s / 1e9
+        instr = (rows // 4 if lanes == 1 else 1) * (bits // (256 if shape in (1, 2) else 128))
+        forms[name] = {"GB_per_s": round(gbs, 1), "bytes_per_cta_copy": region,
+                       "instructions": instr, "ns_per_copy": round(per_copy_s * 1e9, 2),
+                       "launch_ms_repeat1": round(times[1], 4)}
+    t1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    mhz = clocks["sm_mhz"] or 2070.0
+    peak = sms * 128 * mhz * 1e6 / 1e9
+    for f in forms.values():
+        f["frac"] = round(f["GB_per_s"] / peak, 4)
+    best = forms["128x256b"]
+    # The oracle beside it: rebuilding the expected tensor memory of one CTA's
+    # 128x256b copy on the host cores.
+    import numpy as np
+
+    from oracle import tmem_cp as ocp
+    words = np.random.default_rng(0).integers(0, 2 ** 32, (128, 32), dtype=np.uint64).astype(
+        np.uint32)
+    n, c0 = 0, time.perf_counter()
+    while time.perf_counter() - c0 < 2.0:
+        ocp.tmem_image(words, ocp.LANES_ROWS, 0, 0, 32, 0)
+        n += 1
+    cpu_s = (time.perf_counter() - c0) / n
+    cpu = {"value": round(128 * 128 / cpu_s / 1e9, 4), "unit": "GB/s", "cores": 1,
+           "kind": "oracle", "sample": f"{n} rebuilds of one CTA's 128 x 1024-bit copy "
+                                       "(oracle.tmem_cp.tmem_image)"}
+    return {
+        "metric": "tcgen05.cp shared->tensor memory copy bandwidth (shared-memory bytes read)",
+        "value": best["GB_per_s"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "higher_is_better": True, "dtype": "b32", "data": "synthetic (random bytes)",
+        "config": {"workload": "tcgen05_cp_128B_swizzle", "ctas": sms, "repeat": repeat},
+        "clocks": clocks,
+        "roofline": {"bound": "smem", "achieved": best["GB_per_s"], "peak": round(peak, 1),
+                     "unit": "GB/s", "frac": best["frac"],
+                     "peak_kind": f"derived: {sms} SMs x 128 B/clk x {mhz:.0f} MHz (sampled)",
+                     "traffic": None},
+        "forms": forms,
+        "cpu_baseline": cpu,
+        "gpu_launches": 2 * args.steps * len(CP_REGIONS),
+    }
+
+
 # ---------------------------------------------------------- reference arm
 def run_reference(args):
     w = wl.BY_NAME[args.workload]
@@ -414,6 +521,10 @@ def main():
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if args.primitive == "tcgen05_cp":
+        if rank == 0:
+            print(json.dumps(run_primitive_cp(args)), flush=True)
         return 0
     if world > 1:
         import torch

@@ -281,6 +281,17 @@ tpgemm_status tpgemm_cp_roundtrip(uint32_t* tmem_out, const void* smem_image, si
                                   const tpgemm_cp_desc* d, uint32_t fill_base, int ncols,
                                   void* stream);
 
+/* tpgemm_cp_roundtrip on `ctas` CTAs at once (a multiple of cta_group), each
+ * issuing the planned instruction list `repeat` times (1..2^20) before its
+ * commit, for measuring the copy's throughput. Every CTA (every pair for
+ * cta_group 2) reads the same image(s); CTA k writes rows [128 k, 128 k + 128)
+ * of tmem_out, which must hold ctas * 128 * ncols words. With repeat > 1 the
+ * later copies rewrite the same cells, so the result is that of one copy. */
+tpgemm_status tpgemm_cp_roundtrip_repeat(uint32_t* tmem_out, const void* smem_image,
+                                         size_t image_bytes, const tpgemm_cp_desc* d,
+                                         uint32_t fill_base, int ncols, int repeat, int ctas,
+                                         void* stream);
+
 /* Static English name of a status. Never NULL. */
 const char* tpgemm_status_string(tpgemm_status s);
 

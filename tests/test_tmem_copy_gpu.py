@@ -147,3 +147,32 @@ def test_cp_cta_group_2_pair(form):
     w0 = random_words(rows, 2 * bits // 32, seed=995 + form)
     w1 = random_words(rows, 2 * bits // 32, seed=996 + form)
     roundtrip(w0, words2=w1, swz=ocp.SWIZZLE_128B, lanes=lanes, shape=shape, cta_group=2)
+
+
+@pytest.mark.parametrize("form,cta_group", [(0, 1), (5, 1), (0, 2), (4, 2)],
+                         ids=["128x256b", "32x128b_warpx4", "pair_128x256b", "pair_64x128b_01_23"])
+def test_cp_repeat_many_ctas(form, cta_group):
+    # Several CTAs (pairs) at once, each issuing its copy three times: every
+    # CTA ends with the image of one copy.
+    shape, lanes, rows, bits = FORMS[form]
+    swz = ocp.SWIZZLE_128B
+    words = [random_words(rows, 4 * bits // 32, seed=1000 + form + k) for k in range(cta_group)]
+    nw = words[0].shape[1]
+    lbo, sbo = layout(swz, rows, nw // 4)
+    nbytes = image_size(words[0].shape, swz, lbo, sbo, 0)
+    rng = np.random.default_rng(form)
+    imgs = [ocp.smem_image(w, swz, lbo, sbo, 0, nbytes, rng.integers(0, 256, nbytes, dtype=np.uint8))
+            for w in words]
+    image = torch.from_numpy(np.concatenate(imgs)).cuda()
+    ctas, ncols = 6 if cta_group == 2 else 5, 32 * ((nw + 31) // 32)
+    out = torch.empty(ctas * 128 * ncols, dtype=torch.int32, device="cuda")
+    d = tp.cp_desc(rows, nw * 32, swizzle=swz, lbo=lbo, sbo=sbo, lanes=lanes, shape=shape,
+                   cta_group=cta_group)
+    st = tp.tpgemm_cp_roundtrip_repeat(out, image, nbytes, d, 11, ncols, 3, ctas)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK
+    got = out.cpu().numpy().view(np.uint32).reshape(ctas, 128, ncols)
+    for k in range(ctas):
+        exp = ocp.tmem_image(words[k % cta_group], lanes, 0, 0, ncols, 11)
+        assert np.array_equal(got[k], exp), f"CTA {k}"

@@ -120,6 +120,9 @@ def _load():
         lib.tpgemm_cp_roundtrip.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
                                             ctypes.c_uint32, ci, vp]
         lib.tpgemm_cp_roundtrip.restype = ci
+        lib.tpgemm_cp_roundtrip_repeat.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
+                                                   ctypes.c_uint32, ci, ci, ci, vp]
+        lib.tpgemm_cp_roundtrip_repeat.restype = ci
         _lib = lib
         return lib
 
@@ -239,6 +242,15 @@ def tpgemm_cp_roundtrip(tmem_out, smem_image, image_bytes, desc: CpDesc, fill_ba
     return int(_load().tpgemm_cp_roundtrip(_ptr(tmem_out), _ptr(smem_image), int(image_bytes),
                                            ctypes.byref(desc), int(fill_base) & 0xFFFFFFFF,
                                            int(ncols), _stream(stream)))
+
+
+def tpgemm_cp_roundtrip_repeat(tmem_out, smem_image, image_bytes, desc: CpDesc, fill_base, ncols,
+                               repeat, ctas, stream=None) -> int:
+    """The round trip on `ctas` CTAs, each issuing the planned copy `repeat` times."""
+    return int(_load().tpgemm_cp_roundtrip_repeat(_ptr(tmem_out), _ptr(smem_image),
+                                                  int(image_bytes), ctypes.byref(desc),
+                                                  int(fill_base) & 0xFFFFFFFF, int(ncols),
+                                                  int(repeat), int(ctas), _stream(stream)))
 
 
 def tpgemm_version() -> str:

@@ -303,6 +303,7 @@ struct CpKernelParams {
     uint32_t image_words;  // 16-byte words of one CTA's image
     uint32_t fill_base;
     int n, form, ncols, alloc_cols;
+    int repeat;  // times the whole instruction list is issued before the commit
     uint32_t smem_off[kMaxCpInstr];
     uint32_t taddr[kMaxCpInstr];
 };
@@ -327,6 +328,8 @@ __global__ void __launch_bounds__(kCpThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rank = CG == 2 ? int(cluster_ctarank()) : 0;
+    // CTA pairs: each CTA of a pair has its own image; all pairs (or all single
+    // CTAs) share the images and write their own rows of out.
 
     if (warp == 0) {
         tmem_alloc<CG>(&tmem_base, uint32_t(p.alloc_cols));
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kCpThreads, 1)
     }
     // The image, with 16-byte loads and stores; then made visible to the async
     // proxy that tcgen05.cp reads through.
-    const uint4* src = image + size_t(rank) * p.image_words;
+    const uint4* src = image + size_t(CG == 2 ? rank : 0) * p.image_words;
     uint4* dst = reinterpret_cast<uint4*>(buf);
     for (uint32_t i = threadIdx.x; i < p.image_words; i += kCpThreads) dst[i] = src[i];
     fence_proxy_async_smem();
@@ -370,8 +373,10 @@ __global__ void __launch_bounds__(kCpThreads, 1)
     // One thread issues the planned instructions and commits them.
     if (threadIdx.x == 0 && rank == 0) {
         const uint32_t base = smem_u32(buf);
-        for (int i = 0; i < p.n; ++i)
-            tc_cp<CG>(p.form, tmem + p.taddr[i], smem_desc_with_addr(p.desc, base + p.smem_off[i]));
+        for (int k = 0; k < p.repeat; ++k)
+            for (int i = 0; i < p.n; ++i)
+                tc_cp<CG>(p.form, tmem + p.taddr[i],
+                          smem_desc_with_addr(p.desc, base + p.smem_off[i]));
         if (CG == 2)
             tc_commit_pair_multicast(&bar, 0x3);
         else
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(kCpThreads, 1)
     }
     tc_fence_after_sync();
     if (ok) {
-        uint32_t* o = out + (size_t(rank) * 128 + row) * size_t(p.ncols);
+        uint32_t* o = out + (size_t(blockIdx.x) * 128 + row) * size_t(p.ncols);
         for (int c = 0; c < p.ncols; c += 8) {
             uint32_t v[8];
             tmem_ld_32x32b_x8(tmem + lane_base + uint32_t(c), v);
@@ -508,6 +513,14 @@ tpgemm_status tpgemm_cp_plan(const tpgemm_cp_desc* d, char* buf, int buflen) {
 tpgemm_status tpgemm_cp_roundtrip(uint32_t* tmem_out, const void* smem_image, size_t image_bytes,
                                   const tpgemm_cp_desc* d, uint32_t fill_base, int ncols,
                                   void* stream) {
+    return tpgemm_cp_roundtrip_repeat(tmem_out, smem_image, image_bytes, d, fill_base, ncols, 1,
+                                      d ? d->cta_group : 1, stream);
+}
+
+tpgemm_status tpgemm_cp_roundtrip_repeat(uint32_t* tmem_out, const void* smem_image,
+                                         size_t image_bytes, const tpgemm_cp_desc* d,
+                                         uint32_t fill_base, int ncols, int repeat, int ctas,
+                                         void* stream) {
     using namespace tpg;
     set_error_detail("");
     if (!tmem_out || !smem_image) return cp_fail(TPGEMM_ERR_NULL, nullptr, "null device pointer");
@@ -523,6 +536,12 @@ tpgemm_status tpgemm_cp_roundtrip(uint32_t* tmem_out, const void* smem_image, si
     static thread_local CpPlan plan;
     tpgemm_status s = build_plan(d, &plan, nullptr);
     if (s != TPGEMM_OK) return s;
+    if (repeat < 1 || repeat > (1 << 20))
+        return cp_fail(TPGEMM_ERR_SHAPE, nullptr, "repeat=%d must be in 1..2^20", repeat);
+    if (ctas < 1 || ctas > 65536 || ctas % d->cta_group)
+        return cp_fail(TPGEMM_ERR_SHAPE, nullptr,
+                       "ctas=%d must be in 1..65536 and a multiple of cta_group %d", ctas,
+                       d->cta_group);
     if (plan.max_byte > image_bytes)
         return cp_fail(TPGEMM_ERR_SHAPE, nullptr,
                        "the copy reads up to byte %u of a %zu-byte image", plan.max_byte,
@@ -545,6 +564,7 @@ tpgemm_status tpgemm_cp_roundtrip(uint32_t* tmem_out, const void* smem_image, si
     kp.image_words = uint32_t(image_bytes / 16);
     kp.fill_base = fill_base;
     kp.n = plan.n;
+    kp.repeat = repeat;
     kp.form = plan.form;
     kp.ncols = ncols;
     kp.alloc_cols = 32;
@@ -562,7 +582,7 @@ tpgemm_status tpgemm_cp_roundtrip(uint32_t* tmem_out, const void* smem_image, si
         return cp_fail(TPGEMM_ERR_LAUNCH, nullptr, "copy kernel attribute: %s",
                        cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(d->cta_group));
+    cfg.gridDim = dim3(unsigned(ctas));
     cfg.blockDim = dim3(kCpThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
