@@ -292,6 +292,39 @@ tpgemm_status tpgemm_cp_roundtrip_repeat(uint32_t* tmem_out, const void* smem_im
                                          uint32_t fill_base, int ncols, int repeat, int ctas,
                                          void* stream);
 
+/*
+ * ------------------------------------------------------------------------
+ * Tensor memory <-> registers (tcgen05.st / tcgen05.ld), the tmem<->local copy
+ * of the page "TVM TIRx copy_async -> tcgen05_ldst": one warpgroup moves a
+ * 128-lane x `cols`-column tile between tensor memory and its registers, `cols`
+ * registers per thread. Shapes (register of thread t of a warp, in the warp's
+ * 32 lanes; two issues of 16 lanes each, lanes +0 and +16, for the .16x*b
+ * shapes, registers [0, cols/2) then [cols/2, cols)):
+ *   .32x32b   thread t -> lane t, register j -> column j
+ *   .16x64b   16 lanes x 2 columns per repeat
+ *   .16x128b  16 lanes x 4 columns per repeat
+ *   .16x256b  16 lanes x 8 columns per repeat; within one repeat, register s of
+ *             thread t at lane t/4 + 8 (s/2), column 2 (t%4) + s%2 (the m16n8
+ *             accumulator fragment of the mma.sync gemm page, section 三 D_FRAG)
+ */
+typedef enum {
+    TPGEMM_TMEM_32x32b = 0,
+    TPGEMM_TMEM_16x64b = 1,
+    TPGEMM_TMEM_16x128b = 2,
+    TPGEMM_TMEM_16x256b = 3
+} tpgemm_tmem_shape;
+
+/* Round trip, for tests: fill tensor-memory columns [0, 32) of all 128 lanes
+ * with fill_base + 65536 lane + col, store regs_in ([128 threads][cols] uint32,
+ * device) with st_shape at column tmem_col, read the 32 columns back with
+ * .32x32b into tmem_out ([128][32]), then load with ld_shape into regs_out
+ * ([128][cols]). cols: 2, 4, 8 or 16 (at least 2 / 4 / 8 for .16x64b / 128b /
+ * 256b); tmem_col: a multiple of 8 with tmem_col + cols <= 32. */
+tpgemm_status tpgemm_tmem_ldst_roundtrip(uint32_t* regs_out, uint32_t* tmem_out,
+                                        const uint32_t* regs_in, tpgemm_tmem_shape st_shape,
+                                        tpgemm_tmem_shape ld_shape, int cols, int tmem_col,
+                                        uint32_t fill_base, void* stream);
+
 /* Static English name of a status. Never NULL. */
 const char* tpgemm_status_string(tpgemm_status s);
 

@@ -250,3 +250,55 @@ def test_oracle_tmem_image_fill_and_replicas():
     for q in range(4):
         assert np.array_equal(out[32 * q: 32 * q + 32, 8:12], words)
     assert out[5, 0] == 7 + 5 * 65536 and out[127, 31] == 7 + 127 * 65536 + 31
+
+
+# ------------------------------------------- tensor memory <-> registers maps
+from oracle import tmem_frag as ofr  # noqa: E402
+
+LDST_CASES = [(s, c) for s in range(4) for c in (2, 4, 8, 16)
+              if c >= {0: 1, 1: 2, 2: 4, 3: 8}[s]]
+
+
+@pytest.mark.parametrize("shape,cols", [c for c in LDST_CASES if c[0] != ofr.S16x64b])
+def test_ldst_map_is_a_bijection_onto_the_footprint(shape, cols):
+    cells = {ofr.cell(shape, cols, t, j) for t in range(32) for j in range(cols)}
+    assert cells == {(lane, c) for lane in range(32) for c in range(cols)}
+
+
+def test_ldst_16x64b_map_is_declared_unpinned():
+    with pytest.raises(ValueError):
+        ofr.cell(ofr.S16x64b, 2, 0, 0)
+
+
+def test_ldst_16x256b_is_the_mma_accumulator_fragment():
+    # The synchronous gemm page, section 三: thread `lane` holds D registers
+    # c_id = 2 rM + rN at M = lane // 4 + 8 rM, N = 2 (lane % 4) + rN.
+    for lane in range(32):
+        for rM in range(2):
+            for rN in range(2):
+                assert ofr.cell(ofr.S16x256b, 8, lane, 2 * rM + rN) == \
+                    (lane // 4 + 8 * rM, 2 * (lane % 4) + rN)
+    # the second issue of a warp covers its lanes 16..31 with registers 4..7
+    assert ofr.cell(ofr.S16x256b, 8, 5, 6) == (16 + 1 + 8, 2 * 1)
+
+
+def test_ldst_32x32b_is_the_page_3_demo_layout():
+    # 128 x 8 fp16 (4 x 32-bit columns): element (row, col) in thread `row`,
+    # register `col`, lane `row`, column `col`.
+    for t in range(32):
+        for j in range(4):
+            assert ofr.cell(ofr.S32x32b, 4, t, j) == (t, j)
+
+
+def test_ldst_roundtrip_rejections():
+    base = 0x7F0000000000
+    def f(*a):
+        return tp.tpgemm_tmem_ldst_roundtrip(*a, 0)
+    assert f(None, base, base, 0, 0, 8, 0, 0) == tp.TPGEMM_ERR_NULL
+    assert f(base + 4, base, base, 0, 0, 8, 0, 0) == tp.TPGEMM_ERR_ALIGN
+    assert f(base, base, base, 3, 0, 4, 0, 0) == tp.TPGEMM_ERR_SHAPE
+    assert "16x256b moves at least 8 columns" in tp.tpgemm_last_error_detail()
+    assert f(base, base, base, 0, 0, 6, 0, 0) == tp.TPGEMM_ERR_SHAPE
+    assert f(base, base, base, 0, 0, 16, 24, 0) == tp.TPGEMM_ERR_SHAPE
+    assert f(base, base, base, 0, 0, 8, 4, 0) == tp.TPGEMM_ERR_SHAPE
+    assert f(base, base, base, 5, 0, 8, 0, 0) == tp.TPGEMM_ERR_SHAPE

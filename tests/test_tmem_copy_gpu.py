@@ -176,3 +176,76 @@ def test_cp_repeat_many_ctas(form, cta_group):
     for k in range(ctas):
         exp = ocp.tmem_image(words[k % cta_group], lanes, 0, 0, ncols, 11)
         assert np.array_equal(got[k], exp), f"CTA {k}"
+
+
+# ------------------------------------------- tensor memory <-> registers
+from oracle import tmem_frag as ofr  # noqa: E402
+
+LDST = [(a, b, c) for a in range(4) for b in range(4) for c in (2, 4, 8, 16)
+        if c >= max({0: 1, 1: 2, 2: 4, 3: 8}[a], {0: 1, 1: 2, 2: 4, 3: 8}[b])]
+
+
+@pytest.mark.parametrize("st,ld,cols", LDST,
+                         ids=[f"st{ofr.NAMES[a]}-ld{ofr.NAMES[b]}-c{c}" for a, b, c in LDST])
+def test_tmem_ldst_roundtrip(st, ld, cols):
+    tmem_col = 8 if cols <= 16 and cols + 8 <= 32 else 0
+    rng = np.random.default_rng(31 * st + 7 * ld + cols)
+    regs = rng.integers(0, 2 ** 32, (128, cols), dtype=np.uint64).astype(np.uint32)
+    fill = int(rng.integers(0, 2 ** 32))
+    regs_d = torch.from_numpy(regs.view(np.int32)).cuda()
+    regs_out = torch.empty(128 * cols, dtype=torch.int32, device="cuda")
+    tmem_out = torch.empty(128 * 32, dtype=torch.int32, device="cuda")
+    s = tp.tpgemm_tmem_ldst_roundtrip(regs_out, tmem_out, regs_d, st, ld, cols, tmem_col, fill)
+    assert s == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    got_tmem = tmem_out.cpu().numpy().view(np.uint32).reshape(128, 32)
+    got_regs = regs_out.cpu().numpy().view(np.uint32).reshape(128, cols)
+    fill_img = ofr.fill_pattern(fill)
+    if st != ofr.S16x64b:
+        exp_tmem = ofr.store(fill_img, regs, st, cols, tmem_col)
+        bad = np.argwhere(got_tmem != exp_tmem)
+        assert bad.size == 0, f"{len(bad)} cells differ, first {bad[:4].tolist()}"
+    else:
+        # .16x64b (thread map unpinned): outside the footprint nothing changes,
+        # and each warp's 16-lane block holds exactly what the warp stored there.
+        outside = np.ones((128, 32), bool)
+        outside[:, tmem_col: tmem_col + cols] = False
+        assert np.array_equal(got_tmem[outside], fill_img[outside])
+        for w in range(4):
+            for slab in range(2):
+                lanes, _ = ofr.slab_cells(st, cols, slab)
+                block = got_tmem[32 * w + lanes.start: 32 * w + lanes.stop,
+                                 tmem_col: tmem_col + cols]
+                stored = regs[32 * w: 32 * w + 32, ofr.slab_regs(st, cols, slab).start:
+                              ofr.slab_regs(st, cols, slab).stop]
+                assert np.array_equal(np.sort(block, axis=None), np.sort(stored, axis=None))
+    if ld != ofr.S16x64b:
+        assert np.array_equal(got_regs, ofr.load(got_tmem, ld, cols, tmem_col))
+    else:
+        # each warp's registers of one issue are its 16-lane block, permuted
+        for w in range(4):
+            for slab in range(2):
+                lanes, _ = ofr.slab_cells(ld, cols, slab)
+                block = got_tmem[32 * w + lanes.start: 32 * w + lanes.stop,
+                                 tmem_col: tmem_col + cols]
+                r = ofr.slab_regs(ld, cols, slab)
+                loaded = got_regs[32 * w: 32 * w + 32, r.start: r.stop]
+                assert np.array_equal(np.sort(block, axis=None), np.sort(loaded, axis=None))
+    if st == ld:
+        assert np.array_equal(got_regs, regs)
+
+
+def test_tmem_ldst_page_demo_128x8_fp16():
+    # The page's demonstration: a warpgroup round-trips a 128 x 8 fp16 tile
+    # through tensor memory with .32x32b.x4 both ways and gets it back exactly;
+    # row r of the tile is lane r, fp16 pair c is column c.
+    tile = torch.randn(128, 8).half()
+    words = tile.view(torch.int32).contiguous()  # 128 x 4 words
+    regs_out = torch.empty(128 * 4, dtype=torch.int32, device="cuda")
+    tmem_out = torch.empty(128 * 32, dtype=torch.int32, device="cuda")
+    s = tp.tpgemm_tmem_ldst_roundtrip(regs_out, tmem_out, words.cuda(), 0, 0, 4, 0, 0)
+    assert s == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    back = regs_out.cpu().view(128, 4).view(torch.float16)
+    assert torch.equal(back, tile)
+    assert torch.equal(tmem_out.cpu().view(128, 32)[:, :4].contiguous().view(torch.float16), tile)

@@ -52,6 +52,11 @@ TPGEMM_CP_128x128b = 3
 TPGEMM_CP_64x128b_WARPX2_02_13 = 4
 TPGEMM_CP_64x128b_WARPX2_01_23 = 5
 TPGEMM_CP_32x128b_WARPX4 = 6
+# tpgemm_tmem_shape
+TPGEMM_TMEM_32x32b = 0
+TPGEMM_TMEM_16x64b = 1
+TPGEMM_TMEM_16x128b = 2
+TPGEMM_TMEM_16x256b = 3
 # tpgemm_cp_lanes
 TPGEMM_CP_LANES_ROWS = 0
 TPGEMM_CP_LANES_QUADRANTS = 1
@@ -123,6 +128,9 @@ def _load():
         lib.tpgemm_cp_roundtrip_repeat.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
                                                    ctypes.c_uint32, ci, ci, ci, vp]
         lib.tpgemm_cp_roundtrip_repeat.restype = ci
+        lib.tpgemm_tmem_ldst_roundtrip.argtypes = [vp, vp, vp, ci, ci, ci, ci, ctypes.c_uint32,
+                                                   vp]
+        lib.tpgemm_tmem_ldst_roundtrip.restype = ci
         _lib = lib
         return lib
 
@@ -251,6 +259,15 @@ def tpgemm_cp_roundtrip_repeat(tmem_out, smem_image, image_bytes, desc: CpDesc, 
                                                   int(image_bytes), ctypes.byref(desc),
                                                   int(fill_base) & 0xFFFFFFFF, int(ncols),
                                                   int(repeat), int(ctas), _stream(stream)))
+
+
+def tpgemm_tmem_ldst_roundtrip(regs_out, tmem_out, regs_in, st_shape, ld_shape, cols, tmem_col,
+                               fill_base, stream=None) -> int:
+    """Registers -> tensor memory (st_shape) -> .32x32b read-back and ld_shape load."""
+    return int(_load().tpgemm_tmem_ldst_roundtrip(_ptr(regs_out), _ptr(tmem_out), _ptr(regs_in),
+                                                  int(st_shape), int(ld_shape), int(cols),
+                                                  int(tmem_col), int(fill_base) & 0xFFFFFFFF,
+                                                  _stream(stream)))
 
 
 def tpgemm_version() -> str:

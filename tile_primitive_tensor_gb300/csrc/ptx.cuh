@@ -369,6 +369,47 @@ __device__ __forceinline__ void tc_cp(int form, uint32_t taddr, uint64_t sdesc) 
 #undef TPG_CP
 }
 
+// tcgen05.st / tcgen05.ld of any shape with N registers (N = 1, 2, 4, 8, 16):
+// SHAPE_NUM is the literal "<shape>.x<num>" (e.g. "16x256b.x1"); R an array of
+// uint32 registers. The caller issues tcgen05.wait::st / wait::ld.
+#define TPG_TMEM_ARGS_ST1 "{%1}"
+#define TPG_TMEM_ARGS_ST2 "{%1, %2}"
+#define TPG_TMEM_ARGS_ST4 "{%1, %2, %3, %4}"
+#define TPG_TMEM_ARGS_ST8 "{%1, %2, %3, %4, %5, %6, %7, %8}"
+#define TPG_TMEM_ARGS_ST16 \
+    "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16}"
+#define TPG_TMEM_IN1(R) "r"((R)[0])
+#define TPG_TMEM_IN2(R) TPG_TMEM_IN1(R), "r"((R)[1])
+#define TPG_TMEM_IN4(R) TPG_TMEM_IN2(R), "r"((R)[2]), "r"((R)[3])
+#define TPG_TMEM_IN8(R) TPG_TMEM_IN4(R), "r"((R)[4]), "r"((R)[5]), "r"((R)[6]), "r"((R)[7])
+#define TPG_TMEM_IN16(R)                                                                   \
+    TPG_TMEM_IN8(R), "r"((R)[8]), "r"((R)[9]), "r"((R)[10]), "r"((R)[11]), "r"((R)[12]), \
+        "r"((R)[13]), "r"((R)[14]), "r"((R)[15])
+#define TPG_TMEM_ST(SHAPE_NUM, N, TADDR, R)                                                   \
+    asm volatile("tcgen05.st.sync.aligned." SHAPE_NUM ".b32 [%0], " TPG_TMEM_ARGS_ST##N ";" :: \
+                     "r"(TADDR),                                                              \
+                 TPG_TMEM_IN##N(R)                                                            \
+                 : "memory")
+#define TPG_TMEM_ARGS_LD1 "{%0}, [%1]"
+#define TPG_TMEM_ARGS_LD2 "{%0, %1}, [%2]"
+#define TPG_TMEM_ARGS_LD4 "{%0, %1, %2, %3}, [%4]"
+#define TPG_TMEM_ARGS_LD8 "{%0, %1, %2, %3, %4, %5, %6, %7}, [%8]"
+#define TPG_TMEM_ARGS_LD16 \
+    "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16]"
+#define TPG_TMEM_OUT1(R) "=r"((R)[0])
+#define TPG_TMEM_OUT2(R) TPG_TMEM_OUT1(R), "=r"((R)[1])
+#define TPG_TMEM_OUT4(R) TPG_TMEM_OUT2(R), "=r"((R)[2]), "=r"((R)[3])
+#define TPG_TMEM_OUT8(R) \
+    TPG_TMEM_OUT4(R), "=r"((R)[4]), "=r"((R)[5]), "=r"((R)[6]), "=r"((R)[7])
+#define TPG_TMEM_OUT16(R)                                                                   \
+    TPG_TMEM_OUT8(R), "=r"((R)[8]), "=r"((R)[9]), "=r"((R)[10]), "=r"((R)[11]),             \
+        "=r"((R)[12]), "=r"((R)[13]), "=r"((R)[14]), "=r"((R)[15])
+#define TPG_TMEM_LD(SHAPE_NUM, N, TADDR, R)                                                \
+    asm volatile("tcgen05.ld.sync.aligned." SHAPE_NUM ".b32 " TPG_TMEM_ARGS_LD##N ";"      \
+                 : TPG_TMEM_OUT##N(R)                                                      \
+                 : "r"(TADDR)                                                              \
+                 : "memory")
+
 // -------------------------------------------------- descriptors (tcgen05)
 // Shared-memory matrix descriptor, SWIZZLE_128B, start address 0. Fields:
 // bits 0-13 start address >> 4, 16-29 leading-dimension byte offset >> 4,

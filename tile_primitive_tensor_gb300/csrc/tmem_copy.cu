@@ -408,6 +408,172 @@ __global__ void __launch_bounds__(kCpThreads, 1)
     }
 }
 
+// ---------------------------------------------- tensor memory <-> registers
+// The tmem<->local copy of the page "TVM TIRx copy_async -> tcgen05_ldst": a
+// warpgroup moves a 128-lane x C-column tile between tensor memory and its
+// registers (C per thread). .32x32b covers a warp's 32 lanes in one issue;
+// the .16x{64,128,256}b shapes cover 16 lanes, so each warp issues them twice
+// (lanes +0 and +16, section Algorithm step 3), registers [0, C/2) for the
+// first slab and [C/2, C) for the second.
+template <int C>
+__device__ __forceinline__ void ldst_store(int shape, uint32_t taddr, const uint32_t (&v)[C]) {
+    const uint32_t s16 = 16u << 16;
+    if constexpr (C == 2) {
+        if (shape == TPGEMM_TMEM_32x32b) TPG_TMEM_ST("32x32b.x2", 2, taddr, v);
+        if (shape == TPGEMM_TMEM_16x64b) {
+            TPG_TMEM_ST("16x64b.x1", 1, taddr, v);
+            TPG_TMEM_ST("16x64b.x1", 1, taddr + s16, v + 1);
+        }
+    } else if constexpr (C == 4) {
+        if (shape == TPGEMM_TMEM_32x32b) TPG_TMEM_ST("32x32b.x4", 4, taddr, v);
+        if (shape == TPGEMM_TMEM_16x64b) {
+            TPG_TMEM_ST("16x64b.x2", 2, taddr, v);
+            TPG_TMEM_ST("16x64b.x2", 2, taddr + s16, v + 2);
+        }
+        if (shape == TPGEMM_TMEM_16x128b) {
+            TPG_TMEM_ST("16x128b.x1", 2, taddr, v);
+            TPG_TMEM_ST("16x128b.x1", 2, taddr + s16, v + 2);
+        }
+    } else if constexpr (C == 8) {
+        if (shape == TPGEMM_TMEM_32x32b) TPG_TMEM_ST("32x32b.x8", 8, taddr, v);
+        if (shape == TPGEMM_TMEM_16x64b) {
+            TPG_TMEM_ST("16x64b.x4", 4, taddr, v);
+            TPG_TMEM_ST("16x64b.x4", 4, taddr + s16, v + 4);
+        }
+        if (shape == TPGEMM_TMEM_16x128b) {
+            TPG_TMEM_ST("16x128b.x2", 4, taddr, v);
+            TPG_TMEM_ST("16x128b.x2", 4, taddr + s16, v + 4);
+        }
+        if (shape == TPGEMM_TMEM_16x256b) {
+            TPG_TMEM_ST("16x256b.x1", 4, taddr, v);
+            TPG_TMEM_ST("16x256b.x1", 4, taddr + s16, v + 4);
+        }
+    } else {
+        static_assert(C == 16, "C is 2, 4, 8 or 16");
+        if (shape == TPGEMM_TMEM_32x32b) TPG_TMEM_ST("32x32b.x16", 16, taddr, v);
+        if (shape == TPGEMM_TMEM_16x64b) {
+            TPG_TMEM_ST("16x64b.x8", 8, taddr, v);
+            TPG_TMEM_ST("16x64b.x8", 8, taddr + s16, v + 8);
+        }
+        if (shape == TPGEMM_TMEM_16x128b) {
+            TPG_TMEM_ST("16x128b.x4", 8, taddr, v);
+            TPG_TMEM_ST("16x128b.x4", 8, taddr + s16, v + 8);
+        }
+        if (shape == TPGEMM_TMEM_16x256b) {
+            TPG_TMEM_ST("16x256b.x2", 8, taddr, v);
+            TPG_TMEM_ST("16x256b.x2", 8, taddr + s16, v + 8);
+        }
+    }
+}
+
+template <int C>
+__device__ __forceinline__ void ldst_load(int shape, uint32_t taddr, uint32_t (&v)[C]) {
+    const uint32_t s16 = 16u << 16;
+    if constexpr (C == 2) {
+        if (shape == TPGEMM_TMEM_32x32b) TPG_TMEM_LD("32x32b.x2", 2, taddr, v);
+        if (shape == TPGEMM_TMEM_16x64b) {
+            TPG_TMEM_LD("16x64b.x1", 1, taddr, v);
+            TPG_TMEM_LD("16x64b.x1", 1, taddr + s16, v + 1);
+        }
+    } else if constexpr (C == 4) {
+        if (shape == TPGEMM_TMEM_32x32b) TPG_TMEM_LD("32x32b.x4", 4, taddr, v);
+        if (shape == TPGEMM_TMEM_16x64b) {
+            TPG_TMEM_LD("16x64b.x2", 2, taddr, v);
+            TPG_TMEM_LD("16x64b.x2", 2, taddr + s16, v + 2);
+        }
+        if (shape == TPGEMM_TMEM_16x128b) {
+            TPG_TMEM_LD("16x128b.x1", 2, taddr, v);
+            TPG_TMEM_LD("16x128b.x1", 2, taddr + s16, v + 2);
+        }
+    } else if constexpr (C == 8) {
+        if (shape == TPGEMM_TMEM_32x32b) TPG_TMEM_LD("32x32b.x8", 8, taddr, v);
+        if (shape == TPGEMM_TMEM_16x64b) {
+            TPG_TMEM_LD("16x64b.x4", 4, taddr, v);
+            TPG_TMEM_LD("16x64b.x4", 4, taddr + s16, v + 4);
+        }
+        if (shape == TPGEMM_TMEM_16x128b) {
+            TPG_TMEM_LD("16x128b.x2", 4, taddr, v);
+            TPG_TMEM_LD("16x128b.x2", 4, taddr + s16, v + 4);
+        }
+        if (shape == TPGEMM_TMEM_16x256b) {
+            TPG_TMEM_LD("16x256b.x1", 4, taddr, v);
+            TPG_TMEM_LD("16x256b.x1", 4, taddr + s16, v + 4);
+        }
+    } else {
+        if (shape == TPGEMM_TMEM_32x32b) TPG_TMEM_LD("32x32b.x16", 16, taddr, v);
+        if (shape == TPGEMM_TMEM_16x64b) {
+            TPG_TMEM_LD("16x64b.x8", 8, taddr, v);
+            TPG_TMEM_LD("16x64b.x8", 8, taddr + s16, v + 8);
+        }
+        if (shape == TPGEMM_TMEM_16x128b) {
+            TPG_TMEM_LD("16x128b.x4", 8, taddr, v);
+            TPG_TMEM_LD("16x128b.x4", 8, taddr + s16, v + 8);
+        }
+        if (shape == TPGEMM_TMEM_16x256b) {
+            TPG_TMEM_LD("16x256b.x2", 8, taddr, v);
+            TPG_TMEM_LD("16x256b.x2", 8, taddr + s16, v + 8);
+        }
+    }
+    tmem_ld_wait_all();
+}
+
+constexpr int kLdstCols = 32;  // tensor-memory columns allocated and read back
+
+// One warpgroup: fill columns [0, 32) of all 128 lanes with a known pattern,
+// store the C registers of every thread with st_shape at column tmem_col, read
+// all 32 columns back with .32x32b into tmem_out, then load with ld_shape into
+// regs_out.
+template <int C>
+__global__ void __launch_bounds__(128, 1)
+    ldst_roundtrip_kernel(uint32_t* __restrict__ regs_out, uint32_t* __restrict__ tmem_out,
+                          const uint32_t* __restrict__ regs_in, int st_shape, int ld_shape,
+                          int tmem_col, uint32_t fill_base) {
+    __shared__ uint32_t tmem_base;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t row = uint32_t(threadIdx.x);
+    if (warp == 0) {
+        tmem_alloc<1>(&tmem_base, uint32_t(kLdstCols));
+        tmem_relinquish_alloc_permit<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t warp_base = tmem_base + (uint32_t(warp * 32) << 16);
+    for (int c = 0; c < kLdstCols; c += 8) {
+        uint32_t f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = fill_base + row * 65536u + uint32_t(c + j);
+        tmem_st_32x32b_x8(warp_base + uint32_t(c), f);
+    }
+    tmem_st_wait();
+    uint32_t v[C];
+#pragma unroll
+    for (int j = 0; j < C; ++j) v[j] = regs_in[size_t(row) * C + j];
+    ldst_store<C>(st_shape, warp_base + uint32_t(tmem_col), v);
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    for (int c = 0; c < kLdstCols; c += 8) {
+        uint32_t r[8];
+        tmem_ld_32x32b_x8(warp_base + uint32_t(c), r);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tmem_out[size_t(row) * kLdstCols + c + j] = r[j];
+    }
+    uint32_t w[C];
+    ldst_load<C>(ld_shape, warp_base + uint32_t(tmem_col), w);
+#pragma unroll
+    for (int j = 0; j < C; ++j) regs_out[size_t(row) * C + j] = w[j];
+    (void)lane;
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, uint32_t(kLdstCols));
+    }
+}
+
 int describe(const tpgemm_cp_desc& d, const CpPlan& pl, char* buf, int buflen) {
     if (!buf || buflen <= 0) return 0;
     std::string t;
@@ -596,6 +762,66 @@ tpgemm_status tpgemm_cp_roundtrip_repeat(uint32_t* tmem_out, const void* smem_im
     e = cudaLaunchKernelEx(&cfg, kernel, tmem_out, static_cast<const uint4*>(smem_image), kp);
     if (e != cudaSuccess)
         return cp_fail(TPGEMM_ERR_LAUNCH, nullptr, "copy kernel launch: %s",
+                       cudaGetErrorString(e));
+    return TPGEMM_OK;
+}
+
+tpgemm_status tpgemm_tmem_ldst_roundtrip(uint32_t* regs_out, uint32_t* tmem_out,
+                                        const uint32_t* regs_in, tpgemm_tmem_shape st_shape,
+                                        tpgemm_tmem_shape ld_shape, int cols, int tmem_col,
+                                        uint32_t fill_base, void* stream) {
+    using namespace tpg;
+    set_error_detail("");
+    if (!regs_out || !tmem_out || !regs_in)
+        return cp_fail(TPGEMM_ERR_NULL, nullptr, "null device pointer");
+    if ((reinterpret_cast<uintptr_t>(regs_out) | reinterpret_cast<uintptr_t>(tmem_out) |
+         reinterpret_cast<uintptr_t>(regs_in)) & 15)
+        return cp_fail(TPGEMM_ERR_ALIGN, nullptr, "device pointers must be 16-byte aligned");
+    auto min_cols = [](int shape) {
+        switch (shape) {
+            case TPGEMM_TMEM_32x32b: return 1;
+            case TPGEMM_TMEM_16x64b: return 2;
+            case TPGEMM_TMEM_16x128b: return 4;
+            case TPGEMM_TMEM_16x256b: return 8;
+        }
+        return 0;
+    };
+    const char* names[4] = {"32x32b", "16x64b", "16x128b", "16x256b"};
+    for (int sh : {int(st_shape), int(ld_shape)}) {
+        if (sh < 0 || sh > 3)
+            return cp_fail(TPGEMM_ERR_SHAPE, nullptr, "unknown tensor-memory shape %d", sh);
+        if (cols < min_cols(sh))
+            return cp_fail(TPGEMM_ERR_SHAPE, nullptr,
+                           "%s moves at least %d columns per warp; cols=%d", names[sh],
+                           min_cols(sh), cols);
+    }
+    if (cols != 2 && cols != 4 && cols != 8 && cols != 16)
+        return cp_fail(TPGEMM_ERR_SHAPE, nullptr, "cols=%d must be 2, 4, 8 or 16", cols);
+    if (tmem_col < 0 || tmem_col % 8 || tmem_col + cols > kLdstCols)
+        return cp_fail(TPGEMM_ERR_SHAPE, nullptr,
+                       "tmem_col=%d must be a multiple of 8 with tmem_col + cols <= %d",
+                       tmem_col, kLdstCols);
+    int dev = 0, major = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return cp_fail(TPGEMM_ERR_ARCH, nullptr, "no CUDA device available");
+    if (major != 10)
+        return cp_fail(TPGEMM_ERR_ARCH, nullptr, "tcgen05 needs compute capability 10.x");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int a = int(st_shape), b = int(ld_shape);
+    switch (cols) {
+        case 2: ldst_roundtrip_kernel<2><<<1, 128, 0, st>>>(regs_out, tmem_out, regs_in, a, b,
+                                                             tmem_col, fill_base); break;
+        case 4: ldst_roundtrip_kernel<4><<<1, 128, 0, st>>>(regs_out, tmem_out, regs_in, a, b,
+                                                             tmem_col, fill_base); break;
+        case 8: ldst_roundtrip_kernel<8><<<1, 128, 0, st>>>(regs_out, tmem_out, regs_in, a, b,
+                                                             tmem_col, fill_base); break;
+        default: ldst_roundtrip_kernel<16><<<1, 128, 0, st>>>(regs_out, tmem_out, regs_in, a,
+                                                               b, tmem_col, fill_base); break;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cp_fail(TPGEMM_ERR_LAUNCH, nullptr, "ld/st kernel launch: %s",
                        cudaGetErrorString(e));
     return TPGEMM_OK;
 }
