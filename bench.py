@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--primitive", choices=["tcgen05_cp"], default=None,
+    ap.add_argument("--primitive", choices=["tcgen05_cp", "vcopy"], default=None,
                     help="measure a standalone primitive instead of the GEMM step")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -467,6 +467,82 @@ def run_primitive_cp(args):
     }
 
 
+# ------------------------------------------- vectorised global <-> shared copy
+def run_primitive_vcopy(args):
+    """HBM round trip through shared memory with the vectorised copy.
+
+    Every CTA (a CTA scope of 256 threads) moves one 64 x 512 fp16 region
+    (64 KB) of a 1 GiB buffer global -> shared -> global; bytes = read + write,
+    against the measured HBM copy bandwidth (which counts the same way)."""
+    import numpy as np
+    import torch
+
+    import tile_primitive_tensor_gb300 as tp
+    from oracle import vec_copy as ovc
+
+    dev = torch.device("cuda", 0)
+    rows, cols, eb, threads = 64, 512, 2, 256
+    region = rows * cols
+    total = 1 << 30
+    ctas = total // (region * eb)
+    src = torch.empty(total, dtype=torch.uint8, device=dev).random_(0, 256)
+    dst = torch.empty_like(src)
+    d = tp.vcopy_desc(rows, cols, eb, threads=threads)
+    plan = tp.tpgemm_vcopy_plan(d)[1]
+
+    def go():
+        st = tp.tpgemm_vcopy_roundtrip(dst, src, total, d, ctas, region)
+        if st != 0:
+            raise RuntimeError(f"tpgemm_vcopy_roundtrip: {tp.tpgemm_last_error_detail()}")
+
+    for _ in range(max(3, args.warmup)):
+        go()
+    torch.cuda.synchronize()
+    if not torch.equal(dst, src):
+        raise RuntimeError("vectorised copy round trip differs from its source")
+    sampler = ClockSampler(None)
+    sampler.start()
+    time.sleep(0.4)
+    t0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        go()
+    e1.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = 2 * total / (ms * 1e-3) / 1e9
+    peaks, src_kind = load_peaks()
+    # The oracle beside it: the identity copy of one CTA's region on the host.
+    rng = np.random.default_rng(0)
+    host = rng.integers(0, 256, region * eb, dtype=np.uint8)
+    dd = {"rows": rows, "cols": cols, "elem_bytes": eb, "g_row_stride": cols, "g_offset": 0,
+          "s_row_stride": cols, "s_offset": 0, "s_swizzle": 0}
+    n, c0 = 0, time.perf_counter()
+    while time.perf_counter() - c0 < 2.0:
+        ovc.expected_dst(host, host, dd, 1, 0)
+        n += 1
+    cpu_s = (time.perf_counter() - c0) / n
+    return {
+        "metric": "vectorised global->shared->global copy bandwidth (bytes read + written)",
+        "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "dtype": "f16", "data": "synthetic (random bytes)",
+        "config": {"workload": "vcopy_64x512_f16_cta256", "buffer_bytes": total, "ctas": ctas,
+                   "plan": plan, "l2": "inputs larger than L2, no flush"},
+        "clocks": sampler.summary(t0, t1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "peak_kind": f"{src_kind} HBM copy bandwidth", "traffic": None},
+        "cpu_baseline": {"value": round(2 * region * eb / cpu_s / 1e9, 4), "unit": "GB/s",
+                         "cores": 1, "kind": "oracle",
+                         "sample": f"{n} host copies of one CTA's region (oracle.vec_copy)"},
+        "gpu_launches": args.steps,
+    }
+
+
 # ---------------------------------------------------------- reference arm
 def run_reference(args):
     w = wl.BY_NAME[args.workload]
@@ -522,9 +598,10 @@ def main():
             return 0
         print(json.dumps(run_reference(args)), flush=True)
         return 0
-    if args.primitive == "tcgen05_cp":
+    if args.primitive:
         if rank == 0:
-            print(json.dumps(run_primitive_cp(args)), flush=True)
+            fn = {"tcgen05_cp": run_primitive_cp, "vcopy": run_primitive_vcopy}[args.primitive]
+            print(json.dumps(fn(args)), flush=True)
         return 0
     if world > 1:
         import torch

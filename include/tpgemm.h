@@ -325,6 +325,49 @@ tpgemm_status tpgemm_tmem_ldst_roundtrip(uint32_t* regs_out, uint32_t* tmem_out,
                                         tpgemm_tmem_shape ld_shape, int cols, int tmem_col,
                                         uint32_t fill_base, void* stream);
 
+/*
+ * ------------------------------------------------------------------------
+ * Vectorised global <-> shared copy, the gmem_smem path of the vec_auto copy
+ * on the page "TVM TIRx CUDA 向量化内存拷贝实战 (gmem_smem)". A region of rows x
+ * cols elements moves between a global buffer (row stride g_row_stride,
+ * starting g_offset elements in) and a shared buffer (row stride
+ * s_row_stride, starting s_offset elements in), by `threads` threads:
+ *   - partition [outer, threads, vec]: the region's elements in row order,
+ *     thread tid of round f copying the vec elements from (f threads + tid) vec;
+ *   - vec: the widest of 16, 8, 4, 2, 1 bytes (whole elements) that divides the
+ *     contiguous tail (a row, or the whole region when both sides are dense
+ *     along rows), the elements per thread, both row strides and both offsets;
+ *   - a swizzled shared buffer keeps each vector inside one 16-byte chunk and
+ *     XORs byte offset bits [4, 4 + log2(S / 16)) with bits [7, ...), S = 32,
+ *     64 or 128, offsets counted from the start of the shared buffer.
+ * The gate: threads is 1, 32, 128 or a CTA of 64..1024 (whole warps), and the
+ * element count is a multiple of threads (otherwise TPGEMM_ERR_SHAPE).
+ */
+typedef struct {
+    int rows, cols;               /* region, elements                     */
+    int elem_bytes;               /* 1, 2, 4 or 8                          */
+    int64_t g_row_stride;         /* global row stride, elements (>= cols) */
+    int64_t g_offset;             /* region start in the global buffer     */
+    int s_row_stride;             /* shared row stride, elements (>= cols) */
+    int s_offset;                 /* region start in the shared buffer     */
+    tpgemm_cp_swizzle s_swizzle;  /* shared layout                          */
+    int threads;                  /* the copying scope                     */
+} tpgemm_vcopy_desc;
+
+/* The plan as text ("vec_bytes=16 vec=4 outer=8 threads=32 ..."), or the
+ * rejection reason (also in tpgemm_last_error_detail()). */
+tpgemm_status tpgemm_vcopy_plan(const tpgemm_vcopy_desc* d, char* buf, int buflen);
+
+/* Round trip global -> shared -> global on `ctas` CTAs of d->threads threads:
+ * CTA k copies the region starting cta_stride * k elements into src (device,
+ * buffer_bytes) through its shared buffer into the same place of dst (device,
+ * buffer_bytes); nothing else of dst is written. smem_out (device, may be
+ * NULL): each CTA's shared buffer after the first copy, zero outside the
+ * region, at smem_out + k * (shared bytes of the plan). */
+tpgemm_status tpgemm_vcopy_roundtrip(void* dst, const void* src, size_t buffer_bytes,
+                                     const tpgemm_vcopy_desc* d, int ctas, int64_t cta_stride,
+                                     void* smem_out, void* stream);
+
 /* Static English name of a status. Never NULL. */
 const char* tpgemm_status_string(tpgemm_status s);
 

@@ -131,6 +131,11 @@ def _load():
         lib.tpgemm_tmem_ldst_roundtrip.argtypes = [vp, vp, vp, ci, ci, ci, ci, ctypes.c_uint32,
                                                    vp]
         lib.tpgemm_tmem_ldst_roundtrip.restype = ci
+        lib.tpgemm_vcopy_plan.argtypes = [ctypes.POINTER(VcopyDesc), ctypes.c_char_p, ci]
+        lib.tpgemm_vcopy_plan.restype = ci
+        lib.tpgemm_vcopy_roundtrip.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(VcopyDesc),
+                                               ci, i64, vp, vp]
+        lib.tpgemm_vcopy_roundtrip.restype = ci
         _lib = lib
         return lib
 
@@ -221,6 +226,35 @@ def tpgemm_describe_plan(M, N, K, transA, transB, dtype, beta, path=TPGEMM_PATH_
                                           int(bool(transB)), int(dtype), float(beta), int(path),
                                           buf, 512))
     return st, buf.value.decode()
+
+
+class VcopyDesc(ctypes.Structure):
+    """tpgemm_vcopy_desc: a global region, its shared placement and the copying scope."""
+    _fields_ = [("rows", ctypes.c_int), ("cols", ctypes.c_int), ("elem_bytes", ctypes.c_int),
+                ("g_row_stride", ctypes.c_int64), ("g_offset", ctypes.c_int64),
+                ("s_row_stride", ctypes.c_int), ("s_offset", ctypes.c_int),
+                ("s_swizzle", ctypes.c_int), ("threads", ctypes.c_int)]
+
+
+def vcopy_desc(rows, cols, elem_bytes, *, g_row_stride=None, g_offset=0, s_row_stride=None,
+               s_offset=0, s_swizzle=0, threads=32) -> VcopyDesc:
+    return VcopyDesc(int(rows), int(cols), int(elem_bytes),
+                     int(cols if g_row_stride is None else g_row_stride), int(g_offset),
+                     int(cols if s_row_stride is None else s_row_stride), int(s_offset),
+                     int(s_swizzle), int(threads))
+
+
+def tpgemm_vcopy_plan(desc: VcopyDesc):
+    buf = ctypes.create_string_buffer(512)
+    st = int(_load().tpgemm_vcopy_plan(ctypes.byref(desc), buf, 512))
+    return st, buf.value.decode()
+
+
+def tpgemm_vcopy_roundtrip(dst, src, buffer_bytes, desc: VcopyDesc, ctas=1, cta_stride=0,
+                           smem_out=None, stream=None) -> int:
+    return int(_load().tpgemm_vcopy_roundtrip(_ptr(dst), _ptr(src), int(buffer_bytes),
+                                              ctypes.byref(desc), int(ctas), int(cta_stride),
+                                              _ptr(smem_out), _stream(stream)))
 
 
 def cp_desc(rows, row_bits, *, swizzle=TPGEMM_CP_SWIZZLE_NONE, lbo=0, sbo=0, smem_offset=0,
