@@ -471,8 +471,8 @@ def run_primitive_cp(args):
 def run_primitive_vcopy(args):
     """HBM round trip through shared memory with the vectorised copy.
 
-    Every CTA (a CTA scope of 256 threads) moves one 64 x 512 fp16 region
-    (64 KB) of a 1 GiB buffer global -> shared -> global; bytes = read + write,
+    Every CTA (a warpgroup scope, 128 threads) moves one 32 x 512 fp16 region
+    (32 KB) of a 1 GiB buffer global -> shared -> global; bytes = read + write,
     against the measured HBM copy bandwidth (which counts the same way)."""
     import numpy as np
     import torch
@@ -481,7 +481,7 @@ def run_primitive_vcopy(args):
     from oracle import vec_copy as ovc
 
     dev = torch.device("cuda", 0)
-    rows, cols, eb, threads = 64, 512, 2, 256
+    rows, cols, eb, threads = 32, 512, 2, 128
     region = rows * cols
     total = 1 << 30
     ctas = total // (region * eb)
@@ -530,7 +530,7 @@ def run_primitive_vcopy(args):
         "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "dtype": "f16", "data": "synthetic (random bytes)",
-        "config": {"workload": "vcopy_64x512_f16_cta256", "buffer_bytes": total, "ctas": ctas,
+        "config": {"workload": "vcopy_32x512_f16_warpgroup", "buffer_bytes": total, "ctas": ctas,
                    "plan": plan, "l2": "inputs larger than L2, no flush"},
         "clocks": sampler.summary(t0, t1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],

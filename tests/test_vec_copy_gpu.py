@@ -73,5 +73,10 @@ def test_vcopy_swizzled_shared(swizzle, eb):
     run(32, 128 // eb * 2, eb, threads=128, swizzle=swizzle)
 
 
+@pytest.mark.parametrize("eb", [2, 8])
+def test_vcopy_cta_of_1024_threads(eb):
+    run(64, 128, eb, threads=1024)
+
+
 def test_vcopy_many_ctas():
     run(16, 64, 2, threads=128, ctas=5, cta_stride=16 * 80, g_row_stride=80)

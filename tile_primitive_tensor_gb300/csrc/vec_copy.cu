@@ -32,6 +32,7 @@ namespace tpg {
 namespace {
 
 constexpr int kMaxSmemBytes = 200 * 1024;
+constexpr int kBatch = 4;  // vectors in flight per thread
 
 tpgemm_status vc_fail(tpgemm_status s, std::string* why, const char* fmt, ...) {
     char buf[512];
@@ -169,7 +170,7 @@ __device__ __forceinline__ void vc_addr(const VcKernelParams& p, int64_t e, int6
 // buffer (zeroed first, so bytes outside the region are defined) is written out
 // between the two copies.
 template <int VB>
-__global__ void vcopy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
+__global__ void __launch_bounds__(1024) vcopy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
                              uint8_t* __restrict__ smem_out, const VcKernelParams p) {
     using T = typename VecT<VB>::T;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -181,11 +182,22 @@ __global__ void vcopy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restric
         __syncthreads();
     }
     // Serial rounds: round f, thread tid owns elements [(f T + tid) v, + v).
-    for (int64_t f = 0; f < p.outer; ++f) {
-        int64_t g;
-        uint32_t s;
-        vc_addr(p, (f * p.threads + tid) * p.vec, g, s);
-        *reinterpret_cast<T*>(smem + s) = *reinterpret_cast<const T*>(src + base + g);
+    // Rounds go in batches of kBatch: all of a batch's loads are issued before
+    // its stores, so each thread keeps kBatch vectors in flight.
+    for (int64_t f0 = 0; f0 < p.outer; f0 += kBatch) {
+        T v[kBatch];
+        uint32_t so[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (f0 + u < p.outer) {
+                int64_t g;
+                vc_addr(p, ((f0 + u) * p.threads + tid) * p.vec, g, so[u]);
+                v[u] = *reinterpret_cast<const T*>(src + base + g);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (f0 + u < p.outer) *reinterpret_cast<T*>(smem + so[u]) = v[u];
     }
     __syncthreads();
     if (smem_out) {
@@ -193,11 +205,20 @@ __global__ void vcopy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restric
         for (int i = tid; i < p.smem_bytes / 16; i += p.threads)
             o[i] = reinterpret_cast<const uint4*>(smem)[i];
     }
-    for (int64_t f = 0; f < p.outer; ++f) {
-        int64_t g;
-        uint32_t s;
-        vc_addr(p, (f * p.threads + tid) * p.vec, g, s);
-        *reinterpret_cast<T*>(dst + base + g) = *reinterpret_cast<const T*>(smem + s);
+    for (int64_t f0 = 0; f0 < p.outer; f0 += kBatch) {
+        T v[kBatch];
+        int64_t go[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (f0 + u < p.outer) {
+                uint32_t so;
+                vc_addr(p, ((f0 + u) * p.threads + tid) * p.vec, go[u], so);
+                v[u] = *reinterpret_cast<const T*>(smem + so);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (f0 + u < p.outer) *reinterpret_cast<T*>(dst + base + go[u]) = v[u];
     }
 }
 
