@@ -42,16 +42,23 @@
 extern "C" {
 #endif
 
-/* Element type of A and B (both the same). */
+/* Element type of A and B (both the same). The fp8 types run on the tcgen05
+ * kernel only (tcgen05.mma kind::f8f6f4, the fp8 gemm_async the pages mention
+ * beside the f16 one) with A stored [M,K] (transA = 0) and B stored [N,K]
+ * (transB = 1), both K-contiguous, and K % 16 == 0; other orientations return
+ * TPGEMM_ERR_PATH. There is no per-block scale: D = A.B + beta.C exactly as for
+ * f16, with the fp8 values as they are. */
 typedef enum {
     TPGEMM_F16 = 0,  /* IEEE binary16 */
-    TPGEMM_BF16 = 1  /* bfloat16 */
+    TPGEMM_BF16 = 1, /* bfloat16 */
+    TPGEMM_E4M3 = 2, /* fp8 e4m3 (1 sign, 4 exponent bits, bias 7, 3 mantissa bits; no inf) */
+    TPGEMM_E5M2 = 3  /* fp8 e5m2 (1 sign, 5 exponent bits, bias 15, 2 mantissa bits) */
 } tpgemm_dtype;
 
 typedef enum {
     TPGEMM_OK = 0,
-    TPGEMM_ERR_SHAPE = 1,   /* M, N, K not positive, or M%16, N%8, K%8 != 0 */
-    TPGEMM_ERR_DTYPE = 2,   /* dtype not TPGEMM_F16 / TPGEMM_BF16 */
+    TPGEMM_ERR_SHAPE = 1,   /* M, N, K not positive, or M%16, N%8, K%8 != 0 (K%16 for fp8) */
+    TPGEMM_ERR_DTYPE = 2,   /* dtype not one of tpgemm_dtype */
     TPGEMM_ERR_BETA = 3,    /* beta not exactly 0.0f or 1.0f */
     TPGEMM_ERR_NULL = 4,    /* D, A or B NULL, or C NULL with beta == 1 */
     TPGEMM_ERR_ALIGN = 5,   /* a pointer not 16-byte aligned */
@@ -77,7 +84,7 @@ typedef enum {
  *   B or C is rejected with TPGEMM_ERR_ALIAS.
  * M, N, K: logical sizes, positive, M % 16 == 0, N % 8 == 0, K % 8 == 0.
  * transA, transB: 0 or non-zero; select the stored orientation of A and B.
- * dtype: TPGEMM_F16 or TPGEMM_BF16.
+ * dtype: one of tpgemm_dtype (the fp8 ones with the orientation and K rules above).
  * beta: exactly 0.0f or 1.0f.
  * stream: a cudaStream_t (0 for the legacy default stream) on the current
  *   device; the call is asynchronous and returns once the work is enqueued.

@@ -30,6 +30,8 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
 F16 = 0
 BF16 = 1
+E4M3 = 2
+E5M2 = 3
 
 TOL_REL = 2.0 ** -10
 TOL_ABS = 1e-6
@@ -113,7 +115,8 @@ def num_threads() -> int:
 
 
 def decode(bits, dtype: int) -> np.ndarray:
-    """Exact float64 values of 16-bit fp16 (dtype 0) or bf16 (dtype 1) patterns."""
+    """Exact float64 values of fp16 (dtype 0) or bf16 (dtype 1) patterns, or of fp8
+    e4m3 (2) / e5m2 (3) patterns widened to 16 bits."""
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     out = np.empty(b.shape, dtype=np.float64)
     _load().oracle_decode(_ptr(b), _ptr(out), b.size, int(dtype))

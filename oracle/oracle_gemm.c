@@ -10,14 +10,16 @@
  * page "TVM TIRx 同步 GEMM 深度解析：warp 级 mma.sync 的寄存器碎片排布与完整
  * 下放链路", sections 语义定义 and 二 What it accepts):
  *   - D = alpha*A*B + beta*C with alpha fixed at 1 and beta in {0, 1};
- *   - A and B are both float16 or both bfloat16, C and D are float32;
+ *   - A and B are both float16 or both bfloat16, C and D are float32; the
+ *     same with both fp8 e4m3 or both fp8 e5m2 (the fp8 gemm_async the pages
+ *     mention beside the f16 one), patterns passed widened to 16 bits;
  *   - transpose_A / transpose_B only set the logical orientation: the operands
  *     are normalised to A[M,K], B[K,N], C and D [M,N] (section 维度一致性);
  *   - the accumulator is initialised from C when beta = 1 and from zero when
  *     beta = 0, then accumulated over K (section 四 step 3).
  *
- * Precision: every 16-bit input is decoded exactly to double, each product is
- * exact in double (at most 22 significant bits), the sum runs over k in
+ * Precision: every 16-bit (or 8-bit) input is decoded exactly to double, each
+ * product is exact in double (at most 22 significant bits), the sum runs over k in
  * increasing order in double, C is added when beta = 1, and the result is
  * rounded once to float32 (round to nearest even, the C cast). The oracle
  * accepts any positive shape; the divisibility rules belong to the library.
@@ -38,6 +40,8 @@
 
 #define ORACLE_F16 0
 #define ORACLE_BF16 1
+#define ORACLE_E4M3 2
+#define ORACLE_E5M2 3
 
 /* IEEE-754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
  * Exponent field 0 encodes zero and subnormals (fraction * 2^-24); 31 encodes
@@ -75,8 +79,50 @@ double oracle_decode_bf16(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* fp8 e4m3 (the "fn" variant): 1 sign bit, 4 exponent bits (bias 7), 3
+ * fraction bits, in the low byte. Exponent 0 encodes zero and subnormals
+ * (fraction * 2^-9); the all-ones pattern S.1111.111 is NaN and there is no
+ * infinity, so exponent 15 with fraction 0..6 is an ordinary number. */
+double oracle_decode_e4m3(uint16_t h) {
+    int sign = (h >> 7) & 1;
+    int e = (h >> 3) & 0xf;
+    int m = h & 0x7;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -9);
+    } else if (e == 15 && m == 7) {
+        v = NAN;
+    } else {
+        v = ldexp((double)(8 + m), e - 10);
+    }
+    return sign ? -v : v;
+}
+
+/* fp8 e5m2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits, in the
+ * low byte. Exponent 0 encodes zero and subnormals (fraction * 2^-16); 31
+ * encodes infinity (fraction 0) or NaN. */
+double oracle_decode_e5m2(uint16_t h) {
+    int sign = (h >> 7) & 1;
+    int e = (h >> 2) & 0x1f;
+    int m = h & 0x3;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -16);
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(4 + m), e - 17);
+    }
+    return sign ? -v : v;
+}
+
 static double decode(uint16_t h, int dtype) {
-    return dtype == ORACLE_BF16 ? oracle_decode_bf16(h) : oracle_decode_f16(h);
+    switch (dtype) {
+        case ORACLE_BF16: return oracle_decode_bf16(h);
+        case ORACLE_E4M3: return oracle_decode_e4m3(h);
+        case ORACLE_E5M2: return oracle_decode_e5m2(h);
+        default: return oracle_decode_f16(h);
+    }
 }
 
 void oracle_decode(const uint16_t* src, double* dst, int64_t n, int dtype) {
@@ -106,7 +152,7 @@ int oracle_num_threads(void) {
 int oracle_gemm(float* D, double* sumabs, const uint16_t* A, const uint16_t* B, const float* C,
                 int64_t M, int64_t N, int64_t K, int transA, int transB, int dtype, int beta) {
     if (M <= 0 || N <= 0 || K <= 0 || !D || !A || !B || (beta && !C)) return -2;
-    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -2;
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2) return -2;
     /* Decode once into the normalised orientation: a[i*K+k] = a(i,k) and
      * bt[j*K+k] = b(k,j), so the sum over k walks both rows contiguously. */
     double* a = (double*)malloc(sizeof(double) * (size_t)(M * K));
@@ -152,7 +198,7 @@ int oracle_gemm_entries(float* D_out, double* sumabs_out, const int64_t* rows, c
                         int64_t M, int64_t N, int64_t K, int transA, int transB, int dtype,
                         int beta) {
     if (M <= 0 || N <= 0 || K <= 0 || !D_out || !A || !B || (beta && !C) || count < 0) return -2;
-    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -2;
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2) return -2;
     for (int64_t t = 0; t < count; ++t)
         if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -2;
 #pragma omp parallel for schedule(dynamic, 4)
@@ -180,7 +226,7 @@ int oracle_gemm_rows(float* D_rows, const uint16_t* A, const uint16_t* B, const 
                      int transA, int transB, int dtype, int beta) {
     if (M <= 0 || N <= 0 || K <= 0 || !D_rows || !A || !B || (beta && !C)) return -2;
     if (row_begin < 0 || row_end > M || row_begin >= row_end) return -2;
-    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -2;
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2) return -2;
     int64_t R = row_end - row_begin;
     double* a = (double*)malloc(sizeof(double) * (size_t)(R * K));
     double* bt = (double*)malloc(sizeof(double) * (size_t)(N * K));

@@ -64,12 +64,32 @@ def test_rejects_shape(lib, M, N, K, frag):
     assert frag in why
 
 
-@pytest.mark.parametrize("dtype", [2, 3, -1, 7])
+@pytest.mark.parametrize("dtype", [4, 5, -1, 7])
 def test_rejects_dtype(lib, dtype):
     # f16 accumulators, tf32, int8 and mixed types have no enumerator: any
-    # code other than TPGEMM_F16 / TPGEMM_BF16 is refused.
+    # code other than F16 / BF16 / E4M3 / E5M2 is refused.
     st, why = call(dtype=dtype)
     assert st == tp.TPGEMM_ERR_DTYPE and "dtype" in why
+
+
+@pytest.mark.parametrize("dtype", [tp.TPGEMM_E4M3, tp.TPGEMM_E5M2])
+def test_fp8_rules(lib, dtype):
+    # fp8: K a multiple of 16 (whole 16-byte rows), both operands K-contiguous
+    # (A [M,K], B [N,K]), tcgen05 kernel only.
+    st, why = call(K=72, dtype=dtype, tB=1)
+    assert st == tp.TPGEMM_ERR_SHAPE and "multiple of 16" in why
+    for tA, tB in ((0, 0), (1, 1), (1, 0)):
+        st, text = tp.tpgemm_describe_plan(256, 256, 256, tA, tB, dtype, 0.0)
+        assert st == tp.TPGEMM_ERR_PATH and "K-contiguous" in tp.tpgemm_last_error_detail()
+    st, text = tp.tpgemm_describe_plan(256, 256, 256, 0, 1, dtype, 0.0)
+    assert st == tp.TPGEMM_OK and "kind=f8f6f4" in text and "x128 " in text, text
+    st, text = tp.tpgemm_describe_plan(16, 8, 32, 0, 1, dtype, 0.0)
+    assert st == tp.TPGEMM_OK and text.startswith("path=tcgen05"), text
+    st, _ = tp.tpgemm_describe_plan(256, 256, 256, 0, 1, dtype, 0.0, tp.TPGEMM_PATH_MMA_SYNC)
+    assert st == tp.TPGEMM_ERR_PATH
+    # operand bytes for aliasing and the host workspace are one per element
+    n = tp.tpgemm_gemm_host_workspace_bytes(64, 64, 64, dtype, 0.0)
+    assert n == 4096 + 4096 + 16384
 
 
 @pytest.mark.parametrize("beta", [0.5, 2.0, -1.0, float("nan"), 1e-30])

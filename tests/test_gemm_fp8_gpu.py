@@ -1,0 +1,149 @@
+"""fp8 (e4m3 / e5m2) GEMM on the tcgen05 kind::f8f6f4 path, against the oracle.
+
+Same bar as the f16 / bf16 path: bit-exact (by value) on integer-valued
+inputs, else |D - D_ref| <= 2^-10 * sum_k |a b| + 1e-6 elementwise, with the
+oracle decoding the very same fp8 bytes. fp8 operands are K-contiguous (A
+[M,K], B [N,K]); cases cover both formats, beta 0 and 1, ragged M / N / K
+tails (K a multiple of 16, not of the 128-element stage), the swapped
+orientation of small M, CTA pairs and single CTAs, clusters, tail splitting,
+stream-K, and the fp8 workloads at full size (sampled entries plus an fp64
+product of the whole output).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tile_primitive_tensor_gb300 as tp
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TC = tp.TPGEMM_PATH_TCGEN05
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tile_primitive_tensor_gb300 import build as tpbuild
+    tpbuild.build()
+    oracle.build()
+    yield
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+
+
+def case(M, N, K, dtype, beta, dist=("normal", 0.0, 1.0), seed=0):
+    base = wl.BY_NAME["gemm_8192_e4m3_transB_beta1"]
+    return dataclasses.replace(base.with_shape(M, N, K, seed=seed), dtype=dtype, beta=beta,
+                               a_dist=dist, b_dist=dist,
+                               c_dist=("normal", 0.0, 1.0) if beta else None)
+
+
+def check(w, path=tp.TPGEMM_PATH_AUTO):
+    A, B, C = wl.make_inputs(w)
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd = None if C is None else C.cuda()
+    guard = 4096
+    buf = torch.full((w.M * w.N + 2 * guard,), float("nan"), device="cuda")
+    D = buf[guard: guard + w.M * w.N].view(w.M, w.N)
+    st = tp.tpgemm_gemm_path(D, Ad, Bd, Cd, w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta,
+                             None, path)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    h = buf.cpu().numpy()
+    assert np.isnan(h[:guard]).all() and np.isnan(h[guard + w.M * w.N:]).all()
+    Dh = D.cpu().numpy()
+    Dref, S = oracle.gemm(wl.bits(A), wl.bits(B), None if C is None else C.numpy(), w.M, w.N,
+                          w.K, w.transA, w.transB, w.dtype, w.beta)
+    ok, msg = oracle.compare(Dh, Dref, S, exact=w.integer_valued)
+    assert ok, f"{w.name}: {msg}"
+    return Dh
+
+
+FMTS = [wl.E4M3, wl.E5M2]
+
+
+@pytest.mark.parametrize("dtype", FMTS, ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (272, 264, 272), (128, 128, 144),
+                                   (384, 392, 400), (16, 8, 32), (48, 40, 48)])
+def test_fp8_tiled(M, N, K, dtype, beta):
+    check(case(M, N, K, dtype, beta, seed=7 * M + K + dtype))
+
+
+@pytest.mark.parametrize("dtype", FMTS, ids=["e4m3", "e5m2"])
+def test_fp8_swapped_small_m(dtype):
+    w = case(144, 2072, 528, dtype, 1.0, seed=11)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, 0, 1, dtype, 1.0)
+    assert "orientation=swapped" in text and "kind=f8f6f4" in text, text
+    check(w)
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("bn", ["128", "256"])
+def test_fp8_pair_and_width(pair, bn, monkeypatch):
+    monkeypatch.setenv("TPGEMM_TC_PAIR", pair)
+    monkeypatch.setenv("TPGEMM_TC_BN", bn)
+    check(case(784, 1320, 272, wl.E4M3, 1.0, seed=13))
+
+
+@pytest.mark.parametrize("mc", ["2", "4"])
+def test_fp8_clusters(mc, monkeypatch):
+    monkeypatch.setenv("TPGEMM_TC_PAIR", "0")
+    monkeypatch.setenv("TPGEMM_TC_CLUSTER", mc)
+    check(case(1024, 128, 256, wl.E5M2, 0.0, seed=17))
+
+
+def test_fp8_tail_split(monkeypatch):
+    monkeypatch.setenv("TPGEMM_TC_BN", "256")
+    w = case(2048, 2560, 160, wl.E4M3, 1.0, seed=19)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, 0, 1, w.dtype, 1.0)
+    assert "x1 " not in text.split("units=")[1][:12], text
+    check(w)
+
+
+def test_fp8_stream_k(monkeypatch):
+    monkeypatch.setenv("TPGEMM_TC_SK", "1")
+    w = case(1024, 1024, 4096, wl.E4M3, 1.0, seed=23)  # 32 K blocks of 128: enough to split
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, 0, 1, w.dtype, 1.0)
+    assert "stream_k=1" in text, text
+    check(w)
+
+
+def test_fp8_integer_bit_exact():
+    check(case(1024, 1024, 1024, wl.E4M3, 0.0, dist=("int", -3, 3), seed=29))
+    check(case(512, 768, 2048, wl.E5M2, 1.0, dist=("int", -3, 3), seed=31))
+
+
+@pytest.mark.parametrize("name", [w.name for w in wl.FP8_WORKLOADS])
+def test_fp8_workload_full_size(name):
+    w = wl.BY_NAME[name]
+    A, B, C = wl.make_inputs(w)
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd = None if C is None else C.cuda()
+    D = torch.empty(w.M, w.N, device="cuda")
+    st = tp.tpgemm_gemm(D, Ad, Bd, Cd, w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, None)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    Dh = D.cpu().numpy()
+    assert np.isfinite(Dh).all()
+    rng = np.random.default_rng(w.seed)
+    r = np.concatenate([rng.integers(0, w.M, 3000), [0, w.M - 1]])
+    c = np.concatenate([rng.integers(0, w.N, 3000), [w.N - 1, 0]])
+    Dref, S = oracle.gemm_entries(r, c, wl.bits(A), wl.bits(B), None if C is None else C.numpy(),
+                                  w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+    ok, msg = oracle.compare(Dh[r, c], Dref, S, exact=w.integer_valued)
+    assert ok, f"{name} sampled: {msg}"
+    a = Ad.double()
+    b = Bd.double().t()  # B stored [N, K]
+    ref = a @ b
+    if w.beta:
+        ref += Cd.double()
+    bound = (a.abs() @ b.abs()) * (2.0 ** -10) + 1e-6
+    if w.integer_valued:
+        assert torch.equal(D.double(), ref)
+    else:
+        err = (D.double() - ref).abs()
+        assert bool((err <= bound).all()), f"{name}: max err/bound {float((err / bound).max())}"

@@ -478,3 +478,34 @@ def test_golden_fixtures_reproduced(oracle_lib):
                                None if C is None else g["C_f32bits"], w.M, w.N, w.K, w.transA,
                                w.transB, w.dtype, w.beta)
         assert np.array_equal(D.view(np.uint32), g["D_f32bits"].view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# fp8 (the tcgen05 kind::f8f6f4 path): decoders and exactness
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("code,name", [(2, "float8_e4m3fn"), (3, "float8_e5m2")])
+def test_fp8_decode_exhaustive_against_torch(oracle_lib, code, name):
+    # All 256 byte patterns against torch's own fp8 -> float64 conversion.
+    import torch
+    td = getattr(torch, name)
+    pats = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = pats.view(td).to(torch.float64).numpy()
+    got = oracle_lib.decode(pats.numpy().astype(np.uint16), code)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+
+
+def test_fp8_gemm_matches_exact_integer_sums(oracle_lib):
+    # Small integers are exact in both fp8 formats; D must be the exact sum.
+    import torch
+    rng = np.random.default_rng(5)
+    M, N, K = 16, 24, 48
+    a = rng.integers(-3, 4, (M, K))
+    b = rng.integers(-3, 4, (N, K))  # stored [N, K]: transB
+    for code, td in ((2, torch.float8_e4m3fn), (3, torch.float8_e5m2)):
+        A = torch.tensor(a, dtype=torch.float32).to(td)
+        B = torch.tensor(b, dtype=torch.float32).to(td)
+        D, S = oracle_lib.gemm(wl.bits(A), wl.bits(B), None, M, N, K, False, True, code, 0.0)
+        assert np.array_equal(D, (a @ b.T).astype(np.float32))
+        assert np.array_equal(S, (np.abs(a) @ np.abs(b).T).astype(np.float64))

@@ -23,6 +23,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "tpgemm.h")
 # tpgemm_dtype
 TPGEMM_F16 = 0
 TPGEMM_BF16 = 1
+TPGEMM_E4M3 = 2
+TPGEMM_E5M2 = 3
 # tpgemm_status
 TPGEMM_OK = 0
 TPGEMM_ERR_SHAPE = 1
@@ -319,7 +321,12 @@ def dtype_code(torch_dtype) -> int:
         return TPGEMM_F16
     if torch_dtype == torch.bfloat16:
         return TPGEMM_BF16
-    raise TypeError(f"A and B must be float16 or bfloat16, got {torch_dtype}")
+    if torch_dtype == torch.float8_e4m3fn:
+        return TPGEMM_E4M3
+    if torch_dtype == torch.float8_e5m2:
+        return TPGEMM_E5M2
+    raise TypeError(f"A and B must be float16, bfloat16, float8_e4m3fn or float8_e5m2, "
+                    f"got {torch_dtype}")
 
 
 def gemm(A, B, C=None, *, beta=None, transA=False, transB=False, out=None, stream=None,

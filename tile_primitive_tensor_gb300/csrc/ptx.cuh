@@ -282,6 +282,29 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
+// kind::f8f6f4 (e4m3 / e5m2 in, f32 accumulate): the same operand forms and
+// instruction descriptor fields as kind::f16, K = 32 per instruction (32 bytes
+// of each row, as for kind::f16).
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
 // lane (quadrant base + t), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -428,8 +451,9 @@ __device__ __forceinline__ uint64_t smem_desc_with_addr(uint64_t tmpl, uint32_t 
     return (tmpl & ~uint64_t(0x3FFF)) | uint64_t((smem_addr >> 4) & 0x3FFFu);
 }
 
-// Instruction descriptor for kind::f16 with an f32 accumulator: bits 4-5 D
-// format (1 = f32), 7-9 A format and 10-12 B format (0 = f16, 1 = bf16),
+// Instruction descriptor for kind::f16 (and kind::f8f6f4) with an f32
+// accumulator: bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format
+// (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3, 1 = e5m2),
 // 15 / 16 A / B major-ness (0 = K-major, 1 = MN-major), 17-22 N >> 3,
 // 24-28 M >> 4. Dense, no negation, no saturation.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(bool bf16, bool a_mn_major, bool b_mn_major,

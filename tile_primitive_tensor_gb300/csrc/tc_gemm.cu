@@ -1,4 +1,5 @@
-// tcgen05 GEMM for sm_103a:  X = P . Q^T (+ C), f16/bf16 in, f32 accumulate and out.
+// tcgen05 GEMM for sm_103a:  X = P . Q^T (+ C), f16/bf16 (or e4m3/e5m2) in, f32
+// accumulate and out.
 //
 // Persistent, warp-specialised CTA of 10 warps, one CTA per SM:
 //   warp 0      TMA producer: one thread fills a ring of shared-memory stages
@@ -40,8 +41,8 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 namespace {
 
 constexpr int kBM = 128;           // P rows per tile (tensor-memory lanes)
-constexpr int kBK = 64;            // K elements per stage: one 128-byte swizzle row
-constexpr int kUmmaK = 16;         // K per tcgen05.mma (kind::f16)
+constexpr int kBK = 64;            // 16-bit K elements per stage: one 128-byte swizzle row
+constexpr int kUmmaK = 16;         // 16-bit K per tcgen05.mma (kind::f16); 32 for fp8
 constexpr int kEpiWarps = kTcEpiWarps;  // two per lane quadrant
 constexpr int kEpiQuads = 4;
 constexpr int kEpiBufFloats = 32 * 32;  // one 32 x 32 f32 staging tile (4 KB)
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     uint8_t* sp = s.stages + size_t(stage) * (p.p_bytes + p.q_bytes);
                     uint8_t* sq = sp + p.p_bytes;
-                    const int k0 = kb * kBK;
+                    const int k0 = kb * p.bk;
                     if (p.test_stall && blockIdx.x == 0 && first_seg && i == 0) {
                         // Failure-detection test: expect the stage's bytes but
                         // load nothing, so this stage never fills.
@@ -424,10 +425,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                         const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * stepP);
                         const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * stepQ);
-                        if (PAIR)
-                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (i | kk) != 0);
-                        else
-                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, (i | kk) != 0);
+                        const uint32_t acc = (i | kk) != 0;
+                        if (PAIR) {
+                            if (p.fp8)
+                                tc_mma_f8_pair(d_tmem, adesc, bdesc, idesc, acc);
+                            else
+                                tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, acc);
+                        } else {
+                            if (p.fp8)
+                                tc_mma_f8(d_tmem, adesc, bdesc, idesc, acc);
+                            else
+                                tc_mma_f16(d_tmem, adesc, bdesc, idesc, acc);
+                        }
                     }
                     // Stage free (in every CTA that filled or multicast into it)
                     // once these MMAs finish.

@@ -89,6 +89,15 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+bool is_fp8(tpgemm_dtype d) { return d == TPGEMM_E4M3 || d == TPGEMM_E5M2; }
+
+// Bytes of one element of A and B.
+int elem_bytes(tpgemm_dtype d) { return is_fp8(d) ? 1 : 2; }
+
+// The format code the instruction descriptor carries for A and B: kind::f16
+// f16 = 0 / bf16 = 1; kind::f8f6f4 e4m3 = 0 / e5m2 = 1.
+bool format_code1(tpgemm_dtype d) { return d == TPGEMM_BF16 || d == TPGEMM_E5M2; }
+
 tpgemm_status check_shape(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype, float beta) {
     if (M <= 0 || N <= 0 || K <= 0)
         return fail(TPGEMM_ERR_SHAPE, "M=%lld N=%lld K=%lld must all be positive", (long long)M,
@@ -100,16 +109,22 @@ tpgemm_status check_shape(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype, f
     const int64_t lim = int64_t(1) << 30;
     if (M >= lim || N >= lim || K >= lim)
         return fail(TPGEMM_ERR_SHAPE, "M, N, K must each be below 2^30");
-    if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16)
-        return fail(TPGEMM_ERR_DTYPE, "dtype %d is neither TPGEMM_F16 (0) nor TPGEMM_BF16 (1)",
+    if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16 && !is_fp8(dtype))
+        return fail(TPGEMM_ERR_DTYPE,
+                    "dtype %d is not TPGEMM_F16 (0), TPGEMM_BF16 (1), TPGEMM_E4M3 (2) or "
+                    "TPGEMM_E5M2 (3)",
                     int(dtype));
+    if (is_fp8(dtype) && K % 16)
+        return fail(TPGEMM_ERR_SHAPE,
+                    "K=%lld is not a multiple of 16 (fp8 rows must be whole 16-byte units)",
+                    (long long)K);
     if (!(beta == 0.0f || beta == 1.0f))
         return fail(TPGEMM_ERR_BETA, "beta=%g; only 0 and 1 are supported", double(beta));
     return TPGEMM_OK;
 }
 
 tpgemm_status check_pointers(float* D, const void* A, const void* B, const float* C, int64_t M,
-                             int64_t N, int64_t K, float beta) {
+                             int64_t N, int64_t K, float beta, int eb) {
     if (!D) return fail(TPGEMM_ERR_NULL, "D is NULL");
     if (!A) return fail(TPGEMM_ERR_NULL, "A is NULL");
     if (!B) return fail(TPGEMM_ERR_NULL, "B is NULL");
@@ -121,8 +136,10 @@ tpgemm_status check_pointers(float* D, const void* A, const void* B, const float
     if (beta == 1.0f && misaligned(C))
         return fail(TPGEMM_ERR_ALIGN, "C=%p is not 16-byte aligned", (const void*)C);
     const size_t dn = size_t(M) * size_t(N) * 4;
-    if (overlaps(D, dn, A, size_t(M) * size_t(K) * 2)) return fail(TPGEMM_ERR_ALIAS, "D overlaps A");
-    if (overlaps(D, dn, B, size_t(K) * size_t(N) * 2)) return fail(TPGEMM_ERR_ALIAS, "D overlaps B");
+    if (overlaps(D, dn, A, size_t(M) * size_t(K) * size_t(eb)))
+        return fail(TPGEMM_ERR_ALIAS, "D overlaps A");
+    if (overlaps(D, dn, B, size_t(K) * size_t(N) * size_t(eb)))
+        return fail(TPGEMM_ERR_ALIAS, "D overlaps B");
     if (beta == 1.0f && static_cast<const void*>(C) != static_cast<const void*>(D) &&
         overlaps(D, dn, C, dn))
         return fail(TPGEMM_ERR_ALIAS, "D overlaps C without being equal to it");
@@ -182,8 +199,9 @@ int pick_bn(int64_t M, int64_t N, int sms, bool pair) {
     return best;
 }
 
-tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB, bool bf16,
-                      float beta, int sms, Plan* out) {
+tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
+                      tpgemm_dtype dtype, float beta, int sms, Plan* out) {
+    const bool fp8 = is_fp8(dtype);
     tpg::TcParams p{};
     // Small M: swap operands so N runs along the 128 tensor-memory lanes and
     // all of M fits one accumulator (UMMA N = M <= 256, a multiple of 16).
@@ -203,6 +221,11 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     const int64_t Nq = swap ? M : N;
     const bool p_mn = swap ? !transB : transA;
     const bool q_mn = swap ? transA : !transB;
+    // fp8 operands are loaded K-contiguous only (A [M,K], B [N,K]).
+    if (fp8 && (p_mn || q_mn))
+        return fail(TPGEMM_ERR_PATH,
+                    "fp8 A and B must both be K-contiguous: A stored [M,K] (transA = 0) and B "
+                    "stored [N,K] (transB = 1)");
     // The CTA-pair MMA needs at least two 128-row P tiles.
     const bool pair_wanted = Mp > 128;
     const int bn = swap_small ? int(Nq) : pick_bn(Mp, Nq, sms, pair_wanted);
@@ -213,7 +236,9 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.tiles_p = int((Mp + 127) / 128);
     p.tiles_q = int((Nq + bn - 1) / bn);
     p.num_tiles = p.tiles_p * p.tiles_q;
-    p.k_blocks = int((K + 63) / 64);
+    p.bk = fp8 ? 128 : 64;  // one 128-byte swizzle row of K per stage
+    p.fp8 = fp8 ? 1 : 0;
+    p.k_blocks = int((K + p.bk - 1) / p.bk);
     p.p_mn = p_mn;
     p.q_mn = q_mn;
     p.beta = beta == 1.0f;
@@ -233,7 +258,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.pair = pair_ok ? 1 : 0;
     if (const char* f = getenv("TPGEMM_TC_PAIR")) p.pair = (atoi(f) != 0 && pair_ok) ? 1 : 0;
     const int q_rows = p.pair ? bn / 2 : bn;  // Q rows this CTA loads per stage
-    p.idesc = tpg::idesc_f16_f32(bf16, p_mn, q_mn, p.pair ? 256 : 128, bn);
+    p.idesc = tpg::idesc_f16_f32(format_code1(dtype), p_mn, q_mn, p.pair ? 256 : 128, bn);
     p.p_bytes = stage_tile_bytes(128, p_mn);
     p.q_bytes = stage_tile_bytes(q_rows, q_mn);
     p.q_boxes = q_mn ? uint32_t((q_rows + 63) / 64) : 1u;
@@ -365,7 +390,7 @@ constexpr size_t kSkWorkspaceBytes = kSkSlotBytes + kSkFlagBytes;
 // for the next launch's early start.
 // *grid is the persistent grid (at most one cluster per work item); max_grid
 // is every cluster the device holds at once. Stream-K runs on max_grid.
-void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool bf16,
+void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
                       bool force_sk = false) {
     p.sk = 0;
     p.sk_total = 0;
@@ -411,7 +436,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool bf16,
     if (split == 1) p.full_units = p.num_super;
     p.tail_split = split;
     p.num_units = p.full_units + (p.num_super - p.full_units) * split;
-    p.idesc_tail = tpg::idesc_f16_f32(bf16, p.p_mn, p.q_mn, p.pair ? 256 : 128, p.bn / split);
+    p.idesc_tail = tpg::idesc_f16_f32(code1, p.p_mn, p.q_mn, p.pair ? 256 : 128, p.bn / split);
     p.q_box_rows = p.pair ? p.bn / 2 : p.bn / p.mc;
 }
 
@@ -487,8 +512,16 @@ tpgemm_status fit_grid(Plan* plan) {
     return TPGEMM_OK;
 }
 
-tpgemm_status make_plan(int64_t M, int64_t N, int64_t K, bool transA, bool transB, bool bf16,
-                        float beta, tpgemm_path path, int sms, Plan* out) {
+tpgemm_status make_plan(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
+                        tpgemm_dtype dtype, float beta, tpgemm_path path, int sms, Plan* out) {
+    if (is_fp8(dtype)) {
+        // fp8 runs on the tcgen05 kernel only (kind::f8f6f4).
+        if (path == TPGEMM_PATH_MMA_SYNC)
+            return fail(TPGEMM_ERR_PATH, "the mma.sync kernel takes f16 / bf16 only");
+        if (path != TPGEMM_PATH_AUTO && path != TPGEMM_PATH_TCGEN05)
+            return fail(TPGEMM_ERR_PATH, "unknown path %d", int(path));
+        return plan_tc(M, N, K, transA, transB, dtype, beta, sms, out);
+    }
     if (path == TPGEMM_PATH_MMA_SYNC) {
         out->kernel = Kernel::MmaSync;
         return TPGEMM_OK;
@@ -504,7 +537,7 @@ tpgemm_status make_plan(int64_t M, int64_t N, int64_t K, bool transA, bool trans
     } else if (path != TPGEMM_PATH_TCGEN05) {
         return fail(TPGEMM_ERR_PATH, "unknown path %d", int(path));
     }
-    return plan_tc(M, N, K, transA, transB, bf16, beta, sms, out);
+    return plan_tc(M, N, K, transA, transB, dtype, beta, sms, out);
 }
 
 // ---------------------------------------------------------- tensor maps
@@ -527,12 +560,17 @@ tpgemm_status encode_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map,
 // Map of a K x rows operand: K-contiguous -> dims {K, rows}, box {64, box_rows};
 // MN-contiguous -> dims {rows, K}, box {64, 64}.
 tpgemm_status encode_operand(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map,
-                             const void* base, bool bf16, int64_t rows, int64_t K, bool mn,
+                             const void* base, tpgemm_dtype dtype, int64_t rows, int64_t K, bool mn,
                              int box_rows, const char* what) {
-    const CUtensorMapDataType t =
-        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (mn) return encode_2d(enc, map, base, t, 2, uint64_t(rows), uint64_t(K), 64, 64, what);
-    return encode_2d(enc, map, base, t, 2, uint64_t(K), uint64_t(rows), 64, uint32_t(box_rows), what);
+    const CUtensorMapDataType t = is_fp8(dtype)          ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : dtype == TPGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int eb = elem_bytes(dtype);
+    const uint32_t row_elems = uint32_t(128 / eb);  // one 128-byte swizzle row
+    if (mn)
+        return encode_2d(enc, map, base, t, eb, uint64_t(rows), uint64_t(K), row_elems, 64, what);
+    return encode_2d(enc, map, base, t, eb, uint64_t(K), uint64_t(rows), row_elems,
+                     uint32_t(box_rows), what);
 }
 
 // Where a stream-K launch finds its scratch: a per-stream buffer the library
@@ -549,7 +587,7 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     g_detail.clear();
     tpgemm_status s = check_shape(M, N, K, dtype, beta);
     if (s != TPGEMM_OK) return s;
-    s = check_pointers(D, A, B, C, M, N, K, beta);
+    s = check_pointers(D, A, B, C, M, N, K, beta, elem_bytes(dtype));
     if (s != TPGEMM_OK) return s;
     DeviceInfo dev;
     s = device_info(&dev);
@@ -559,7 +597,7 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
                     dev.major, dev.minor);
     const bool bf16 = dtype == TPGEMM_BF16;
     Plan plan;
-    s = make_plan(M, N, K, transA != 0, transB != 0, bf16, beta, path, dev.sms, &plan);
+    s = make_plan(M, N, K, transA != 0, transB != 0, dtype, beta, path, dev.sms, &plan);
     if (s != TPGEMM_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -581,16 +619,17 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     // P / Q operands: normal P = A (rows M), Q = B^T (rows N); swapped P = B^T, Q = A.
     const void* pp = plan.swap ? B : A;
     const void* qq = plan.swap ? A : B;
-    s = encode_operand(enc, &maps.P, pp, bf16, p.Mp, K, p.p_mn, 128, "P operand");
+    s = encode_operand(enc, &maps.P, pp, dtype, p.Mp, K, p.p_mn, 128, "P operand");
     if (s != TPGEMM_OK) return s;
     s = fit_grid(&plan);
     if (s != TPGEMM_OK) return s;
-    apply_tail_split(plan.tc, &plan.grid, plan.max_grid, bf16, scratch == Scratch::Static);
+    apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code1(dtype),
+                     scratch == Scratch::Static);
     choose_epi_groups(plan.tc, plan.grid);
-    s = encode_operand(enc, &maps.Q, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
+    s = encode_operand(enc, &maps.Q, qq, dtype, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
     if (s != TPGEMM_OK) return s;
     if (p.tail_split > 1) {
-        s = encode_operand(enc, &maps.Qt, qq, bf16, p.Nq, K, p.q_mn, p.q_box_rows / p.tail_split,
+        s = encode_operand(enc, &maps.Qt, qq, dtype, p.Nq, K, p.q_mn, p.q_box_rows / p.tail_split,
                            "Q operand (tail units)");
         if (s != TPGEMM_OK) return s;
     }
@@ -658,13 +697,13 @@ struct HostWsLayout {
     size_t a, b, c, d, total;  // byte offsets in the workspace, and its size
 };
 
-HostWsLayout host_ws_layout(int64_t M, int64_t N, int64_t K, bool beta) {
+HostWsLayout host_ws_layout(int64_t M, int64_t N, int64_t K, bool beta, int eb) {
     HostWsLayout L;
     size_t off = 0;
     L.a = off;
-    off = align_up(off + size_t(M) * size_t(K) * 2, kWsAlign);
+    off = align_up(off + size_t(M) * size_t(K) * size_t(eb), kWsAlign);
     L.b = off;
-    off = align_up(off + size_t(K) * size_t(N) * 2, kWsAlign);
+    off = align_up(off + size_t(K) * size_t(N) * size_t(eb), kWsAlign);
     L.c = off;
     if (beta) off = align_up(off + size_t(M) * size_t(N) * 4, kWsAlign);
     L.d = off;
@@ -710,7 +749,8 @@ tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* C
     if (reinterpret_cast<uintptr_t>(ws) % kWsAlign)
         return fail(TPGEMM_ERR_ALIGN, "workspace is not 256-byte aligned");
     const bool use_c = beta == 1.0f;
-    const HostWsLayout L = host_ws_layout(M, N, K, use_c);
+    const size_t eb = size_t(elem_bytes(dtype));
+    const HostWsLayout L = host_ws_layout(M, N, K, use_c, int(eb));
     if (ws_bytes < L.total)
         return fail(TPGEMM_ERR_NULL, "workspace of %zu bytes; %zu needed", ws_bytes, L.total);
     DeviceInfo dev;
@@ -754,7 +794,7 @@ tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* C
     TPG_CK(cudaEventRecord(start, st), "event");
     TPG_CK(cudaStreamWaitEvent(hp->in, start, 0), "stream wait");
     TPG_CK(cudaStreamWaitEvent(hp->out, start, 0), "stream wait");
-    TPG_CK(cudaMemcpyAsync(dB, hB, size_t(K) * size_t(N) * 2, cudaMemcpyHostToDevice, hp->in),
+    TPG_CK(cudaMemcpyAsync(dB, hB, size_t(K) * size_t(N) * eb, cudaMemcpyHostToDevice, hp->in),
            "copy of B");
     // A block i: rows [m0, m1) of the logical A, packed densely in the
     // workspace (for transA a column block of the stored [K, M] matrix).
@@ -764,12 +804,12 @@ tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* C
         const int64_t mb = std::min(blk, M - m0);
         uint8_t* dAi = dA + a_off;
         if (!transA) {
-            TPG_CK(cudaMemcpyAsync(dAi, hA + size_t(m0) * size_t(K) * 2, size_t(mb) * size_t(K) * 2,
-                                   cudaMemcpyHostToDevice, hp->in),
+            TPG_CK(cudaMemcpyAsync(dAi, hA + size_t(m0) * size_t(K) * eb,
+                                   size_t(mb) * size_t(K) * eb, cudaMemcpyHostToDevice, hp->in),
                    "copy of A");
         } else {
-            TPG_CK(cudaMemcpy2DAsync(dAi, size_t(mb) * 2, hA + size_t(m0) * 2, size_t(M) * 2,
-                                     size_t(mb) * 2, size_t(K), cudaMemcpyHostToDevice, hp->in),
+            TPG_CK(cudaMemcpy2DAsync(dAi, size_t(mb) * eb, hA + size_t(m0) * eb, size_t(M) * eb,
+                                     size_t(mb) * eb, size_t(K), cudaMemcpyHostToDevice, hp->in),
                    "copy of A");
         }
         if (use_c)
@@ -786,7 +826,7 @@ tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* C
         TPG_CK(cudaMemcpyAsync(Dh + size_t(m0) * size_t(N), dD + size_t(m0) * size_t(N),
                                size_t(mb) * size_t(N) * 4, cudaMemcpyDeviceToHost, hp->out),
                "copy of D");
-        a_off += size_t(mb) * size_t(K) * 2;
+        a_off += size_t(mb) * size_t(K) * eb;
     }
     TPG_CK(cudaEventRecord(done, hp->out), "event");
     TPG_CK(cudaStreamWaitEvent(st, done, 0), "stream wait");
@@ -815,7 +855,7 @@ size_t tpgemm_gemm_host_workspace_bytes(int64_t M, int64_t N, int64_t K, tpgemm_
     const bool ok = check_shape(M, N, K, dtype, beta) == TPGEMM_OK;
     g_detail = keep;
     if (!ok) return 0;
-    return host_ws_layout(M, N, K, beta == 1.0f).total;
+    return host_ws_layout(M, N, K, beta == 1.0f, elem_bytes(dtype)).total;
 }
 
 tpgemm_status tpgemm_gemm_host(float* D_host, const void* A_host, const void* B_host,
@@ -898,11 +938,11 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     else
         cudaGetLastError();
     Plan plan;
-    s = make_plan(M, N, K, transA != 0, transB != 0, dtype == TPGEMM_BF16, beta, path, sms, &plan);
+    s = make_plan(M, N, K, transA != 0, transB != 0, dtype, beta, path, sms, &plan);
     if (s != TPGEMM_OK) return s;
     char text[512];
     if (plan.kernel == Kernel::Tc) {
-        apply_tail_split(plan.tc, &plan.grid, plan.max_grid, dtype == TPGEMM_BF16);
+        apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code1(dtype));
         choose_epi_groups(plan.tc, plan.grid);
     }
     if (plan.kernel == Kernel::MmaSync) {
@@ -913,10 +953,11 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     } else {
         const tpg::TcParams& p = plan.tc;
         snprintf(text, sizeof(text),
-                 "path=tcgen05 orientation=%s tile=128x%dx64 umma=%dx%dx16 stages=%d "
+                 "path=tcgen05 orientation=%s tile=128x%dx%d umma=%dx%dx%d kind=%s stages=%d "
                  "epi_bufs=%d epi_groups=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d "
                  "grid=%d units=%d+%dx%d stream_k=%d p_major=%s q_major=%s smem=%zu",
-                 plan.swap ? "swapped" : "normal", p.bn, p.pair ? 256 : 128, p.bn, p.stages,
+                 plan.swap ? "swapped" : "normal", p.bn, p.bk, p.pair ? 256 : 128, p.bn,
+                 p.fp8 ? 32 : 16, p.fp8 ? "f8f6f4" : "f16", p.stages,
                  p.epi_bufs, p.epi_groups, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
                  p.full_units, p.num_super - p.full_units, p.tail_split, p.sk, p.p_mn ? "mn" : "k",
                  p.q_mn ? "mn" : "k",

@@ -61,6 +61,8 @@ struct TcParams {
     int swap;               // orientation, for the epilogue's D coordinates
     int epi_bufs;           // 32 x 32 f32 staging tiles per lane quadrant (2..8), split
                             // between the quadrant's active epilogue warps
+    int bk;                 // K elements per stage (128 bytes of a row): 64, or 128 for fp8
+    int fp8;                // operands are e4m3 / e5m2: kind::f8f6f4 MMAs
     int epi_groups;         // active epilogue warpgroups (1 or 2); warp 2 + 4 g + i
                             // reads lane quadrant (i + 2) % 4, chunks c % groups == g
     int k_rotate;           // 0, or tiles per group sharing a rotated first K block

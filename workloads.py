@@ -8,9 +8,9 @@ Storage conventions (dense, row-major, no leading dimensions):
   A is [M, K], or [K, M] when transA is set (the logical A is its transpose);
   B is [K, N], or [N, K] when transB is set;
   C and D are [M, N] float32.
-A and B are float16 or bfloat16 (the same dtype). Values are drawn in float32
-and rounded to the 16-bit dtype with round-to-nearest-even (torch's cast), so
-both sides consume the very same 16-bit patterns.
+A and B are float16 or bfloat16 (the same dtype), or both fp8 e4m3 / e5m2.
+Values are drawn in float32 and rounded to the dtype with round-to-nearest-even
+(torch's cast), so both sides consume the very same bit patterns.
 
 The five workloads are the shapes of the method's test matrix: a single
 m16n8k16 atom, a 256^3 transposed-B case with beta = 1, a 4096^3 square case
@@ -26,8 +26,15 @@ import torch
 
 F16 = 0
 BF16 = 1
-_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
-_DTYPE_NAME = {F16: "f16", BF16: "bf16"}
+E4M3 = 2
+E5M2 = 3
+_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, E4M3: torch.float8_e4m3fn,
+                E5M2: torch.float8_e5m2}
+_DTYPE_NAME = {F16: "f16", BF16: "bf16", E4M3: "e4m3", E5M2: "e5m2"}
+
+
+def elem_bytes(dtype: int) -> int:
+    return 1 if dtype in (E4M3, E5M2) else 2
 
 
 @dataclasses.dataclass(frozen=True)
@@ -38,7 +45,7 @@ class Workload:
     M: int
     N: int
     K: int
-    dtype: int            # F16 or BF16
+    dtype: int            # F16, BF16, E4M3 or E5M2
     a_dist: tuple         # ("int", lo, hi) | ("uniform", lo, hi) | ("normal", mean, std)
     b_dist: tuple
     c_dist: Optional[tuple]  # None when beta == 0
@@ -54,7 +61,7 @@ class Workload:
     @property
     def algorithmic_bytes(self) -> int:
         """Each operand read once, D written once; C only when beta = 1."""
-        e = 2
+        e = elem_bytes(self.dtype)
         b = e * (self.M * self.K + self.K * self.N) + 4 * self.M * self.N
         if self.beta != 0.0:
             b += 4 * self.M * self.N
@@ -95,7 +102,21 @@ WORKLOADS = [
 WORKLOAD_4096_INT = Workload("gemm_4096_f16_int", 4096, 4096, 4096, F16, ("int", -3, 3),
                              ("int", -3, 3), None, 0.0, False, False, 1031)
 
-BY_NAME = {w.name: w for w in WORKLOADS + [WORKLOAD_4096_INT]}
+# fp8 cases of the tcgen05 kind::f8f6f4 path: both operands K-contiguous (A
+# [M,K], B [N,K]); an integer-valued variant is exact (|sum| <= 9 * 4096).
+FP8_WORKLOADS = [
+    Workload("gemm_8192_e4m3_transB_beta1", 8192, 8192, 8192, E4M3, ("normal", 0.0, 1.0),
+             ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), 1.0, False, True, 1040),
+    Workload("gemm_4096_e5m2_transB", 4096, 4096, 4096, E5M2, ("uniform", -1.0, 1.0),
+             ("uniform", -1.0, 1.0), None, 0.0, False, True, 1041),
+    Workload("gemm_4096_e4m3_int_transB", 4096, 4096, 4096, E4M3, ("int", -3, 3),
+             ("int", -3, 3), None, 0.0, False, True, 1042),
+    Workload("skinny_144x16392x4112_e4m3_transB_beta1", 144, 16392, 4112, E4M3,
+             ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), 1.0, False, True,
+             1043),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + [WORKLOAD_4096_INT] + FP8_WORKLOADS}
 
 
 def _draw(shape, dist, gen: torch.Generator) -> torch.Tensor:
@@ -121,7 +142,7 @@ def stored_shapes(w: Workload):
 def make_inputs(w: Workload, c_fill: Optional[float] = None):
     """Return CPU tensors (A, B, C) for a workload.
 
-    A and B are in the workload's 16-bit dtype and stored orientation; C is
+    A and B are in the workload's dtype and stored orientation; C is
     float32 [M, N], or None when beta == 0 (unless c_fill is given, in which
     case C is a constant-filled tensor, e.g. NaN to prove C is not read).
     """
@@ -139,7 +160,10 @@ def make_inputs(w: Workload, c_fill: Optional[float] = None):
 
 
 def bits(t: torch.Tensor):
-    """The raw 16-bit patterns of a float16/bfloat16 CPU tensor as numpy uint16."""
+    """The raw bit patterns of a float16/bfloat16 CPU tensor as numpy uint16; of an
+    fp8 tensor, its byte patterns widened to uint16."""
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return t.contiguous().view(torch.uint8).numpy().astype("uint16")
     assert t.dtype in (torch.float16, torch.bfloat16)
     return t.contiguous().view(torch.int16).numpy().view("uint16")
 
