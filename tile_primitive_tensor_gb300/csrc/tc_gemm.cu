@@ -25,6 +25,7 @@
 // in time; on expiry the kernel records a status word, stops every role, waits
 // for its own copies and MMAs in flight, frees tensor memory and returns.
 #include <mutex>
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "tpgemm_internal.h"
@@ -399,12 +400,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t stepP = p.p_mn ? kUmmaK * 128 : kUmmaK * 2;
             const uint32_t stepQ = p.q_mn ? kUmmaK * 128 : kUmmaK * 2;
             const uint32_t stage_base = smem_u32(s.stages);
+            // Loop invariants in registers: each issue below is an asm with a
+            // memory clobber, after which parameters would be read again.
+            const uint32_t stage_bytes = p.p_bytes + p.q_bytes;
+            const uint32_t p_bytes = p.p_bytes;
+            const int nstages = p.stages;
+            const bool mc_multi = p.mc > 1;
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
             SegIter iter(cid, ncl, p);
             Seg u;
+            // The MMA kind is fixed per launch: the issue loop is instantiated
+            // once per kind and chosen once, so no test sits between MMAs.
+            auto issue_all = [&](auto fp8_tag) {
+            constexpr bool FP8 = decltype(fp8_tag)::value;
             for (; ok && iter.next(ncl, p, u); ++it) {
                 const uint32_t idesc = u.width == p.bn ? p.idesc : p.idesc_tail;
                 const int nk = u.kb1 - u.kb0;
@@ -419,20 +430,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t ap = stage_base + uint32_t(stage) * (p.p_bytes + p.q_bytes);
-                    const uint32_t aq = ap + p.p_bytes;
+                    const uint32_t ap = stage_base + uint32_t(stage) * stage_bytes;
+                    const uint32_t aq = ap + p_bytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                         const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * stepP);
                         const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * stepQ);
                         const uint32_t acc = (i | kk) != 0;
-                        if (PAIR) {
-                            if (p.fp8)
+                        if constexpr (PAIR) {
+                            if constexpr (FP8)
                                 tc_mma_f8_pair(d_tmem, adesc, bdesc, idesc, acc);
                             else
                                 tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, acc);
                         } else {
-                            if (p.fp8)
+                            if constexpr (FP8)
                                 tc_mma_f8(d_tmem, adesc, bdesc, idesc, acc);
                             else
                                 tc_mma_f16(d_tmem, adesc, bdesc, idesc, acc);
@@ -442,11 +453,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // once these MMAs finish.
                     if (PAIR)
                         tc_commit_pair_multicast(&s.empty[stage], mc_mask);
-                    else if (p.mc > 1)
+                    else if (mc_multi)
                         tc_commit_multicast(&s.empty[stage], mc_mask);
                     else
                         tc_commit(&s.empty[stage]);
-                    if (++stage == p.stages) {
+                    if (++stage == nstages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -458,6 +469,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 else
                     tc_commit(&s.acc_full[b]);
             }
+            };
+            if (p.fp8)
+                issue_all(std::true_type{});
+            else
+                issue_all(std::false_type{});
             // Drain: every MMA this thread issued has completed before teardown.
             if (PAIR)
                 tc_commit_pair(s.drain);
