@@ -489,10 +489,22 @@ tpgemm_status stream_k_workspace(cudaStream_t st, float** slots, uint32_t** flag
 
 // Persistent grid: no more clusters than fit the device at once (clusters are
 // placed within GPCs, so with mc > 1 that can be fewer than SMs / mc).
+// Tuning override: at most TPGEMM_TC_MAX_CLUSTERS clusters in the persistent
+// grid (used to measure fewer, longer-lived CTAs).
+int cluster_cap(int n) {
+    if (const char* f = getenv("TPGEMM_TC_MAX_CLUSTERS")) {
+        const int c = atoi(f);
+        if (c >= 1) return std::min(n, c);
+    }
+    return n;
+}
+
 tpgemm_status fit_grid(Plan* plan) {
     tpg::TcParams& p = plan->tc;
     if (p.mc == 1) {
-        plan->max_grid = plan->sms;
+        const int n = cluster_cap(plan->sms);
+        plan->grid = std::min(p.num_super, n);
+        plan->max_grid = n;
         return TPGEMM_OK;
     }
     static std::mutex m;
@@ -507,8 +519,9 @@ tpgemm_status fit_grid(Plan* plan) {
                         cudaGetErrorString(e));
         n = v;
     }
-    plan->grid = std::min(p.num_super, n) * p.mc;
-    plan->max_grid = n * p.mc;
+    const int avail = cluster_cap(n);
+    plan->grid = std::min(p.num_super, avail) * p.mc;
+    plan->max_grid = avail * p.mc;
     return TPGEMM_OK;
 }
 
