@@ -147,3 +147,9 @@ def test_fp8_workload_full_size(name):
     else:
         err = (D.double() - ref).abs()
         assert bool((err <= bound).all()), f"{name}: max err/bound {float((err / bound).max())}"
+
+
+@pytest.mark.parametrize("M,N,K,dtype", [(4096, 16, 4096, wl.E4M3), (16, 16392, 128, wl.E5M2),
+                                         (16, 8, 16, wl.E4M3), (2048, 2056, 16, wl.E5M2)])
+def test_fp8_extreme_shapes(M, N, K, dtype):
+    check(case(M, N, K, dtype, 1.0, seed=M + N + K))

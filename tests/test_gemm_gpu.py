@@ -500,3 +500,21 @@ def test_bounded_wait_reports_timeout_and_context_survives(case, monkeypatch):
     ok, msg = oracle.compare(Dh, Dref, S)
     assert ok, msg
     assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK
+
+
+# ------------------------------------------------------------ extreme shapes
+@pytest.mark.parametrize("case", [
+    ("n8_tall", 8192, 8, 64, False, True, wl.BF16, 1.0, AUTO),
+    ("n8_tall_tc", 8192, 8, 64, True, True, wl.F16, 0.0, TC),
+    ("long_k_tiny", 16, 8, 65536, False, True, wl.F16, 0.0, AUTO),
+    ("long_k_tc", 256, 256, 16384, True, False, wl.BF16, 1.0, AUTO),
+    ("m16_wide_tc", 16, 16392, 520, False, False, wl.F16, 1.0, TC),
+    ("k8_tc", 1024, 1024, 8, False, True, wl.BF16, 1.0, TC),
+], ids=lambda c: c[0])
+def test_extreme_shapes(case):
+    name, M, N, K, tA, tB, dtype, beta, path = case
+    base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
+    w = dataclasses.replace(base.with_shape(M, N, K, seed=7000 + M + N + K), transA=tA,
+                            transB=tB, dtype=dtype, beta=beta,
+                            c_dist=("normal", 0.0, 1.0) if beta else None)
+    check_full(w, path)
