@@ -162,6 +162,23 @@ class ClockSampler:
                 "samples": len(s), "power_w_max": max(pw) if pw else None}
 
 
+# ---------------------------------------------------------- across ranks
+def max_over_ranks(ms: float, world: int, device="cpu") -> float:
+    """The slowest rank's time, on every rank (one replica per GPU: the job
+    takes as long as its slowest replica)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: the work of all replicas over the slowest one's time."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 # -------------------------------------------------------------- CPU oracle
 def oracle_sample(w, A, B, C, seconds: float, seed: int = 0):
     """Time the CPU oracle on a bounded sample of output entries of workload w.
@@ -269,13 +286,10 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     sampler.stop()
     tp.check(tp.tpgemm_last_device_error())
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     launch_ms = ms_per_step  # one launch of the kernel per step
-    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(world, w.flops, args.steps, total_ms)
     clocks = sampler.summary(t_wall0, t_wall1)
 
     # ---- end to end through the host-buffer entry point: every step copies A,
@@ -312,11 +326,8 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / ne
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * w.flops / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = job_tflops(world, w.flops, 1, e2e_ms)
 
     # ---- roofline of the (single) kernel of a step
     peaks, src = load_peaks()
