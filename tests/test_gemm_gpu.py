@@ -449,8 +449,8 @@ def test_workload_full_size(name):
 @pytest.mark.parametrize("M,N,K,tA,tB,beta", [
     (16, 8, 16, False, False, 0.0),       # one block, mma.sync
     (528, 392, 200, True, False, 1.0),    # 4 blocks of 144 (last 96), A column blocks
-    (2320, 1000, 264, False, True, 1.0),  # 8 blocks of 512 (last 272), tcgen05 per block
-    (4096, 520, 136, True, True, 0.0),
+    (2320, 1000, 264, False, True, 1.0),  # 10 blocks of 256 (last 16), tcgen05 per block
+    (4096, 520, 136, True, True, 0.0),    # 8 blocks of 512, A column blocks
 ])
 def test_gemm_host_buffers(M, N, K, tA, tB, beta):
     base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]

@@ -779,9 +779,13 @@ tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* C
     const uint8_t* hA = static_cast<const uint8_t*>(Ah);
     const uint8_t* hB = static_cast<const uint8_t*>(Bh);
 
-    // Row blocks of M, multiples of 16 (of 256 when large), at most 8 of them.
+    // Row blocks of M, multiples of 16 (of 256 when large), about 12 of them
+    // for large M: 8192^3 bf16 took 3.14 ms with 8 blocks, 3.08 with 12 and 3.12
+    // with 16 (TPGEMM_HOST_BLOCKS, 1..16, overrides the count).
     int64_t blk = M;
-    if (M >= 2048) blk = ((M / 8 + 255) / 256) * 256;
+    int want = 12;
+    if (const char* f = getenv("TPGEMM_HOST_BLOCKS")) want = std::min(16, std::max(1, atoi(f)));
+    if (M >= 2048) blk = ((M / want + 255) / 256) * 256;
     else if (M >= 512) blk = ((M / 4 + 15) / 16) * 16;
     const int nblk = int((M + blk - 1) / blk);
 
