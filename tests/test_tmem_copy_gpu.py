@@ -149,9 +149,10 @@ def test_cp_cta_group_2_pair(form):
     roundtrip(w0, words2=w1, swz=ocp.SWIZZLE_128B, lanes=lanes, shape=shape, cta_group=2)
 
 
+@pytest.mark.parametrize("issuers", [1, 2, 4])
 @pytest.mark.parametrize("form,cta_group", [(0, 1), (5, 1), (0, 2), (4, 2)],
                          ids=["128x256b", "32x128b_warpx4", "pair_128x256b", "pair_64x128b_01_23"])
-def test_cp_repeat_many_ctas(form, cta_group):
+def test_cp_repeat_many_ctas(form, cta_group, issuers):
     # Several CTAs (pairs) at once, each issuing its copy three times: every
     # CTA ends with the image of one copy.
     shape, lanes, rows, bits = FORMS[form]
@@ -168,7 +169,7 @@ def test_cp_repeat_many_ctas(form, cta_group):
     out = torch.empty(ctas * 128 * ncols, dtype=torch.int32, device="cuda")
     d = tp.cp_desc(rows, nw * 32, swizzle=swz, lbo=lbo, sbo=sbo, lanes=lanes, shape=shape,
                    cta_group=cta_group)
-    st = tp.tpgemm_cp_roundtrip_repeat(out, image, nbytes, d, 11, ncols, 3, ctas)
+    st = tp.tpgemm_cp_roundtrip_repeat(out, image, nbytes, d, 11, ncols, 3, ctas, issuers)
     assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
     torch.cuda.synchronize()
     assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK

@@ -128,7 +128,7 @@ def _load():
                                             ctypes.c_uint32, ci, vp]
         lib.tpgemm_cp_roundtrip.restype = ci
         lib.tpgemm_cp_roundtrip_repeat.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
-                                                   ctypes.c_uint32, ci, ci, ci, vp]
+                                                   ctypes.c_uint32, ci, ci, ci, ci, vp]
         lib.tpgemm_cp_roundtrip_repeat.restype = ci
         lib.tpgemm_tmem_ldst_roundtrip.argtypes = [vp, vp, vp, ci, ci, ci, ci, ctypes.c_uint32,
                                                    vp]
@@ -289,12 +289,14 @@ def tpgemm_cp_roundtrip(tmem_out, smem_image, image_bytes, desc: CpDesc, fill_ba
 
 
 def tpgemm_cp_roundtrip_repeat(tmem_out, smem_image, image_bytes, desc: CpDesc, fill_base, ncols,
-                               repeat, ctas, stream=None) -> int:
-    """The round trip on `ctas` CTAs, each issuing the planned copy `repeat` times."""
+                               repeat, ctas, issuers=1, stream=None) -> int:
+    """The round trip on `ctas` CTAs, each issuing the planned copy `repeat` times from
+    `issuers` threads."""
     return int(_load().tpgemm_cp_roundtrip_repeat(_ptr(tmem_out), _ptr(smem_image),
                                                   int(image_bytes), ctypes.byref(desc),
                                                   int(fill_base) & 0xFFFFFFFF, int(ncols),
-                                                  int(repeat), int(ctas), _stream(stream)))
+                                                  int(repeat), int(ctas), int(issuers),
+                                                  _stream(stream)))
 
 
 def tpgemm_tmem_ldst_roundtrip(regs_out, tmem_out, regs_in, st_shape, ld_shape, cols, tmem_col,

@@ -303,7 +303,8 @@ struct CpKernelParams {
     uint32_t image_words;  // 16-byte words of one CTA's image
     uint32_t fill_base;
     int n, form, ncols, alloc_cols;
-    int repeat;  // times the whole instruction list is issued before the commit
+    int repeat;   // times the whole instruction list is issued before the commit
+    int issuers;  // threads (lane 0 of warps 0..issuers-1) sharing the list, each committing
     uint32_t smem_off[kMaxCpInstr];
     uint32_t taddr[kMaxCpInstr];
 };
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(kCpThreads, 1)
         tmem_relinquish_alloc_permit<CG>();
     }
     if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
+        mbar_init(&bar, uint32_t(p.issuers));
         fence_mbarrier_init();
     }
     // The image, with 16-byte loads and stores; then made visible to the async
@@ -370,11 +371,13 @@ __global__ void __launch_bounds__(kCpThreads, 1)
         __syncthreads();
     tc_fence_after_sync();
 
-    // One thread issues the planned instructions and commits them.
-    if (threadIdx.x == 0 && rank == 0) {
+    // One thread issues the planned instructions and commits them (the page's
+    // protocol); with issuers > 1, lane 0 of each of the first `issuers` warps
+    // takes every issuers-th instruction and commits its own.
+    if (lane == 0 && warp < p.issuers && rank == 0) {
         const uint32_t base = smem_u32(buf);
         for (int k = 0; k < p.repeat; ++k)
-            for (int i = 0; i < p.n; ++i)
+            for (int i = warp; i < p.n; i += p.issuers)
                 tc_cp<CG>(p.form, tmem + p.taddr[i],
                           smem_desc_with_addr(p.desc, base + p.smem_off[i]));
         if (CG == 2)
@@ -680,13 +683,13 @@ tpgemm_status tpgemm_cp_roundtrip(uint32_t* tmem_out, const void* smem_image, si
                                   const tpgemm_cp_desc* d, uint32_t fill_base, int ncols,
                                   void* stream) {
     return tpgemm_cp_roundtrip_repeat(tmem_out, smem_image, image_bytes, d, fill_base, ncols, 1,
-                                      d ? d->cta_group : 1, stream);
+                                      d ? d->cta_group : 1, 1, stream);
 }
 
 tpgemm_status tpgemm_cp_roundtrip_repeat(uint32_t* tmem_out, const void* smem_image,
                                          size_t image_bytes, const tpgemm_cp_desc* d,
                                          uint32_t fill_base, int ncols, int repeat, int ctas,
-                                         void* stream) {
+                                         int issuers, void* stream) {
     using namespace tpg;
     set_error_detail("");
     if (!tmem_out || !smem_image) return cp_fail(TPGEMM_ERR_NULL, nullptr, "null device pointer");
@@ -702,6 +705,9 @@ tpgemm_status tpgemm_cp_roundtrip_repeat(uint32_t* tmem_out, const void* smem_im
     static thread_local CpPlan plan;
     tpgemm_status s = build_plan(d, &plan, nullptr);
     if (s != TPGEMM_OK) return s;
+    if (issuers < 1 || issuers > kCpThreads / 32)
+        return cp_fail(TPGEMM_ERR_SHAPE, nullptr, "issuers=%d must be 1..%d (one per warp)",
+                       issuers, kCpThreads / 32);
     if (repeat < 1 || repeat > (1 << 20))
         return cp_fail(TPGEMM_ERR_SHAPE, nullptr, "repeat=%d must be in 1..2^20", repeat);
     if (ctas < 1 || ctas > 65536 || ctas % d->cta_group)
@@ -731,6 +737,7 @@ tpgemm_status tpgemm_cp_roundtrip_repeat(uint32_t* tmem_out, const void* smem_im
     kp.fill_base = fill_base;
     kp.n = plan.n;
     kp.repeat = repeat;
+    kp.issuers = issuers;
     kp.form = plan.form;
     kp.ncols = ncols;
     kp.alloc_cols = 32;
