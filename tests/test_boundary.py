@@ -189,3 +189,40 @@ def test_host_path_workspace_and_rejections(lib):
     assert host(ws=None) == tp.TPGEMM_ERR_NULL
     assert host(ws=BASE + 64) == tp.TPGEMM_ERR_ALIGN
     assert host(wsb=n - 1) == tp.TPGEMM_ERR_NULL and "needed" in tp.tpgemm_last_error_detail()
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/tpgemm.h compiles as C99 and a C program links against libtpgemm.so,
+    calling entry points that need no GPU (status strings, plans, a rejection)."""
+    src = tmp_path / "use.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "tpgemm.h"
+int main(void) {
+    char buf[512];
+    tpgemm_cp_desc d;
+    tpgemm_cp_shape sh;
+    memset(&d, 0, sizeof d);
+    if (tpgemm_describe_plan(8192, 8192, 8192, 0, 1, TPGEMM_BF16, 1.0f, TPGEMM_PATH_AUTO, buf,
+                             (int)sizeof buf) != TPGEMM_OK) return 1;
+    if (strncmp(buf, "path=tcgen05", 12) != 0) return 2;
+    if (tpgemm_cp_parse_shape("64x128b", &sh) != TPGEMM_ERR_SHAPE) return 3;
+    d.rows = 128; d.row_bits = 256; d.lbo_bytes = 2048; d.sbo_bytes = 128; d.cta_group = 1;
+    if (tpgemm_cp_plan(&d, buf, (int)sizeof buf) != TPGEMM_OK) return 4;
+    if (tpgemm_gemm(NULL, NULL, NULL, NULL, 16, 8, 16, 0, 0, TPGEMM_F16, 0.0f, NULL)
+        != TPGEMM_ERR_NULL) return 5;
+    printf("%s|%s\n", tpgemm_version(), tpgemm_status_string(TPGEMM_ERR_ALIAS));
+    return 0;
+}
+""")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    libdir = os.path.dirname(tp.LIB_PATH)
+    exe = tmp_path / "use"
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-L", libdir,
+                        "-ltpgemm", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.strip() == f"{tp.tpgemm_version()}|{tp.tpgemm_status_string(6)}"
