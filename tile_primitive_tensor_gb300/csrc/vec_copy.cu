@@ -23,6 +23,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <type_traits>
 #include <string>
 
 #include "tpgemm.h"
@@ -32,7 +33,6 @@ namespace tpg {
 namespace {
 
 constexpr int kMaxSmemBytes = 200 * 1024;
-constexpr int kBatch = 4;  // vectors in flight per thread
 
 tpgemm_status vc_fail(tpgemm_status s, std::string* why, const char* fmt, ...) {
     char buf[512];
@@ -126,7 +126,8 @@ tpgemm_status vc_plan(const tpgemm_vcopy_desc* dp, VcPlan* p, std::string* why) 
 
 struct VcKernelParams {
     int rows, cols, elem_bytes, threads, vec;
-    int64_t outer;
+    int outer;           // rounds per thread
+    int step_r, step_c;  // divmod(threads * vec, cols)
     int64_t g_row_stride, g_offset, cta_stride;
     int s_row_stride, s_offset, swizzle_mask;  // mask of the 16-byte chunk XOR (0: none)
     int smem_bytes;
@@ -155,23 +156,39 @@ struct VecT<1> {
     using T = uint8_t;
 };
 
-// Byte offsets of the vector starting at fused element e (global relative to
-// this CTA's region base, shared after the swizzle).
-__device__ __forceinline__ void vc_addr(const VcKernelParams& p, int64_t e, int64_t& g,
-                                        uint32_t& s) {
-    const int64_t r = e / p.cols;
-    const int64_t c = e - r * p.cols;
-    g = (p.g_offset + r * p.g_row_stride + c) * p.elem_bytes;
-    uint32_t a = uint32_t((p.s_offset + r * p.s_row_stride + c) * p.elem_bytes);
-    s = a ^ (((a >> 7) & uint32_t(p.swizzle_mask)) << 4);
-}
+// Thread tid's vectors start at fused elements e = (f T + tid) v, f = 0, 1, ...
+// The region fits in shared memory, so e, its row r = e / cols and its column
+// c = e % cols are 32-bit; one division places the first vector and each later
+// one moves (r, c) on by (step_r, step_c) = divmod(T v, cols) with one carry.
+struct VcCursor {
+    int r, c;
+    __device__ __forceinline__ void advance(const VcKernelParams& p) {
+        r += p.step_r;
+        c += p.step_c;
+        if (c >= p.cols) {
+            c -= p.cols;
+            ++r;
+        }
+    }
+    // Byte offset in global memory (from this CTA's region base).
+    __device__ __forceinline__ int64_t global(const VcKernelParams& p) const {
+        return (p.g_offset + int64_t(r) * p.g_row_stride + c) * p.elem_bytes;
+    }
+    // Byte offset in shared memory, after the 16-byte chunk XOR.
+    __device__ __forceinline__ uint32_t shared(const VcKernelParams& p) const {
+        const uint32_t a = uint32_t((p.s_offset + r * p.s_row_stride + c) * p.elem_bytes);
+        return a ^ (((a >> 7) & uint32_t(p.swizzle_mask)) << 4);
+    }
+};
 
 // global -> shared -> global for this CTA's region; with smem_out, the shared
 // buffer (zeroed first, so bytes outside the region are defined) is written out
-// between the two copies.
-template <int VB>
-__global__ void __launch_bounds__(1024) vcopy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
-                             uint8_t* __restrict__ smem_out, const VcKernelParams p) {
+// between the two copies. Rounds go in batches of kBatch: all of a batch's loads
+// are issued before its stores, so each thread keeps kBatch vectors in flight.
+template <int VB, int kBatch, int kMaxThreads>
+__global__ void __launch_bounds__(kMaxThreads)
+    vcopy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
+                 uint8_t* __restrict__ smem_out, const VcKernelParams p) {
     using T = typename VecT<VB>::T;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x;
@@ -181,18 +198,19 @@ __global__ void __launch_bounds__(1024) vcopy_kernel(uint8_t* __restrict__ dst, 
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
         __syncthreads();
     }
-    // Serial rounds: round f, thread tid owns elements [(f T + tid) v, + v).
-    // Rounds go in batches of kBatch: all of a batch's loads are issued before
-    // its stores, so each thread keeps kBatch vectors in flight.
-    for (int64_t f0 = 0; f0 < p.outer; f0 += kBatch) {
+    VcCursor first;
+    first.r = tid * p.vec / p.cols;
+    first.c = tid * p.vec - first.r * p.cols;
+    VcCursor at = first;
+    for (int f0 = 0; f0 < p.outer; f0 += kBatch) {
         T v[kBatch];
         uint32_t so[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             if (f0 + u < p.outer) {
-                int64_t g;
-                vc_addr(p, ((f0 + u) * p.threads + tid) * p.vec, g, so[u]);
-                v[u] = *reinterpret_cast<const T*>(src + base + g);
+                so[u] = at.shared(p);
+                v[u] = *reinterpret_cast<const T*>(src + base + at.global(p));
+                at.advance(p);
             }
         }
 #pragma unroll
@@ -205,15 +223,16 @@ __global__ void __launch_bounds__(1024) vcopy_kernel(uint8_t* __restrict__ dst, 
         for (int i = tid; i < p.smem_bytes / 16; i += p.threads)
             o[i] = reinterpret_cast<const uint4*>(smem)[i];
     }
-    for (int64_t f0 = 0; f0 < p.outer; f0 += kBatch) {
+    at = first;
+    for (int f0 = 0; f0 < p.outer; f0 += kBatch) {
         T v[kBatch];
         int64_t go[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             if (f0 + u < p.outer) {
-                uint32_t so;
-                vc_addr(p, ((f0 + u) * p.threads + tid) * p.vec, go[u], so);
-                v[u] = *reinterpret_cast<const T*>(smem + so);
+                go[u] = at.global(p);
+                v[u] = *reinterpret_cast<const T*>(smem + at.shared(p));
+                at.advance(p);
             }
         }
 #pragma unroll
@@ -277,7 +296,9 @@ tpgemm_status tpgemm_vcopy_roundtrip(void* dst, const void* src, size_t buffer_b
     kp.elem_bytes = d->elem_bytes;
     kp.threads = d->threads;
     kp.vec = p.vec;
-    kp.outer = p.outer;
+    kp.outer = int(p.outer);
+    kp.step_r = d->threads * p.vec / d->cols;
+    kp.step_c = d->threads * p.vec % d->cols;
     kp.g_row_stride = d->g_row_stride;
     kp.g_offset = d->g_offset;
     kp.cta_stride = cta_stride;
@@ -299,13 +320,21 @@ tpgemm_status tpgemm_vcopy_roundtrip(void* dst, const void* src, size_t buffer_b
             e = cudaGetLastError();
         }
     };
-    switch (p.vec_bytes) {
-        case 16: launch(vcopy_kernel<16>); break;
-        case 8: launch(vcopy_kernel<8>); break;
-        case 4: launch(vcopy_kernel<4>); break;
-        case 2: launch(vcopy_kernel<2>); break;
-        default: launch(vcopy_kernel<1>); break;
-    }
+    auto dispatch = [&](auto small) {
+        constexpr bool S = decltype(small)::value;
+        constexpr int B = S ? 8 : 4, T = S ? 256 : 1024;
+        switch (p.vec_bytes) {
+            case 16: launch(vcopy_kernel<16, B, T>); break;
+            case 8: launch(vcopy_kernel<8, B, T>); break;
+            case 4: launch(vcopy_kernel<4, B, T>); break;
+            case 2: launch(vcopy_kernel<2, B, T>); break;
+            default: launch(vcopy_kernel<1, B, T>); break;
+        }
+    };
+    if (d->threads <= 256)
+        dispatch(std::true_type{});
+    else
+        dispatch(std::false_type{});
     if (e != cudaSuccess)
         return vc_fail(TPGEMM_ERR_LAUNCH, nullptr, "copy kernel launch: %s", cudaGetErrorString(e));
     return TPGEMM_OK;
