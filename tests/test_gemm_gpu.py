@@ -471,8 +471,10 @@ def test_gemm_host_buffers(M, N, K, tA, tB, beta):
 
 
 # ------------------------------------------------------- failure detection
+@pytest.mark.parametrize("producers", ["1", "4"])
 @pytest.mark.parametrize("case", ["one_cta", "pair", "swapped_small"])
-def test_bounded_wait_reports_timeout_and_context_survives(case, monkeypatch):
+def test_bounded_wait_reports_timeout_and_context_survives(case, producers, monkeypatch):
+    monkeypatch.setenv("TPGEMM_TC_PRODUCERS", producers)
     # A stage fill that never arrives (no TMA is issued for it) must not hang
     # the GPU: the kernel's bounded wait expires, the status word is set, every
     # role stops, in-flight copies and MMAs drain, tensor memory is freed, and
@@ -518,3 +520,98 @@ def test_extreme_shapes(case):
                             transB=tB, dtype=dtype, beta=beta,
                             c_dist=("normal", 0.0, 1.0) if beta else None)
     check_full(w, path)
+
+
+# ------------------------------------------------- P rows per tile (bp < 128)
+# Single-wave plans whose tiles share the one Q tile give each CTA bp < 128 P
+# rows. Lanes bp .. 127 of the accumulator then hold results nobody stores; a
+# lane quadrant half inside the tile (bp = 80, 112) uses the half-width C / D
+# boxes, quadrants past bp are idle, and an MN-contiguous P tile is one full
+# 64-row box plus a narrower one. Every combination is checked against the
+# oracle; the last tile along P is ragged.
+@pytest.mark.parametrize("bp", [64, 80, 96, 112, 128])
+@pytest.mark.parametrize("orient,tA,tB", [
+    ("swap", False, False),   # P = B^T MN-contiguous
+    ("swap", False, True),    # P = B^T K-contiguous
+    ("normal", False, True),  # P = A K-contiguous
+    ("normal", True, True),   # P = A MN-contiguous
+])
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_p_rows_per_tile(bp, orient, tA, tB, beta, monkeypatch):
+    monkeypatch.setenv("TPGEMM_TC_ORIENT", orient)
+    monkeypatch.setenv("TPGEMM_TC_BP", str(bp))
+    M, N = (144, 1304) if orient == "swap" else (1040, 200)
+    base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
+    w = dataclasses.replace(base.with_shape(M, N, 264, seed=7100 + bp + int(tA) + 2 * int(tB)),
+                            transA=tA, transB=tB, dtype=wl.F16, beta=beta,
+                            c_dist=("normal", 0.0, 1.0) if beta else None)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert st == tp.TPGEMM_OK and f"tile={bp}x" in text and f"orientation={'swapped' if orient == 'swap' else 'normal'}" in text, text
+    check_full(w, TC)
+
+
+@pytest.mark.parametrize("bp", [80, 112])
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_p_rows_integer_bit_exact_and_in_place(bp, pair, monkeypatch):
+    # Integer-valued inputs: exact. Then D = C in place over the same plan.
+    monkeypatch.setenv("TPGEMM_TC_BP", str(bp))
+    monkeypatch.setenv("TPGEMM_TC_PAIR", pair)
+    w = wl.WORKLOAD_4096_INT.with_shape(144, 2072, 520, seed=7200 + bp)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert f"tile={bp}x" in text and f"pair={pair}" in text, text
+    check_full(w, TC)
+    w1 = dataclasses.replace(wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(
+        144, 2072, 264, seed=7250 + bp))
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w1)
+    D = run_gpu(w1, Ad, Bd, Cd, TC, D=Cd)
+    Dref, S = oracle_full(w1, A, B, C)
+    ok, msg = oracle.compare(D, Dref, S)
+    assert ok, msg
+
+
+@pytest.mark.parametrize("bp", [64, 112])
+@pytest.mark.parametrize("name", ["skinny_144x16392x4112_e4m3_transB_beta1"])
+def test_p_rows_fp8(bp, name, monkeypatch):
+    monkeypatch.setenv("TPGEMM_TC_BP", str(bp))
+    w = wl.BY_NAME[name].with_shape(144, 2072, 528, seed=7300 + bp)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert f"tile={bp}x" in text and "kind=f8f6f4" in text, text
+    check_full(w, TC)
+
+
+def test_p_rows_default_skinny_plan():
+    # The planner's own choice for the 144 x 16392 x 4104 shape: 112 rows, one wave.
+    st, text = tp.tpgemm_describe_plan(144, 16392, 4104, 0, 0, wl.F16, 1.0, TC)
+    assert st == tp.TPGEMM_OK and "tile=112x144x64" in text and "grid=148" in text, text
+
+
+# ------------------------------------------------ several TMA-issuing threads
+# Fill g of the ring is issued by producer g % P (warp 0, then warps 6, 7, 8).
+# The K order of the MMAs does not depend on P, so every P gives the same bits;
+# each is also checked against the oracle. Cases: multi-wave with a tail split
+# (one epilogue group: warps 6..8 only produce), single-wave with two epilogue
+# groups (warps 6..8 produce, then run their epilogue), no CTA pair, stream-K,
+# fp8 and a two-stage ring (P capped at the ring depth).
+@pytest.mark.parametrize("case", [
+    ("multi_wave_tail", "gemm_256_bf16_transB_beta1", 2048, 2560, 264, {"TPGEMM_TC_BN": "256"}),
+    ("single_wave_two_groups", "skinny_144x16392x4104_f16_beta1", 144, 4104, 520, {}),
+    ("no_pair", "gemm_4096_f16", 784, 1320, 264, {"TPGEMM_TC_PAIR": "0"}),
+    ("stream_k", "gemm_256_bf16_transB_beta1", 1024, 1024, 2048, {"TPGEMM_TC_SK": "1"}),
+    ("fp8", "gemm_4096_e4m3_int_transB", 1024, 1536, 528, {}),
+    ("two_stages", "gemm_4096_f16", 512, 768, 520, {"TPGEMM_TC_STAGES": "2"}),
+], ids=lambda c: c[0])
+def test_producer_counts(case, monkeypatch):
+    name, wname, M, N, K, env = case
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    w = wl.BY_NAME[wname].with_shape(M, N, K, seed=7400 + M + K)
+    out = []
+    for n in ("1", "2", "3", "4"):
+        monkeypatch.setenv("TPGEMM_TC_PRODUCERS", n)
+        st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+        assert st == tp.TPGEMM_OK, text
+        stages = int(text.split("stages=")[1].split()[0])
+        assert f"producers={min(int(n), stages)}" in text, text
+        out.append(check_full(w, TC))
+    for D in out[1:]:
+        assert np.array_equal(out[0].view(np.uint32), D.view(np.uint32))

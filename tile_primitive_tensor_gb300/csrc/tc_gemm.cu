@@ -41,7 +41,6 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 namespace {
 
-constexpr int kBM = 128;           // P rows per tile (tensor-memory lanes)
 constexpr int kBK = 64;            // 16-bit K elements per stage: one 128-byte swizzle row
 constexpr int kUmmaK = 16;         // 16-bit K per tcgen05.mma (kind::f16); 32 for fp8
 constexpr int kEpiWarps = kTcEpiWarps;  // two per lane quadrant
@@ -218,7 +217,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
                    const __grid_constant__ CUtensorMap mapQt, const __grid_constant__ CUtensorMap mapW,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap mapPh, const __grid_constant__ CUtensorMap mapCh,
+                   const __grid_constant__ CUtensorMap mapDh, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
@@ -236,11 +236,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------------------------------------------------------- set-up
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&mapP);
+        if (p.p_mn) prefetch_tensormap(&mapPh);
         prefetch_tensormap(&mapQ);
         if (p.tail_split > 1) prefetch_tensormap(&mapQt);
         if (p.sk) prefetch_tensormap(&mapW);
         if (p.beta) prefetch_tensormap(&mapC);
         prefetch_tensormap(&mapD);
+        if (p.bp % 32) {
+            if (p.beta) prefetch_tensormap(&mapCh);
+            prefetch_tensormap(&mapDh);
+        }
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&s.full[i], 1);
             // Freed by the MMA thread of every CTA sharing the stage (one
@@ -282,11 +287,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t cphase = 0;         // epilogue: bit i = parity of the next C fill of buffer i
     uint32_t cpend = 0;          // epilogue: bit i = a C fill into staging buffer i in flight
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+    // ---------------------------------------------------------- TMA producers
+    // Lane 0 of warp 0 and, with p.producers > 1, of warps 6, 7, 8 (the second
+    // epilogue warpgroup, which has no epilogue work before an accumulator is
+    // ready, and none at all in one-group plans). Producer r issues the fills
+    // of ring iterations g = r, r + P, r + 2P, ..., so one thread's wake-up and
+    // issue latency sits on the path of only every P-th fill. With P no larger
+    // than the ring, a producer waiting on a stage's empty barrier is never
+    // more than one phase behind it.
+    const int prod_r = warp == 0 ? 0 : ((warp >= 6 && warp - 5 < p.producers) ? warp - 5 : -1);
+    // The producer's body is inline (not a lambda): kernel parameters are then
+    // read from parameter space, not through a generic reference, which the
+    // TMA issue's memory clobbers would reload on every fill.
+    if (prod_r >= 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            // Whose fill the current ring iteration is: producer `turn`, cycling
+            // through 0 .. producers - 1 over every fill of the CTA.
+            int turn = 0;
+            const int nprod = p.producers;
             bool ok = true;
             SegIter iter(cid, ncl, p);
             Seg u;
@@ -294,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (; ok && iter.next(ncl, p, u); first_seg = false) {
                 int tps, tq;
                 tile_coords(u.T, p, tps, tq);
-                const int p0 = (tps * p.mc + rank) * kBM;
+                const int p0 = (tps * p.mc + rank) * p.bp;
                 const int q0 = tq * p.bn + u.q_off;
                 // Q rows this CTA loads per stage, and the bytes they fill.
                 const int q_rows = PAIR ? u.width / 2 : u.width;
@@ -302,11 +322,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // K-contiguous Q: one box per stage, from the map whose box
                 // height is this unit's share (whole tile or tail unit).
                 const CUtensorMap* mq = u.width == p.bn ? &mapQ : &mapQt;
-                const uint32_t tx = p.p_bytes + (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
-                                                        : uint32_t(q_rows) * 128u);
+                const uint32_t tx = p.p_tx + (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
+                                                     : uint32_t(q_rows) * 128u);
                 const int nk = u.kb1 - u.kb0;
                 int kb = nk == p.k_blocks ? first_k_block(u.T, p) : u.kb0;
-                for (int i = 0; i < nk; ++i, kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
+                for (int i = 0; i < nk;
+                     ++i, turn = (turn + 1 == nprod) ? 0 : turn + 1,
+                     kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
+                    if (turn != prod_r) {  // another producer's fill
+                        if (++stage == p.stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     if (!wait_phase(&s.empty[stage], phase ^ 1u, s.abort, tmo)) {
                         ok = false;
                         break;
@@ -331,7 +360,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * tx);
                         if (p.p_mn) {
                             tma_load_2d_pair(sp, &mapP, fb, p0, k0);
-                            tma_load_2d_pair(sp + kAtomBytes, &mapP, fb, p0 + 64, k0);
+                            if (p.bp > 64)
+                                tma_load_2d_pair(sp + kAtomBytes, &mapPh, fb, p0 + 64, k0);
                         } else {
                             tma_load_2d_pair(sp, &mapP, fb, k0, p0);
                         }
@@ -353,7 +383,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_expect_tx(&s.full[stage], tx);
                     if (p.p_mn) {
                         tma_load_2d(sp, &mapP, &s.full[stage], p0, k0);
-                        tma_load_2d(sp + kAtomBytes, &mapP, &s.full[stage], p0 + 64, k0);
+                        if (p.bp > 64)
+                            tma_load_2d(sp + kAtomBytes, &mapPh, &s.full[stage], p0 + 64, k0);
                     } else {
                         tma_load_2d(sp, &mapP, &s.full[stage], k0, p0);
                     }
@@ -386,7 +417,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+        if (warp != 0) __syncwarp();  // a second-group warp goes on to its epilogue
+    }
+    if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         // (in pair mode only the leader CTA issues, for both CTAs)
         if (lane == 0 && (!PAIR || rank == 0)) {
@@ -481,7 +514,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_commit(s.drain);
             wait_phase(s.drain, 0, s.abort, tmo, true);
         }
-    } else if (warp < 2 + kEpiQuads * p.epi_groups) {
+    } else if (warp >= 2 && warp < 2 + kEpiQuads * p.epi_groups) {
+        // (A producing warp of the second group has issued its fills first.)
         // --------------------------------------------------------- epilogue
         const int ew = warp - 2;           // 0 .. 4 epi_groups - 1
         const int quad = warp & 3;         // tensor-memory lane quadrant of this warp
@@ -503,10 +537,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int tps, tq;
             tile_coords(u.T, p, tps, tq);
             const int tp = tps * p.mc + rank;
-            const int pw = tp * kBM + quad * 32;  // first P row of this warp's quadrant
+            const int pw = tp * p.bp + quad * 32;  // first P row of this warp's quadrant
             const int q0 = tq * p.bn + u.q_off;
             const int nchunks = (u.width + 31) / 32;
-            const bool warp_live = pw < lim_p;
+            // Lanes of this quadrant inside the tile's bp rows: 32, 16 (the
+            // half-width boxes) or none.
+            const int q_lanes = min(32, p.bp - quad * 32);
+            const bool half_q = q_lanes == 16;
+            const bool warp_live = pw < lim_p && q_lanes > 0;
             int live_chunks = 0;
             if (warp_live) live_chunks = min(nchunks, (lim_q - q0 + 31) / 32);
             // This warp's chunks: c = ng j + half for j < my_chunks.
@@ -527,8 +565,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             auto slot_y = [&](int slot, int c) {
                 return slot * p.sk_slot_rows + (SWAP ? 32 * c : qw);
             };
-            const CUtensorMap* src_map = from_slot ? &mapW : &mapC;
-            const CUtensorMap* dst_map = to_slot ? &mapW : &mapD;
+            // Stream-K plans keep bp = 128, so a half quadrant never uses a slot.
+            const CUtensorMap* src_map = from_slot ? &mapW : (half_q ? &mapCh : &mapC);
+            const CUtensorMap* dst_map = to_slot ? &mapW : (half_q ? &mapDh : &mapD);
+            const uint32_t src_bytes = half_q ? kEpiBufFloats * 2 : kEpiBufFloats * 4;
             auto src_x = [&](int c) { return from_slot ? slot_x(c) : box_x(c); };
             auto src_y = [&](int c) { return from_slot ? slot_y(src_slot, c) : box_y(c); };
             auto dst_x = [&](int c) { return to_slot ? slot_x(c) : box_x(c); };
@@ -552,7 +592,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int j = 0; j < nbw && j < my_chunks; ++j) {
                     const int c = ng * j + half;
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&cb[j], kEpiBufFloats * 4);
+                        mbar_arrive_expect_tx(&cb[j], src_bytes);
                         tma_load_2d(bufs + j * kEpiBufFloats, src_map, &cb[j], src_x(c), src_y(c));
                     }
                     cpend |= 1u << j;
@@ -631,7 +671,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (add_src && j + nbw < my_chunks) {
                         const int cn = c + ng * nbw;  // this warp's chunk j + nbw
                         bulk_wait_group_read<0>();  // the store just issued has read buf
-                        mbar_arrive_expect_tx(&cb[bi], kEpiBufFloats * 4);
+                        mbar_arrive_expect_tx(&cb[bi], src_bytes);
                         tma_load_2d(buf, src_map, &cb[bi], src_x(cn), src_y(cn));
                     }
                 }
@@ -677,7 +717,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // An aborted CTA lets every TMA fill it issued land before it exits.
         // (In pair mode both CTAs' fills complete on the leader's barriers,
         // so the leader drains for both before the final cluster sync.)
-        if (warp == 0 && lane == 0 && (!PAIR || rank == 0))
+        if (prod_r >= 0 && lane == 0 && (!PAIR || rank == 0))
             for (int i = 0; i < p.stages; ++i)
                 if (issued_any & (1u << i))
                     wait_phase(&s.full[i], (issued_parity >> i) & 1u, s.abort, tmo, true);
@@ -701,7 +741,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }  // namespace
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
-                            CUtensorMap, TcParams);
+                            CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
 
 TcKernelFn pick_kernel(const TcParams& p) {
     if (p.pair) return p.swap ? tc_gemm_kernel<true, true> : tc_gemm_kernel<false, true>;
@@ -717,6 +757,7 @@ size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_buf
 
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
     if (p.epi_bufs < 2 || p.epi_bufs > kTcMaxEpiBufs || p.stages < 2 || p.stages > 32 ||
+        p.producers < 1 || p.producers > 4 || p.producers > p.stages ||
         !(p.epi_groups == 1 || p.epi_groups == 2) ||
         !(p.mc == 1 || p.mc == 2 || p.mc == 4) || grid % p.mc != 0 || (p.pair && p.mc != 2) ||
         !(p.tmem_cols == 64 || p.tmem_cols == 128 || p.tmem_cols == 256 || p.tmem_cols == 512) ||
@@ -745,7 +786,8 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.mc > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, maps.Qt, maps.W, p);
+    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, maps.Qt, maps.W, maps.Ph,
+                              maps.Ch, maps.Dh, p);
 }
 
 cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters) {

@@ -233,6 +233,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.Nq = int(Nq);
     p.K = int(K);
     p.bn = bn;
+    p.bp = 128;
     p.tiles_p = int((Mp + 127) / 128);
     p.tiles_q = int((Nq + bn - 1) / bn);
     p.num_tiles = p.tiles_p * p.tiles_q;
@@ -260,6 +261,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     const int q_rows = p.pair ? bn / 2 : bn;  // Q rows this CTA loads per stage
     p.idesc = tpg::idesc_f16_f32(format_code1(dtype), p_mn, q_mn, p.pair ? 256 : 128, bn);
     p.p_bytes = stage_tile_bytes(128, p_mn);
+    p.p_tx = 128u * 128u;
     p.q_bytes = stage_tile_bytes(q_rows, q_mn);
     p.q_boxes = q_mn ? uint32_t((q_rows + 63) / 64) : 1u;
     p.tx_bytes = p.p_bytes + p.q_bytes;
@@ -347,6 +349,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.q_box_rows = p.pair ? bn / 2 : bn / p.mc;
     if (stages == 0) return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
     p.stages = stages;
+    p.producers = 1;  // set with the grid (choose_producers)
     p.epi_bufs = epi_bufs;
     p.epi_groups = 1;  // set with the grid (choose_epi_groups)
     // The epilogue stores 32-column boxes; a tile width that is not a multiple
@@ -440,6 +443,55 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
     p.q_box_rows = p.pair ? p.bn / 2 : p.bn / p.mc;
 }
 
+// P rows per tile. A single-wave plan whose tiles all share the one Q tile
+// (small M, or small N in the swapped orientation) streams P from memory once
+// and is bound by each streaming SM's load rate (measured on 144 x N x 4104 f16:
+// 128 -> 152 SMs streaming the same bytes each took 33.9 -> 35.8 us for 19 %
+// more data), so it gives each CTA fewer P rows and uses more SMs: the
+// smallest bp of 64 .. 112 (steps of 16) whose tiles still fit one wave.
+// Stream-K plans keep 128 rows (their scratch slots are whole tiles).
+// TPGEMM_TC_BP (64 .. 128, a multiple of 16) overrides where it fits one wave.
+void choose_p_rows(tpg::TcParams& p, int* grid, int max_grid, bool sk_requested) {
+    if (sk_requested || p.tiles_q != 1 || p.bp != 128) return;
+    const int avail = std::max(1, max_grid / p.mc);
+    if (p.num_super > avail) return;
+    auto supers = [&](int bp) {
+        const int tiles = int((int64_t(p.Mp) + bp - 1) / bp);
+        return (tiles + p.mc - 1) / p.mc;
+    };
+    auto fits = [&](int bp) {
+        const int tiles = int((int64_t(p.Mp) + bp - 1) / bp);
+        return supers(bp) <= avail && (!p.pair || tiles >= 2);
+    };
+    int bp = 128;
+    for (int c = 64; c < 128; c += 16)
+        if (fits(c)) {
+            bp = c;
+            break;
+        }
+    if (const char* f = getenv("TPGEMM_TC_BP")) {
+        const int v = atoi(f);
+        if (v >= 64 && v <= 128 && v % 16 == 0 && fits(v)) bp = v;
+    }
+    if (bp == 128) return;
+    p.bp = bp;
+    p.p_tx = uint32_t(bp) * 128u;
+    p.tx_bytes = p.p_tx + p.q_bytes;
+    p.tiles_p = int((int64_t(p.Mp) + bp - 1) / bp);
+    p.num_tiles = p.tiles_p * p.tiles_q;
+    p.tiles_ps = supers(bp);
+    p.num_super = p.tiles_ps * p.tiles_q;
+    p.full_units = p.num_super;
+    p.num_units = p.num_super;
+    *grid = p.num_super * p.mc;
+}
+
+bool stream_k_requested(bool force_sk) {
+    if (force_sk) return true;
+    const char* f = getenv("TPGEMM_TC_SK");
+    return f && atoi(f) != 0;
+}
+
 // Epilogue warpgroups. With at most one work unit per cluster (a single wave)
 // no later tile's MMAs run under the epilogue, so both warpgroups drain it;
 // with more, one group keeps up and the second only competes with the MMA and
@@ -452,6 +504,30 @@ void choose_epi_groups(tpg::TcParams& p, int grid) {
         const int v = atoi(f);
         if (v == 1 || v == 2) p.epi_groups = v;
     }
+}
+
+// TMA-issuing threads: warp 0, and with more than one producer warps 6, 7, 8,
+// fill g going to producer g % producers. One issuing thread puts its own
+// wake-up and issue latency on the path of every fill; two halve that and
+// issue the first ring fill twice as fast. Measured on GB300 against one
+// producer: 144 x 16392 x 4104 32.9 -> 32.7 us, 4096^3 105 -> 98.8 us; on
+// 8192^3 (power-capped, 14 work units per cluster) a second producer cost
+// 0.4 % and four 1 %, so plans with 8 or more units per cluster keep one.
+// Warps 6, 7, 8 belong to the second epilogue warpgroup; when that group is
+// active they issue their fills before their epilogue work, which is only
+// safe when the cluster has a single work unit (with more, the MMA of a third
+// unit would wait for an epilogue they have not reached).
+// TPGEMM_TC_PRODUCERS (1..4) overrides within those limits.
+void choose_producers(tpg::TcParams& p, int grid) {
+    const int ncl = std::max(1, grid / p.mc);
+    const int units_per_cluster = (p.num_units + ncl - 1) / ncl;
+    int n = std::min(units_per_cluster >= 8 ? 1 : 2, p.stages);
+    if (const char* f = getenv("TPGEMM_TC_PRODUCERS")) {
+        const int v = atoi(f);
+        if (v >= 1 && v <= 4) n = std::min(v, p.stages);
+    }
+    if (p.epi_groups == 2 && (p.sk || p.num_units > ncl)) n = 1;
+    p.producers = n;
 }
 
 // Stream-K scratch per (device, stream): allocated on first use, kept until
@@ -572,16 +648,25 @@ tpgemm_status encode_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map,
 
 // Map of a K x rows operand: K-contiguous -> dims {K, rows}, box {64, box_rows};
 // MN-contiguous -> dims {rows, K}, box {64, 64}.
+CUtensorMapDataType operand_type(tpgemm_dtype dtype) {
+    return is_fp8(dtype)          ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+           : dtype == TPGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// mn_box: MN-contiguous box width along MN (default: the whole 64-row atom).
+// A box narrower than the 128-byte swizzle row fills the leading 16-byte
+// units of each row, in the same swizzled positions as a full box (measured
+// on GB300), so it is the leading part of the atom.
 tpgemm_status encode_operand(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map,
                              const void* base, tpgemm_dtype dtype, int64_t rows, int64_t K, bool mn,
-                             int box_rows, const char* what) {
-    const CUtensorMapDataType t = is_fp8(dtype)          ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                  : dtype == TPGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+                             int box_rows, const char* what, int mn_box = 0) {
+    const CUtensorMapDataType t = operand_type(dtype);
     const int eb = elem_bytes(dtype);
     const uint32_t row_elems = uint32_t(128 / eb);  // one 128-byte swizzle row
     if (mn)
-        return encode_2d(enc, map, base, t, eb, uint64_t(rows), uint64_t(K), row_elems, 64, what);
+        return encode_2d(enc, map, base, t, eb, uint64_t(rows), uint64_t(K),
+                         mn_box > 0 ? uint32_t(mn_box) : row_elems, 64, what);
     return encode_2d(enc, map, base, t, eb, uint64_t(K), uint64_t(rows), row_elems,
                      uint32_t(box_rows), what);
 }
@@ -632,13 +717,25 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     // P / Q operands: normal P = A (rows M), Q = B^T (rows N); swapped P = B^T, Q = A.
     const void* pp = plan.swap ? B : A;
     const void* qq = plan.swap ? A : B;
-    s = encode_operand(enc, &maps.P, pp, dtype, p.Mp, K, p.p_mn, 128, "P operand");
-    if (s != TPGEMM_OK) return s;
     s = fit_grid(&plan);
     if (s != TPGEMM_OK) return s;
+    choose_p_rows(plan.tc, &plan.grid, plan.max_grid,
+                  stream_k_requested(scratch == Scratch::Static));
     apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code1(dtype),
                      scratch == Scratch::Static);
+    // P: K-contiguous, one box of bp rows; MN-contiguous, a 64-row atom from
+    // maps.P and rows 64 .. bp - 1 from maps.Ph.
+    s = encode_operand(enc, &maps.P, pp, dtype, p.Mp, K, p.p_mn, p.bp, "P operand");
+    if (s != TPGEMM_OK) return s;
+    if (p.p_mn && p.bp > 64) {
+        s = encode_operand(enc, &maps.Ph, pp, dtype, p.Mp, K, true, 0,
+                           "P operand (rows 64 .. bp of a tile)", p.bp - 64);
+        if (s != TPGEMM_OK) return s;
+    } else {
+        maps.Ph = maps.P;
+    }
     choose_epi_groups(plan.tc, plan.grid);
+    choose_producers(plan.tc, plan.grid);
     s = encode_operand(enc, &maps.Q, qq, dtype, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
     if (s != TPGEMM_OK) return s;
     if (p.tail_split > 1) {
@@ -694,6 +791,21 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
         s = encode_2d(enc, &maps.C, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M),
                       32, 32, "C");
         if (s != TPGEMM_OK) return s;
+    }
+    // Half-quadrant boxes (16 tensor-memory lanes = 16 P rows): 16 rows of D
+    // (normal) or 16 columns (swapped), read from the same swizzled staging tile.
+    maps.Dh = maps.D;
+    maps.Ch = maps.C;
+    if (p.bp % 32) {
+        const uint32_t hx = plan.swap ? 16 : 32, hy = plan.swap ? 32 : 16;
+        s = encode_2d(enc, &maps.Dh, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N),
+                      uint64_t(M), hx, hy, "D (half-quadrant box)");
+        if (s != TPGEMM_OK) return s;
+        if (p.beta) {
+            s = encode_2d(enc, &maps.Ch, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N),
+                          uint64_t(M), hx, hy, "C (half-quadrant box)");
+            if (s != TPGEMM_OK) return s;
+        }
     }
     cudaError_t e = tpg::launch_tc(maps, p, plan.grid, st);
     if (e != cudaSuccess)
@@ -959,8 +1071,10 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     if (s != TPGEMM_OK) return s;
     char text[512];
     if (plan.kernel == Kernel::Tc) {
+        choose_p_rows(plan.tc, &plan.grid, plan.max_grid, stream_k_requested(false));
         apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code1(dtype));
         choose_epi_groups(plan.tc, plan.grid);
+        choose_producers(plan.tc, plan.grid);
     }
     if (plan.kernel == Kernel::MmaSync) {
         snprintf(text, sizeof(text),
@@ -970,12 +1084,12 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     } else {
         const tpg::TcParams& p = plan.tc;
         snprintf(text, sizeof(text),
-                 "path=tcgen05 orientation=%s tile=128x%dx%d umma=%dx%dx%d kind=%s stages=%d "
-                 "epi_bufs=%d epi_groups=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d "
+                 "path=tcgen05 orientation=%s tile=%dx%dx%d umma=%dx%dx%d kind=%s stages=%d "
+                 "epi_bufs=%d epi_groups=%d producers=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d "
                  "grid=%d units=%d+%dx%d stream_k=%d p_major=%s q_major=%s smem=%zu",
-                 plan.swap ? "swapped" : "normal", p.bn, p.bk, p.pair ? 256 : 128, p.bn,
+                 plan.swap ? "swapped" : "normal", p.bp, p.bn, p.bk, p.pair ? 256 : 128, p.bn,
                  p.fp8 ? 32 : 16, p.fp8 ? "f8f6f4" : "f16", p.stages,
-                 p.epi_bufs, p.epi_groups, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
+                 p.epi_bufs, p.epi_groups, p.producers, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
                  p.full_units, p.num_super - p.full_units, p.tail_split, p.sk, p.p_mn ? "mn" : "k",
                  p.q_mn ? "mn" : "k",
                  tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));

@@ -44,7 +44,14 @@ cudaError_t launch_mma_sync(const MmaSyncArgs& a, cudaStream_t stream);
 // which the epilogue writes back transposed so that D stays [M, N].
 struct TcParams {
     int Mp, Nq, K;          // rows of P, rows of Q, reduction length
-    int tiles_p, tiles_q;   // tile counts along P (128 rows) and Q (bn rows)
+    int tiles_p, tiles_q;   // tile counts along P (bp rows) and Q (bn rows)
+    // P rows of one CTA's tile: 128 (every tensor-memory lane), or 64..112 in
+    // steps of 16 for single-wave plans whose tiles share the one Q tile, so
+    // that more SMs stream P. Lanes bp..127 then hold unused results; the lane
+    // quadrant holding row bp - 16 (when bp % 32 == 16) stores through the
+    // half-width C / D maps.
+    int bp;
+    uint32_t p_tx;          // bytes the P boxes deliver per stage (bp rows of 128 bytes)
     int num_tiles;
     int k_blocks;           // ceil(K / 64)
     int bn;                 // accumulator columns per tile = UMMA N (16..256, %16)
@@ -66,6 +73,8 @@ struct TcParams {
     int epi_groups;         // active epilogue warpgroups (1 or 2); warp 2 + 4 g + i
                             // reads lane quadrant (i + 2) % 4, chunks c % groups == g
     int k_rotate;           // 0, or tiles per group sharing a rotated first K block
+    int producers;          // TMA-issuing threads (1..4, at most the ring depth): warp 0,
+                            // then warps 6, 7, 8; fill g is issued by producer g % producers
     int mc;                 // CTAs per cluster sharing one Q tile (1, 2 or 4): each
                             // loads 1/mc of it and multicasts it to the others
     int tiles_ps;           // groups of mc consecutive P tiles: ceil(tiles_p / mc)
@@ -99,6 +108,8 @@ struct TcParams {
 
 struct TcMaps {
     CUtensorMap P, Q, C, D;
+    CUtensorMap Ph;         // MN-contiguous P: box of P rows 64 .. bp - 1 of a tile
+    CUtensorMap Ch, Dh;     // C / D with a half-quadrant box (16 tensor-memory lanes)
     CUtensorMap Qt;         // Q with the (narrower) box of a tail unit
     CUtensorMap W;          // stream-K scratch slots, laid out like D tiles
 };
