@@ -615,3 +615,36 @@ def test_producer_counts(case, monkeypatch):
         out.append(check_full(w, TC))
     for D in out[1:]:
         assert np.array_equal(out[0].view(np.uint32), D.view(np.uint32))
+
+
+# ---------------------------------------- back-to-back launches on one stream
+# Each launch may start while the previous one drains (programmatic dependent
+# launch). Its threads wait for the previous grid before their first global
+# access: after set-up (dep_early = 0) or each just before it (dep_early = 1).
+# Four in-place accumulations D += A.B issued back to back read the D the
+# previous launch is still writing; integer inputs make D = C0 + 4 A.B exact.
+@pytest.mark.parametrize("early", ["0", "1"])
+@pytest.mark.parametrize("case", [
+    ("skinny_single_wave", "skinny_144x16392x4104_f16_beta1", 144, 4104, 520),
+    ("multi_wave", "gemm_4096_f16", 2320, 2600, 264),
+    ("fp8", "gemm_4096_e4m3_int_transB", 1024, 1536, 528),
+], ids=lambda c: c[0])
+def test_chained_in_place_launches(case, early, monkeypatch):
+    name, wname, M, N, K = case
+    monkeypatch.setenv("TPGEMM_TC_DEP_EARLY", early)
+    base = wl.BY_NAME[wname].with_shape(M, N, K, seed=7500 + M)
+    w = dataclasses.replace(base, a_dist=("int", -3, 3), b_dist=("int", -3, 3),
+                            c_dist=("int", -8, 8), beta=1.0)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert st == tp.TPGEMM_OK and f"dep_early={early}" in text, text
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+    D = Cd.clone()
+    for _ in range(4):
+        st = tp.tpgemm_gemm_path(D, Ad, Bd, D, w.M, w.N, w.K, w.transA, w.transB, w.dtype,
+                                 1.0, None, TC)
+        assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    w0 = dataclasses.replace(w, beta=0.0, c_dist=None)
+    AB, S = oracle_full(w0, A, B, None)
+    ok, msg = oracle.compare(D.cpu().numpy(), C.numpy() + 4.0 * AB, 4.0 * S, exact=True)
+    assert ok, msg

@@ -212,7 +212,7 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t v, volatil
     }
 }
 
-template <bool SWAP, bool PAIR>
+template <bool SWAP, bool PAIR, bool EARLY>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
@@ -275,10 +275,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     else
         __syncthreads();
     tc_fence_after_sync();
-    // Set-up above overlaps the previous grid's tail when launched with a
-    // programmatic dependency; global memory is touched only after this wait.
+    // Launched with a programmatic dependency, this grid starts while the
+    // previous one drains; griddepcontrol.wait then holds each thread that
+    // calls it until that grid has finished and its writes are visible. With
+    // EARLY (p.dep_early), only the threads that touch global memory wait, each just
+    // before its first access: a producer before its first K loop, an
+    // epilogue warp before its first C load or D store. Until then the
+    // producers run their first work unit's bookkeeping, whose instruction
+    // fetch otherwise costs about 1 us after the wait on a 144 x 16392 x 4104
+    // step (measured on GB300); the MMA warp (shared and tensor memory only)
+    // never waits. Otherwise every thread waits here.
     grid_launch_dependents();
-    grid_dependency_wait();
+    if constexpr (!EARLY) grid_dependency_wait();
     const uint32_t tmem = *s.tmem_base;
     const uint64_t tmo = p.timeout_ns;
     // In-flight bookkeeping kept to teardown, where an aborted CTA drains it.
@@ -326,6 +334,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                      : uint32_t(q_rows) * 128u);
                 const int nk = u.kb1 - u.kb0;
                 int kb = nk == p.k_blocks ? first_k_block(u.T, p) : u.kb0;
+                if constexpr (EARLY) {
+                    if (first_seg) grid_dependency_wait();
+                }
                 for (int i = 0; i < nk;
                      ++i, turn = (turn + 1 == nprod) ? 0 : turn + 1,
                      kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
@@ -517,6 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp >= 2 && warp < 2 + kEpiQuads * p.epi_groups) {
         // (A producing warp of the second group has issued its fills first.)
         // --------------------------------------------------------- epilogue
+        if constexpr (EARLY) grid_dependency_wait();
         const int ew = warp - 2;           // 0 .. 4 epi_groups - 1
         const int quad = warp & 3;         // tensor-memory lane quadrant of this warp
         const EpiShare es = epi_share(s, p, ew);
@@ -743,9 +755,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                             CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
 
+template <bool EARLY>
+TcKernelFn pick_kernel_dep(const TcParams& p) {
+    if (p.pair)
+        return p.swap ? tc_gemm_kernel<true, true, EARLY> : tc_gemm_kernel<false, true, EARLY>;
+    return p.swap ? tc_gemm_kernel<true, false, EARLY> : tc_gemm_kernel<false, false, EARLY>;
+}
+
+// The early-start choice is a template parameter, not a runtime test: a
+// runtime test of it cost 8192^3 about 1.4 % (same register use).
 TcKernelFn pick_kernel(const TcParams& p) {
-    if (p.pair) return p.swap ? tc_gemm_kernel<true, true> : tc_gemm_kernel<false, true>;
-    return p.swap ? tc_gemm_kernel<true, false> : tc_gemm_kernel<false, false>;
+    return p.dep_early ? pick_kernel_dep<true>(p) : pick_kernel_dep<false>(p);
 }
 
 

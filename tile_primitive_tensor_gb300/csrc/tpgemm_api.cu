@@ -528,6 +528,12 @@ void choose_producers(tpg::TcParams& p, int grid) {
     }
     if (p.epi_groups == 2 && (p.sk || p.num_units > ncl)) n = 1;
     p.producers = n;
+    // Early start: each thread waits for the previous grid just before its
+    // first global access (measured on GB300: 144 x 16392 x 4104 32.9 -> 31.9
+    // us, 4096^3 96.5 -> 96.0 us, 8192^3 unchanged). TPGEMM_TC_DEP_EARLY=0
+    // makes every thread wait after set-up.
+    p.dep_early = 1;
+    if (const char* f = getenv("TPGEMM_TC_DEP_EARLY")) p.dep_early = atoi(f) != 0;
 }
 
 // Stream-K scratch per (device, stream): allocated on first use, kept until
@@ -1085,11 +1091,11 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
         const tpg::TcParams& p = plan.tc;
         snprintf(text, sizeof(text),
                  "path=tcgen05 orientation=%s tile=%dx%dx%d umma=%dx%dx%d kind=%s stages=%d "
-                 "epi_bufs=%d epi_groups=%d producers=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d "
+                 "epi_bufs=%d epi_groups=%d producers=%d dep_early=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d "
                  "grid=%d units=%d+%dx%d stream_k=%d p_major=%s q_major=%s smem=%zu",
                  plan.swap ? "swapped" : "normal", p.bp, p.bn, p.bk, p.pair ? 256 : 128, p.bn,
                  p.fp8 ? 32 : 16, p.fp8 ? "f8f6f4" : "f16", p.stages,
-                 p.epi_bufs, p.epi_groups, p.producers, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
+                 p.epi_bufs, p.epi_groups, p.producers, p.dep_early, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
                  p.full_units, p.num_super - p.full_units, p.tail_split, p.sk, p.p_mn ? "mn" : "k",
                  p.q_mn ? "mn" : "k",
                  tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));

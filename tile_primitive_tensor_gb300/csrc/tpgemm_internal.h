@@ -73,6 +73,8 @@ struct TcParams {
     int epi_groups;         // active epilogue warpgroups (1 or 2); warp 2 + 4 g + i
                             // reads lane quadrant (i + 2) % 4, chunks c % groups == g
     int k_rotate;           // 0, or tiles per group sharing a rotated first K block
+    int dep_early;          // 1: only threads touching global memory wait for the previous
+                            // grid, each just before its first access; 0: all wait after set-up
     int producers;          // TMA-issuing threads (1..4, at most the ring depth): warp 0,
                             // then warps 6, 7, 8; fill g is issued by producer g % producers
     int mc;                 // CTAs per cluster sharing one Q tile (1, 2 or 4): each
