@@ -389,6 +389,11 @@ CP_REGIONS = [  # (form, lane pattern, rows, row bits): 16 KB or less per CTA pe
 ]
 
 
+# Issuing threads measured per tcgen05.cp form (lane 0 of warps 0..n-1 of the
+# round-trip kernel); the reported value is the largest count's.
+CP_ISSUERS = (1, 4, 8)
+
+
 def run_primitive_cp(args):
     """Shared-memory -> tensor-memory copy throughput of every tcgen05.cp form.
 
@@ -427,7 +432,7 @@ def run_primitive_cp(args):
         region = rows * bits // 8
         instr = (rows // 4 if lanes == 1 else 1) * (bits // (256 if shape in (1, 2) else 128))
         forms[name] = {"bytes_per_cta_copy": region, "instructions": instr}
-        for issuers in (1, 4):
+        for issuers in CP_ISSUERS:
             for _ in range(3):
                 go(repeat, issuers)
             torch.cuda.synchronize()
@@ -452,8 +457,10 @@ def run_primitive_cp(args):
     peak = sms * 128 * mhz * 1e6 / 1e9
     for f in forms.values():
         f["frac"] = round(f["GB_per_s"] / peak, 4)
-        f["frac_4_issuers"] = round(f["GB_per_s_4_issuers"] / peak, 4)
+        for i in CP_ISSUERS[1:]:
+            f[f"frac_{i}_issuers"] = round(f[f"GB_per_s_{i}_issuers"] / peak, 4)
     best = forms["128x256b"]
+    top = CP_ISSUERS[-1]
     # The oracle beside it: rebuilding the expected tensor memory of one CTA's
     # 128x256b copy on the host cores.
     import numpy as np
@@ -471,18 +478,19 @@ def run_primitive_cp(args):
                                        "(oracle.tmem_cp.tmem_image)"}
     return {
         "metric": "tcgen05.cp shared->tensor memory copy bandwidth (shared-memory bytes read)",
-        "value": best["GB_per_s_4_issuers"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "value": best[f"GB_per_s_{top}_issuers"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "higher_is_better": True, "dtype": "b32", "data": "synthetic (random bytes)",
         "config": {"workload": "tcgen05_cp_128B_swizzle", "ctas": sms, "repeat": repeat},
         "clocks": clocks,
-        "roofline": {"bound": "smem", "achieved": best["GB_per_s_4_issuers"],
-                     "peak": round(peak, 1), "unit": "GB/s", "frac": best["frac_4_issuers"],
+        "roofline": {"bound": "smem", "achieved": best[f"GB_per_s_{top}_issuers"],
+                     "peak": round(peak, 1), "unit": "GB/s", "frac": best[f"frac_{top}_issuers"],
+                     "issuers": top,
                      "single_issuer_frac": best["frac"],
                      "peak_kind": f"derived: {sms} SMs x 128 B/clk x {mhz:.0f} MHz (sampled)",
                      "traffic": None},
         "forms": forms,
         "cpu_baseline": cpu,
-        "gpu_launches": 4 * args.steps * len(CP_REGIONS),
+        "gpu_launches": 2 * len(CP_ISSUERS) * args.steps * len(CP_REGIONS),
     }
 
 

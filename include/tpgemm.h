@@ -294,7 +294,7 @@ tpgemm_status tpgemm_cp_roundtrip(uint32_t* tmem_out, const void* smem_image, si
  * cta_group 2) reads the same image(s); CTA k writes rows [128 k, 128 k + 128)
  * of tmem_out, which must hold ctas * 128 * ncols words. With repeat > 1 the
  * later copies rewrite the same cells, so the result is that of one copy.
- * issuers (1..4): threads that share the list, lane 0 of warps 0..issuers-1,
+ * issuers (1..8): threads that share the list, lane 0 of warps 0..issuers-1,
  * each taking every issuers-th instruction and committing its own to the
  * mbarrier (1 is the single-thread protocol of the page; a tcgen05.cp holds
  * its issuing thread for about 90 ns, so more issuers copy proportionally

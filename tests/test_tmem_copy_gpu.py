@@ -149,7 +149,7 @@ def test_cp_cta_group_2_pair(form):
     roundtrip(w0, words2=w1, swz=ocp.SWIZZLE_128B, lanes=lanes, shape=shape, cta_group=2)
 
 
-@pytest.mark.parametrize("issuers", [1, 2, 4])
+@pytest.mark.parametrize("issuers", [1, 2, 4, 8])
 @pytest.mark.parametrize("form,cta_group", [(0, 1), (5, 1), (0, 2), (4, 2)],
                          ids=["128x256b", "32x128b_warpx4", "pair_128x256b", "pair_64x128b_01_23"])
 def test_cp_repeat_many_ctas(form, cta_group, issuers):

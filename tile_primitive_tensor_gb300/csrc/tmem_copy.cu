@@ -36,7 +36,7 @@ namespace {
 
 constexpr int kMaxCpInstr = 256;
 constexpr uint32_t kMaxImageBytes = 196608;
-constexpr int kCpThreads = 128;
+constexpr int kCpThreads = 256;  // 8 warps: up to 8 issuers; warps 0..3 hold the lane quadrants
 
 struct Form {
     const char* name;
@@ -353,17 +353,22 @@ __global__ void __launch_bounds__(kCpThreads, 1)
         __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base;
+    // Warps 0..3 reach tensor-memory lane quadrants 0..3; warps 4..7 only
+    // stage the image and issue.
+    const bool quad_warp = warp < 4;
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
     const uint32_t row = uint32_t(warp * 32 + lane);
 
     // Every column that is read back starts from a known value.
-    for (int c = 0; c < p.ncols; c += 8) {
-        uint32_t v[8];
+    if (quad_warp) {
+        for (int c = 0; c < p.ncols; c += 8) {
+            uint32_t v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = p.fill_base + row * 65536u + uint32_t(c + j);
-        tmem_st_32x32b_x8(tmem + lane_base + uint32_t(c), v);
+            for (int j = 0; j < 8; ++j) v[j] = p.fill_base + row * 65536u + uint32_t(c + j);
+            tmem_st_32x32b_x8(tmem + lane_base + uint32_t(c), v);
+        }
+        tmem_st_wait();
     }
-    tmem_st_wait();
     tc_fence_before_sync();
     if (CG == 2)
         cluster_sync();
@@ -391,7 +396,7 @@ __global__ void __launch_bounds__(kCpThreads, 1)
         ok = cp_wait(&bar, p.timeout_ns);  // let the copies finish before dealloc
     }
     tc_fence_after_sync();
-    if (ok) {
+    if (ok && quad_warp) {
         uint32_t* o = out + (size_t(blockIdx.x) * 128 + row) * size_t(p.ncols);
         for (int c = 0; c < p.ncols; c += 8) {
             uint32_t v[8];
