@@ -1,9 +1,12 @@
 // tcgen05 GEMM for sm_103a:  X = P . Q^T (+ C), f16/bf16 (or e4m3/e5m2) in, f32
 // accumulate and out.
 //
-// Persistent, warp-specialised CTA of 10 warps, one CTA per SM:
+// Persistent, warp-specialised CTA of 10 warps, one CTA per SM (or per SM of
+// a CTA pair); a tile has bp <= 128 P rows, one per tensor-memory lane:
 //   warp 0      TMA producer: one thread fills a ring of shared-memory stages
-//               with 128-byte-swizzled P and Q tiles (cp.async.bulk.tensor).
+//               with 128-byte-swizzled P and Q tiles (cp.async.bulk.tensor);
+//               with the plan's producers > 1, lane 0 of warps 6, 7, 8 issues
+//               every producers-th fill as well.
 //   warp 1      owns tensor memory (tcgen05.alloc / dealloc, whole warp) and
 //               one thread issues tcgen05.mma for every 16-deep K step into a
 //               double-buffered accumulator, committing stage releases and
