@@ -648,3 +648,4 @@ def test_chained_in_place_launches(case, early, monkeypatch):
     AB, S = oracle_full(w0, A, B, None)
     ok, msg = oracle.compare(D.cpu().numpy(), C.numpy() + 4.0 * AB, 4.0 * S, exact=True)
     assert ok, msg
+
