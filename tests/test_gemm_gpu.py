@@ -649,3 +649,44 @@ def test_chained_in_place_launches(case, early, monkeypatch):
     ok, msg = oracle.compare(D.cpu().numpy(), C.numpy() + 4.0 * AB, 4.0 * S, exact=True)
     assert ok, msg
 
+
+
+# ------------------------------------------- several host threads, own streams
+def test_concurrent_host_threads_own_streams():
+    # Four host threads each run a different plan (tcgen05 pair, one CTA per
+    # tile, the swapped skinny plan, mma.sync) five times on their own stream.
+    # The library's caches are shared under its locks and the error detail is
+    # per thread; every result is checked against the oracle.
+    import concurrent.futures
+
+    base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
+    shapes = [(512, 512, 256, {}), (784, 1320, 264, {}), (144, 2072, 264, {}), (64, 64, 72, {})]
+    works = []
+    for i, (M, N, K, _) in enumerate(shapes):
+        w = dataclasses.replace(base.with_shape(M, N, K, seed=7800 + i), transB=bool(i % 2),
+                                beta=1.0, c_dist=("normal", 0.0, 1.0))
+        (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+        Dref, S = oracle_full(w, A, B, C)
+        works.append((w, Ad, Bd, Cd, Dref, S))
+    torch.cuda.synchronize()
+
+    def run(idx):
+        w, Ad, Bd, Cd, Dref, S = works[idx]
+        stream = torch.cuda.Stream()
+        outs = []
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                D = torch.empty(w.M, w.N, device="cuda")
+                st = tp.tpgemm_gemm(D, Ad, Bd, Cd, w.M, w.N, w.K, w.transA, w.transB, w.dtype,
+                                    w.beta, stream)
+                assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+                outs.append(D)
+        stream.synchronize()
+        return [oracle.compare(D.cpu().numpy(), Dref, S) for D in outs]
+
+    with concurrent.futures.ThreadPoolExecutor(4) as ex:
+        results = list(ex.map(run, range(len(works))))
+    for res in results:
+        for ok, msg in res:
+            assert ok, msg
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK
