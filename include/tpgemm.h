@@ -82,7 +82,9 @@ typedef enum {
  * D, A, B, C: device pointers, 16-byte aligned, layouts as above. D == C is
  *   allowed (in-place D += A·B when beta == 1); any other overlap of D with A,
  *   B or C is rejected with TPGEMM_ERR_ALIAS.
- * M, N, K: logical sizes, positive, M % 16 == 0, N % 8 == 0, K % 8 == 0.
+ * M, N, K: logical sizes, positive, M % 16 == 0, N % 8 == 0, K % 8 == 0, each
+ *   below 2^30, with M·N <= 2^36 and M·K, K·N <= 2^37 elements (no operand larger
+ *   than one GPU holds); otherwise TPGEMM_ERR_SHAPE.
  * transA, transB: 0 or non-zero; select the stored orientation of A and B.
  * dtype: one of tpgemm_dtype (the fp8 ones with the orientation and K rules above).
  * beta: exactly 0.0f or 1.0f.

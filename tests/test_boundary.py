@@ -57,6 +57,8 @@ def test_status_strings(lib):
     (8, 64, 64, "M=8"), (64, 12, 64, "N=12"), (64, 64, 4, "K=4"), (0, 64, 64, "positive"),
     (64, -8, 64, "positive"), (64, 64, 0, "positive"), (24, 64, 64, "M=24"),
     (1 << 30, 64, 64, "2^30"),
+    (1 << 19, 1 << 18, 64, "one GPU's memory"), (1 << 20, 64, 1 << 18, "one GPU's memory"),
+    (64, 1 << 20, 1 << 18, "one GPU's memory"),
 ])
 def test_rejects_shape(lib, M, N, K, frag):
     st, why = call(M=M, N=N, K=K)

@@ -109,6 +109,13 @@ tpgemm_status check_shape(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype, f
     const int64_t lim = int64_t(1) << 30;
     if (M >= lim || N >= lim || K >= lim)
         return fail(TPGEMM_ERR_SHAPE, "M, N, K must each be below 2^30");
+    // No operand larger than one GPU can hold (this also keeps tile counts,
+    // whose product is at most M N / 2^11, within 32 bits).
+    if (M * N > (int64_t(1) << 36) || M * K > (int64_t(1) << 37) || K * N > (int64_t(1) << 37))
+        return fail(TPGEMM_ERR_SHAPE,
+                    "M=%lld N=%lld K=%lld: an operand exceeds one GPU's memory (at most 2^36 "
+                    "elements of C / D and 2^37 of A or B)",
+                    (long long)M, (long long)N, (long long)K);
     if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16 && !is_fp8(dtype))
         return fail(TPGEMM_ERR_DTYPE,
                     "dtype %d is not TPGEMM_F16 (0), TPGEMM_BF16 (1), TPGEMM_E4M3 (2) or "
