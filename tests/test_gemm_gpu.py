@@ -512,6 +512,8 @@ def test_bounded_wait_reports_timeout_and_context_survives(case, producers, monk
     ("long_k_tc", 256, 256, 16384, True, False, wl.BF16, 1.0, AUTO),
     ("m16_wide_tc", 16, 16392, 520, False, False, wl.F16, 1.0, TC),
     ("k8_tc", 1024, 1024, 8, False, True, wl.BF16, 1.0, TC),
+    ("m16_n131072", 16, 131072, 64, False, False, wl.F16, 1.0, TC),
+    ("m65536_n16", 65536, 16, 128, True, True, wl.BF16, 1.0, TC),
 ], ids=lambda c: c[0])
 def test_extreme_shapes(case):
     name, M, N, K, tA, tB, dtype, beta, path = case
