@@ -7,12 +7,17 @@ hot path (TMA ring -> tcgen05.mma -> tensor-memory epilogue with beta.C) in
 one kernel launch. The default workload is the 8192^3 bf16 problem with B
 stored [N, K] and beta = 1, the shape the GEMM TFLOP/s metric is quoted on.
 
-Prints ONE JSON line (rank 0): metric, value (whole-job TFLOP/s), timing,
-clocks sampled during the timed region, the roofline of the kernel, an
-end-to-end number through host buffers, and the CPU oracle timed on a bounded
-sample of the same workload. ``--impl reference`` times that oracle alone, as
-the reference arm. With several GPUs (torchrun) every rank runs an independent
-replica: the method has no exchange step.
+Prints ONE JSON line: metric, value (TFLOP/s), timing, clocks sampled during
+the timed region, the roofline of the kernel, an end-to-end number through host
+buffers, the other measured configurations (4096^3 f16, and the skinny
+144 x 16392 x 4104 shape both with L2 flushed before every launch and back to
+back), and the CPU oracle timed on a bounded sample of the same workload.
+``--impl reference`` times that oracle alone, as the reference arm.
+
+The design is single-GPU: the multiply has no exchange step, and more GPUs
+would only run independent copies of it, which this program does not do.
+``--gpus`` above 1 (or a launch with WORLD_SIZE above 1) is refused with a
+message, except for the reference arm, whose ranks other than 0 exit quietly.
 """
 from __future__ import annotations
 
@@ -43,7 +48,7 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
@@ -59,7 +64,11 @@ def parse_args():
     ap.add_argument("--flush-l2", action="store_true",
                     help="overwrite a buffer larger than L2 before every timed step (the GEMM "
                          "alone is timed, with events around each launch)")
-    return ap.parse_args()
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations (4096^3, skinny cold and warm)")
+    ap.add_argument("--config-steps", type=int, default=50,
+                    help="timed launches per configuration of the configs block")
+    return ap.parse_args(argv)
 
 
 def code_only(src: str) -> str:
@@ -118,32 +127,111 @@ def load_traffic(workload: str):
 
 
 # ------------------------------------------------------------------ clocks
-class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons for one GPU."""
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*).
+_NVML_REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                 "hw_thermal_slowdown": 0x40}
 
-    FIELDS = ("timestamp,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
-              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+
+class _Nvml:
+    """The few read-only NVML queries the sampler needs, through ctypes on the
+    driver's libnvidia-ml (no Python NVML package is required)."""
+
+    NVML_CLOCK_SM = 1
 
     def __init__(self, bus_id: str | None):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        r = -1
+        if bus_id:
+            r = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.dev))
+        if r != 0:
+            r = self.lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.dev))
+        if r != 0:
+            raise OSError("no NVML device handle")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_sm = self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.NVML_CLOCK_SM)
+
+    def _uint(self, fn, *args):
+        v = self.c.c_uint()
+        if fn(self.dev, *args, self.c.byref(v)) != 0:
+            return None
+        return v.value
+
+    def sample(self) -> dict | None:
+        sm = self._uint(self.lib.nvmlDeviceGetClockInfo, self.NVML_CLOCK_SM)
+        if sm is None:
+            return None
+        mw = self._uint(self.lib.nvmlDeviceGetPowerUsage)
+        rs = self.c.c_ulonglong()
+        bits = rs.value if self.reasons_fn(self.dev, self.c.byref(rs)) == 0 else 0
+        d = {"t": time.time(), "sm": float(sm), "sm_max": float(self.max_sm or sm),
+             "power": None if mw is None else mw / 1000.0}
+        d.update({k: bool(bits & m) for k, m in _NVML_REASONS.items()})
+        return d
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+class ClockSampler:
+    """SM clock, power and clock-event reasons of one GPU during a timed region.
+
+    NVML is polled about every millisecond from a thread, so even a region of
+    a few milliseconds holds samples; when NVML cannot be loaded, nvidia-smi
+    samples every 50 ms. The summary uses only samples taken inside the
+    region; if none fell inside it the clocks are null, with the reason."""
+
+    SMI_FIELDS = ("timestamp,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+                  "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None, period_s: float = 0.001):
         self.bus_id = (bus_id or "").lower()
+        self.period = period_s
         self.samples = []
+        self.source = None
         self.proc = None
         self.thread = None
+        self.stop_flag = threading.Event()
 
     def start(self):
         try:
+            nvml = _Nvml(self.bus_id or None)
+        except (OSError, AttributeError):
+            nvml = None
+        if nvml is not None:
+            self.source = f"nvml every {self.period * 1e3:g} ms"
+            self.thread = threading.Thread(target=self._poll, args=(nvml,), daemon=True)
+            self.thread.start()
+            return
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi every 50 ms"
+        self.thread = threading.Thread(target=self._read_smi, daemon=True)
         self.thread.start()
 
-    def _read(self):
+    def _poll(self, nvml):
+        try:
+            while not self.stop_flag.is_set():
+                d = nvml.sample()
+                if d is not None:
+                    self.samples.append(d)
+                time.sleep(self.period)
+        finally:
+            nvml.close()
+
+    def _read_smi(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
@@ -164,6 +252,7 @@ class ClockSampler:
                 continue
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -173,35 +262,39 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self, t0: float, t1: float):
-        s = [x for x in self.samples if t0 <= x["t"] <= t1]
-        if not s:
-            s = self.samples[-3:]
-        if not s:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        reasons = [r for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                               "sw_power_cap") if any(x[r] for x in s)]
-        pw = [x["power"] for x in s if x["power"] is not None]
-        return {"sm_mhz": statistics.median(x["sm"] for x in s),
-                "sm_max_mhz": max(x["sm_max"] for x in s), "reasons": reasons,
-                "samples": len(s), "power_w_max": max(pw) if pw else None}
+    def summary(self, t0: float, t1: float) -> dict:
+        return summarize_clocks(self.samples, t0, t1, self.source)
 
 
-# ---------------------------------------------------------- across ranks
-def max_over_ranks(ms: float, world: int, device="cpu") -> float:
-    """The slowest rank's time, on every rank (one replica per GPU: the job
-    takes as long as its slowest replica)."""
-    if world <= 1:
-        return ms
-    import torch
-    t = torch.tensor([ms], device=device, dtype=torch.float64)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    return float(t.item())
+def summarize_clocks(samples, t0: float, t1: float, source) -> dict:
+    """Median SM clock, max clock and active reasons of the samples taken in
+    [t0, t1]; null clocks with a reason when no sample fell inside."""
+    s = [x for x in samples if t0 <= x["t"] <= t1]
+    if not s:
+        why = ("no clock sampler could be started" if source is None else
+               f"no sample ({source}) fell inside the {1e3 * (t1 - t0):.1f} ms timed region")
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                "source": source, "null_reason": why}
+    reasons = [r for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                           "sw_power_cap") if any(x[r] for x in s)]
+    pw = [x["power"] for x in s if x["power"] is not None]
+    return {"sm_mhz": statistics.median(x["sm"] for x in s),
+            "sm_max_mhz": max(x["sm_max"] for x in s), "reasons": reasons,
+            "samples": len(s), "power_w_max": max(pw) if pw else None, "source": source}
 
 
-def job_tflops(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
-    """Whole-job throughput: the work of all replicas over the slowest one's time."""
-    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+def host_cpu() -> dict:
+    """Model name and logical CPU count of the host the oracle runs on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return {"cpu_model": model, "logical_cpus": os.cpu_count()}
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -238,34 +331,156 @@ def sample_text(n, w):
             f"full {w.K}-long fp64 dot product from the 16-bit operands (oracle_gemm_entries)")
 
 
+def oracle_full(w, A, B, C):
+    """Seconds the CPU oracle takes for the whole output of workload w."""
+    import oracle
+    oracle.build()
+    Ab, Bb = wl.bits(A), wl.bits(B)
+    Cn = None if C is None else C.numpy()
+    t = time.perf_counter()
+    oracle.gemm(Ab, Bb, Cn, w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+    return time.perf_counter() - t
+
+
+# Whole-output oracle runs reported beside the sampled baseline: the shapes the
+# oracle finishes in seconds on the host cores.
+FULL_ORACLE_WORKLOADS = ("atom_16x8x16_f16_int", "gemm_256_bf16_transB_beta1",
+                         "skinny_144x16392x4104_f16_beta1")
+
+
 # ---------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
+class Problem:
+    """One workload's operands resident on the device and its launch."""
+
+    def __init__(self, tp, w, dev, stream):
+        import torch
+        self.tp, self.w = tp, w
+        self.A, self.B, self.C = wl.make_inputs(w)
+        self.Ad, self.Bd = self.A.to(dev), self.B.to(dev)
+        self.Cd = None if self.C is None else self.C.to(dev)
+        self.D = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
+        self.sh = int(stream.cuda_stream)
+        self.lib = tp.library()
+        self.args = (self.D.data_ptr(), self.Ad.data_ptr(), self.Bd.data_ptr(),
+                     None if self.Cd is None else self.Cd.data_ptr(), w.M, w.N, w.K,
+                     int(w.transA), int(w.transB), w.dtype, float(w.beta), self.sh)
+        self.plan = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype,
+                                            w.beta)[1]
+
+    def step(self):
+        st = self.lib.tpgemm_gemm(*self.args)
+        if st != 0:
+            raise RuntimeError(f"tpgemm_gemm: {st} {self.tp.tpgemm_last_error_detail()}")
+
+    def release(self):
+        del self.Ad, self.Bd, self.Cd, self.D
+
+
+def time_back_to_back(step, stream, steps: int) -> float:
+    """Total ms of `steps` launches between two events. No event sits between
+    launches: one there would stop the next launch's set-up from overlapping
+    the previous launch (programmatic dependent launch)."""
+    import torch
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1)
+
+
+def time_cold(step, stream, steps: int, scrub) -> list:
+    """ms of each launch timed alone, after a write of a buffer larger than L2
+    (outside its events), so every launch starts from a cold L2."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        scrub.fill_(1.0)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def roofline_of(w, launch_ms: float, peaks: dict, src: str) -> dict:
+    """Achieved rate of one launch against the bound of its workload: tensor
+    peak above the ridge point, HBM bandwidth below it."""
+    # fp8 runs at twice the dense bf16 rate (nominal 4.5 / 2.25 PFLOP/s): its
+    # peak is the measured bf16 one times that ratio.
+    ratio = 2.0 if w.dtype in (wl.E4M3, wl.E5M2) else 1.0
+    t_peak = peaks["bf16_tflops"] * ratio
+    t_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
+    ridge = t_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
+    if w.flops / w.algorithmic_bytes > ridge:
+        achieved = w.flops / (launch_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(t_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / t_peak, 4),
+                "peak_kind": f"{src} bf16 dense burst" + (
+                    " x 2 (nominal fp8 : bf16 ratio)" if ratio != 1.0 else ""),
+                "frac_of_sustained": round(achieved / t_sust, 4)}
+    achieved = w.algorithmic_bytes / (launch_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "peak_kind": f"{src} HBM copy bandwidth"}
+
+
+def config_entry(w, ms: float, peaks: dict, src: str, how: str) -> dict:
+    r = roofline_of(w, ms, peaks, src)
+    return {"us": round(ms * 1e3, 2), "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2),
+            "gbs": round(w.algorithmic_bytes / (ms * 1e-3) / 1e9, 1), "bound": r["bound"],
+            "frac": r["frac"], "of": r["peak_kind"], "timing": how}
+
+
+def measure_configs(args, tp, dev, stream, scrub, peaks, src) -> dict:
+    """The other targets: 4096^3 f16 (tensor-bound) back to back, and the skinny
+    144 x 16392 x 4104 shape (HBM-bound) both cold (L2 flushed before every
+    launch, each launch timed alone) and back to back."""
+    import torch
+    out = {}
+    n = max(3, args.config_steps)
+    for name, modes in (("gemm_4096_f16", ("warm",)),
+                        ("skinny_144x16392x4104_f16_beta1", ("cold", "warm"))):
+        w = wl.BY_NAME[name]
+        pr = Problem(tp, w, dev, stream)
+        for _ in range(5):
+            pr.step()
+        torch.cuda.synchronize()
+        e = {"plan": pr.plan}
+        if "cold" in modes:
+            t = sorted(time_cold(pr.step, stream, n, scrub))
+            e["cold"] = config_entry(w, statistics.median(t), peaks, src,
+                                     f"median of {n} launches, each alone after a "
+                                     f"{scrub.numel() * 4 >> 20} MB write")
+            e["cold"]["best_us"] = round(t[0] * 1e3, 2)
+        if "warm" in modes:
+            ms = time_back_to_back(pr.step, stream, n) / n
+            e["warm"] = config_entry(w, ms, peaks, src,
+                                     f"mean of {n} launches back to back, no L2 flush")
+        tp.check(tp.tpgemm_last_device_error())
+        pr.release()
+        torch.cuda.empty_cache()
+        out[name] = e
+    return out
+
+
+def run_ours(args):
     import torch
 
     import tile_primitive_tensor_gb300 as tp
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     w = wl.BY_NAME[args.workload]
-    A, B, C = wl.make_inputs(w)
-    Ad, Bd = A.to(dev), B.to(dev)
-    Cd = None if C is None else C.to(dev)
-    D = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    sh = int(stream.cuda_stream)
-    lib = tp.library()
-    plan = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)[1]
-    dp, ap_, bp = D.data_ptr(), Ad.data_ptr(), Bd.data_ptr()
-    cp = None if Cd is None else Cd.data_ptr()
-
-    def step():
-        st = lib.tpgemm_gemm(dp, ap_, bp, cp, w.M, w.N, w.K, int(w.transA), int(w.transB),
-                             w.dtype, float(w.beta), sh)
-        if st != 0:
-            raise RuntimeError(f"tpgemm_gemm: {st} {tp.tpgemm_last_error_detail()}")
+    pr = Problem(tp, w, dev, stream)
+    A, B, C = pr.A, pr.B, pr.C
 
     for _ in range(args.warmup):
-        step()
+        pr.step()
     torch.cuda.synchronize()
     tp.check(tp.tpgemm_last_device_error())
 
@@ -276,50 +491,38 @@ def run_ours(args, rank, world, local_rank):
               f"{getattr(props, 'pci_device_id', 0):02x}.0"
     sampler = ClockSampler(bus)
     sampler.start()
-    time.sleep(0.4)  # let nvidia-smi start before the timed region
+    time.sleep(0.2)  # let the sampler start before the timed region
+    # 512 MB: larger than L2 (129 MB), written before each launch in the cold modes.
+    scrub = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
 
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     if args.flush_l2:
-        # Cold L2 for every step: a 512 MB write between launches, outside the
-        # per-launch events.
-        scrub = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for a, b in evs:
-            scrub.fill_(1.0)
-            a.record(stream)
-            step()
-            b.record(stream)
-        torch.cuda.synchronize()
-        total_ms = sum(a.elapsed_time(b) for a, b in evs)
+        total_ms = sum(time_cold(pr.step, stream, args.steps, scrub))
     else:
-        # Events only around the whole timed loop: an event between two launches
-        # would stop the next launch's set-up from overlapping the previous one.
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        total_ms = ev0.elapsed_time(ev1)
+        total_ms = time_back_to_back(pr.step, stream, args.steps)
     t_wall1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
     sampler.stop()
     tp.check(tp.tpgemm_last_device_error())
-    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     launch_ms = ms_per_step  # one launch of the kernel per step
-    value = job_tflops(world, w.flops, args.steps, total_ms)
+    value = w.flops * args.steps / (total_ms * 1e-3) / 1e12
     clocks = sampler.summary(t_wall0, t_wall1)
+    plan = pr.plan
+    pr.release()
+    torch.cuda.empty_cache()
+
+    peaks, src = load_peaks()
+    configs = None if args.no_configs else measure_configs(args, tp, dev, stream, scrub, peaks,
+                                                            src)
+    del scrub
+    torch.cuda.empty_cache()
 
     # ---- end to end through the host-buffer entry point: every step copies A,
     # B (and C) in from page-locked host memory and D back out, pipelined by
     # the library against the multiply of each row block.
+    lib = tp.library()
+    sh = int(stream.cuda_stream)
     pin = lambda t: t.pin_memory()  # noqa: E731
     Ah, Bh = pin(A), pin(B)
     Ch = None if C is None else pin(C)
@@ -327,8 +530,6 @@ def run_ours(args, rank, world, local_rank):
     h2d = A.numel() * A.element_size() + B.numel() * B.element_size() + \
         (0 if C is None else C.numel() * 4)
     d2h = w.M * w.N * 4
-    del Ad, Bd, Cd, D
-    torch.cuda.empty_cache()
     ws_bytes = lib.tpgemm_gemm_host_workspace_bytes(w.M, w.N, w.K, w.dtype, float(w.beta))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     hp = (Dh.data_ptr(), Ah.data_ptr(), Bh.data_ptr(), None if Ch is None else Ch.data_ptr())
@@ -343,45 +544,18 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     torch.cuda.synchronize()
     ne = max(1, min(args.e2e_steps, args.steps))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(ne):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / ne
-    e2e_ms = max_over_ranks(e2e_ms, world, dev)
-    e2e_value = job_tflops(world, w.flops, 1, e2e_ms)
+    e2e_ms = time_back_to_back(e2e_step, stream, ne) / ne
+    tp.check(tp.tpgemm_last_device_error())
+    e2e_value = w.flops / (e2e_ms * 1e-3) / 1e12
 
     # ---- roofline of the (single) kernel of a step
-    peaks, src = load_peaks()
-    # fp8 runs at twice the dense bf16 rate (nominal 4.5 / 2.25 PFLOP/s): its
-    # peak is the measured bf16 one times that ratio.
-    ratio = 2.0 if w.dtype in (wl.E4M3, wl.E5M2) else 1.0
-    t_peak = peaks["bf16_tflops"] * ratio
-    t_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
-    ridge = t_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
-    tensor_bound = w.flops / w.algorithmic_bytes > ridge
-    if tensor_bound:
-        achieved = w.flops / (launch_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2),
-                "peak": round(t_peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / t_peak, 4),
-                "peak_kind": f"{src} bf16 dense burst" + (
-                    " x 2 (nominal fp8 : bf16 ratio)" if ratio != 1.0 else ""),
-                "frac_of_sustained": round(achieved / t_sust, 4)}
-    else:
-        achieved = w.algorithmic_bytes / (launch_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "peak_kind": f"{src} HBM copy bandwidth"}
+    roof = roofline_of(w, launch_ms, peaks, src)
     roof["traffic"] = load_traffic(w.name)
-    roof["algorithmic"] = w.flops if tensor_bound else w.algorithmic_bytes
+    roof["algorithmic"] = w.flops if roof["bound"] == "tensor" else w.algorithmic_bytes
     roof["kernel"] = plan
 
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
             {wl.F16: "f16", wl.BF16: "bf16", wl.E4M3: "e4m3", wl.E5M2: "e5m2"}[w.dtype],
@@ -389,17 +563,25 @@ def run_ours(args, rank, world, local_rank):
         "config": {**w.describe(), "l2": "flushed before every step (512 MB write)" if
                    args.flush_l2 else ("inputs larger than L2, no flush" if
                                        w.algorithmic_bytes > 129e6 else "warm L2 (inputs fit)"),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": "single GPU"},
         "clocks": clocks,
         "gpu_launches": args.steps,
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if configs is not None:
+        out["configs"] = configs
+    if not args.no_cpu_baseline:
         v, n, el, cores = oracle_sample(w, A, B, C, args.cpu_seconds)
+        full = {}
+        for name in FULL_ORACLE_WORKLOADS:
+            fw = wl.BY_NAME[name]
+            full[name] = round(oracle_full(fw, *wl.make_inputs(fw)), 4)
         out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                               "sample": sample_text(n, w), "seconds": round(el, 2)}
+                               "omp_threads": cores, **host_cpu(),
+                               "sample": sample_text(n, w), "seconds": round(el, 2),
+                               "full_output_seconds": full}
     return out
 
 
@@ -640,33 +822,27 @@ def run_reference(args):
     }
 
 
-def main():
-    args = parse_args()
+SINGLE_GPU = ("bench.py: single-GPU design; the multiply has no exchange step and this "
+              "program runs no replicas, so --gpus must be 1 (WORLD_SIZE 1)")
+
+
+def main(argv=None):
+    args = parse_args(argv)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args)), flush=True)
         return 0
+    if args.gpus != 1 or world != 1:
+        log(SINGLE_GPU)
+        return 2
     if args.primitive:
-        if rank == 0:
-            fn = {"tcgen05_cp": run_primitive_cp, "vcopy": run_primitive_vcopy}[args.primitive]
-            print(json.dumps(fn(args)), flush=True)
+        fn = {"tcgen05_cp": run_primitive_cp, "vcopy": run_primitive_vcopy}[args.primitive]
+        print(json.dumps(fn(args)), flush=True)
         return 0
-    if world > 1:
-        import torch
-        torch.cuda.set_device(local_rank)
-        torch.distributed.init_process_group("nccl")
-    try:
-        out = run_ours(args, rank, world, local_rank)
-    finally:
-        if world > 1:
-            import torch
-            torch.distributed.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(out), flush=True)
+    print(json.dumps(run_ours(args)), flush=True)
     return 0
 
 

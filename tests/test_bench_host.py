@@ -36,3 +36,34 @@ def test_traffic_table_is_keyed_by_a_current_hash_or_reads_null():
             assert got == row["traffic_bytes_per_launch"]
         else:
             assert got is None
+
+
+def _sample(t, sm, **reasons):
+    d = {"t": t, "sm": sm, "sm_max": 2070.0, "power": 900.0, "hw_slowdown": False,
+         "hw_thermal_slowdown": False, "sw_thermal_slowdown": False, "sw_power_cap": False}
+    d.update(reasons)
+    return d
+
+
+def test_clock_summary_uses_only_samples_inside_the_timed_region():
+    samples = [_sample(0.5, 900.0, sw_thermal_slowdown=True), _sample(1.01, 2070.0),
+               _sample(1.02, 1900.0, sw_power_cap=True), _sample(1.03, 2000.0),
+               _sample(2.5, 800.0, hw_slowdown=True)]
+    s = bench.summarize_clocks(samples, 1.0, 1.05, "nvml every 1 ms")
+    assert s["samples"] == 3 and s["sm_mhz"] == 2000.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_summary_is_null_when_no_sample_fell_inside():
+    # Samples before and after a short region are not substituted for it.
+    samples = [_sample(0.5, 900.0), _sample(2.0, 2070.0)]
+    s = bench.summarize_clocks(samples, 1.0, 1.012, "nvidia-smi every 50 ms")
+    assert s["sm_mhz"] is None and s["samples"] == 0
+    assert "12.0 ms timed region" in s["null_reason"]
+    assert bench.summarize_clocks([], 1.0, 2.0, None)["null_reason"].startswith("no clock")
+
+
+def test_host_cpu_reports_a_cpu_count():
+    h = bench.host_cpu()
+    assert h["logical_cpus"] == os.cpu_count()
+    assert "cpu_model" in h

@@ -161,19 +161,31 @@ def test_multi_tile_waves_tc():
     check_full(w, TC)
 
 
-@pytest.mark.parametrize("mc", [1, 2, 4])
 @pytest.mark.parametrize("case", ["normal_kmajor", "normal_mnmajor", "swapped"])
-def test_cluster_sizes(mc, case, monkeypatch):
-    # 1, 2 or 4 CTAs per cluster sharing the Q tile through TMA multicast,
-    # including a P-tile count that is not a multiple of the cluster size.
-    monkeypatch.setenv("TPGEMM_TC_CLUSTER", str(mc))
+def test_single_cta_plans(case, monkeypatch):
+    # With the CTA pair off every CTA is its own cluster and loads the whole Q
+    # tile itself (no plan shares a tile between CTAs), including a P-tile
+    # count that is odd.
     monkeypatch.setenv("TPGEMM_TC_PAIR", "0")
     if case == "swapped":
         w = dataclasses.replace(wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(
-            128, 1416, 520, seed=6270 + mc))
+            128, 1416, 520, seed=6272))
     else:
         w = dataclasses.replace(wl.BY_NAME["gemm_8192_bf16_transB_beta1"].with_shape(
-            656, 536, 392, seed=6280 + mc), transB=(case == "normal_kmajor"))
+            656, 536, 392, seed=6282), transB=(case == "normal_kmajor"))
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+    assert st == tp.TPGEMM_OK and " cluster=1 pair=0 " in text, text
+    check_full(w, TC)
+
+
+def test_small_m_mn_major_q_runs_unclustered():
+    # Small M with A stored [K, M]: the only Q tile is MN-contiguous and 144
+    # wide, too narrow to split between a pair, so the plan runs one CTA per
+    # cluster (earlier builds shared that tile between CTAs by multicast).
+    w = dataclasses.replace(wl.BY_NAME["skinny_144x16392x4104_f16_beta1"].with_shape(
+        144, 2064, 264, seed=6290), transA=True)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+    assert st == tp.TPGEMM_OK and " cluster=1 " in text, text
     check_full(w, TC)
 
 

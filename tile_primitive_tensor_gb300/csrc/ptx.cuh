@@ -62,19 +62,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
-// Multicast form: the box lands at the same shared offset in every CTA of the
-// cluster named by cta_mask, and completes bytes on each one's mbarrier at the
-// same offset.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map,
-                                                      uint64_t* bar, int32_t x, int32_t y,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // CTA-pair form: the box lands in this CTA's shared memory and its bytes
 // complete on an mbarrier that may live in the peer CTA of the pair (a
 // shared::cluster address, e.g. from mapa).
@@ -229,16 +216,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
-        : "memory");
-}
-
-// As tc_commit, arriving on the mbarrier at the same offset in every CTA of
-// the cluster named by cta_mask.
-__device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 

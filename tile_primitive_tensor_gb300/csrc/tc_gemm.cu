@@ -226,12 +226,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const Smem s = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Cluster of p.mc CTAs sharing each Q tile: rank within it, which cluster,
-    // and how many clusters the persistent grid has.
-    const int rank = p.mc > 1 ? int(cluster_ctarank()) : 0;
-    const int cid = blockIdx.x / p.mc;
-    const int ncl = gridDim.x / p.mc;
-    const uint16_t mc_mask = uint16_t((1u << p.mc) - 1u);
+    // A CTA pair is a cluster of two; otherwise every CTA is its own cluster.
+    // Rank within the cluster, which cluster, and how many clusters the
+    // persistent grid has.
+    constexpr int MC = PAIR ? 2 : 1;
+    const int rank = PAIR ? int(cluster_ctarank()) : 0;
+    const int cid = blockIdx.x / MC;
+    const int ncl = gridDim.x / MC;
+    constexpr uint16_t pair_mask = 3;
     constexpr int CG = PAIR ? 2 : 1;
     // Accumulator buffer b starts at column b * acc_stride.
     const int acc_stride = p.tmem_cols / 2;
@@ -251,9 +253,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&s.full[i], 1);
-            // Freed by the MMA thread of every CTA sharing the stage (one
-            // multicast commit from the pair's leader in pair mode).
-            mbar_init(&s.empty[i], PAIR ? 1 : p.mc);
+            // Freed by one commit of the MMA thread (in pair mode the leader's,
+            // arriving on the barriers of both CTAs).
+            mbar_init(&s.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.acc_full[i], 1);
@@ -271,9 +273,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_relinquish_alloc_permit<CG>();
     }
     tc_fence_before_sync();
-    // With a cluster, no CTA may multicast into a peer before the peer's
-    // barriers exist: the set-up sync spans the cluster.
-    if (p.mc > 1)
+    // In a pair, no CTA may complete bytes on or arrive at a peer's barrier
+    // before the peer's barriers exist: the set-up sync spans the pair.
+    if constexpr (PAIR)
         cluster_sync();
     else
         __syncthreads();
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (; ok && iter.next(ncl, p, u); first_seg = false) {
                 int tps, tq;
                 tile_coords(u.T, p, tps, tq);
-                const int p0 = (tps * p.mc + rank) * p.bp;
+                const int p0 = (tps * MC + rank) * p.bp;
                 const int q0 = tq * p.bn + u.q_off;
                 // Q rows this CTA loads per stage, and the bytes they fill.
                 const int q_rows = PAIR ? u.width / 2 : u.width;
@@ -402,25 +404,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     } else {
                         tma_load_2d(sp, &mapP, &s.full[stage], k0, p0);
                     }
-                    if (p.mc == 1) {
-                        if (p.q_mn) {
-                            for (int a = 0; a < q_atoms; ++a)
-                                tma_load_2d(sq + a * kAtomBytes, &mapQ, &s.full[stage], q0 + 64 * a,
-                                            k0);
-                        } else {
-                            tma_load_2d(sq, mq, &s.full[stage], k0, q0);
-                        }
-                    } else if (p.q_mn) {
-                        // This CTA's share of the Q tile's 64-row atoms, to every CTA.
-                        const uint32_t per = p.q_boxes / p.mc;
-                        for (uint32_t a = rank * per; a < (rank + 1) * per; ++a)
-                            tma_load_2d_multicast(sq + a * kAtomBytes, &mapQ, &s.full[stage],
-                                                  q0 + 64 * int(a), k0, mc_mask);
+                    if (p.q_mn) {
+                        for (int a = 0; a < q_atoms; ++a)
+                            tma_load_2d(sq + a * kAtomBytes, &mapQ, &s.full[stage], q0 + 64 * a, k0);
                     } else {
-                        // This CTA's bn / mc rows of the Q tile, to every CTA.
-                        const int rows = p.bn / p.mc;
-                        tma_load_2d_multicast(sq + size_t(rank) * rows * 128, &mapQ, &s.full[stage],
-                                              k0, q0 + rank * rows, mc_mask);
+                        tma_load_2d(sq, mq, &s.full[stage], k0, q0);
                     }
                     issued_any |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -452,7 +440,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t stage_bytes = p.p_bytes + p.q_bytes;
             const uint32_t p_bytes = p.p_bytes;
             const int nstages = p.stages;
-            const bool mc_multi = p.mc > 1;
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -496,12 +483,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 tc_mma_f16(d_tmem, adesc, bdesc, idesc, acc);
                         }
                     }
-                    // Stage free (in every CTA that filled or multicast into it)
-                    // once these MMAs finish.
+                    // Stage free (in both CTAs of a pair) once these MMAs finish.
                     if (PAIR)
-                        tc_commit_pair_multicast(&s.empty[stage], mc_mask);
-                    else if (mc_multi)
-                        tc_commit_multicast(&s.empty[stage], mc_mask);
+                        tc_commit_pair_multicast(&s.empty[stage], pair_mask);
                     else
                         tc_commit(&s.empty[stage]);
                     if (++stage == nstages) {
@@ -512,7 +496,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!ok) break;
                 // Accumulator ready for the epilogue (of both CTAs in pair mode).
                 if (PAIR)
-                    tc_commit_pair_multicast(&s.acc_full[b], mc_mask);
+                    tc_commit_pair_multicast(&s.acc_full[b], pair_mask);
                 else
                     tc_commit(&s.acc_full[b]);
             }
@@ -551,7 +535,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (; iter.next(ncl, p, u); ++it) {
             int tps, tq;
             tile_coords(u.T, p, tps, tq);
-            const int tp = tps * p.mc + rank;
+            const int tp = tps * MC + rank;
             const int pw = tp * p.bp + quad * 32;  // first P row of this warp's quadrant
             const int q0 = tq * p.bn + u.q_off;
             const int nchunks = (u.width + 31) / 32;
@@ -571,7 +555,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool to_slot = !u.owner;
             const bool from_slot = u.has_next;
             const bool add_src = from_slot || p.beta;
-            const int src_slot = (cid + 1) * p.mc + rank;
+            const int src_slot = (cid + 1) * MC + rank;
             const int dst_slot = int(blockIdx.x);
             const int qw = quad * 32;
             auto box_x = [&](int c) { return SWAP ? pw : q0 + 32 * c; };
@@ -744,8 +728,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncthreads();
     }
-    // No CTA leaves while a peer may still multicast into it or arrive on it.
-    if (p.mc > 1) cluster_sync();
+    // No CTA of a pair leaves while its peer may still arrive on its barriers.
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
@@ -782,7 +766,7 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
     if (p.epi_bufs < 2 || p.epi_bufs > kTcMaxEpiBufs || p.stages < 2 || p.stages > 32 ||
         p.producers < 1 || p.producers > 4 || p.producers > p.stages ||
         !(p.epi_groups == 1 || p.epi_groups == 2) ||
-        !(p.mc == 1 || p.mc == 2 || p.mc == 4) || grid % p.mc != 0 || (p.pair && p.mc != 2) ||
+        p.mc != (p.pair ? 2 : 1) || grid % p.mc != 0 ||
         !(p.tmem_cols == 64 || p.tmem_cols == 128 || p.tmem_cols == 256 || p.tmem_cols == 512) ||
         p.tmem_cols / 2 < 32 * ((p.bn + 31) / 32))
         return cudaErrorInvalidValue;

@@ -270,7 +270,6 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.p_bytes = stage_tile_bytes(128, p_mn);
     p.p_tx = 128u * 128u;
     p.q_bytes = stage_tile_bytes(q_rows, q_mn);
-    p.q_boxes = q_mn ? uint32_t((q_rows + 63) / 64) : 1u;
     p.tx_bytes = p.p_bytes + p.q_bytes;
     p.timeout_ns = wait_timeout_ns();
     // Test only: TPGEMM_TEST_STALL=1 withholds CTA 0's first stage fill so the
@@ -329,23 +328,9 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         if (v >= 2 && v <= 8 && fits(v, epi_bufs)) stages = v;
     }
     if (const char* f = getenv("TPGEMM_TC_KROTATE")) p.k_rotate = std::max(0, atoi(f));
-    // Clusters: mc CTAs with consecutive P tiles share the Q tile, each TMA-
-    // loading 1/mc of it with multicast. A share must be whole 8-row swizzle
-    // groups (K-contiguous Q) or whole 64-row atoms (MN-contiguous Q). Used by
-    // default only when every tile shares the one Q tile (small M): there it
-    // halves the L2 reads of that tile; with many Q tiles the lock-step of
-    // the cluster's CTAs costs more than the traffic it saves (measured).
-    auto mc_ok = [&](int mc) {
-        if (mc == 1) return true;
-        if (p.tiles_p < mc) return false;
-        return p.q_mn ? (p.q_boxes % uint32_t(mc) == 0) : ((bn / mc) % 8 == 0 && bn % mc == 0);
-    };
-    p.mc = (p.tiles_q == 1 && mc_ok(2)) ? 2 : 1;
-    if (const char* f = getenv("TPGEMM_TC_CLUSTER")) {
-        const int v = atoi(f);
-        if ((v == 1 || v == 2 || v == 4) && mc_ok(v)) p.mc = v;
-    }
-    if (p.pair) p.mc = 2;  // the pair is a cluster of two
+    // Clusters: a CTA pair is a cluster of two; every other plan runs one CTA
+    // per cluster. No plan shares a tile between CTAs by TMA multicast.
+    p.mc = p.pair ? 2 : 1;
     p.tiles_ps = (p.tiles_p + p.mc - 1) / p.mc;
     p.num_super = p.tiles_ps * p.tiles_q;
     // Work units before any tail split (set by apply_tail_split once the grid is known).
@@ -353,7 +338,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.tail_split = 1;
     p.num_units = p.num_super;
     p.idesc_tail = p.idesc;
-    p.q_box_rows = p.pair ? bn / 2 : bn / p.mc;
+    p.q_box_rows = p.pair ? bn / 2 : bn;
     if (stages == 0) return fail(TPGEMM_ERR_PATH, "tile does not fit in shared memory");
     p.stages = stages;
     p.producers = 1;  // set with the grid (choose_producers)
@@ -411,7 +396,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
         const int ncl = std::max(1, max_grid / p.mc);
         const int full = (p.num_super / ncl) * ncl;
         const int rem = p.num_super - full;
-        if (sk_on && rem > 0 && (p.pair || p.mc == 1) && max_grid <= kSkMaxGrid &&
+        if (sk_on && rem > 0 && max_grid <= kSkMaxGrid &&
             int64_t(rem) * p.k_blocks >= int64_t(4) * ncl) {
             *grid = ncl * p.mc;
             p.full_units = full;
@@ -421,7 +406,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
             p.tail_split = 1;
             p.num_units = p.full_units;
             p.idesc_tail = p.idesc;
-            p.q_box_rows = p.pair ? p.bn / 2 : p.bn / p.mc;
+            p.q_box_rows = p.pair ? p.bn / 2 : p.bn;
             p.sk_slot_rows = p.swap ? 32 * ((p.bn + 31) / 32) : 128;
             return;
         }
@@ -430,7 +415,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
     p.full_units = (p.num_super / ncl) * ncl;
     const int rem = p.num_super - p.full_units;
     int split = 1;
-    const bool allowed = p.tiles_q > 1 && (p.pair || p.mc == 1) && rem > 0;
+    const bool allowed = p.tiles_q > 1 && rem > 0;
     if (allowed) {
         for (int sp = 4; sp >= 2; sp /= 2) {
             const int w = p.bn / sp;
@@ -447,7 +432,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
     p.tail_split = split;
     p.num_units = p.full_units + (p.num_super - p.full_units) * split;
     p.idesc_tail = tpg::idesc_f16_f32(code1, p.p_mn, p.q_mn, p.pair ? 256 : 128, p.bn / split);
-    p.q_box_rows = p.pair ? p.bn / 2 : p.bn / p.mc;
+    p.q_box_rows = p.pair ? p.bn / 2 : p.bn;
 }
 
 // P rows per tile. A single-wave plan whose tiles all share the one Q tile
@@ -577,7 +562,7 @@ tpgemm_status stream_k_workspace(cudaStream_t st, float** slots, uint32_t** flag
 }
 
 // Persistent grid: no more clusters than fit the device at once (clusters are
-// placed within GPCs, so with mc > 1 that can be fewer than SMs / mc).
+// placed within GPCs, so CTA pairs can be fewer than SMs / 2).
 // Tuning override: at most TPGEMM_TC_MAX_CLUSTERS clusters in the persistent
 // grid (used to measure fewer, longer-lived CTAs).
 int cluster_cap(int n) {
@@ -597,9 +582,9 @@ tpgemm_status fit_grid(Plan* plan) {
         return TPGEMM_OK;
     }
     static std::mutex m;
-    static int cache[2][2][5] = {};  // [swap][pair][mc]: 0 = unknown
+    static int cache[2] = {};  // [swap] of a pair plan: 0 = unknown
     std::lock_guard<std::mutex> lock(m);
-    int& n = cache[p.swap ? 1 : 0][p.pair ? 1 : 0][p.mc];
+    int& n = cache[p.swap ? 1 : 0];
     if (n == 0) {
         int v = 0;
         cudaError_t e = tpg::tc_max_active_clusters(p, &v);

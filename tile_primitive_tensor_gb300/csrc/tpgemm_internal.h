@@ -62,7 +62,6 @@ struct TcParams {
     uint32_t idesc;         // tcgen05 instruction descriptor
     uint32_t p_bytes;       // shared bytes of one P stage tile
     uint32_t q_bytes;       // shared bytes of one Q stage tile
-    uint32_t q_boxes;       // TMA boxes per Q stage tile
     uint32_t tx_bytes;      // bytes the TMA delivers per stage
     uint64_t timeout_ns;    // bound on every mbarrier wait
     int swap;               // orientation, for the epilogue's D coordinates
@@ -77,8 +76,7 @@ struct TcParams {
                             // grid, each just before its first access; 0: all wait after set-up
     int producers;          // TMA-issuing threads (1..4, at most the ring depth): warp 0,
                             // then warps 6, 7, 8; fill g is issued by producer g % producers
-    int mc;                 // CTAs per cluster sharing one Q tile (1, 2 or 4): each
-                            // loads 1/mc of it and multicasts it to the others
+    int mc;                 // CTAs per cluster: 2 for a CTA pair, else 1
     int tiles_ps;           // groups of mc consecutive P tiles: ceil(tiles_p / mc)
     int num_super;          // tiles_ps * tiles_q: work items of one cluster
     int pair;               // 1: CTA-pair MMA (cta_group::2, M = 256 per pair, mc = 2);
