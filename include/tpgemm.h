@@ -120,7 +120,11 @@ tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const flo
  * stream-K mode whenever the plan has a partial last wave, with its scratch
  * (partial tiles and flags) in one file-scope static device array of
  * TPGEMM_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds
- * until exit. It calls no cudaMalloc, cudaFree or other allocating routine.
+ * until exit. When a problem's stream-K scratch would not fit that array, the
+ * call runs the plan that needs no scratch (the last wave split along N, as
+ * tpgemm_gemm does by default) instead of failing. tpgemm_last_plan() tells
+ * which plan ran ("stream_k=1 scratch=static" for the static array). It calls
+ * no cudaMalloc, cudaFree or other allocating routine.
  *
  * The first call on a device takes the array's device address
  * (cudaGetSymbolAddress) and zeroes its flag area, synchronising the device;
@@ -128,14 +132,36 @@ tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const flo
  * share the array and it keeps the last call's contents: calls that overlap
  * on the GPU (e.g. on two streams at once) race, so serialise them.
  *
- * Returns TPGEMM_ERR_SHAPE, with the sizes in tpgemm_last_error_detail(), when
- * the problem's stream-K scratch would exceed TPGEMM_NOALLOC_SCRATCH_BYTES;
- * otherwise as tpgemm_gemm.
+ * Returns as tpgemm_gemm.
  */
 #define TPGEMM_NOALLOC_SCRATCH_BYTES (20u << 20)
 tpgemm_status tpgemm_gemm_noalloc(float* D, const void* A, const void* B, const float* C,
                                   int64_t M, int64_t N, int64_t K, int transA, int transB,
                                   tpgemm_dtype dtype, float beta, void* stream);
+
+/*
+ * Planner overrides (not on the pages; for measurement and tests). The
+ * environment variables TPGEMM_TC_* (tile width, P rows, ring depth, staging
+ * tiles, epilogue groups, producers, raster group, K rotation, CTA pair,
+ * orientation, tail split, stream-K, cluster cap), TPGEMM_HOST_BLOCKS and
+ * TPGEMM_WAIT_TIMEOUT_MS (the bound of every in-kernel wait, default 2000 ms)
+ * are read once per process, at the first call that plans a GEMM. This call
+ * reads them again; calls already running keep the values they started with.
+ */
+void tpgemm_reload_tuning(void);
+
+/*
+ * Test aid for failure detection (not on the pages): tpgemm_gemm on the
+ * tcgen05 path, except that CTA 0 never issues the TMA fill of its first ring
+ * stage. The kernel's bounded waits then expire (TPGEMM_WAIT_TIMEOUT_MS), it
+ * records TPGEMM_ERR_TIMEOUT for tpgemm_last_device_error(), drains its own
+ * copies and MMAs, frees tensor memory and returns; D is left undefined. The
+ * context stays usable. No GPU fault or hang is involved.
+ */
+tpgemm_status tpgemm_test_gemm_withhold_fill(float* D, const void* A, const void* B,
+                                             const float* C, int64_t M, int64_t N, int64_t K,
+                                             int transA, int transB, tpgemm_dtype dtype,
+                                             float beta, void* stream);
 
 /* Bytes of device workspace tpgemm_gemm_host needs for this problem: room for
  * A, B, D and (beta == 1) C, each 256-byte aligned. Returns 0 for a shape,
@@ -215,6 +241,24 @@ typedef enum {
     TPGEMM_CP_SWIZZLE_64B = 2,
     TPGEMM_CP_SWIZZLE_128B = 3
 } tpgemm_cp_swizzle;
+
+/*
+ * The tcgen05 descriptor encoders the kernels use, callable on the host (not on
+ * the pages: test aids). They let each field position be checked against the
+ * PTX ISA's descriptor tables without a GPU. Pure functions; no CUDA calls.
+ *
+ * tpgemm_encode_smem_desc: the 64-bit shared-memory matrix descriptor with
+ *   start address start_addr (bytes; its bits 4-17 are kept), leading- and
+ *   stride-dimension byte offsets lbo_bytes / sbo_bytes (multiples of 16, below
+ *   2^18), relative LBO mode, base offset 0 and the layout type of `swizzle`.
+ * tpgemm_encode_idesc: the 32-bit instruction descriptor of a dense
+ *   tcgen05.mma with an f32 accumulator: kind::f16 for TPGEMM_F16 / _BF16,
+ *   kind::f8f6f4 for TPGEMM_E4M3 / _E5M2, A and B of `dtype`, each K-major (0)
+ *   or MN-major (1), UMMA shape m x n. Returns 0 for an unknown dtype.
+ */
+uint64_t tpgemm_encode_smem_desc(uint32_t start_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                 tpgemm_cp_swizzle swizzle);
+uint32_t tpgemm_encode_idesc(tpgemm_dtype dtype, int a_mn_major, int b_mn_major, int m, int n);
 
 /* tcgen05.cp shape with its multicast qualifier. AUTO: the widest form whose
  * pattern matches the destination lanes (the page's candidate order
@@ -402,6 +446,14 @@ tpgemm_status tpgemm_last_device_error(void);
 tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, int transB,
                                    tpgemm_dtype dtype, float beta, tpgemm_path path, char* buf,
                                    int buflen);
+
+/* The plan of the last GEMM this thread enqueued (tpgemm_gemm, tpgemm_gemm_path,
+ * tpgemm_gemm_noalloc, or a block of tpgemm_gemm_host), as text in the format of
+ * tpgemm_describe_plan, with the grid actually launched and where its stream-K
+ * scratch lived ("scratch=none", "allocated" or "static"). Thread-local.
+ * Returns TPGEMM_ERR_NULL (and an empty string) if this thread has enqueued
+ * none. (Not on the pages: an introspection aid.) */
+tpgemm_status tpgemm_last_plan(char* buf, int buflen);
 
 /* Library version as "major.minor.patch". */
 const char* tpgemm_version(void);

@@ -21,16 +21,18 @@ registers, C registers per thread. For thread t of warp w, register j:
     synchronous gemm page (section 三, D_FRAG (2, 8, 4, 2) : (2, 4@laneid,
     1@laneid, 1), register c_id = 2 rM + rN at M = lane/4 + 8 rM,
     N = 2 (lane%4) + rN). Pinned to that page.
-  - .16x128b: register h of a repeat at lane t/4 + 8 h, column t%4. Not on the
-    pages: restated from the PTX ISA's fragment figure for this shape. Parity
-    unpinned.
-  - .16x64b: no thread map is stated here. The pages do not give it, and this
-    module's first restatement (lane t/2, column t%2) disagreed with the
-    hardware, so it was withdrawn rather than refitted to the GPU's output.
-    Parity unpinned; the tests check only what holds whatever the map: each
-    warp's 16-lane x 2-column block of a repeat holds exactly the registers the
-    warp stored there, nothing outside the footprint changes, and a .16x64b
-    store followed by a .16x64b load returns the registers unchanged.
+  - .16x128b: register h of a repeat at lane t/4 + 8 h, column t%4. Not on
+    the pages: restated from the PTX ISA's tcgen05 matrix-fragment figure for
+    this shape, and pinned cell by cell (with .16x256b) to the golden table
+    tests/golden/tcgen05_ldst_thread_maps.txt transcribed from those figures.
+  - .16x64b: no thread map is stated here; parity unpinned. The pages do not
+    give it, and two restatements of the PTX ISA figure written from memory
+    (lane t/2, column t%2; and lane t/4 + 8 ((t%4)/2), column t%2) each
+    disagreed with the hardware. Neither was refitted to the GPU's output. The
+    tests check only what holds whatever the map: each warp's 16-lane x
+    2-column block of a repeat holds exactly the registers the warp stored
+    there, nothing outside the footprint changes, and a .16x64b store followed
+    by a .16x64b load returns the registers unchanged.
 """
 from __future__ import annotations
 

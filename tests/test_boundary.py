@@ -228,3 +228,19 @@ int main(void) {
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.strip() == f"{tp.tpgemm_version()}|{tp.tpgemm_status_string(6)}"
+
+
+def test_last_plan_before_any_gemm_reports_none():
+    # A fresh thread has enqueued nothing (the record is thread-local).
+    import threading
+    got = {}
+    t = threading.Thread(target=lambda: got.update(r=tp.tpgemm_last_plan()))
+    t.start()
+    t.join()
+    st, text = got["r"]
+    assert st == tp.TPGEMM_ERR_NULL and text == ""
+
+
+def test_describe_plan_names_its_scratch(lib):
+    st, text = tp.tpgemm_describe_plan(8192, 8192, 8192, 0, 1, tp.TPGEMM_BF16, 1.0)
+    assert st == tp.TPGEMM_OK and " stream_k=0 scratch=none " in text, text

@@ -83,28 +83,28 @@ def test_fp8_swapped_small_m(dtype):
 
 @pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("bn", ["128", "256"])
-def test_fp8_pair_and_width(pair, bn, monkeypatch):
-    monkeypatch.setenv("TPGEMM_TC_PAIR", pair)
-    monkeypatch.setenv("TPGEMM_TC_BN", bn)
+def test_fp8_pair_and_width(pair, bn, tune):
+    tune.setenv("TPGEMM_TC_PAIR", pair)
+    tune.setenv("TPGEMM_TC_BN", bn)
     check(case(784, 1320, 272, wl.E4M3, 1.0, seed=13))
 
 
-def test_fp8_single_cta_shared_q(monkeypatch):
+def test_fp8_single_cta_shared_q(tune):
     # Every tile shares the one Q tile and each CTA loads it itself.
-    monkeypatch.setenv("TPGEMM_TC_PAIR", "0")
+    tune.setenv("TPGEMM_TC_PAIR", "0")
     check(case(1024, 128, 256, wl.E5M2, 0.0, seed=17))
 
 
-def test_fp8_tail_split(monkeypatch):
-    monkeypatch.setenv("TPGEMM_TC_BN", "256")
+def test_fp8_tail_split(tune):
+    tune.setenv("TPGEMM_TC_BN", "256")
     w = case(2048, 2560, 160, wl.E4M3, 1.0, seed=19)
     st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, 0, 1, w.dtype, 1.0)
     assert "x1 " not in text.split("units=")[1][:12], text
     check(w)
 
 
-def test_fp8_stream_k(monkeypatch):
-    monkeypatch.setenv("TPGEMM_TC_SK", "1")
+def test_fp8_stream_k(tune):
+    tune.setenv("TPGEMM_TC_SK", "1")
     w = case(1024, 1024, 4096, wl.E4M3, 1.0, seed=23)  # 32 K blocks of 128: enough to split
     st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, 0, 1, w.dtype, 1.0)
     assert "stream_k=1" in text, text
@@ -127,25 +127,12 @@ def test_fp8_workload_full_size(name):
     assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
     torch.cuda.synchronize()
     Dh = D.cpu().numpy()
-    assert np.isfinite(Dh).all()
-    rng = np.random.default_rng(w.seed)
-    r = np.concatenate([rng.integers(0, w.M, 3000), [0, w.M - 1]])
-    c = np.concatenate([rng.integers(0, w.N, 3000), [w.N - 1, 0]])
-    Dref, S = oracle.gemm_entries(r, c, wl.bits(A), wl.bits(B), None if C is None else C.numpy(),
-                                  w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
-    ok, msg = oracle.compare(Dh[r, c], Dref, S, exact=w.integer_valued)
-    assert ok, f"{name} sampled: {msg}"
-    a = Ad.double()
-    b = Bd.double().t()  # B stored [N, K]
-    ref = a @ b
-    if w.beta:
-        ref += Cd.double()
-    bound = (a.abs() @ b.abs()) * (2.0 ** -10) + 1e-6
-    if w.integer_valued:
-        assert torch.equal(D.double(), ref)
-    else:
-        err = (D.double() - ref).abs()
-        assert bool((err <= bound).all()), f"{name}: max err/bound {float((err / bound).max())}"
+    del D, Ad, Bd, Cd
+    # Every element against the oracle's whole output.
+    Dref, S = oracle.gemm(wl.bits(A), wl.bits(B), None if C is None else C.numpy(), w.M, w.N, w.K,
+                          w.transA, w.transB, w.dtype, w.beta)
+    ok, msg = oracle.compare(Dh, Dref, S, exact=w.integer_valued)
+    assert ok, f"{name}: {msg}"
 
 
 @pytest.mark.parametrize("M,N,K,dtype", [(4096, 16, 4096, wl.E4M3), (16, 16392, 128, wl.E5M2),

@@ -244,6 +244,47 @@ def test_oracle_swizzle_is_a_permutation_of_each_atom(swz):
                 assert ocp.unit_address(r, u, swz, 0, 1024, 0) == r * 128 + 16 * (u ^ r)
 
 
+def read_swizzle_cells():
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "smem_swizzle_cells.txt")
+    rows = []
+    with open(path) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append(tuple(int(v) for v in line.split()))
+    return rows
+
+
+SWIZZLE_OF_BYTES = {32: ocp.SWIZZLE_32B, 64: ocp.SWIZZLE_64B, 128: ocp.SWIZZLE_128B}
+
+
+def test_oracle_swizzle_matches_golden_cells():
+    # Byte offsets of single units read off the PTX ISA's swizzle figures: a
+    # wrong XOR field (other bits, another width) moves at least one of them.
+    cells = read_swizzle_cells()
+    assert {c[0] for c in cells} == {32, 64, 128}
+    for s, r, u, want in cells:
+        got = ocp.unit_address(r, u, SWIZZLE_OF_BYTES[s], 0, 8 * s, 0)
+        assert got == want, (s, r, u, got, want)
+
+
+@pytest.mark.parametrize("bad", ["phase_bits_6", "phase_mod_4"])
+def test_planted_swizzle_mistakes_fail_the_golden_cells(bad, monkeypatch):
+    # Two plausible slips, planted in the oracle: the row phase read from
+    # address bits starting at 6 instead of 7, and the 128-byte phase taken
+    # modulo 4. Both still permute each atom, and both fail the golden cells.
+    def planted(r, u, swizzle, lbo, sbo, offset):
+        s = ocp.ROW_BYTES[swizzle]
+        per_row = s // 16
+        a = offset + (u // per_row) * lbo + (r // 8) * sbo + (r % 8) * s + 16 * (u % per_row)
+        if bad == "phase_bits_6":
+            return a ^ (((a >> 6) & (per_row - 1)) << 4)
+        return a ^ (((a >> 7) & min(per_row - 1, 3)) << 4)
+    monkeypatch.setattr(ocp, "unit_address", planted)
+    with pytest.raises(AssertionError):
+        test_oracle_swizzle_matches_golden_cells()
+
+
 def test_oracle_tmem_image_fill_and_replicas():
     words = np.arange(32 * 4, dtype=np.uint32).reshape(32, 4)
     out = ocp.tmem_image(words, ocp.LANES_ALL_QUADS, 0, 8, 32, 7)
@@ -265,9 +306,60 @@ def test_ldst_map_is_a_bijection_onto_the_footprint(shape, cols):
     assert cells == {(lane, c) for lane in range(32) for c in range(cols)}
 
 
+def read_thread_maps():
+    """The golden table: shape name -> {(lane, column): (thread, register)}."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "tcgen05_ldst_thread_maps.txt")
+    maps, cur = {}, None
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("shape "):
+                cur = maps.setdefault(line.split()[1], {})
+                continue
+            head, cells = line.split(":")
+            lane = int(head.split()[1])
+            for col, e in enumerate(cells.split()):
+                t, r = e.split(".")
+                cur[(lane, col)] = (int(t[1:]), int(r[1:]))
+    return maps
+
+
 def test_ldst_16x64b_map_is_declared_unpinned():
     with pytest.raises(ValueError):
         ofr.cell(ofr.S16x64b, 2, 0, 0)
+
+
+@pytest.mark.parametrize("shape", [ofr.S16x128b, ofr.S16x256b], ids=lambda s: ofr.NAMES[s])
+def test_ldst_map_matches_the_golden_figure_table(shape):
+    # One .x1 issue (the first 16 lanes of a warp): every cell of the table
+    # names the (thread, register) the oracle places there, and the table
+    # covers the shape's 16 x w block exactly once.
+    table = read_thread_maps()[ofr.NAMES[shape]]
+    w, regs = ofr.REPEAT_COLS[shape], ofr.REPEAT_REGS[shape]
+    assert set(table) == {(lane, c) for lane in range(16) for c in range(w)}
+    assert sorted(table.values()) == sorted((t, r) for t in range(32) for r in range(regs))
+    for (lane, col), (t, r) in table.items():
+        assert ofr.cell(shape, 2 * regs, t, r) == (lane, col), (lane, col, t, r)
+
+
+def test_ldst_planted_16x128b_mistake_fails_the_table(monkeypatch):
+    # A plausible slip, planted in the oracle: .16x128b with two threads per
+    # lane (lane t/2, column 2 (t%2) + h) instead of four; it fails the table.
+    real = ofr.cell
+
+    def planted(shape, cols, t, j):
+        if shape == ofr.S16x128b:
+            half = cols // 2
+            slab, k = divmod(j, half)
+            rep, h = divmod(k, 2)
+            return 16 * slab + t // 2, 4 * rep + 2 * (t % 2) + h
+        return real(shape, cols, t, j)
+    monkeypatch.setattr(ofr, "cell", planted)
+    with pytest.raises(AssertionError):
+        test_ldst_map_matches_the_golden_figure_table(ofr.S16x128b)
 
 
 def test_ldst_16x256b_is_the_mma_accumulator_fragment():

@@ -202,6 +202,8 @@ def test_tmem_ldst_roundtrip(st, ld, cols):
     got_tmem = tmem_out.cpu().numpy().view(np.uint32).reshape(128, 32)
     got_regs = regs_out.cpu().numpy().view(np.uint32).reshape(128, cols)
     fill_img = ofr.fill_pattern(fill)
+    # .32x32b, .16x128b and .16x256b: the oracle's map, pinned to the page's
+    # demo and to the PTX ISA figure table, cell by cell.
     if st != ofr.S16x64b:
         exp_tmem = ofr.store(fill_img, regs, st, cols, tmem_col)
         bad = np.argwhere(got_tmem != exp_tmem)
@@ -217,8 +219,8 @@ def test_tmem_ldst_roundtrip(st, ld, cols):
                 lanes, _ = ofr.slab_cells(st, cols, slab)
                 block = got_tmem[32 * w + lanes.start: 32 * w + lanes.stop,
                                  tmem_col: tmem_col + cols]
-                stored = regs[32 * w: 32 * w + 32, ofr.slab_regs(st, cols, slab).start:
-                              ofr.slab_regs(st, cols, slab).stop]
+                r = ofr.slab_regs(st, cols, slab)
+                stored = regs[32 * w: 32 * w + 32, r.start: r.stop]
                 assert np.array_equal(np.sort(block, axis=None), np.sort(stored, axis=None))
     if ld != ofr.S16x64b:
         assert np.array_equal(got_regs, ofr.load(got_tmem, ld, cols, tmem_col))

@@ -105,6 +105,10 @@ def _load():
         lib.tpgemm_gemm_path.restype = ci
         lib.tpgemm_gemm_noalloc.argtypes = gemm_args
         lib.tpgemm_gemm_noalloc.restype = ci
+        lib.tpgemm_test_gemm_withhold_fill.argtypes = gemm_args
+        lib.tpgemm_test_gemm_withhold_fill.restype = ci
+        lib.tpgemm_reload_tuning.argtypes = []
+        lib.tpgemm_reload_tuning.restype = None
         lib.tpgemm_gemm_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, cf, vp,
                                          ctypes.c_size_t, vp]
         lib.tpgemm_gemm_host.restype = ci
@@ -118,6 +122,13 @@ def _load():
         lib.tpgemm_last_device_error.restype = ci
         lib.tpgemm_describe_plan.argtypes = [i64, i64, i64, ci, ci, ci, cf, ci, ctypes.c_char_p, ci]
         lib.tpgemm_describe_plan.restype = ci
+        lib.tpgemm_last_plan.argtypes = [ctypes.c_char_p, ci]
+        lib.tpgemm_last_plan.restype = ci
+        u32 = ctypes.c_uint32
+        lib.tpgemm_encode_smem_desc.argtypes = [u32, u32, u32, ci]
+        lib.tpgemm_encode_smem_desc.restype = ctypes.c_uint64
+        lib.tpgemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
+        lib.tpgemm_encode_idesc.restype = u32
         lib.tpgemm_version.argtypes = []
         lib.tpgemm_version.restype = ctypes.c_char_p
         lib.tpgemm_cp_parse_shape.argtypes = [ctypes.c_char_p, ctypes.POINTER(ci)]
@@ -196,6 +207,19 @@ def tpgemm_gemm_noalloc(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream
                                            int(dtype), float(beta), _stream(stream)))
 
 
+def tpgemm_test_gemm_withhold_fill(D, A, B, C, M, N, K, transA, transB, dtype, beta,
+                                   stream=None) -> int:
+    """Test aid: the tcgen05 GEMM with CTA 0's first stage fill withheld."""
+    return int(_load().tpgemm_test_gemm_withhold_fill(
+        _ptr(D), _ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), int(bool(transA)),
+        int(bool(transB)), int(dtype), float(beta), _stream(stream)))
+
+
+def tpgemm_reload_tuning() -> None:
+    """Re-read the TPGEMM_* planner overrides from the environment."""
+    _load().tpgemm_reload_tuning()
+
+
 def tpgemm_gemm_host_workspace_bytes(M, N, K, dtype, beta) -> int:
     return int(_load().tpgemm_gemm_host_workspace_bytes(int(M), int(N), int(K), int(dtype),
                                                         float(beta)))
@@ -223,10 +247,26 @@ def tpgemm_last_device_error() -> int:
 
 
 def tpgemm_describe_plan(M, N, K, transA, transB, dtype, beta, path=TPGEMM_PATH_AUTO):
-    buf = ctypes.create_string_buffer(512)
+    buf = ctypes.create_string_buffer(640)
     st = int(_load().tpgemm_describe_plan(int(M), int(N), int(K), int(bool(transA)),
                                           int(bool(transB)), int(dtype), float(beta), int(path),
-                                          buf, 512))
+                                          buf, 640))
+    return st, buf.value.decode()
+
+
+def tpgemm_encode_smem_desc(start_addr, lbo_bytes, sbo_bytes, swizzle) -> int:
+    return int(_load().tpgemm_encode_smem_desc(int(start_addr), int(lbo_bytes), int(sbo_bytes),
+                                               int(swizzle)))
+
+
+def tpgemm_encode_idesc(dtype, a_mn_major, b_mn_major, m, n) -> int:
+    return int(_load().tpgemm_encode_idesc(int(dtype), int(bool(a_mn_major)),
+                                           int(bool(b_mn_major)), int(m), int(n)))
+
+
+def tpgemm_last_plan():
+    buf = ctypes.create_string_buffer(640)
+    st = int(_load().tpgemm_last_plan(buf, 640))
     return st, buf.value.decode()
 
 

@@ -411,28 +411,43 @@ __device__ __forceinline__ void tc_cp(int form, uint32_t taddr, uint64_t sdesc) 
                  : "memory")
 
 // -------------------------------------------------- descriptors (tcgen05)
-// Shared-memory matrix descriptor, SWIZZLE_128B, start address 0. Fields:
-// bits 0-13 start address >> 4, 16-29 leading-dimension byte offset >> 4,
-// 32-45 stride-dimension byte offset >> 4, 46-48 fixed 0b001, 49-51 base
-// offset (0: stage buffers are 1024-byte aligned), 52 LBO mode (relative),
-// 61-63 swizzle mode (2 = 128-byte swizzle). Encoded once; each use ORs in the
-// 14-bit start address (the tile stays inside the 256 KB shared window).
-__host__ __device__ constexpr uint64_t smem_desc_sw128_template(uint32_t lbo_bytes,
-                                                                uint32_t sbo_bytes) {
+// Shared-memory matrix descriptor (the PTX ISA's tcgen05 "shared memory
+// descriptor" table). Fields: bits 0-13 start address >> 4, 16-29
+// leading-dimension byte offset >> 4, 32-45 stride-dimension byte offset >> 4,
+// 46-48 fixed 0b001, 49-51 base offset (0: buffers are aligned to the swizzle
+// pattern's repeat), 52 LBO mode (0, relative), 61-63 layout type: 0 no swizzle,
+// 2 128-byte, 4 64-byte, 6 32-byte swizzle.
+enum : uint32_t {
+    kDescLayoutNone = 0,
+    kDescLayoutSw128 = 2,
+    kDescLayoutSw64 = 4,
+    kDescLayoutSw32 = 6,
+};
+
+// Encoded once with start address 0; each use ORs in the 14-bit start
+// address (a tile stays inside the 256 KB shared window).
+__host__ __device__ constexpr uint64_t smem_desc_template(uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                                          uint32_t layout) {
     return (uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16) |
            (uint64_t((sbo_bytes >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) |
-           (uint64_t(2) << 61);
+           (uint64_t(layout & 7u) << 61);
 }
 
-__device__ __forceinline__ uint64_t smem_desc_with_addr(uint64_t tmpl, uint32_t smem_addr) {
+__host__ __device__ constexpr uint64_t smem_desc_sw128_template(uint32_t lbo_bytes,
+                                                                uint32_t sbo_bytes) {
+    return smem_desc_template(lbo_bytes, sbo_bytes, kDescLayoutSw128);
+}
+
+__host__ __device__ constexpr uint64_t smem_desc_with_addr(uint64_t tmpl, uint32_t smem_addr) {
     return (tmpl & ~uint64_t(0x3FFF)) | uint64_t((smem_addr >> 4) & 0x3FFFu);
 }
 
 // Instruction descriptor for kind::f16 (and kind::f8f6f4) with an f32
-// accumulator: bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format
-// (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3, 1 = e5m2),
-// 15 / 16 A / B major-ness (0 = K-major, 1 = MN-major), 17-22 N >> 3,
-// 24-28 M >> 4. Dense, no negation, no saturation.
+// accumulator (the PTX ISA's instruction-descriptor table for those kinds):
+// bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (kind::f16:
+// 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3, 1 = e5m2), 15 / 16 A / B
+// major-ness (0 = K-major, 1 = MN-major), 17-22 N >> 3, 24-28 M >> 4. Dense,
+// no negation, no saturation.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(bool bf16, bool a_mn_major, bool b_mn_major,
                                                      int m, int n) {
     return (1u << 4) | (uint32_t(bf16) << 7) | (uint32_t(bf16) << 10) |

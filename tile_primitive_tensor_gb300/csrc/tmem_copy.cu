@@ -99,12 +99,12 @@ uint32_t row_stride(tpgemm_cp_swizzle s) {
 }
 
 // Layout-type field (bits 61-63) of the shared-memory matrix descriptor.
-uint64_t layout_code(tpgemm_cp_swizzle s) {
+uint32_t layout_code(tpgemm_cp_swizzle s) {
     switch (s) {
-        case TPGEMM_CP_SWIZZLE_32B: return 6;
-        case TPGEMM_CP_SWIZZLE_64B: return 4;
-        case TPGEMM_CP_SWIZZLE_128B: return 2;
-        default: return 0;
+        case TPGEMM_CP_SWIZZLE_32B: return kDescLayoutSw32;
+        case TPGEMM_CP_SWIZZLE_64B: return kDescLayoutSw64;
+        case TPGEMM_CP_SWIZZLE_128B: return kDescLayoutSw128;
+        default: return kDescLayoutNone;
     }
 }
 
@@ -256,9 +256,7 @@ tpgemm_status build_plan(const tpgemm_cp_desc* dp, CpPlan* plan, std::string* wh
     // Swizzled K-major rows: the descriptor's LBO field is not used within one
     // swizzle row (every instruction stays inside one); it is set to 16 bytes.
     const uint32_t lbo = d.swizzle == TPGEMM_CP_SWIZZLE_NONE ? d.lbo_bytes : 16;
-    plan->desc = (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
-                 (uint64_t((d.sbo_bytes >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) |
-                 (layout_code(d.swizzle) << 61);
+    plan->desc = smem_desc_template(lbo, d.sbo_bytes, layout_code(d.swizzle));
     for (int i = 0; i < tiles; ++i) {
         for (int s = 0; s < steps; ++s) {
             const int r0 = tiles > 1 ? 4 * i : 0;

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -81,6 +82,63 @@ tpgemm_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     }
     *fn = g_encode;
     return TPGEMM_OK;
+}
+
+// ---------------------------------------------------------- tuning overrides
+// Planner overrides read from the environment, used to sweep plans on real
+// problems and by the tests to cover every plan the heuristics can choose.
+// They are read once per process (on first use) into an immutable snapshot;
+// tpgemm_reload_tuning() takes a new one. -1 (or 0 for orient) = not set.
+struct Tuning {
+    int bn = -1, bp = -1, dep_early = -1, epi_bufs = -1, epi_groups = -1, group = -1;
+    int krotate = -1, max_clusters = -1, pair = -1, producers = -1, sk = -1, stages = -1;
+    int tail = -1, host_blocks = -1;
+    int orient = 0;  // 1 "swap", 2 "normal"
+    long long wait_ms = -1;
+};
+
+Tuning read_tuning() {
+    Tuning t;
+    auto geti = [](const char* name, int* out) {
+        if (const char* f = getenv(name)) *out = atoi(f);
+    };
+    geti("TPGEMM_TC_BN", &t.bn);
+    geti("TPGEMM_TC_BP", &t.bp);
+    geti("TPGEMM_TC_DEP_EARLY", &t.dep_early);
+    geti("TPGEMM_TC_EPI_BUFS", &t.epi_bufs);
+    geti("TPGEMM_TC_EPI_GROUPS", &t.epi_groups);
+    geti("TPGEMM_TC_GROUP", &t.group);
+    geti("TPGEMM_TC_KROTATE", &t.krotate);
+    geti("TPGEMM_TC_MAX_CLUSTERS", &t.max_clusters);
+    geti("TPGEMM_TC_PAIR", &t.pair);
+    geti("TPGEMM_TC_PRODUCERS", &t.producers);
+    geti("TPGEMM_TC_SK", &t.sk);
+    geti("TPGEMM_TC_STAGES", &t.stages);
+    geti("TPGEMM_TC_TAIL", &t.tail);
+    geti("TPGEMM_HOST_BLOCKS", &t.host_blocks);
+    if (const char* f = getenv("TPGEMM_TC_ORIENT")) {
+        if (!strcmp(f, "swap")) t.orient = 1;
+        if (!strcmp(f, "normal")) t.orient = 2;
+    }
+    if (const char* f = getenv("TPGEMM_WAIT_TIMEOUT_MS")) t.wait_ms = atoll(f);
+    return t;
+}
+
+std::atomic<const Tuning*> g_tuning{nullptr};
+std::mutex g_tuning_mutex;
+
+// Snapshots are never freed (a reload is rare), so a reference stays valid
+// for the rest of the call that took it.
+const Tuning& tuning() {
+    const Tuning* t = g_tuning.load(std::memory_order_acquire);
+    if (t) return *t;
+    std::lock_guard<std::mutex> lock(g_tuning_mutex);
+    t = g_tuning.load(std::memory_order_acquire);
+    if (!t) {
+        t = new Tuning(read_tuning());
+        g_tuning.store(t, std::memory_order_release);
+    }
+    return *t;
 }
 
 // ------------------------------------------------------------- validation
@@ -185,8 +243,8 @@ uint32_t stage_tile_bytes(int rows, bool mn) {
 int pick_bn(int64_t M, int64_t N, int sms, bool pair) {
     // TPGEMM_TC_BN (a multiple of 32 in [32, 256]) forces the width; the
     // tests use it to cover every width the heuristic can choose.
-    if (const char* f = getenv("TPGEMM_TC_BN")) {
-        const int v = atoi(f);
+    {
+        const int v = tuning().bn;
         if (v >= 32 && v <= 256 && v % 32 == 0) return v;
     }
     if (N <= 64) return int(((N + 15) / 16) * 16);
@@ -220,10 +278,8 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     // with B [K,N]: 726 -> 674 us). TPGEMM_TC_ORIENT=swap|normal overrides.
     const bool swap_small = M <= 256 && N > M;
     bool swap = swap_small || (!transA && !transB);
-    if (const char* f = getenv("TPGEMM_TC_ORIENT")) {
-        if (!strcmp(f, "swap")) swap = true;
-        if (!strcmp(f, "normal") && !swap_small) swap = false;
-    }
+    if (tuning().orient == 1) swap = true;
+    if (tuning().orient == 2 && !swap_small) swap = false;
     const int64_t Mp = swap ? N : M;
     const int64_t Nq = swap ? M : N;
     const bool p_mn = swap ? !transB : transA;
@@ -264,7 +320,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     // On by default where it applies (measured: 8192^3 1449 -> 1563 TFLOP/s,
     // 4096^3 1105 -> 1383, skinny 36.1 -> 33.5 us); TPGEMM_TC_PAIR=0 turns it off.
     p.pair = pair_ok ? 1 : 0;
-    if (const char* f = getenv("TPGEMM_TC_PAIR")) p.pair = (atoi(f) != 0 && pair_ok) ? 1 : 0;
+    if (tuning().pair >= 0) p.pair = (tuning().pair != 0 && pair_ok) ? 1 : 0;
     const int q_rows = p.pair ? bn / 2 : bn;  // Q rows this CTA loads per stage
     p.idesc = tpg::idesc_f16_f32(format_code1(dtype), p_mn, q_mn, p.pair ? 256 : 128, bn);
     p.p_bytes = stage_tile_bytes(128, p_mn);
@@ -272,14 +328,12 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.q_bytes = stage_tile_bytes(q_rows, q_mn);
     p.tx_bytes = p.p_bytes + p.q_bytes;
     p.timeout_ns = wait_timeout_ns();
-    // Test only: TPGEMM_TEST_STALL=1 withholds CTA 0's first stage fill so the
-    // failure-detection path (bounded wait -> status word -> clean exit) runs.
-    if (const char* f = getenv("TPGEMM_TEST_STALL")) p.test_stall = atoi(f) != 0;
+    p.test_stall = 0;  // set only by tpgemm_test_gemm_withhold_fill
     p.swap = swap;
     // Raster: runs of 8 P groups sweep all Q tiles (measured best at 8192^3:
     // fewer panel re-reads from HBM than 16 or 32, less power, higher clock).
     p.group = 8;
-    if (const char* f = getenv("TPGEMM_TC_GROUP")) p.group = std::max(1, atoi(f));
+    if (tuning().group >= 0) p.group = std::max(1, tuning().group);
     // Every tile shares the one Q tile when all of Q fits it: spread the CTAs'
     // starting K blocks so they do not contend for the same lines of it.
     p.k_rotate = (p.tiles_q == 1 && p.tiles_p > 1) ? 1 : 0;
@@ -316,18 +370,18 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     }
     // Tuning overrides (TPGEMM_TC_STAGES, TPGEMM_TC_EPI_BUFS, TPGEMM_TC_KROTATE),
     // used to sweep the ring depth, staging and K rotation on real problems.
-    if (const char* f = getenv("TPGEMM_TC_EPI_BUFS")) {
-        const int v = atoi(f);
+    {
+        const int v = tuning().epi_bufs;
         if (v >= 2 && v <= tpg::kTcMaxEpiBufs) {
             epi_bufs = v;
             stages = deepest(v);
         }
     }
-    if (const char* f = getenv("TPGEMM_TC_STAGES")) {
-        const int v = atoi(f);
+    {
+        const int v = tuning().stages;
         if (v >= 2 && v <= 8 && fits(v, epi_bufs)) stages = v;
     }
-    if (const char* f = getenv("TPGEMM_TC_KROTATE")) p.k_rotate = std::max(0, atoi(f));
+    if (tuning().krotate >= 0) p.k_rotate = tuning().krotate;
     // Clusters: a CTA pair is a cluster of two; every other plan runs one CTA
     // per cluster. No plan shares a tile between CTAs by TMA multicast.
     p.mc = p.pair ? 2 : 1;
@@ -385,13 +439,21 @@ constexpr size_t kSkWorkspaceBytes = kSkSlotBytes + kSkFlagBytes;
 // for the next launch's early start.
 // *grid is the persistent grid (at most one cluster per work item); max_grid
 // is every cluster the device holds at once. Stream-K runs on max_grid.
+// Whether a plan may use stream-K: as TPGEMM_TC_SK says (default off), always
+// (the static scratch of tpgemm_gemm_noalloc), or never (its fallback when the
+// stream-K scratch would not fit that array).
+enum class SkMode { Env, Force, Off };
+
+bool stream_k_requested(SkMode m) {
+    if (m != SkMode::Env) return m == SkMode::Force;
+    return tuning().sk > 0;
+}
+
 void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
-                      bool force_sk = false) {
+                      SkMode sk_mode = SkMode::Env) {
     p.sk = 0;
     p.sk_total = 0;
-    bool sk_on = false;
-    if (const char* f = getenv("TPGEMM_TC_SK")) sk_on = atoi(f) != 0;
-    if (force_sk) sk_on = true;
+    const bool sk_on = stream_k_requested(sk_mode);
     {
         const int ncl = std::max(1, max_grid / p.mc);
         const int full = (p.num_super / ncl) * ncl;
@@ -426,8 +488,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
             }
         }
     }
-    if (const char* f = getenv("TPGEMM_TC_TAIL"))
-        if (atoi(f) == 0) split = 1;
+    if (tuning().tail == 0) split = 1;
     if (split == 1) p.full_units = p.num_super;
     p.tail_split = split;
     p.num_units = p.full_units + (p.num_super - p.full_units) * split;
@@ -461,8 +522,8 @@ void choose_p_rows(tpg::TcParams& p, int* grid, int max_grid, bool sk_requested)
             bp = c;
             break;
         }
-    if (const char* f = getenv("TPGEMM_TC_BP")) {
-        const int v = atoi(f);
+    {
+        const int v = tuning().bp;
         if (v >= 64 && v <= 128 && v % 16 == 0 && fits(v)) bp = v;
     }
     if (bp == 128) return;
@@ -478,12 +539,6 @@ void choose_p_rows(tpg::TcParams& p, int* grid, int max_grid, bool sk_requested)
     *grid = p.num_super * p.mc;
 }
 
-bool stream_k_requested(bool force_sk) {
-    if (force_sk) return true;
-    const char* f = getenv("TPGEMM_TC_SK");
-    return f && atoi(f) != 0;
-}
-
 // Epilogue warpgroups. With at most one work unit per cluster (a single wave)
 // no later tile's MMAs run under the epilogue, so both warpgroups drain it;
 // with more, one group keeps up and the second only competes with the MMA and
@@ -492,8 +547,8 @@ bool stream_k_requested(bool force_sk) {
 void choose_epi_groups(tpg::TcParams& p, int grid) {
     const int ncl = std::max(1, grid / p.mc);
     p.epi_groups = (!p.sk && p.num_units <= ncl) ? 2 : 1;
-    if (const char* f = getenv("TPGEMM_TC_EPI_GROUPS")) {
-        const int v = atoi(f);
+    {
+        const int v = tuning().epi_groups;
         if (v == 1 || v == 2) p.epi_groups = v;
     }
 }
@@ -514,8 +569,8 @@ void choose_producers(tpg::TcParams& p, int grid) {
     const int ncl = std::max(1, grid / p.mc);
     const int units_per_cluster = (p.num_units + ncl - 1) / ncl;
     int n = std::min(units_per_cluster >= 8 ? 1 : 2, p.stages);
-    if (const char* f = getenv("TPGEMM_TC_PRODUCERS")) {
-        const int v = atoi(f);
+    {
+        const int v = tuning().producers;
         if (v >= 1 && v <= 4) n = std::min(v, p.stages);
     }
     if (p.epi_groups == 2 && (p.sk || p.num_units > ncl)) n = 1;
@@ -525,7 +580,7 @@ void choose_producers(tpg::TcParams& p, int grid) {
     // us, 4096^3 96.5 -> 96.0 us, 8192^3 unchanged). TPGEMM_TC_DEP_EARLY=0
     // makes every thread wait after set-up.
     p.dep_early = 1;
-    if (const char* f = getenv("TPGEMM_TC_DEP_EARLY")) p.dep_early = atoi(f) != 0;
+    if (tuning().dep_early >= 0) p.dep_early = tuning().dep_early != 0;
 }
 
 // Stream-K scratch per (device, stream): allocated on first use, kept until
@@ -566,10 +621,7 @@ tpgemm_status stream_k_workspace(cudaStream_t st, float** slots, uint32_t** flag
 // Tuning override: at most TPGEMM_TC_MAX_CLUSTERS clusters in the persistent
 // grid (used to measure fewer, longer-lived CTAs).
 int cluster_cap(int n) {
-    if (const char* f = getenv("TPGEMM_TC_MAX_CLUSTERS")) {
-        const int c = atoi(f);
-        if (c >= 1) return std::min(n, c);
-    }
+    if (tuning().max_clusters >= 1) return std::min(n, tuning().max_clusters);
     return n;
 }
 
@@ -673,13 +725,87 @@ tpgemm_status encode_operand(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap*
 // allocates on first use, or the static array of tpgemm_gemm_noalloc.
 enum class Scratch { Allocated, Static };
 
+// The grid-dependent part of a tcgen05 plan: persistent grid, P rows per
+// tile, tail split or stream-K, epilogue groups and producers. Pure host work.
+tpgemm_status finish_tc_plan(Plan* plan, tpgemm_dtype dtype, SkMode sk_mode) {
+    if (plan->kernel != Kernel::Tc) return TPGEMM_OK;
+    tpgemm_status s = fit_grid(plan);
+    if (s != TPGEMM_OK) return s;
+    choose_p_rows(plan->tc, &plan->grid, plan->max_grid, stream_k_requested(sk_mode));
+    apply_tail_split(plan->tc, &plan->grid, plan->max_grid, format_code1(dtype), sk_mode);
+    choose_epi_groups(plan->tc, plan->grid);
+    choose_producers(plan->tc, plan->grid);
+    return TPGEMM_OK;
+}
+
+// Bytes of the static array a stream-K plan uses: one partial-tile slot per
+// CTA (laid out like a D tile, 32-column chunks) and the flag area at its end.
+// Plans with more CTAs than the flag area has rows for never fit.
+size_t static_scratch_need(const Plan& plan) {
+    const tpg::TcParams& p = plan.tc;
+    if (plan.grid > int(tpg::kStaticScratchFlagBytes / (tpg::kTcEpiWarps * sizeof(uint32_t))))
+        return ~size_t(0);
+    return size_t(plan.grid) * size_t(p.sk_slot_rows) *
+               size_t(p.swap ? 128 : 32 * ((p.bn + 31) / 32)) * sizeof(float) +
+           tpg::kStaticScratchFlagBytes;
+}
+
+// The calling thread's last launched plan (tpgemm_last_plan).
+struct LastPlan {
+    bool valid = false;
+    Plan plan;
+    int64_t M = 0, N = 0, K = 0;
+    const char* scratch = "none";
+};
+thread_local LastPlan g_last;
+
+void record_last_plan(const Plan& plan, int64_t M, int64_t N, int64_t K, const char* scratch) {
+    g_last.valid = true;
+    g_last.plan = plan;
+    g_last.M = M;
+    g_last.N = N;
+    g_last.K = K;
+    g_last.scratch = scratch;
+}
+
+// One line of text describing a plan (tpgemm_describe_plan, tpgemm_last_plan).
+void format_plan(const Plan& plan, int64_t M, int64_t N, int64_t K, const char* scratch,
+                 char* text, size_t len) {
+    if (plan.kernel == Kernel::MmaSync) {
+        snprintf(text, len, "path=mma_sync tile=%dx%dx32 grid=%lldx%lld warps=4 k_inst=%s",
+                 tpg::kMmaTileM, tpg::kMmaTileN, (long long)((N + 63) / 64),
+                 (long long)((M + 63) / 64), (K % 16) ? "m16n8k16+m16n8k8" : "m16n8k16");
+        return;
+    }
+    const tpg::TcParams& p = plan.tc;
+    snprintf(text, len,
+             "path=tcgen05 orientation=%s tile=%dx%dx%d umma=%dx%dx%d kind=%s stages=%d "
+             "epi_bufs=%d epi_groups=%d producers=%d dep_early=%d k_rotate=%d cluster=%d pair=%d "
+             "tmem=%d tiles=%dx%d grid=%d units=%d+%dx%d stream_k=%d scratch=%s p_major=%s "
+             "q_major=%s smem=%zu",
+             plan.swap ? "swapped" : "normal", p.bp, p.bn, p.bk, p.pair ? 256 : 128, p.bn,
+             p.fp8 ? 32 : 16, p.fp8 ? "f8f6f4" : "f16", p.stages, p.epi_bufs, p.epi_groups,
+             p.producers, p.dep_early, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p,
+             p.tiles_q, plan.grid, p.full_units, p.num_super - p.full_units, p.tail_split, p.sk,
+             scratch, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
+             tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));
+}
+
+void copy_text(const char* text, char* buf, int buflen) {
+    if (buf && buflen > 0) {
+        strncpy(buf, text, size_t(buflen) - 1);
+        buf[buflen - 1] = '\0';
+    }
+}
+
 // Per-device epoch counter of the static scratch (all its calls share it).
 std::mutex g_static_epoch_mutex;
 uint32_t g_static_epoch[tpg::kMaxStaticScratchDevices] = {};
 
 tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_t M, int64_t N,
                   int64_t K, int transA, int transB, tpgemm_dtype dtype, float beta, void* stream,
-                  tpgemm_path path, Scratch scratch = Scratch::Allocated) {
+                  tpgemm_path path, Scratch scratch = Scratch::Allocated,
+                  bool withhold_fill = false) {
     g_detail.clear();
     tpgemm_status s = check_shape(M, N, K, dtype, beta);
     if (s != TPGEMM_OK) return s;
@@ -703,6 +829,7 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
         cudaError_t e = tpg::launch_mma_sync(a, st);
         if (e != cudaSuccess)
             return fail(TPGEMM_ERR_LAUNCH, "mma.sync kernel launch: %s", cudaGetErrorString(e));
+        record_last_plan(plan, M, N, K, "none");
         return TPGEMM_OK;
     }
 
@@ -712,15 +839,21 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     const tpg::TcParams& p = plan.tc;
     tpg::TcMaps maps;
     std::memset(&maps, 0, sizeof(maps));
+    const SkMode sk_mode = scratch == Scratch::Static ? SkMode::Force : SkMode::Env;
+    s = finish_tc_plan(&plan, dtype, sk_mode);
+    if (s != TPGEMM_OK) return s;
+    if (scratch == Scratch::Static && plan.tc.sk && static_scratch_need(plan) > tpg::kStaticScratchBytes) {
+        // The stream-K scratch would not fit the static array: plan again
+        // without stream-K. The tail split needs no scratch at all.
+        s = make_plan(M, N, K, transA != 0, transB != 0, dtype, beta, path, dev.sms, &plan);
+        if (s != TPGEMM_OK) return s;
+        s = finish_tc_plan(&plan, dtype, SkMode::Off);
+        if (s != TPGEMM_OK) return s;
+    }
+    plan.tc.test_stall = withhold_fill ? 1 : 0;
     // P / Q operands: normal P = A (rows M), Q = B^T (rows N); swapped P = B^T, Q = A.
     const void* pp = plan.swap ? B : A;
     const void* qq = plan.swap ? A : B;
-    s = fit_grid(&plan);
-    if (s != TPGEMM_OK) return s;
-    choose_p_rows(plan.tc, &plan.grid, plan.max_grid,
-                  stream_k_requested(scratch == Scratch::Static));
-    apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code1(dtype),
-                     scratch == Scratch::Static);
     // P: K-contiguous, one box of bp rows; MN-contiguous, a 64-row atom from
     // maps.P and rows 64 .. bp - 1 from maps.Ph.
     s = encode_operand(enc, &maps.P, pp, dtype, p.Mp, K, p.p_mn, p.bp, "P operand");
@@ -732,8 +865,6 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     } else {
         maps.Ph = maps.P;
     }
-    choose_epi_groups(plan.tc, plan.grid);
-    choose_producers(plan.tc, plan.grid);
     s = encode_operand(enc, &maps.Q, qq, dtype, p.Nq, K, p.q_mn, p.q_box_rows, "Q operand");
     if (s != TPGEMM_OK) return s;
     if (p.tail_split > 1) {
@@ -747,13 +878,11 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
         if (scratch == Scratch::Static) {
             // No allocation: slots at the start of the static array, flags at
             // its end; the plan must fit, else the call is refused.
-            const size_t need = size_t(plan.grid) * size_t(p.sk_slot_rows) *
-                                    size_t(p.swap ? 128 : 32 * ((p.bn + 31) / 32)) * sizeof(float) +
-                                tpg::kStaticScratchFlagBytes;
-            if (need > tpg::kStaticScratchBytes || plan.grid > 256)
+            const size_t need = static_scratch_need(plan);
+            if (need > tpg::kStaticScratchBytes)
                 return fail(TPGEMM_ERR_SHAPE,
-                            "stream-K scratch for this problem needs %zu bytes; the static scratch "
-                            "holds %zu",
+                            "internal: stream-K scratch for this plan needs %zu bytes; the static "
+                            "scratch holds %zu",
                             need, tpg::kStaticScratchBytes);
             void* base = nullptr;
             cudaError_t e = tpg::tc_static_scratch(&base);
@@ -808,6 +937,8 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     cudaError_t e = tpg::launch_tc(maps, p, plan.grid, st);
     if (e != cudaSuccess)
         return fail(TPGEMM_ERR_LAUNCH, "tcgen05 kernel launch: %s", cudaGetErrorString(e));
+    record_last_plan(plan, M, N, K,
+                     !p.sk ? "none" : (scratch == Scratch::Static ? "static" : "allocated"));
     return TPGEMM_OK;
 }
 
@@ -894,7 +1025,7 @@ tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* C
     // with 16 (TPGEMM_HOST_BLOCKS, 1..16, overrides the count).
     int64_t blk = M;
     int want = 12;
-    if (const char* f = getenv("TPGEMM_HOST_BLOCKS")) want = std::min(16, std::max(1, atoi(f)));
+    if (tuning().host_blocks >= 0) want = std::min(16, std::max(1, tuning().host_blocks));
     if (M >= 2048) blk = ((M / want + 255) / 256) * 256;
     else if (M >= 512) blk = ((M / 4 + 15) / 16) * 16;
     const int nblk = int((M + blk - 1) / blk);
@@ -967,8 +1098,7 @@ namespace tpg {
 void set_error_detail(const char* text) { g_detail = text ? text : ""; }
 
 uint64_t wait_timeout_ns() {
-    const char* s = getenv("TPGEMM_WAIT_TIMEOUT_MS");
-    long long ms = s ? atoll(s) : 0;
+    long long ms = tuning().wait_ms;
     if (ms <= 0) ms = 2000;
     return uint64_t(ms) * 1000000ull;
 }
@@ -1012,6 +1142,19 @@ tpgemm_status tpgemm_gemm_noalloc(float* D, const void* A, const void* B, const 
                                   tpgemm_dtype dtype, float beta, void* stream) {
     return run(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream, TPGEMM_PATH_AUTO,
                Scratch::Static);
+}
+
+tpgemm_status tpgemm_test_gemm_withhold_fill(float* D, const void* A, const void* B,
+                                             const float* C, int64_t M, int64_t N, int64_t K,
+                                             int transA, int transB, tpgemm_dtype dtype, float beta,
+                                             void* stream) {
+    return run(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream, TPGEMM_PATH_TCGEN05,
+               Scratch::Allocated, true);
+}
+
+void tpgemm_reload_tuning(void) {
+    std::lock_guard<std::mutex> lock(g_tuning_mutex);
+    g_tuning.store(new Tuning(read_tuning()), std::memory_order_release);
 }
 
 const char* tpgemm_status_string(tpgemm_status s) {
@@ -1067,36 +1210,47 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     Plan plan;
     s = make_plan(M, N, K, transA != 0, transB != 0, dtype, beta, path, sms, &plan);
     if (s != TPGEMM_OK) return s;
-    char text[512];
     if (plan.kernel == Kernel::Tc) {
-        choose_p_rows(plan.tc, &plan.grid, plan.max_grid, stream_k_requested(false));
+        // As tpgemm_gemm plans it, except that the grid is one CTA (pair) per
+        // SM without the device's cluster-occupancy query.
+        choose_p_rows(plan.tc, &plan.grid, plan.max_grid, stream_k_requested(SkMode::Env));
         apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code1(dtype));
         choose_epi_groups(plan.tc, plan.grid);
         choose_producers(plan.tc, plan.grid);
     }
-    if (plan.kernel == Kernel::MmaSync) {
-        snprintf(text, sizeof(text),
-                 "path=mma_sync tile=%dx%dx32 grid=%lldx%lld warps=4 k_inst=%s",
-                 tpg::kMmaTileM, tpg::kMmaTileN, (long long)((N + 63) / 64),
-                 (long long)((M + 63) / 64), (K % 16) ? "m16n8k16+m16n8k8" : "m16n8k16");
-    } else {
-        const tpg::TcParams& p = plan.tc;
-        snprintf(text, sizeof(text),
-                 "path=tcgen05 orientation=%s tile=%dx%dx%d umma=%dx%dx%d kind=%s stages=%d "
-                 "epi_bufs=%d epi_groups=%d producers=%d dep_early=%d k_rotate=%d cluster=%d pair=%d tmem=%d tiles=%dx%d "
-                 "grid=%d units=%d+%dx%d stream_k=%d p_major=%s q_major=%s smem=%zu",
-                 plan.swap ? "swapped" : "normal", p.bp, p.bn, p.bk, p.pair ? 256 : 128, p.bn,
-                 p.fp8 ? 32 : 16, p.fp8 ? "f8f6f4" : "f16", p.stages,
-                 p.epi_bufs, p.epi_groups, p.producers, p.dep_early, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p, p.tiles_q, plan.grid,
-                 p.full_units, p.num_super - p.full_units, p.tail_split, p.sk, p.p_mn ? "mn" : "k",
-                 p.q_mn ? "mn" : "k",
-                 tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));
-    }
-    if (buf && buflen > 0) {
-        strncpy(buf, text, size_t(buflen) - 1);
-        buf[buflen - 1] = '\0';
-    }
+    char text[640];
+    format_plan(plan, M, N, K, plan.tc.sk ? "allocated" : "none", text, sizeof(text));
+    copy_text(text, buf, buflen);
     return TPGEMM_OK;
+}
+
+tpgemm_status tpgemm_last_plan(char* buf, int buflen) {
+    if (!g_last.valid) {
+        copy_text("", buf, buflen);
+        return fail(TPGEMM_ERR_NULL, "no GEMM has been enqueued on this thread");
+    }
+    char text[640];
+    format_plan(g_last.plan, g_last.M, g_last.N, g_last.K, g_last.scratch, text, sizeof(text));
+    copy_text(text, buf, buflen);
+    return TPGEMM_OK;
+}
+
+uint64_t tpgemm_encode_smem_desc(uint32_t start_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                 tpgemm_cp_swizzle swizzle) {
+    uint32_t layout = tpg::kDescLayoutNone;
+    switch (swizzle) {
+        case TPGEMM_CP_SWIZZLE_32B: layout = tpg::kDescLayoutSw32; break;
+        case TPGEMM_CP_SWIZZLE_64B: layout = tpg::kDescLayoutSw64; break;
+        case TPGEMM_CP_SWIZZLE_128B: layout = tpg::kDescLayoutSw128; break;
+        default: break;
+    }
+    return tpg::smem_desc_with_addr(tpg::smem_desc_template(lbo_bytes, sbo_bytes, layout),
+                                    start_addr);
+}
+
+uint32_t tpgemm_encode_idesc(tpgemm_dtype dtype, int a_mn_major, int b_mn_major, int m, int n) {
+    if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16 && !is_fp8(dtype)) return 0;
+    return tpg::idesc_f16_f32(format_code1(dtype), a_mn_major != 0, b_mn_major != 0, m, n);
 }
 
 const char* tpgemm_version(void) { return "0.1.0"; }

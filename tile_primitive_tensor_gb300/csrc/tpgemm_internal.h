@@ -15,7 +15,7 @@ constexpr int kStatusTimeout = 9;  // matches TPGEMM_ERR_TIMEOUT
 void set_error_detail(const char* text);
 
 // Bound of every wait inside a kernel: TPGEMM_WAIT_TIMEOUT_MS (default 2 s),
-// read on each call.
+// from the planner-override snapshot (tpgemm_reload_tuning).
 uint64_t wait_timeout_ns();
 
 // Device status words of the GEMM kernel and of the tensor-memory copy kernel
@@ -90,8 +90,9 @@ struct TcParams {
     int num_units;          // full_units + (num_super - full_units) * tail_split
     uint32_t idesc_tail;    // instruction descriptor of a tail unit (N = bn / tail_split)
     int q_box_rows;         // rows of one K-contiguous Q TMA box of a whole tile
-    int test_stall;         // test only: CTA 0 never fills its first stage, so the
-                            // bounded waits expire and the kernel reports a timeout
+    int test_stall;         // tpgemm_test_gemm_withhold_fill only: CTA 0 never fills its
+                            // first stage, so the bounded waits expire and the kernel
+                            // reports a timeout
     // Stream-K: work items [full_units, num_super) are not given whole to one
     // cluster; their K blocks (sk_total of them) are divided evenly among all
     // clusters. A tile's segment holding its last K blocks adds C and writes a
