@@ -298,6 +298,28 @@ def host_cpu() -> dict:
 
 
 # -------------------------------------------------------------- CPU oracle
+def oracle_sample_mx(w, A, B, C, seconds: float):
+    """The block-scaled oracle on the first rows of workload w (whole rows of D,
+    each entry a full K-long dot product); returns as oracle_sample."""
+    import oracle
+    oracle.build()
+    SFA, SFB = wl.make_scales(w)
+    Bb, sfb = wl.bits(B), SFB.numpy()
+    Ab, sfa = wl.bits(A).reshape(w.M, w.K), SFA.numpy()
+    Cn = None if C is None else C.numpy()
+
+    def run(rows):
+        t = time.perf_counter()
+        oracle.gemm_mx(Ab[:rows], Bb, None if Cn is None else Cn[:rows], sfa[:rows], sfb, rows,
+                       w.N, w.K, False, True, w.dtype, w.beta)
+        return time.perf_counter() - t
+
+    tp_ = run(1)
+    rows = int(max(1, min(w.M, seconds / max(tp_, 1e-6))))
+    el = run(rows)
+    return 2.0 * rows * w.N * w.K / el / 1e12, rows * w.N, el, oracle.num_threads()
+
+
 def oracle_sample(w, A, B, C, seconds: float, seed: int = 0):
     """Time the CPU oracle on a bounded sample of output entries of workload w.
 
@@ -307,6 +329,8 @@ def oracle_sample(w, A, B, C, seconds: float, seed: int = 0):
     import numpy as np
 
     import oracle
+    if isinstance(w, wl.MxWorkload):
+        return oracle_sample_mx(w, A, B, C, seconds)
     oracle.build()
     Ab, Bb = wl.bits(A), wl.bits(B)
     Cn = None if C is None else C.numpy()
@@ -327,6 +351,9 @@ def oracle_sample(w, A, B, C, seconds: float, seed: int = 0):
 
 
 def sample_text(n, w):
+    if isinstance(w, wl.MxWorkload):
+        return (f"{n} output entries (the first {n // w.N} rows of D), each a full {w.K}-long "
+                "fp64 dot product of the block-scaled fp8 operands (oracle_gemm_mx)")
     return (f"{n} output entries of D at seeded uniform positions (of {w.M}x{w.N}), each a "
             f"full {w.K}-long fp64 dot product from the 16-bit operands (oracle_gemm_entries)")
 
@@ -361,14 +388,31 @@ class Problem:
         self.D = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
         self.sh = int(stream.cuda_stream)
         self.lib = tp.library()
-        self.args = (self.D.data_ptr(), self.Ad.data_ptr(), self.Bd.data_ptr(),
-                     None if self.Cd is None else self.Cd.data_ptr(), w.M, w.N, w.K,
-                     int(w.transA), int(w.transB), w.dtype, float(w.beta), self.sh)
-        self.plan = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype,
-                                            w.beta)[1]
+        self.mx = isinstance(w, wl.MxWorkload)
+        cp = None if self.Cd is None else self.Cd.data_ptr()
+        if self.mx:
+            # Block-scaled fp8: scales and the scale-packing workspace (the
+            # packing runs inside every step, before the GEMM).
+            self.SFA, self.SFB = wl.make_scales(w)
+            self.sfa, self.sfb = self.SFA.to(dev), self.SFB.to(dev)
+            wsb = tp.tpgemm_gemm_mx_workspace_bytes(w.M, w.N, w.K)
+            self.ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            self.fn = self.lib.tpgemm_gemm_mx
+            self.args = (self.D.data_ptr(), self.Ad.data_ptr(), self.Bd.data_ptr(), cp,
+                         self.sfa.data_ptr(), self.sfb.data_ptr(), w.M, w.N, w.K, w.dtype,
+                         float(w.beta), self.ws.data_ptr(), wsb, self.sh)
+            self.step()
+            torch.cuda.synchronize()
+            self.plan = tp.tpgemm_last_plan()[1]
+        else:
+            self.fn = self.lib.tpgemm_gemm
+            self.args = (self.D.data_ptr(), self.Ad.data_ptr(), self.Bd.data_ptr(), cp, w.M, w.N,
+                         w.K, int(w.transA), int(w.transB), w.dtype, float(w.beta), self.sh)
+            self.plan = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype,
+                                                w.beta)[1]
 
     def step(self):
-        st = self.lib.tpgemm_gemm(*self.args)
+        st = self.fn(*self.args)
         if st != 0:
             raise RuntimeError(f"tpgemm_gemm: {st} {self.tp.tpgemm_last_error_detail()}")
 
@@ -378,6 +422,8 @@ class Problem:
         operands in L2 when their total exceeds it."""
         import torch
         sets, keep = [self.args], []
+        if self.mx:
+            raise ValueError("rotating copies are for the plain multiply")
         for _ in range(n - 1):
             t = (self.Ad.clone(), self.Bd.clone(), None if self.Cd is None else self.Cd.clone(),
                  torch.empty_like(self.D))
@@ -398,6 +444,8 @@ class Problem:
     def release(self):
         del self.Ad, self.Bd, self.Cd, self.D
         self._copies = []
+        if self.mx:
+            del self.sfa, self.sfb, self.ws
 
 
 def time_back_to_back(step, stream, steps: int) -> float:
@@ -483,7 +531,9 @@ def measure_configs(args, tp, dev, stream, scrub, peaks, src) -> dict:
     out = {}
     n = max(3, args.config_steps)
     for name, modes in (("gemm_4096_f16", ("warm",)),
-                        ("skinny_144x16392x4104_f16_beta1", ("cold", "cold_alone", "warm"))):
+                        ("skinny_144x16392x4104_f16_beta1", ("cold", "cold_alone", "warm")),
+                        ("gemm_8192_e4m3_transB_beta1", ("warm",)),
+                        ("mx_8192_e4m3_transB_beta1", ("warm",))):
         w = wl.BY_NAME[name]
         pr = Problem(tp, w, dev, stream)
         for _ in range(5):
@@ -571,7 +621,11 @@ def run_ours(args):
 
     # ---- end to end through the host-buffer entry point: every step copies A,
     # B (and C) in from page-locked host memory and D back out, pipelined by
-    # the library against the multiply of each row block.
+    # the library against the multiply of each row block. (The block-scaled
+    # multiply has no host-buffer entry point.)
+    if isinstance(w, wl.MxWorkload):
+        return finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src,
+                           configs, A, B, C, None)
     lib = tp.library()
     sh = int(stream.cuda_stream)
     pin = lambda t: t.pin_memory()  # noqa: E731
@@ -598,7 +652,15 @@ def run_ours(args):
     e2e_ms = time_back_to_back(e2e_step, stream, ne) / ne
     tp.check(tp.tpgemm_last_device_error())
     e2e_value = w.flops / (e2e_ms * 1e-3) / 1e12
+    e2e = {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+    return finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src, configs,
+                       A, B, C, e2e)
 
+
+def finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src, configs,
+                A, B, C, e2e):
+    """The JSON line: roofline of the (single) kernel of a step, configs, CPU baseline."""
     # ---- roofline of the (single) kernel of a step
     roof = roofline_of(w, launch_ms, peaks, src)
     roof["traffic"] = load_traffic(w.name)
@@ -616,10 +678,10 @@ def run_ours(args):
                                        w.algorithmic_bytes > 129e6 else "warm L2 (inputs fit)"),
                    "parallelism": "single GPU"},
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        # block-scaled steps launch the two scale-packing kernels before the GEMM
+        "gpu_launches": args.steps * (3 if isinstance(w, wl.MxWorkload) else 1),
         "roofline": roof,
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "e2e": e2e,
     }
     if configs is not None:
         out["configs"] = configs

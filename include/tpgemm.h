@@ -163,6 +163,43 @@ tpgemm_status tpgemm_test_gemm_withhold_fill(float* D, const void* A, const void
                                              int transA, int transB, tpgemm_dtype dtype,
                                              float beta, void* stream);
 
+/*
+ * Block-scaled fp8 multiply (MX):
+ *   D[i,j] = sum_k (A[i,k] * 2^(SFA[i, k/32] - 127)) * (B[k,j] * 2^(SFB[j, k/32] - 127))
+ *            + beta * C[i,j].
+ * The sync-gemm page ("TVM TIRx 同步 GEMM 深度解析", section 七) lists block
+ * scaling (SFA, SFB) among gemm_async's operand forms without defining it;
+ * this is the OCP Microscaling reading: every 32 consecutive K elements of a
+ * row of A (of a column of B) share one E8M0 scale, 2^(e - 127), e = 255 NaN.
+ * Runs on the tcgen05 kernel as tcgen05.mma kind::mxf8f6f4.block_scale with
+ * the scales copied into tensor memory by tcgen05.cp.
+ *
+ * A: [M,K] fp8 (dtype TPGEMM_E4M3 or TPGEMM_E5M2), K-contiguous. B: [N,K] fp8
+ *   of the same dtype (stored as for tpgemm_gemm with transB = 1).
+ * SFA: [M][ceil(K/32)] E8M0 bytes, row-major. SFB: [N][ceil(K/32)] E8M0 bytes.
+ * C, D, M, N, K, beta, stream: as tpgemm_gemm (K % 16 == 0 as for fp8).
+ * workspace: caller-owned device memory of at least
+ *   tpgemm_gemm_mx_workspace_bytes(M, N, K) bytes, 256-byte aligned, that the
+ *   call packs the scales into (the library allocates nothing); it must not
+ *   overlap any operand and must stay untouched until the GEMM has run.
+ * Returns as tpgemm_gemm, plus TPGEMM_ERR_NULL for a NULL scale matrix or a
+ * missing / short workspace and TPGEMM_ERR_ALIAS for overlaps with it.
+ */
+tpgemm_status tpgemm_gemm_mx(float* D, const void* A, const void* B, const float* C,
+                             const uint8_t* SFA, const uint8_t* SFB, int64_t M, int64_t N,
+                             int64_t K, tpgemm_dtype dtype, float beta, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace tpgemm_gemm_mx needs: the packed scales, 512 bytes per
+ * (128 rows, 128 K) of A and of B. 0 for non-positive or oversized shapes. */
+size_t tpgemm_gemm_mx_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Host copy of the block-scaled instruction descriptor encoder (test aid, as
+ * tpgemm_encode_idesc): kind::mxf8f6f4 with E8M0 scales, A and B of `dtype`
+ * (TPGEMM_E4M3 / _E5M2), both K-major, UMMA shape m x n, and the scale-factor
+ * IDs of A and B (0..3). Returns 0 for another dtype. */
+uint32_t tpgemm_encode_idesc_mx(tpgemm_dtype dtype, int m, int n, int a_sf_id, int b_sf_id);
+
 /* Bytes of device workspace tpgemm_gemm_host needs for this problem: room for
  * A, B, D and (beta == 1) C, each 256-byte aligned. Returns 0 for a shape,
  * dtype or beta that tpgemm_gemm would reject. */

@@ -80,6 +80,10 @@ def _load():
         lib.oracle_gemm_entries.restype = ci
         lib.oracle_gemm_rows.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, ci, ci, ci, ci]
         lib.oracle_gemm_rows.restype = ci
+        lib.oracle_decode_e8m0.argtypes = [ctypes.c_uint8]
+        lib.oracle_decode_e8m0.restype = ctypes.c_double
+        lib.oracle_gemm_mx.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, ci, ci, ci, ci, i64]
+        lib.oracle_gemm_mx.restype = ci
         _lib = lib
         return lib
 
@@ -136,6 +140,36 @@ def gemm(A_bits, B_bits, C, M: int, N: int, K: int, transA: bool, transB: bool,
                              int(bool(transB)), int(dtype), int(beta != 0.0))
     if rc != 0:
         raise RuntimeError(f"oracle_gemm failed with code {rc}")
+    return D, S
+
+
+def decode_e8m0(e: int) -> float:
+    """Value of one E8M0 block scale: 2^(e - 127); 255 is NaN."""
+    return float(_load().oracle_decode_e8m0(int(e)))
+
+
+def gemm_mx(A_bits, B_bits, C, SFA, SFB, M: int, N: int, K: int, transA: bool, transB: bool,
+            dtype: int, beta: float, block: int = 32):
+    """Block-scaled fp8 (MX): full D_ref [M, N] float32 and S [M, N] float64.
+
+    SFA is [M, ceil(K / block)] and SFB [N, ceil(K / block)] E8M0 bytes; each
+    scales `block` consecutive K elements of a row of A / a column of B."""
+    _check_beta(beta)
+    A = _as_bits(A_bits, M * K)
+    B = _as_bits(B_bits, K * N)
+    c = _as_c(C, M, N, beta)
+    kb = (K + block - 1) // block
+    sfa = np.ascontiguousarray(SFA, dtype=np.uint8)
+    sfb = np.ascontiguousarray(SFB, dtype=np.uint8)
+    if sfa.size != M * kb or sfb.size != N * kb:
+        raise ValueError(f"scales must be [M, {kb}] and [N, {kb}]")
+    D = np.empty((M, N), dtype=np.float32)
+    S = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_mx(_ptr(D), _ptr(S), _ptr(A), _ptr(B), _ptr(c), _ptr(sfa),
+                                _ptr(sfb), M, N, K, int(bool(transA)), int(bool(transB)),
+                                int(dtype), int(beta != 0.0), int(block))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_mx failed with code {rc}")
     return D, S
 
 

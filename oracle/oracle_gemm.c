@@ -29,6 +29,18 @@
  *
  * Alongside D it can return S[i,j] = sum_k |a(i,k) * b(k,j)| in double, the
  * scale of the elementwise acceptance bound |D - D_ref| <= 2^-10 * S + 1e-6.
+ *
+ * Block-scaled fp8 (oracle_gemm_mx): the same page lists block scaling (SFA,
+ * SFB) among the operand forms of gemm_async (section 七) without defining
+ * it. The reading taken is the OCP Microscaling (MX) one: every run of
+ * `block` consecutive K elements of a row of A (of a column of B) shares one
+ * scale, an 8-bit power of two (E8M0: 2^(e - 127), e = 255 is NaN), and the
+ * element's value is its fp8 value times that scale:
+ *   D[i,j] = sum_k (a(i,k) * sa(i, k / block)) * (b(k,j) * sb(j, k / block))
+ *            (+ C[i,j] when beta = 1),
+ * with SFA stored [M][KB] and SFB stored [N][KB], KB = ceil(K / block),
+ * whatever the orientation of A and B. Every scaled element and every product
+ * is exact in double; the sum runs in increasing k and is rounded once.
  */
 #include <math.h>
 #include <stdint.h>
@@ -251,6 +263,61 @@ int oracle_gemm_rows(float* D_rows, const uint16_t* A, const uint16_t* B, const 
             for (int64_t k = 0; k < K; ++k) s += ai[k] * bj[k];
             if (beta) s += (double)C[(row_begin + r) * N + j];
             D_rows[r * N + j] = (float)s;
+        }
+    }
+    free(a);
+    free(bt);
+    return 0;
+}
+
+/* E8M0 scale: an unsigned 8-bit biased exponent, 2^(e - 127); e = 255 is NaN. */
+double oracle_decode_e8m0(uint8_t e) {
+    return e == 255 ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+/* Block-scaled D (see the header comment): A and B fp8 (dtype E4M3 or E5M2,
+ * patterns widened to 16 bits as for oracle_gemm), SFA [M][KB] and SFB [N][KB]
+ * E8M0 bytes. Returns 0 on success, -1 if the decode buffers cannot be
+ * allocated, -2 on a bad argument. sumabs may be NULL. */
+int oracle_gemm_mx(float* D, double* sumabs, const uint16_t* A, const uint16_t* B,
+                   const float* C, const uint8_t* SFA, const uint8_t* SFB, int64_t M, int64_t N,
+                   int64_t K, int transA, int transB, int dtype, int beta, int64_t block) {
+    if (M <= 0 || N <= 0 || K <= 0 || block <= 0 || !D || !A || !B || !SFA || !SFB ||
+        (beta && !C))
+        return -2;
+    if (dtype != ORACLE_E4M3 && dtype != ORACLE_E5M2) return -2;
+    const int64_t KB = (K + block - 1) / block;
+    double* a = (double*)malloc(sizeof(double) * (size_t)(M * K));
+    double* bt = (double*)malloc(sizeof(double) * (size_t)(N * K));
+    if (!a || !bt) {
+        free(a);
+        free(bt);
+        return -1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t k = 0; k < K; ++k)
+            a[i * K + k] = decode(a_bits(A, i, k, M, K, transA), dtype) *
+                           oracle_decode_e8m0(SFA[i * KB + k / block]);
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t k = 0; k < K; ++k)
+            bt[j * K + k] = decode(b_bits(B, k, j, N, K, transB), dtype) *
+                            oracle_decode_e8m0(SFB[j * KB + k / block]);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        const double* ai = a + i * K;
+        for (int64_t j = 0; j < N; ++j) {
+            const double* bj = bt + j * K;
+            double s = 0.0, sa = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = ai[k] * bj[k];
+                s += p;
+                sa += fabs(p);
+            }
+            if (beta) s += (double)C[i * N + j];
+            D[i * N + j] = (float)s;
+            if (sumabs) sumabs[i * N + j] = sa;
         }
     }
     free(a);

@@ -244,3 +244,39 @@ def test_last_plan_before_any_gemm_reports_none():
 def test_describe_plan_names_its_scratch(lib):
     st, text = tp.tpgemm_describe_plan(8192, 8192, 8192, 0, 1, tp.TPGEMM_BF16, 1.0)
     assert st == tp.TPGEMM_OK and " stream_k=0 scratch=none " in text, text
+
+
+# ------------------------------------------------ block-scaled fp8 (MX) boundary
+def call_mx(M=256, N=256, K=256, D=BASE, A=BASE + 64 * MB, B=BASE + 128 * MB, C=BASE + 192 * MB,
+            SFA=BASE + 256 * MB, SFB=BASE + 257 * MB, dtype=tp.TPGEMM_E4M3, beta=1.0,
+            ws=BASE + 320 * MB, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = tp.tpgemm_gemm_mx_workspace_bytes(M, N, K)
+    st = tp.tpgemm_gemm_mx(D, A, B, C, SFA, SFB, M, N, K, dtype, beta, ws, ws_bytes, 0)
+    return st, tp.tpgemm_last_error_detail()
+
+
+def test_mx_workspace_size(lib):
+    # 512 bytes per (128 rows, 128 K) of A, then of B from a 256-byte boundary:
+    # 256 x 256 x 256 is 2 x 2 chunks each; 144 x 16392 x 4112 is 2 x 33 and
+    # 129 x 33 chunks.
+    assert tp.tpgemm_gemm_mx_workspace_bytes(256, 256, 256) == 4096
+    assert tp.tpgemm_gemm_mx_workspace_bytes(144, 16392, 4112) == (2 * 33 + 129 * 33) * 512
+    assert tp.tpgemm_gemm_mx_workspace_bytes(0, 8, 16) == 0
+
+
+@pytest.mark.parametrize("kw,status,frag", [
+    ({"dtype": tp.TPGEMM_F16}, tp.TPGEMM_ERR_DTYPE, "E4M3"),
+    ({"K": 264}, tp.TPGEMM_ERR_SHAPE, "multiple of 16"),
+    ({"SFA": None}, tp.TPGEMM_ERR_NULL, "SFA is NULL"),
+    ({"SFB": None}, tp.TPGEMM_ERR_NULL, "SFB is NULL"),
+    ({"ws": None}, tp.TPGEMM_ERR_NULL, "workspace is NULL"),
+    ({"ws_bytes": 4095}, tp.TPGEMM_ERR_NULL, "4096 needed"),
+    ({"ws": BASE + 320 * MB + 16}, tp.TPGEMM_ERR_ALIGN, "256-byte aligned"),
+    ({"ws": BASE}, tp.TPGEMM_ERR_ALIAS, "workspace overlaps"),
+    ({"SFA": BASE + 16}, tp.TPGEMM_ERR_ALIAS, "scale matrix"),
+])
+def test_mx_rejections(lib, kw, status, frag):
+    st, why = call_mx(**kw)
+    assert st == status, why
+    assert frag in why

@@ -111,3 +111,31 @@ def test_tcgen05_cp_plan_descriptor(swz, lbo, sbo, expected):
     assert st == tp.TPGEMM_OK, text
     got = int(re.search(r"desc=(0x[0-9a-f]+)", text).group(1), 16)
     assert got == expected, f"got {got:#018x}, want {expected:#018x}"
+
+
+# Block-scaled kind::mxf8f6f4 instruction descriptor (32 bits), hand-assembled
+# from the PTX ISA's table for the block-scaled kinds:
+#   bits  4-5   B scale-factor ID     bits 17-22  N >> 3
+#   bits  7-9   A format (e4m3 0,     bit  23     scale type (1: E8M0)
+#               e5m2 1)               bits 24-28  M >> 4
+#   bits 10-12  B format              bits 29-30  A scale-factor ID
+#   bits 15/16  A/B major (0: K)      (no D-format field: always f32)
+IDESC_MX_CASES = [
+    (tp.TPGEMM_E4M3, 128, 128, 0, 0, 0x08A00000,
+     "e4m3 128x128 ids 0/0: 16 << 17, 1 << 23, 8 << 24"),
+    (tp.TPGEMM_E5M2, 128, 144, 3, 2, 0x68A404A0,
+     "e5m2 128x144 ids 3/2: 2 << 4, 1 << 7, 1 << 10, 18 << 17, 1 << 23, 8 << 24, 3 << 29"),
+    (tp.TPGEMM_E4M3, 128, 16, 1, 1, 0x28840010,
+     "e4m3 128x16 ids 1/1: 1 << 4, 2 << 17, 1 << 23, 8 << 24, 1 << 29"),
+]
+
+
+@pytest.mark.parametrize("dtype,m,n,a_id,b_id,expected,how", IDESC_MX_CASES,
+                         ids=[c[-1].split(":")[0] for c in IDESC_MX_CASES])
+def test_block_scaled_instruction_descriptor(dtype, m, n, a_id, b_id, expected, how):
+    got = tp.tpgemm_encode_idesc_mx(dtype, m, n, a_id, b_id)
+    assert got == expected, f"{how}: got {got:#010x}, want {expected:#010x}"
+
+
+def test_block_scaled_descriptor_takes_fp8_only():
+    assert tp.tpgemm_encode_idesc_mx(tp.TPGEMM_BF16, 128, 128, 0, 0) == 0

@@ -1,0 +1,165 @@
+"""Parity of the block-scaled fp8 (MX) multiply with the CPU oracle (GPU only).
+
+tpgemm_gemm_mx runs tcgen05.mma kind::mxf8f6f4.block_scale on the tcgen05
+kernel, the E8M0 scales packed by a pre-pass and copied into tensor memory by
+tcgen05.cp. Every case draws seeded operands and scales and compares every
+element with ``oracle.gemm_mx`` (the OCP Microscaling reading of the block
+scaling the synchronous gemm page lists for gemm_async, section 七): bit-exact
+for integer operands with scales in [1/2, 2], else |D - D_ref| <= 2^-10 * S +
+1e-6. Shapes cover one tile, ragged M / N / K (a partial last scale block and
+a partial last 128-element stage), both orientations (small M is swapped, so
+B's scales become the MMA's A scales), both formats, beta 0 / 1, guard bands
+around D, and the MX workloads at full size.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tile_primitive_tensor_gb300 as tp
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+GUARD = 4096
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tile_primitive_tensor_gb300 import build as tpbuild
+    tpbuild.build()
+    oracle.build()
+    yield
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+
+
+def case(M, N, K, dtype, beta, dist=("normal", 0.0, 1.0), sf=(120, 134), seed=0):
+    base = wl.BY_NAME["mx_256_e4m3_transB_beta1"]
+    return dataclasses.replace(base, name=f"mx_{M}x{N}x{K}_{dtype}_{beta}", M=M, N=N, K=K,
+                               dtype=dtype, a_dist=dist, b_dist=dist,
+                               c_dist=("normal", 0.0, 1.0) if beta else None, beta=beta,
+                               seed=seed, sf_dist=sf)
+
+
+def run_mx(w):
+    """Run the library on workload w; returns (D host, plan text)."""
+    A, B, C = wl.make_inputs(w)
+    SFA, SFB = wl.make_scales(w)
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd = None if C is None else C.cuda()
+    sa, sb = SFA.cuda(), SFB.cuda()
+    n = w.M * w.N
+    buf = torch.full((n + 2 * GUARD,), float("nan"), device="cuda")
+    D = buf[GUARD:GUARD + n].view(w.M, w.N)
+    wsb = tp.tpgemm_gemm_mx_workspace_bytes(w.M, w.N, w.K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    st = tp.tpgemm_gemm_mx(D, Ad, Bd, Cd, sa, sb, w.M, w.N, w.K, w.dtype, w.beta, ws, wsb)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    plan = tp.tpgemm_last_plan()[1]
+    h = buf.cpu().numpy()
+    assert np.isnan(h[:GUARD]).all() and np.isnan(h[GUARD + n:]).all(), "write outside D"
+    return h[GUARD:GUARD + n].reshape(w.M, w.N), plan, (A, B, C, SFA, SFB)
+
+
+def check(w):
+    D, plan, (A, B, C, SFA, SFB) = run_mx(w)
+    assert "kind=mxf8f6f4" in plan, plan
+    Dref, S = oracle.gemm_mx(wl.bits(A), wl.bits(B), None if C is None else C.numpy(),
+                             SFA.numpy(), SFB.numpy(), w.M, w.N, w.K, w.transA, w.transB,
+                             w.dtype, w.beta)
+    ok, msg = oracle.compare(D, Dref, S, exact=w.integer_valued)
+    assert ok, f"{w.name} [{plan}]: {msg}"
+    return plan
+
+
+def test_mx_one_tile_integer_exact():
+    # One 128 x 128 tile, one 128-element stage: integer operands and scales
+    # in {1/2, 1, 2} make every partial sum exact.
+    check(case(128, 128, 128, wl.E4M3, 0.0, dist=("int", -3, 3), sf=(126, 128), seed=1))
+
+
+@pytest.mark.parametrize("dtype", [wl.E4M3, wl.E5M2])
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_mx_multi_tile(dtype, beta):
+    check(case(784, 1320, 528, dtype, beta, seed=2 + dtype + int(beta)))
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (272, 392, 272),    # partial last scale block (K % 32 = 16) and stage (K % 128 = 16)
+    (256, 136, 4112),   # a last Q tile of 8 rows, long K
+    (1040, 16, 2048),   # N = 16: one narrow Q tile
+    (2048, 4096, 128),  # one K stage, many tiles
+])
+def test_mx_ragged_normal(M, N, K):
+    plan = check(case(M, N, K, wl.E4M3, 1.0, seed=M + N + K))
+    assert "orientation=normal" in plan, plan
+
+
+@pytest.mark.parametrize("M", [16, 64, 144, 160])
+def test_mx_small_m_swapped(M):
+    # All of M fits one accumulator: P = B, so B's scales are the MMA's A
+    # scales and A's (up to 160 rows, two 128-row chunks) the B scales.
+    plan = check(case(M, 4104 if M != 160 else 2056, 1040, wl.E5M2 if M % 32 else wl.E4M3, 1.0,
+                      seed=50 + M))
+    assert "orientation=swapped" in plan, plan
+
+
+def test_mx_m176_stays_normal():
+    plan = check(case(176, 2048, 512, wl.E4M3, 0.0, seed=61))
+    assert "orientation=normal" in plan, plan
+
+
+def test_mx_integer_bit_exact_large():
+    check(case(1024, 1024, 1024, wl.E4M3, 1.0, dist=("int", -3, 3), sf=(126, 128), seed=71))
+    check(case(512, 768, 2048, wl.E5M2, 0.0, dist=("int", -3, 3), sf=(126, 128), seed=72))
+
+
+def test_mx_unit_scales_equal_plain_fp8():
+    # With every scale 1 the block-scaled multiply is the plain fp8 one, and the
+    # library's two paths agree within the bound (the oracle agrees bit for bit).
+    w = case(512, 640, 384, wl.E4M3, 1.0, sf=(127, 127), seed=81)
+    D, _, (A, B, C, _, _) = run_mx(w)
+    Dp = torch.empty(w.M, w.N, device="cuda")
+    st = tp.tpgemm_gemm(Dp, A.cuda(), B.cuda(), C.cuda(), w.M, w.N, w.K, 0, 1, w.dtype, 1.0)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    Dref, S = oracle.gemm(wl.bits(A), wl.bits(B), C.numpy(), w.M, w.N, w.K, False, True, w.dtype,
+                          1.0)
+    for got in (D, Dp.cpu().numpy()):
+        ok, msg = oracle.compare(got, Dref, S)
+        assert ok, msg
+
+
+def test_mx_back_to_back_calls_share_nothing():
+    # Two different problems enqueued back to back on one stream, each with
+    # its own workspace, then checked: the second launch may start while the
+    # first drains (programmatic dependent launch).
+    ws = [case(384, 512, 256, wl.E4M3, 1.0, seed=91), case(256, 640, 384, wl.E5M2, 0.0, seed=92)]
+    outs = []
+    for w in ws:
+        A, B, C = wl.make_inputs(w)
+        SFA, SFB = wl.make_scales(w)
+        D = torch.empty(w.M, w.N, device="cuda")
+        wsb = tp.tpgemm_gemm_mx_workspace_bytes(w.M, w.N, w.K)
+        buf = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        keep = (A.cuda(), B.cuda(), None if C is None else C.cuda(), SFA.cuda(), SFB.cuda(), buf)
+        st = tp.tpgemm_gemm_mx(D, keep[0], keep[1], keep[2], keep[3], keep[4], w.M, w.N, w.K,
+                               w.dtype, w.beta, buf, wsb)
+        assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+        outs.append((w, D, keep, (A, B, C, SFA, SFB)))
+    torch.cuda.synchronize()
+    for w, D, _, (A, B, C, SFA, SFB) in outs:
+        Dref, S = oracle.gemm_mx(wl.bits(A), wl.bits(B), None if C is None else C.numpy(),
+                                 SFA.numpy(), SFB.numpy(), w.M, w.N, w.K, False, True, w.dtype,
+                                 w.beta)
+        ok, msg = oracle.compare(D.cpu().numpy(), Dref, S)
+        assert ok, msg
+
+
+@pytest.mark.parametrize("name", [w.name for w in wl.MX_WORKLOADS])
+def test_mx_workload_full_size(name):
+    # Every element against the oracle's whole output.
+    check(wl.BY_NAME[name])

@@ -129,6 +129,13 @@ def _load():
         lib.tpgemm_encode_smem_desc.restype = ctypes.c_uint64
         lib.tpgemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
         lib.tpgemm_encode_idesc.restype = u32
+        lib.tpgemm_encode_idesc_mx.argtypes = [ci, ci, ci, ci, ci]
+        lib.tpgemm_encode_idesc_mx.restype = u32
+        sz = ctypes.c_size_t
+        lib.tpgemm_gemm_mx.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, cf, vp, sz, vp]
+        lib.tpgemm_gemm_mx.restype = ci
+        lib.tpgemm_gemm_mx_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.tpgemm_gemm_mx_workspace_bytes.restype = sz
         lib.tpgemm_version.argtypes = []
         lib.tpgemm_version.restype = ctypes.c_char_p
         lib.tpgemm_cp_parse_shape.argtypes = [ctypes.c_char_p, ctypes.POINTER(ci)]
@@ -205,6 +212,24 @@ def tpgemm_gemm_noalloc(D, A, B, C, M, N, K, transA, transB, dtype, beta, stream
     return int(_load().tpgemm_gemm_noalloc(_ptr(D), _ptr(A), _ptr(B), _ptr(C), int(M), int(N),
                                            int(K), int(bool(transA)), int(bool(transB)),
                                            int(dtype), float(beta), _stream(stream)))
+
+
+def tpgemm_gemm_mx(D, A, B, C, SFA, SFB, M, N, K, dtype, beta, workspace, workspace_bytes,
+                   stream=None) -> int:
+    """Enqueue the block-scaled fp8 multiply (A [M,K], B [N,K], E8M0 scales
+    SFA [M, ceil(K/32)], SFB [N, ceil(K/32)]); returns the tpgemm_status code."""
+    return int(_load().tpgemm_gemm_mx(_ptr(D), _ptr(A), _ptr(B), _ptr(C), _ptr(SFA), _ptr(SFB),
+                                      int(M), int(N), int(K), int(dtype), float(beta),
+                                      _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def tpgemm_gemm_mx_workspace_bytes(M, N, K) -> int:
+    return int(_load().tpgemm_gemm_mx_workspace_bytes(int(M), int(N), int(K)))
+
+
+def tpgemm_encode_idesc_mx(dtype, m, n, a_sf_id, b_sf_id) -> int:
+    return int(_load().tpgemm_encode_idesc_mx(int(dtype), int(m), int(n), int(a_sf_id),
+                                              int(b_sf_id)))
 
 
 def tpgemm_test_gemm_withhold_fill(D, A, B, C, M, N, K, transA, transB, dtype, beta,
@@ -369,6 +394,29 @@ def dtype_code(torch_dtype) -> int:
         return TPGEMM_E5M2
     raise TypeError(f"A and B must be float16, bfloat16, float8_e4m3fn or float8_e5m2, "
                     f"got {torch_dtype}")
+
+
+def gemm_mx(A, B, SFA, SFB, C=None, *, beta=None, out=None, workspace=None, stream=None):
+    """Block-scaled fp8 D = (A.SA)(B.SB)^T + beta.C on CUDA tensors.
+
+    A is fp8 [M, K], B fp8 [N, K] (same dtype), SFA uint8 [M, ceil(K/32)] and
+    SFB uint8 [N, ceil(K/32)] E8M0 scales, C float32 [M, N]. The scale-packing
+    workspace is allocated here with torch unless given."""
+    import torch
+    if beta is None:
+        beta = 0.0 if C is None else 1.0
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or A.dtype != B.dtype:
+        raise ValueError("A must be [M, K] and B [N, K] of the same fp8 dtype")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    wsb = tpgemm_gemm_mx_workspace_bytes(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=A.device)
+    check(tpgemm_gemm_mx(out, A, B, C, SFA, SFB, M, N, K, dtype_code(A.dtype), beta, workspace,
+                         workspace.numel() * workspace.element_size(), stream))
+    return out
 
 
 def gemm(A, B, C=None, *, beta=None, transA=False, transB=False, out=None, stream=None,

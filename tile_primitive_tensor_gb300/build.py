@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtpgemm.so")
-SOURCES = ["tpgemm_api.cu", "tc_gemm.cu", "mma_sync_gemm.cu", "tmem_copy.cu", "vec_copy.cu"]
+SOURCES = ["tpgemm_api.cu", "tc_gemm.cu", "mma_sync_gemm.cu", "tmem_copy.cu", "vec_copy.cu",
+           "mx_scales.cu"]
 HEADERS = ["ptx.cuh", "tpgemm_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -74,6 +74,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
         : "memory");
 }
 
+// 1-D bulk copy global -> this CTA's shared memory; `bytes` a multiple of 16,
+// both addresses 16-byte aligned; the bytes complete on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src,
                                              int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::
@@ -282,6 +293,23 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// Block-scaled MMA (kind::mxf8f6f4, one E8M0 scale per 32 K: scale_vec::1X):
+// D[tmem] (+)= (A . SA) * (B . SB) with e4m3 / e5m2 operands from shared-memory
+// descriptors, K = 32 per instruction. sfa_tmem / sfb_tmem address the scale
+// columns in tensor memory; the instruction descriptor's scale-factor IDs pick
+// the byte of each 32-bit scale cell.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
 // lane (quadrant base + t), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -453,6 +481,19 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(bool bf16, bool a_mn_major,
     return (1u << 4) | (uint32_t(bf16) << 7) | (uint32_t(bf16) << 10) |
            (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
            (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+// Instruction descriptor for the block-scaled kind::mxf8f6f4 (the PTX ISA's
+// instruction-descriptor table for the block-scaled kinds; the accumulator is
+// always f32): bits 4-5 B scale-factor ID, 7-9 A format and 10-12 B format
+// (0 = e4m3, 1 = e5m2), 15 / 16 A / B major-ness (0 = K-major), 17-22 N >> 3,
+// 23 scale type (1 = E8M0), 24-28 M >> 4, 29-30 A scale-factor ID. Dense, no
+// negation. A scale-factor ID selects the byte of each 32-bit scale cell.
+__host__ __device__ constexpr uint32_t idesc_mx_f32(bool e5m2, int m, int n, uint32_t a_sf_id,
+                                                    uint32_t b_sf_id) {
+    return ((b_sf_id & 3u) << 4) | (uint32_t(e5m2) << 7) | (uint32_t(e5m2) << 10) |
+           (uint32_t(n >> 3) << 17) | (1u << 23) | (uint32_t(m >> 4) << 24) |
+           ((a_sf_id & 3u) << 29);
 }
 
 // ------------------------------------------------------- warp-level mma.sync

@@ -69,7 +69,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const TcParams& p) {
     uintptr_t a = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
     uint8_t* b = reinterpret_cast<uint8_t*>(a);
     s.stages = b;
-    b += size_t(p.stages) * (p.p_bytes + p.q_bytes);
+    b += size_t(p.stages) * (p.p_bytes + p.q_bytes + p.sf_bytes);
     s.epi = reinterpret_cast<float*>(b);
     b += size_t(kEpiQuads) * p.epi_bufs * kEpiBufFloats * sizeof(float);
     uint64_t* bars = reinterpret_cast<uint64_t*>(b);
@@ -215,7 +215,7 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t v, volatil
     }
 }
 
-template <bool SWAP, bool PAIR, bool EARLY>
+template <bool SWAP, bool PAIR, bool EARLY, bool MX>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
@@ -335,8 +335,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // K-contiguous Q: one box per stage, from the map whose box
                 // height is this unit's share (whole tile or tail unit).
                 const CUtensorMap* mq = u.width == p.bn ? &mapQ : &mapQt;
-                const uint32_t tx = p.p_tx + (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
-                                                     : uint32_t(q_rows) * 128u);
+                const uint32_t tx = p.p_tx +
+                                    (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
+                                            : uint32_t(q_rows) * 128u) +
+                                    (MX ? 512u * uint32_t(1 + p.sf_q_chunks) : 0u);
                 const int nk = u.kb1 - u.kb0;
                 int kb = nk == p.k_blocks ? first_k_block(u.T, p) : u.kb0;
                 if constexpr (EARLY) {
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* sp = s.stages + size_t(stage) * (p.p_bytes + p.q_bytes);
+                    uint8_t* sp = s.stages + size_t(stage) * (p.p_bytes + p.q_bytes + p.sf_bytes);
                     uint8_t* sq = sp + p.p_bytes;
                     const int k0 = kb * p.bk;
                     if (p.test_stall && blockIdx.x == 0 && first_seg && i == 0) {
@@ -410,6 +412,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     } else {
                         tma_load_2d(sq, mq, &s.full[stage], k0, q0);
                     }
+                    if constexpr (MX) {
+                        // This stage's packed scales: 512 bytes for the P tile,
+                        // then 512 per 128 rows of the Q tile (tiles start on
+                        // 128-row boundaries in MX plans).
+                        uint8_t* sf = sq + p.q_bytes;
+                        const size_t ks = size_t(p.k_blocks);
+                        bulk_load(sf, p.sf_p + (size_t(p0 / 128) * ks + kb) * 128, 512u,
+                                  &s.full[stage]);
+                        for (int j = 0; j < p.sf_q_chunks; ++j)
+                            bulk_load(sf + 512 * (1 + j),
+                                      p.sf_q + (size_t(q0 / 128 + j) * ks + kb) * 128, 512u,
+                                      &s.full[stage]);
+                    }
                     issued_any |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == p.stages) {
@@ -437,7 +452,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t stage_base = smem_u32(s.stages);
             // Loop invariants in registers: each issue below is an asm with a
             // memory clobber, after which parameters would be read again.
-            const uint32_t stage_bytes = p.p_bytes + p.q_bytes;
+            const uint32_t stage_bytes = p.p_bytes + p.q_bytes + p.sf_bytes;
+            const uint32_t pq_bytes = p.p_bytes + p.q_bytes;
+            // Scale slots (MX): a no-swizzle K-major source of 16-byte rows, 8-row
+            // groups 128 bytes apart; each stage has its own slot in tensor memory.
+            const uint64_t dSF = smem_desc_template(512, 128, kDescLayoutNone);
+            const uint32_t sf_slot0 = tmem + uint32_t(p.sf_col0);
+            const uint32_t sf_cols = uint32_t(p.sf_cols);
+            const int sf_q_chunks = p.sf_q_chunks;
             const uint32_t p_bytes = p.p_bytes;
             const int nstages = p.stages;
             int stage = 0;
@@ -466,6 +488,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t ap = stage_base + uint32_t(stage) * stage_bytes;
                     const uint32_t aq = ap + p_bytes;
+                    if constexpr (MX) {
+                        // The stage's scales into its slot: tcgen05.cp and the
+                        // MMAs below, issued by this thread, run in issue order.
+                        // The slot is reused one ring later, after the producer
+                        // has seen this stage's MMAs complete.
+                        const uint32_t sfs = ap + pq_bytes;
+                        const uint32_t slot = sf_slot0 + uint32_t(stage) * sf_cols;
+                        tc_cp<1>(6, slot, smem_desc_with_addr(dSF, sfs));
+                        for (int j = 0; j < sf_q_chunks; ++j)
+                            tc_cp<1>(6, slot + 4u * uint32_t(1 + j),
+                                     smem_desc_with_addr(dSF, sfs + 512u * uint32_t(1 + j)));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * 32);
+                            const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * 32);
+                            // scale-factor IDs (bits 29-30 for A, 4-5 for B) = kk
+                            const uint32_t id = idesc | (uint32_t(kk) << 29) | (uint32_t(kk) << 4);
+                            tc_mma_mx(d_tmem, adesc, bdesc, id, slot, slot + 4u, (i | kk) != 0);
+                        }
+                        tc_commit(&s.empty[stage]);
+                        if (++stage == nstages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                         const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * stepP);
@@ -744,9 +792,14 @@ using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, 
 
 template <bool EARLY>
 TcKernelFn pick_kernel_dep(const TcParams& p) {
+    if (p.mx)  // single-CTA plans only
+        return p.swap ? tc_gemm_kernel<true, false, EARLY, true>
+                      : tc_gemm_kernel<false, false, EARLY, true>;
     if (p.pair)
-        return p.swap ? tc_gemm_kernel<true, true, EARLY> : tc_gemm_kernel<false, true, EARLY>;
-    return p.swap ? tc_gemm_kernel<true, false, EARLY> : tc_gemm_kernel<false, false, EARLY>;
+        return p.swap ? tc_gemm_kernel<true, true, EARLY, false>
+                      : tc_gemm_kernel<false, true, EARLY, false>;
+    return p.swap ? tc_gemm_kernel<true, false, EARLY, false>
+                  : tc_gemm_kernel<false, false, EARLY, false>;
 }
 
 // The early-start choice is a template parameter, not a runtime test: a
@@ -756,8 +809,8 @@ TcKernelFn pick_kernel(const TcParams& p) {
 }
 
 
-size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs) {
-    return 1024 + size_t(stages) * (p_bytes + q_bytes) +
+size_t tc_smem_bytes(int stages, uint32_t stage_bytes, int epi_bufs) {
+    return 1024 + size_t(stages) * stage_bytes +
            size_t(kEpiQuads) * epi_bufs * kEpiBufFloats * sizeof(float) +
            sizeof(uint64_t) * (2 * size_t(stages) + 4 + kTcMaxEpiBufs * kEpiQuads + 1) + 16;
 }
@@ -770,7 +823,17 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
         !(p.tmem_cols == 64 || p.tmem_cols == 128 || p.tmem_cols == 256 || p.tmem_cols == 512) ||
         p.tmem_cols / 2 < 32 * ((p.bn + 31) / 32))
         return cudaErrorInvalidValue;
-    const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs);
+    // MX: single-CTA, 128-row P tiles, one scale slot per stage inside the
+    // first accumulator half past the tile's columns, 1024-aligned stages.
+    if (p.mx && (p.pair || p.bp != 128 || p.tail_split != 1 || p.sk || p.tmem_cols != 512 ||
+                 !(p.sf_q_chunks == 1 || p.sf_q_chunks == 2) ||
+                 p.sf_cols != 4 + 4 * p.sf_q_chunks || p.sf_col0 < 32 * ((p.bn + 31) / 32) ||
+                 p.sf_col0 + p.stages * p.sf_cols > 256 || !p.sf_p || !p.sf_q ||
+                 p.sf_bytes < 512u * uint32_t(1 + p.sf_q_chunks) ||
+                 (p.p_bytes + p.q_bytes + p.sf_bytes) % 1024 != 0))
+        return cudaErrorInvalidValue;
+    if (!p.mx && p.sf_bytes != 0) return cudaErrorInvalidValue;
+    const size_t smem = tc_smem_bytes(p.stages, p.p_bytes + p.q_bytes + p.sf_bytes, p.epi_bufs);
     if (smem > size_t(kTcMaxSmem)) return cudaErrorInvalidConfiguration;
     auto kernel = pick_kernel(p);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -798,7 +861,7 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
 }
 
 cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters) {
-    const size_t smem = tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs);
+    const size_t smem = tc_smem_bytes(p.stages, p.p_bytes + p.q_bytes + p.sf_bytes, p.epi_bufs);
     auto kernel = pick_kernel(p);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));

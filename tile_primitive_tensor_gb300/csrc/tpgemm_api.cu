@@ -265,7 +265,7 @@ int pick_bn(int64_t M, int64_t N, int sms, bool pair) {
 }
 
 tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
-                      tpgemm_dtype dtype, float beta, int sms, Plan* out) {
+                      tpgemm_dtype dtype, float beta, int sms, Plan* out, bool mx = false) {
     const bool fp8 = is_fp8(dtype);
     tpg::TcParams p{};
     // Small M: swap operands so N runs along the 128 tensor-memory lanes and
@@ -276,7 +276,10 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     // the swapped orientation makes Q = A. Measured on GB300: an MN-contiguous
     // B operand costs 7-11 %, an MN-contiguous A operand about 2 % (8192^3
     // with B [K,N]: 726 -> 674 us). TPGEMM_TC_ORIENT=swap|normal overrides.
-    const bool swap_small = M <= 256 && N > M;
+    // Block-scaled plans (mx) keep the first half of tensor memory past the
+    // tile's columns for the scale slots, so their swapped tiles are at most
+    // 160 wide.
+    const bool swap_small = mx ? (M <= 160 && N > M) : (M <= 256 && N > M);
     bool swap = swap_small || (!transA && !transB);
     if (tuning().orient == 1) swap = true;
     if (tuning().orient == 2 && !swap_small) swap = false;
@@ -289,9 +292,14 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         return fail(TPGEMM_ERR_PATH,
                     "fp8 A and B must both be K-contiguous: A stored [M,K] (transA = 0) and B "
                     "stored [N,K] (transB = 1)");
-    // The CTA-pair MMA needs at least two 128-row P tiles.
-    const bool pair_wanted = Mp > 128;
-    const int bn = swap_small ? int(Nq) : pick_bn(Mp, Nq, sms, pair_wanted);
+    // The CTA-pair MMA needs at least two 128-row P tiles (and is not used
+    // for block-scaled plans).
+    const bool pair_wanted = Mp > 128 && !mx;
+    // Block-scaled tiles start on 128-row boundaries of Q (the packed scales'
+    // granularity): 128 wide, or all of Q when it is narrower.
+    const int bn = swap_small ? int(Nq)
+                   : mx       ? (Nq <= 128 ? int(((Nq + 15) / 16) * 16) : 128)
+                              : pick_bn(Mp, Nq, sms, pair_wanted);
     p.Mp = int(Mp);
     p.Nq = int(Nq);
     p.K = int(K);
@@ -316,13 +324,24 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     // between the pair at bn / 2). A K-contiguous half must be whole 8-row
     // swizzle groups; an MN-contiguous half starts on a 16-row boundary and is
     // loaded as whole 64-row atoms (rows past the half are not read).
-    const bool pair_ok = p.tiles_p >= 2 && (q_mn ? (bn % 32 == 0) : (bn % 16 == 0));
+    const bool pair_ok = !mx && p.tiles_p >= 2 && (q_mn ? (bn % 32 == 0) : (bn % 16 == 0));
     // On by default where it applies (measured: 8192^3 1449 -> 1563 TFLOP/s,
     // 4096^3 1105 -> 1383, skinny 36.1 -> 33.5 us); TPGEMM_TC_PAIR=0 turns it off.
     p.pair = pair_ok ? 1 : 0;
     if (tuning().pair >= 0) p.pair = (tuning().pair != 0 && pair_ok) ? 1 : 0;
     const int q_rows = p.pair ? bn / 2 : bn;  // Q rows this CTA loads per stage
-    p.idesc = tpg::idesc_f16_f32(format_code1(dtype), p_mn, q_mn, p.pair ? 256 : 128, bn);
+    p.idesc = mx ? tpg::idesc_mx_f32(format_code1(dtype), 128, bn, 0, 0)
+                 : tpg::idesc_f16_f32(format_code1(dtype), p_mn, q_mn, p.pair ? 256 : 128, bn);
+    p.mx = mx ? 1 : 0;
+    if (mx) {
+        // Scale slots: one per ring stage, in columns [bn rounded to 32, 256)
+        // of tensor memory (the first accumulator's half past its tile).
+        p.tmem_cols = 512;
+        p.sf_q_chunks = (bn + 127) / 128;
+        p.sf_cols = 4 + 4 * p.sf_q_chunks;
+        p.sf_col0 = 32 * ((bn + 31) / 32);
+        p.sf_bytes = uint32_t(((512 * (1 + p.sf_q_chunks)) + 1023) / 1024 * 1024);
+    }
     p.p_bytes = stage_tile_bytes(128, p_mn);
     p.p_tx = 128u * 128u;
     p.q_bytes = stage_tile_bytes(q_rows, q_mn);
@@ -345,7 +364,9 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     // 144 x 16392 x 4104, 7 stages of 25 KB measured 1.4 us slower than 6 --
     // and the space left over stages more of C.
     auto fits = [&](int st, int eb) {
-        return tpg::tc_smem_bytes(st, p.p_bytes, p.q_bytes, eb) <= size_t(tpg::kTcMaxSmem);
+        if (mx && p.sf_col0 + st * p.sf_cols > 256) return false;
+        return tpg::tc_smem_bytes(st, p.p_bytes + p.q_bytes + p.sf_bytes, eb) <=
+               size_t(tpg::kTcMaxSmem);
     };
     auto deepest = [&](int eb) {
         int st = 8;
@@ -453,6 +474,15 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
                       SkMode sk_mode = SkMode::Env) {
     p.sk = 0;
     p.sk_total = 0;
+    // Block-scaled plans keep whole 128-wide units (their Q tiles start on the
+    // packed scales' 128-row boundaries) and use no stream-K.
+    if (p.mx) {
+        p.full_units = p.num_super;
+        p.tail_split = 1;
+        p.num_units = p.num_super;
+        p.idesc_tail = p.idesc;
+        return;
+    }
     const bool sk_on = stream_k_requested(sk_mode);
     {
         const int ncl = std::max(1, max_grid / p.mc);
@@ -505,7 +535,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
 // Stream-K plans keep 128 rows (their scratch slots are whole tiles).
 // TPGEMM_TC_BP (64 .. 128, a multiple of 16) overrides where it fits one wave.
 void choose_p_rows(tpg::TcParams& p, int* grid, int max_grid, bool sk_requested) {
-    if (sk_requested || p.tiles_q != 1 || p.bp != 128) return;
+    if (sk_requested || p.mx || p.tiles_q != 1 || p.bp != 128) return;
     const int avail = std::max(1, max_grid / p.mc);
     if (p.num_super > avail) return;
     auto supers = [&](int bp) {
@@ -784,11 +814,12 @@ void format_plan(const Plan& plan, int64_t M, int64_t N, int64_t K, const char* 
              "tmem=%d tiles=%dx%d grid=%d units=%d+%dx%d stream_k=%d scratch=%s p_major=%s "
              "q_major=%s smem=%zu",
              plan.swap ? "swapped" : "normal", p.bp, p.bn, p.bk, p.pair ? 256 : 128, p.bn,
-             p.fp8 ? 32 : 16, p.fp8 ? "f8f6f4" : "f16", p.stages, p.epi_bufs, p.epi_groups,
+             p.fp8 ? 32 : 16, p.mx ? "mxf8f6f4" : (p.fp8 ? "f8f6f4" : "f16"), p.stages,
+             p.epi_bufs, p.epi_groups,
              p.producers, p.dep_early, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p,
              p.tiles_q, plan.grid, p.full_units, p.num_super - p.full_units, p.tail_split, p.sk,
              scratch, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
-             tpg::tc_smem_bytes(p.stages, p.p_bytes, p.q_bytes, p.epi_bufs));
+             tpg::tc_smem_bytes(p.stages, p.p_bytes + p.q_bytes + p.sf_bytes, p.epi_bufs));
 }
 
 void copy_text(const char* text, char* buf, int buflen) {
@@ -798,6 +829,22 @@ void copy_text(const char* text, char* buf, int buflen) {
     }
 }
 
+// Block-scaled operands of tpgemm_gemm_mx: E8M0 scales and the caller's
+// workspace for their packed form.
+struct MxArgs {
+    const uint8_t* SFA;
+    const uint8_t* SFB;
+    void* ws;
+    size_t ws_bytes;
+};
+
+// Workspace of tpgemm_gemm_mx: the packed scales of A, then (256-byte aligned)
+// those of B.
+size_t mx_ws_b_offset(int64_t M, int64_t K) { return (tpg::mx_packed_bytes(M, K) + 255) / 256 * 256; }
+size_t mx_ws_bytes(int64_t M, int64_t N, int64_t K) {
+    return mx_ws_b_offset(M, K) + tpg::mx_packed_bytes(N, K);
+}
+
 // Per-device epoch counter of the static scratch (all its calls share it).
 std::mutex g_static_epoch_mutex;
 uint32_t g_static_epoch[tpg::kMaxStaticScratchDevices] = {};
@@ -805,12 +852,39 @@ uint32_t g_static_epoch[tpg::kMaxStaticScratchDevices] = {};
 tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_t M, int64_t N,
                   int64_t K, int transA, int transB, tpgemm_dtype dtype, float beta, void* stream,
                   tpgemm_path path, Scratch scratch = Scratch::Allocated,
-                  bool withhold_fill = false) {
+                  bool withhold_fill = false, const MxArgs* mx = nullptr) {
     g_detail.clear();
     tpgemm_status s = check_shape(M, N, K, dtype, beta);
     if (s != TPGEMM_OK) return s;
     s = check_pointers(D, A, B, C, M, N, K, beta, elem_bytes(dtype));
     if (s != TPGEMM_OK) return s;
+    if (mx) {
+        if (!is_fp8(dtype))
+            return fail(TPGEMM_ERR_DTYPE,
+                        "block-scaled A and B must be TPGEMM_E4M3 or TPGEMM_E5M2 (dtype %d)",
+                        int(dtype));
+        if (!mx->SFA) return fail(TPGEMM_ERR_NULL, "SFA is NULL");
+        if (!mx->SFB) return fail(TPGEMM_ERR_NULL, "SFB is NULL");
+        if (!mx->ws) return fail(TPGEMM_ERR_NULL, "workspace is NULL");
+        if (reinterpret_cast<uintptr_t>(mx->ws) % 256)
+            return fail(TPGEMM_ERR_ALIGN, "workspace=%p is not 256-byte aligned", mx->ws);
+        const size_t need = mx_ws_bytes(M, N, K);
+        if (mx->ws_bytes < need)
+            return fail(TPGEMM_ERR_NULL, "workspace of %zu bytes; %zu needed", mx->ws_bytes, need);
+        const int64_t kb = (K + tpg::kMxBlock - 1) / tpg::kMxBlock;
+        const size_t dn = size_t(M) * size_t(N) * 4;
+        if (overlaps(D, dn, mx->SFA, size_t(M) * size_t(kb)) ||
+            overlaps(D, dn, mx->SFB, size_t(N) * size_t(kb)))
+            return fail(TPGEMM_ERR_ALIAS, "D overlaps a scale matrix");
+        const void* ops[5] = {D, A, B, mx->SFA, mx->SFB};
+        const size_t lens[5] = {dn, size_t(M) * size_t(K), size_t(K) * size_t(N),
+                                size_t(M) * size_t(kb), size_t(N) * size_t(kb)};
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(mx->ws, need, ops[i], lens[i]))
+                return fail(TPGEMM_ERR_ALIAS, "the workspace overlaps an operand");
+        if (beta == 1.0f && overlaps(mx->ws, need, C, dn))
+            return fail(TPGEMM_ERR_ALIAS, "the workspace overlaps C");
+    }
     DeviceInfo dev;
     s = device_info(&dev);
     if (s != TPGEMM_OK) return s;
@@ -819,7 +893,11 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
                     dev.major, dev.minor);
     const bool bf16 = dtype == TPGEMM_BF16;
     Plan plan;
-    s = make_plan(M, N, K, transA != 0, transB != 0, dtype, beta, path, dev.sms, &plan);
+    if (mx) {
+        s = plan_tc(M, N, K, transA != 0, transB != 0, dtype, beta, dev.sms, &plan, true);
+    } else {
+        s = make_plan(M, N, K, transA != 0, transB != 0, dtype, beta, path, dev.sms, &plan);
+    }
     if (s != TPGEMM_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -933,6 +1011,19 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
                           uint64_t(M), hx, hy, "C (half-quadrant box)");
             if (s != TPGEMM_OK) return s;
         }
+    }
+    if (mx) {
+        // Pack both scale matrices into the workspace (ordered before the GEMM
+        // on the same stream); P's scales are A's in the normal orientation.
+        uint32_t* wa = static_cast<uint32_t*>(mx->ws);
+        uint32_t* wb = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(mx->ws) +
+                                                   mx_ws_b_offset(M, K));
+        cudaError_t e = tpg::launch_mx_pack_scales(mx->SFA, M, K, wa, st);
+        if (e == cudaSuccess) e = tpg::launch_mx_pack_scales(mx->SFB, N, K, wb, st);
+        if (e != cudaSuccess)
+            return fail(TPGEMM_ERR_LAUNCH, "scale packing launch: %s", cudaGetErrorString(e));
+        plan.tc.sf_p = plan.swap ? wb : wa;
+        plan.tc.sf_q = plan.swap ? wa : wb;
     }
     cudaError_t e = tpg::launch_tc(maps, p, plan.grid, st);
     if (e != cudaSuccess)
@@ -1144,6 +1235,22 @@ tpgemm_status tpgemm_gemm_noalloc(float* D, const void* A, const void* B, const 
                Scratch::Static);
 }
 
+size_t tpgemm_gemm_mx_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || M >= (int64_t(1) << 30) || N >= (int64_t(1) << 30) ||
+        K >= (int64_t(1) << 30))
+        return 0;
+    return mx_ws_bytes(M, N, K);
+}
+
+tpgemm_status tpgemm_gemm_mx(float* D, const void* A, const void* B, const float* C,
+                             const uint8_t* SFA, const uint8_t* SFB, int64_t M, int64_t N,
+                             int64_t K, tpgemm_dtype dtype, float beta, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    const MxArgs mx{SFA, SFB, workspace, workspace_bytes};
+    return run(D, A, B, C, M, N, K, 0, 1, dtype, beta, stream, TPGEMM_PATH_TCGEN05,
+               Scratch::Allocated, false, &mx);
+}
+
 tpgemm_status tpgemm_test_gemm_withhold_fill(float* D, const void* A, const void* B,
                                              const float* C, int64_t M, int64_t N, int64_t K,
                                              int transA, int transB, tpgemm_dtype dtype, float beta,
@@ -1246,6 +1353,11 @@ uint64_t tpgemm_encode_smem_desc(uint32_t start_addr, uint32_t lbo_bytes, uint32
     }
     return tpg::smem_desc_with_addr(tpg::smem_desc_template(lbo_bytes, sbo_bytes, layout),
                                     start_addr);
+}
+
+uint32_t tpgemm_encode_idesc_mx(tpgemm_dtype dtype, int m, int n, int a_sf_id, int b_sf_id) {
+    if (!is_fp8(dtype)) return 0;
+    return tpg::idesc_mx_f32(format_code1(dtype), m, n, uint32_t(a_sf_id), uint32_t(b_sf_id));
 }
 
 uint32_t tpgemm_encode_idesc(tpgemm_dtype dtype, int a_mn_major, int b_mn_major, int m, int n) {

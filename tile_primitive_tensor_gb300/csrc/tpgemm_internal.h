@@ -105,6 +105,23 @@ struct TcParams {
     uint32_t* sk_flags;     // [gridDim.x][kTcEpiWarps] epoch flags, one per epilogue warp
     uint32_t sk_epoch;      // value of a flag once its slot holds this launch's data
     int sk_slot_rows;       // rows of one slot in mapW's frame (128, or bn rounded to 32)
+    // Block-scaled fp8 (kind::mxf8f6f4, one E8M0 scale per 32 K). The scales
+    // are packed by mx_pack_scales per (128-row tile, 128-element K stage) into
+    // 512 bytes: word 4 r + c holds the 4 scales of row 32 c + r of the tile for
+    // the stage's 4 K blocks (byte b for block b). That is the source layout a
+    // tcgen05.cp.32x128b.warpx4 copy spreads so that row m's word sits in
+    // tensor-memory column m / 32 of lane m (every lane quadrant gets the 32
+    // rows' 16 bytes). Each stage's words are bulk-loaded beside its operand
+    // tiles; the MMA thread copies them into the stage's scale slot in tensor
+    // memory (columns sf_col0 + stage * sf_cols: 4 for P, then 4 per 128 Q
+    // rows) and issues the four K = 32 MMAs with scale-factor IDs 0..3.
+    int mx;                 // 0 / 1 (single-CTA plans only)
+    const uint32_t* sf_p;   // packed scales of P: [ceil(Mp / 128)][k_blocks][128] words
+    const uint32_t* sf_q;   // packed scales of Q: [ceil(Nq / 128)][k_blocks][128] words
+    int sf_q_chunks;        // 128-row chunks of a Q tile's scales (1 or 2)
+    uint32_t sf_bytes;      // shared bytes of a stage's scale area (0 without MX)
+    int sf_col0;            // first tensor-memory column of the scale slots
+    int sf_cols;            // tensor-memory columns of one stage's slot
 };
 
 struct TcMaps {
@@ -118,7 +135,7 @@ struct TcMaps {
 
 
 constexpr int kTcMaxEpiBufs = 8;
-size_t tc_smem_bytes(int stages, uint32_t p_bytes, uint32_t q_bytes, int epi_bufs);
+size_t tc_smem_bytes(int stages, uint32_t stage_bytes, int epi_bufs);
 // Producer warp, MMA warp, then kTcEpiWarps epilogue warps: up to two per
 // tensor-memory lane quadrant (TcParams::epi_groups), splitting the
 // accumulator's 32-column chunks between them.
@@ -137,6 +154,14 @@ constexpr size_t kStaticScratchBytes = size_t(20) << 20;
 constexpr size_t kStaticScratchFlagBytes = size_t(256) * kTcEpiWarps * sizeof(uint32_t);
 constexpr int kMaxStaticScratchDevices = 64;
 cudaError_t tc_static_scratch(void** ptr);
+
+// ---- block-scaled fp8: scale packing pre-pass (mx_scales.cu) ----
+// sf [rows][kb] E8M0 bytes -> out [ceil(rows / 128)][ksteps][128] words in the
+// layout TcParams describes; rows or blocks past the ends read as 127 (scale 1).
+constexpr int kMxBlock = 32;                 // K elements per scale
+size_t mx_packed_bytes(int64_t rows, int64_t K);
+cudaError_t launch_mx_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint32_t* out,
+                                  cudaStream_t stream);
 
 
 }  // namespace tpg

@@ -116,7 +116,54 @@ FP8_WORKLOADS = [
              1043),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS + [WORKLOAD_4096_INT] + FP8_WORKLOADS}
+
+# Block-scaled (MX) fp8 cases: the fp8 operands above plus E8M0 block scales,
+# one per MX_BLOCK consecutive K elements of each row of A (SFA [M, KB]) and of
+# each column of B (SFB [N, KB]), KB = ceil(K / MX_BLOCK), drawn uniformly from
+# the integers sf_dist = (lo, hi) (127 is a scale of 1).
+MX_BLOCK = 32
+
+
+@dataclasses.dataclass(frozen=True)
+class MxWorkload(Workload):
+    sf_dist: tuple = (120, 134)
+
+    @property
+    def kb(self) -> int:
+        return -(-self.K // MX_BLOCK)
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """The fp8 operands, C and D as for Workload, plus one byte per scale."""
+        return super().algorithmic_bytes + (self.M + self.N) * self.kb
+
+    @property
+    def integer_valued(self) -> bool:
+        # integer operands and scales within [126, 128] keep every partial sum
+        # a multiple of 1/4 below 2^22: exact in float32
+        lo, hi = self.sf_dist
+        return super().integer_valued and lo >= 126 and hi <= 128
+
+    def describe(self) -> dict:
+        return {**super().describe(), "block_scale": f"E8M0 per {MX_BLOCK} K",
+                "scales": list(self.sf_dist)}
+
+
+MX_WORKLOADS = [
+    MxWorkload("mx_256_e4m3_transB_beta1", 256, 256, 256, E4M3, ("normal", 0.0, 1.0),
+               ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), 1.0, False, True, 1050),
+    MxWorkload("mx_8192_e4m3_transB_beta1", 8192, 8192, 8192, E4M3, ("normal", 0.0, 1.0),
+               ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), 1.0, False, True, 1051),
+    MxWorkload("mx_4096_e5m2_transB", 4096, 4096, 4096, E5M2, ("uniform", -1.0, 1.0),
+               ("uniform", -1.0, 1.0), None, 0.0, False, True, 1052),
+    MxWorkload("mx_4096_e4m3_int_transB", 4096, 4096, 4096, E4M3, ("int", -3, 3),
+               ("int", -3, 3), None, 0.0, False, True, 1053, sf_dist=(126, 128)),
+    MxWorkload("mx_skinny_144x16392x4112_e4m3_transB_beta1", 144, 16392, 4112, E4M3,
+               ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), ("normal", 0.0, 1.0), 1.0, False,
+               True, 1054),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + [WORKLOAD_4096_INT] + FP8_WORKLOADS + MX_WORKLOADS}
 
 
 def _draw(shape, dist, gen: torch.Generator) -> torch.Tensor:
@@ -157,6 +204,17 @@ def make_inputs(w: Workload, c_fill: Optional[float] = None):
     if c_fill is not None:
         C = torch.full(sc, c_fill, dtype=torch.float32)
     return A, B, C
+
+
+def make_scales(w: MxWorkload):
+    """E8M0 block scales (SFA [M, KB], SFB [N, KB]) of an MX workload as uint8
+    CPU tensors, from their own seeded stream (the operands stay those of
+    make_inputs for the same seed)."""
+    gen = torch.Generator("cpu").manual_seed(w.seed + 7919)
+    lo, hi = w.sf_dist
+    sfa = torch.randint(lo, hi + 1, (w.M, w.kb), generator=gen, dtype=torch.int32)
+    sfb = torch.randint(lo, hi + 1, (w.N, w.kb), generator=gen, dtype=torch.int32)
+    return sfa.to(torch.uint8), sfb.to(torch.uint8)
 
 
 def bits(t: torch.Tensor):
