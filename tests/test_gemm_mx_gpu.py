@@ -163,3 +163,33 @@ def test_mx_back_to_back_calls_share_nothing():
 def test_mx_workload_full_size(name):
     # Every element against the oracle's whole output.
     check(wl.BY_NAME[name])
+
+
+def test_mx_pair_and_192_wide_tiles():
+    # The default for large problems: CTA pairs (cta_group::2 block-scaled MMA,
+    # each CTA holding its own A scales and all of the tile's B scales) on
+    # 192-wide tiles, so Q tiles start at multiples of 192 and their scales
+    # span two 128-row chunks.
+    plan = check(case(784, 1320, 528, wl.E4M3, 1.0, seed=101))
+    assert "pair=1" in plan and "tile=128x192x128" in plan, plan
+
+
+def test_mx_single_cta_when_one_p_tile():
+    # One 128-row P tile: no pair.
+    plan = check(case(128, 64, 512, wl.E5M2, 1.0, seed=102))
+    assert "pair=0" in plan and "orientation=normal" in plan, plan
+
+
+@pytest.mark.parametrize("shape", [(784, 1320, 528), (144, 4104, 1040)])
+def test_mx_pair_off(shape, tune):
+    # The single-CTA block-scaled path on multi-tile and swapped problems.
+    tune.setenv("TPGEMM_TC_PAIR", "0")
+    plan = check(case(*shape, wl.E4M3, 1.0, seed=103 + shape[0]))
+    assert "pair=0" in plan, plan
+
+
+def test_mx_8192_plan_is_a_pair():
+    w = wl.BY_NAME["mx_8192_e4m3_transB_beta1"]
+    A, B, C = wl.make_inputs(w.with_shape(512, 512, 256))
+    plan = check(w.with_shape(512, 512, 256, seed=104))
+    assert "pair=1" in plan, plan

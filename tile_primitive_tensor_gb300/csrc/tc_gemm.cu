@@ -127,7 +127,9 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 
 // Work item T of a cluster -> (group of mc P tiles, Q tile); runs of `group`
 // P groups sweep all Q tiles so one wave of clusters shares a few P and Q
-// panels in L2. The CTA of cluster rank r then owns P tile tps * mc + r.
+// panels in L2. With p.snake, odd runs sweep Q backwards, so a run starts on
+// the Q panels the previous run used last (still in L2). The CTA of cluster
+// rank r then owns P tile tps * mc + r.
 __device__ __forceinline__ void tile_coords(int T, const TcParams& p, int& tps, int& tq) {
     const int per_group = p.group * p.tiles_q;
     const int g = T / per_group;
@@ -136,6 +138,7 @@ __device__ __forceinline__ void tile_coords(int T, const TcParams& p, int& tps, 
     const int r = T - g * per_group;
     tps = first + r % gsz;
     tq = r / gsz;
+    if (p.snake && (g & 1)) tq = p.tiles_q - 1 - tq;
 }
 
 // First K block of tile t. With rotation, groups of k_rotate consecutive tiles
@@ -221,7 +224,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
                    const __grid_constant__ CUtensorMap mapQt, const __grid_constant__ CUtensorMap mapW,
                    const __grid_constant__ CUtensorMap mapPh, const __grid_constant__ CUtensorMap mapCh,
-                   const __grid_constant__ CUtensorMap mapDh, const TcParams p) {
+                   const __grid_constant__ CUtensorMap mapDh, const __grid_constant__ CUtensorMap mapSP,
+                   const __grid_constant__ CUtensorMap mapSQ, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
@@ -245,6 +249,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&mapQ);
         if (p.tail_split > 1) prefetch_tensormap(&mapQt);
         if (p.sk) prefetch_tensormap(&mapW);
+        if (MX) {
+            prefetch_tensormap(&mapSP);
+            prefetch_tensormap(&mapSQ);
+        }
         if (p.beta) prefetch_tensormap(&mapC);
         prefetch_tensormap(&mapD);
         if (p.bp % 32) {
@@ -320,6 +328,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // through 0 .. producers - 1 over every fill of the CTA.
             int turn = 0;
             const int nprod = p.producers;
+            const uint64_t pol_p = l2_policy(p.l2_p);
+            const uint64_t pol_q = l2_policy(p.l2_q);
             bool ok = true;
             SegIter iter(cid, ncl, p);
             Seg u;
@@ -377,18 +387,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint32_t fb = mapa_shared(smem_u32(&s.full[stage]), 0);
                         if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * tx);
                         if (p.p_mn) {
-                            tma_load_2d_pair(sp, &mapP, fb, p0, k0);
+                            tma_load_2d_pair_hint(sp, &mapP, fb, p0, k0, pol_p);
                             if (p.bp > 64)
-                                tma_load_2d_pair(sp + kAtomBytes, &mapPh, fb, p0 + 64, k0);
+                                tma_load_2d_pair_hint(sp + kAtomBytes, &mapPh, fb, p0 + 64, k0,
+                                                      pol_p);
                         } else {
-                            tma_load_2d_pair(sp, &mapP, fb, k0, p0);
+                            tma_load_2d_pair_hint(sp, &mapP, fb, k0, p0, pol_p);
                         }
                         const int qh = q0 + rank * q_rows;  // this CTA's half of the unit's Q
                         if (p.q_mn) {
                             for (int a = 0; a < q_atoms; ++a)
-                                tma_load_2d_pair(sq + a * kAtomBytes, &mapQ, fb, qh + 64 * a, k0);
+                                tma_load_2d_pair_hint(sq + a * kAtomBytes, &mapQ, fb, qh + 64 * a,
+                                                      k0, pol_q);
                         } else {
-                            tma_load_2d_pair(sq, mq, fb, k0, qh);
+                            tma_load_2d_pair_hint(sq, mq, fb, k0, qh, pol_q);
+                        }
+                        if constexpr (MX) {
+                            // This CTA's P chunk and all of the tile's Q chunks.
+                            uint8_t* sf = sq + p.q_bytes;
+                            tma_load_2d_pair(sf, &mapSP, fb, 0, (p0 / 128) * p.k_blocks + kb);
+                            tma_load_2d_pair(sf + 512, &mapSQ, fb, 0,
+                                             (tq * p.k_blocks + kb) * p.sf_q_chunks);
                         }
                         issued_any |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -400,30 +419,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     mbar_arrive_expect_tx(&s.full[stage], tx);
                     if (p.p_mn) {
-                        tma_load_2d(sp, &mapP, &s.full[stage], p0, k0);
+                        tma_load_2d_hint(sp, &mapP, &s.full[stage], p0, k0, pol_p);
                         if (p.bp > 64)
-                            tma_load_2d(sp + kAtomBytes, &mapPh, &s.full[stage], p0 + 64, k0);
+                            tma_load_2d_hint(sp + kAtomBytes, &mapPh, &s.full[stage], p0 + 64, k0,
+                                             pol_p);
                     } else {
-                        tma_load_2d(sp, &mapP, &s.full[stage], k0, p0);
+                        tma_load_2d_hint(sp, &mapP, &s.full[stage], k0, p0, pol_p);
                     }
                     if (p.q_mn) {
                         for (int a = 0; a < q_atoms; ++a)
-                            tma_load_2d(sq + a * kAtomBytes, &mapQ, &s.full[stage], q0 + 64 * a, k0);
+                            tma_load_2d_hint(sq + a * kAtomBytes, &mapQ, &s.full[stage],
+                                             q0 + 64 * a, k0, pol_q);
                     } else {
-                        tma_load_2d(sq, mq, &s.full[stage], k0, q0);
+                        tma_load_2d_hint(sq, mq, &s.full[stage], k0, q0, pol_q);
                     }
                     if constexpr (MX) {
-                        // This stage's packed scales: 512 bytes for the P tile,
-                        // then 512 per 128 rows of the Q tile (tiles start on
-                        // 128-row boundaries in MX plans).
+                        // This stage's packed scales: the P tile's chunk, then
+                        // the Q tile's chunks.
                         uint8_t* sf = sq + p.q_bytes;
-                        const size_t ks = size_t(p.k_blocks);
-                        bulk_load(sf, p.sf_p + (size_t(p0 / 128) * ks + kb) * 128, 512u,
-                                  &s.full[stage]);
-                        for (int j = 0; j < p.sf_q_chunks; ++j)
-                            bulk_load(sf + 512 * (1 + j),
-                                      p.sf_q + (size_t(q0 / 128 + j) * ks + kb) * 128, 512u,
-                                      &s.full[stage]);
+                        tma_load_2d(sf, &mapSP, &s.full[stage], 0, (p0 / 128) * p.k_blocks + kb);
+                        tma_load_2d(sf + 512, &mapSQ, &s.full[stage], 0,
+                                    (tq * p.k_blocks + kb) * p.sf_q_chunks);
                     }
                     issued_any |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -457,9 +473,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Scale slots (MX): a no-swizzle K-major source of 16-byte rows, 8-row
             // groups 128 bytes apart; each stage has its own slot in tensor memory.
             const uint64_t dSF = smem_desc_template(512, 128, kDescLayoutNone);
+            const int sf_q_chunks = p.sf_q_chunks;
             const uint32_t sf_slot0 = tmem + uint32_t(p.sf_col0);
             const uint32_t sf_cols = uint32_t(p.sf_cols);
-            const int sf_q_chunks = p.sf_q_chunks;
+            const int sf_spr = p.sf_spr > 0 ? p.sf_spr : 1;
+            const uint32_t half_cols = uint32_t(p.tmem_cols / 2);
             const uint32_t p_bytes = p.p_bytes;
             const int nstages = p.stages;
             int stage = 0;
@@ -490,24 +508,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t aq = ap + p_bytes;
                     if constexpr (MX) {
                         // The stage's scales into its slot: tcgen05.cp and the
-                        // MMAs below, issued by this thread, run in issue order.
-                        // The slot is reused one ring later, after the producer
-                        // has seen this stage's MMAs complete.
+                        // MMAs below, issued by this thread, run in issue order
+                        // (in a pair, the copy fills both CTAs' slots, each from
+                        // its own shared memory). A slot is rewritten one ring
+                        // later: that fill has landed only after the producer
+                        // saw this stage's MMAs complete.
                         const uint32_t sfs = ap + pq_bytes;
-                        const uint32_t slot = sf_slot0 + uint32_t(stage) * sf_cols;
-                        tc_cp<1>(6, slot, smem_desc_with_addr(dSF, sfs));
+                        const int hs = stage / sf_spr;
+                        const uint32_t slot = sf_slot0 + uint32_t(hs) * half_cols +
+                                              uint32_t(stage - hs * sf_spr) * sf_cols;
+                        tc_cp<CG>(6, slot, smem_desc_with_addr(dSF, sfs));
                         for (int j = 0; j < sf_q_chunks; ++j)
-                            tc_cp<1>(6, slot + 4u * uint32_t(1 + j),
-                                     smem_desc_with_addr(dSF, sfs + 512u * uint32_t(1 + j)));
+                            tc_cp<CG>(6, slot + 4u * uint32_t(1 + j),
+                                      smem_desc_with_addr(dSF, sfs + 512u * uint32_t(1 + j)));
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * 32);
                             const uint64_t bdesc = smem_desc_with_addr(dQ, aq + kk * 32);
                             // scale-factor IDs (bits 29-30 for A, 4-5 for B) = kk
                             const uint32_t id = idesc | (uint32_t(kk) << 29) | (uint32_t(kk) << 4);
-                            tc_mma_mx(d_tmem, adesc, bdesc, id, slot, slot + 4u, (i | kk) != 0);
+                            if constexpr (PAIR)
+                                tc_mma_mx_pair(d_tmem, adesc, bdesc, id, slot, slot + 4u,
+                                               (i | kk) != 0);
+                            else
+                                tc_mma_mx(d_tmem, adesc, bdesc, id, slot, slot + 4u, (i | kk) != 0);
                         }
-                        tc_commit(&s.empty[stage]);
+                        if (PAIR)
+                            tc_commit_pair_multicast(&s.empty[stage], pair_mask);
+                        else
+                            tc_commit(&s.empty[stage]);
                         if (++stage == nstages) {
                             stage = 0;
                             phase ^= 1u;
@@ -573,6 +602,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float* bufs = es.bufs;
         uint64_t* cb = es.cb;
         const uint32_t lane_base = uint32_t(quad * 32) << 16;
+        // C is read once and D written once: their lines should not push the
+        // operand panels that later tiles reuse out of L2. Stream-K partial
+        // tiles are re-read, so they keep the normal policy.
+        const uint64_t pol_cd = l2_policy(p.l2_cd);
 
         // Output extents in the kernel's (P, Q) frame, for skipping empty chunks.
         const int lim_p = p.Mp;
@@ -640,7 +673,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int c = ng * j + half;
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&cb[j], src_bytes);
-                        tma_load_2d(bufs + j * kEpiBufFloats, src_map, &cb[j], src_x(c), src_y(c));
+                        tma_load_2d_hint(bufs + j * kEpiBufFloats, src_map, &cb[j], src_x(c),
+                                         src_y(c), from_slot ? l2_policy(0) : pol_cd);
                     }
                     cpend |= 1u << j;
                 }
@@ -713,13 +747,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(dst_map, buf, dst_x(c), dst_y(c));
+                    tma_store_2d_hint(dst_map, buf, dst_x(c), dst_y(c),
+                                      to_slot ? l2_policy(0) : pol_cd);
                     bulk_commit_group();
                     if (add_src && j + nbw < my_chunks) {
                         const int cn = c + ng * nbw;  // this warp's chunk j + nbw
                         bulk_wait_group_read<0>();  // the store just issued has read buf
                         mbar_arrive_expect_tx(&cb[bi], src_bytes);
-                        tma_load_2d(buf, src_map, &cb[bi], src_x(cn), src_y(cn));
+                        tma_load_2d_hint(buf, src_map, &cb[bi], src_x(cn), src_y(cn),
+                                         from_slot ? l2_policy(0) : pol_cd);
                     }
                 }
                 if (add_src && j + nbw < my_chunks) cpend |= 1u << bi;
@@ -788,13 +824,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }  // namespace
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
-                            CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
+                            CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                            CUtensorMap, TcParams);
 
 template <bool EARLY>
 TcKernelFn pick_kernel_dep(const TcParams& p) {
-    if (p.mx)  // single-CTA plans only
+    if (p.mx) {
+        if (p.pair)
+            return p.swap ? tc_gemm_kernel<true, true, EARLY, true>
+                          : tc_gemm_kernel<false, true, EARLY, true>;
         return p.swap ? tc_gemm_kernel<true, false, EARLY, true>
                       : tc_gemm_kernel<false, false, EARLY, true>;
+    }
     if (p.pair)
         return p.swap ? tc_gemm_kernel<true, true, EARLY, false>
                       : tc_gemm_kernel<false, true, EARLY, false>;
@@ -823,13 +864,13 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
         !(p.tmem_cols == 64 || p.tmem_cols == 128 || p.tmem_cols == 256 || p.tmem_cols == 512) ||
         p.tmem_cols / 2 < 32 * ((p.bn + 31) / 32))
         return cudaErrorInvalidValue;
-    // MX: single-CTA, 128-row P tiles, one scale slot per stage inside the
-    // first accumulator half past the tile's columns, 1024-aligned stages.
-    if (p.mx && (p.pair || p.bp != 128 || p.tail_split != 1 || p.sk || p.tmem_cols != 512 ||
+    // MX: 128-row P tiles, one scale slot per stage in the accumulator halves
+    // past the tile's columns, 1024-aligned stages.
+    if (p.mx && (p.bp != 128 || p.tail_split != 1 || p.sk || p.tmem_cols != 512 ||
                  !(p.sf_q_chunks == 1 || p.sf_q_chunks == 2) ||
                  p.sf_cols != 4 + 4 * p.sf_q_chunks || p.sf_col0 < 32 * ((p.bn + 31) / 32) ||
-                 p.sf_col0 + p.stages * p.sf_cols > 256 || !p.sf_p || !p.sf_q ||
-                 p.sf_bytes < 512u * uint32_t(1 + p.sf_q_chunks) ||
+                 p.sf_spr < 1 || p.sf_col0 + p.sf_spr * p.sf_cols > 256 ||
+                 p.stages > 2 * p.sf_spr || p.sf_bytes < 512u * uint32_t(1 + p.sf_q_chunks) ||
                  (p.p_bytes + p.q_bytes + p.sf_bytes) % 1024 != 0))
         return cudaErrorInvalidValue;
     if (!p.mx && p.sf_bytes != 0) return cudaErrorInvalidValue;
@@ -857,7 +898,7 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
     cfg.attrs = attr;
     cfg.numAttrs = p.mc > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, maps.Qt, maps.W, maps.Ph,
-                              maps.Ch, maps.Dh, p);
+                              maps.Ch, maps.Dh, maps.SP, maps.SQ, p);
 }
 
 cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters) {

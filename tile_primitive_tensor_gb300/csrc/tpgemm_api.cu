@@ -92,7 +92,7 @@ tpgemm_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 struct Tuning {
     int bn = -1, bp = -1, dep_early = -1, epi_bufs = -1, epi_groups = -1, group = -1;
     int krotate = -1, max_clusters = -1, pair = -1, producers = -1, sk = -1, stages = -1;
-    int tail = -1, host_blocks = -1;
+    int tail = -1, host_blocks = -1, l2_p = -1, l2_q = -1, l2_cd = -1, snake = -1;
     int orient = 0;  // 1 "swap", 2 "normal"
     long long wait_ms = -1;
 };
@@ -116,6 +116,10 @@ Tuning read_tuning() {
     geti("TPGEMM_TC_STAGES", &t.stages);
     geti("TPGEMM_TC_TAIL", &t.tail);
     geti("TPGEMM_HOST_BLOCKS", &t.host_blocks);
+    geti("TPGEMM_TC_L2_P", &t.l2_p);
+    geti("TPGEMM_TC_L2_Q", &t.l2_q);
+    geti("TPGEMM_TC_L2_CD", &t.l2_cd);
+    geti("TPGEMM_TC_SNAKE", &t.snake);
     if (const char* f = getenv("TPGEMM_TC_ORIENT")) {
         if (!strcmp(f, "swap")) t.orient = 1;
         if (!strcmp(f, "normal")) t.orient = 2;
@@ -292,13 +296,13 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         return fail(TPGEMM_ERR_PATH,
                     "fp8 A and B must both be K-contiguous: A stored [M,K] (transA = 0) and B "
                     "stored [N,K] (transB = 1)");
-    // The CTA-pair MMA needs at least two 128-row P tiles (and is not used
-    // for block-scaled plans).
-    const bool pair_wanted = Mp > 128 && !mx;
-    // Block-scaled tiles start on 128-row boundaries of Q (the packed scales'
-    // granularity): 128 wide, or all of Q when it is narrower.
+    // The CTA-pair MMA needs at least two 128-row P tiles.
+    const bool pair_wanted = Mp > 128;
+    // Block-scaled tiles are at most 192 wide: each accumulator half keeps the
+    // columns past its tile for the scale slots (at 192, five 12-column slots
+    // per half).
     const int bn = swap_small ? int(Nq)
-                   : mx       ? (Nq <= 128 ? int(((Nq + 15) / 16) * 16) : 128)
+                   : mx       ? (Nq <= 192 ? int(((Nq + 15) / 16) * 16) : 192)
                               : pick_bn(Mp, Nq, sms, pair_wanted);
     p.Mp = int(Mp);
     p.Nq = int(Nq);
@@ -324,23 +328,25 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     // between the pair at bn / 2). A K-contiguous half must be whole 8-row
     // swizzle groups; an MN-contiguous half starts on a 16-row boundary and is
     // loaded as whole 64-row atoms (rows past the half are not read).
-    const bool pair_ok = !mx && p.tiles_p >= 2 && (q_mn ? (bn % 32 == 0) : (bn % 16 == 0));
+    const bool pair_ok = p.tiles_p >= 2 && (q_mn ? (bn % 32 == 0) : (bn % 16 == 0));
     // On by default where it applies (measured: 8192^3 1449 -> 1563 TFLOP/s,
     // 4096^3 1105 -> 1383, skinny 36.1 -> 33.5 us); TPGEMM_TC_PAIR=0 turns it off.
     p.pair = pair_ok ? 1 : 0;
     if (tuning().pair >= 0) p.pair = (tuning().pair != 0 && pair_ok) ? 1 : 0;
     const int q_rows = p.pair ? bn / 2 : bn;  // Q rows this CTA loads per stage
-    p.idesc = mx ? tpg::idesc_mx_f32(format_code1(dtype), 128, bn, 0, 0)
+    p.idesc = mx ? tpg::idesc_mx_f32(format_code1(dtype), p.pair ? 256 : 128, bn, 0, 0)
                  : tpg::idesc_f16_f32(format_code1(dtype), p_mn, q_mn, p.pair ? 256 : 128, bn);
     p.mx = mx ? 1 : 0;
     if (mx) {
-        // Scale slots: one per ring stage, in columns [bn rounded to 32, 256)
-        // of tensor memory (the first accumulator's half past its tile).
+        // Scale slots: one per ring stage, in each accumulator half's columns
+        // past its tile ([bn rounded to 32, 256) of the half).
         p.tmem_cols = 512;
         p.sf_q_chunks = (bn + 127) / 128;
         p.sf_cols = 4 + 4 * p.sf_q_chunks;
         p.sf_col0 = 32 * ((bn + 31) / 32);
+        p.sf_spr = (256 - p.sf_col0) / p.sf_cols;
         p.sf_bytes = uint32_t(((512 * (1 + p.sf_q_chunks)) + 1023) / 1024 * 1024);
+        if (p.sf_spr < 1) return fail(TPGEMM_ERR_PATH, "internal: no room for scale slots");
     }
     p.p_bytes = stage_tile_bytes(128, p_mn);
     p.p_tx = 128u * 128u;
@@ -349,10 +355,17 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.timeout_ns = wait_timeout_ns();
     p.test_stall = 0;  // set only by tpgemm_test_gemm_withhold_fill
     p.swap = swap;
+    // L2 policies (set with the grid in choose_l2_policies); C and D stream
+    // through once.
+    p.l2_p = 2;
+    p.l2_q = 2;
+    p.l2_cd = 1;
     // Raster: runs of 8 P groups sweep all Q tiles (measured best at 8192^3:
     // fewer panel re-reads from HBM than 16 or 32, less power, higher clock).
     p.group = 8;
     if (tuning().group >= 0) p.group = std::max(1, tuning().group);
+    p.snake = 1;
+    if (tuning().snake >= 0) p.snake = tuning().snake != 0;
     // Every tile shares the one Q tile when all of Q fits it: spread the CTAs'
     // starting K blocks so they do not contend for the same lines of it.
     p.k_rotate = (p.tiles_q == 1 && p.tiles_p > 1) ? 1 : 0;
@@ -364,7 +377,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     // 144 x 16392 x 4104, 7 stages of 25 KB measured 1.4 us slower than 6 --
     // and the space left over stages more of C.
     auto fits = [&](int st, int eb) {
-        if (mx && p.sf_col0 + st * p.sf_cols > 256) return false;
+        if (mx && st > 2 * p.sf_spr) return false;
         return tpg::tc_smem_bytes(st, p.p_bytes + p.q_bytes + p.sf_bytes, eb) <=
                size_t(tpg::kTcMaxSmem);
     };
@@ -382,7 +395,9 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         if (p.beta)
             while (epi_bufs < std::min(nchunks, tpg::kTcMaxEpiBufs) && fits(stages, epi_bufs + 1))
                 ++epi_bufs;
-    } else if (p.beta && nchunks > 2 && nchunks <= tpg::kTcMaxEpiBufs) {
+    } else if (p.beta && nchunks > 2 && nchunks <= tpg::kTcMaxEpiBufs && !mx) {
+        // (Block-scaled stages hold 128 K per stage and carry scales: their
+        // plans keep the deepest ring instead.)
         const int st = deepest(nchunks);
         if (st >= 4) {
             epi_bufs = nchunks;
@@ -613,6 +628,29 @@ void choose_producers(tpg::TcParams& p, int grid) {
     if (tuning().dep_early >= 0) p.dep_early = tuning().dep_early != 0;
 }
 
+// L2 eviction priorities of the TMA traffic. C and D are read / written once
+// (evict first). Operand panels that later tiles reuse are kept (evict last):
+// on 8192^3 bf16, measured on one box interleaved, 645 -> 630 us burst and
+// 722 -> 702 us sustained against normal priority for all (evict first on C
+// and D alone changed nothing). A single-wave plan whose tiles share the one
+// Q tile streams P once: P evict first, the shared Q tile evict last (on
+// 144 x 16392 x 4104, back to back: P normal 37.9 us, evict last 32.3, evict
+// first 31.4). TPGEMM_TC_L2_P / _Q / _CD (0 normal, 1 evict first, 2 evict
+// last) override.
+void choose_l2_policies(tpg::TcParams& p, int grid) {
+    const int ncl = std::max(1, grid / p.mc);
+    const bool streamed_p = p.tiles_q == 1 && p.num_units <= ncl;
+    p.l2_p = streamed_p ? 1 : 2;
+    p.l2_q = 2;
+    p.l2_cd = 1;
+    auto pick = [](int v, int* dst) {
+        if (v >= 0 && v <= 2) *dst = v;
+    };
+    pick(tuning().l2_p, &p.l2_p);
+    pick(tuning().l2_q, &p.l2_q);
+    pick(tuning().l2_cd, &p.l2_cd);
+}
+
 // Stream-K scratch per (device, stream): allocated on first use, kept until
 // exit, flags zeroed once; launches on one stream are ordered, so each takes
 // the next epoch and never sees an earlier launch's flags as its own.
@@ -726,6 +764,24 @@ tpgemm_status encode_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map,
     return TPGEMM_OK;
 }
 
+// Packed block scales: rows of 128 32-bit words (one 512-byte chunk each),
+// boxes of box_rows whole chunks, no swizzle.
+tpgemm_status encode_u32_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map,
+                              const void* base, uint64_t rows, uint32_t box_rows,
+                              const char* what) {
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {512};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TPGEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
+                    int(r));
+    return TPGEMM_OK;
+}
+
 // Map of a K x rows operand: K-contiguous -> dims {K, rows}, box {64, box_rows};
 // MN-contiguous -> dims {rows, K}, box {64, 64}.
 CUtensorMapDataType operand_type(tpgemm_dtype dtype) {
@@ -765,6 +821,7 @@ tpgemm_status finish_tc_plan(Plan* plan, tpgemm_dtype dtype, SkMode sk_mode) {
     apply_tail_split(plan->tc, &plan->grid, plan->max_grid, format_code1(dtype), sk_mode);
     choose_epi_groups(plan->tc, plan->grid);
     choose_producers(plan->tc, plan->grid);
+    choose_l2_policies(plan->tc, plan->grid);
     return TPGEMM_OK;
 }
 
@@ -812,13 +869,13 @@ void format_plan(const Plan& plan, int64_t M, int64_t N, int64_t K, const char* 
              "path=tcgen05 orientation=%s tile=%dx%dx%d umma=%dx%dx%d kind=%s stages=%d "
              "epi_bufs=%d epi_groups=%d producers=%d dep_early=%d k_rotate=%d cluster=%d pair=%d "
              "tmem=%d tiles=%dx%d grid=%d units=%d+%dx%d stream_k=%d scratch=%s p_major=%s "
-             "q_major=%s smem=%zu",
+             "q_major=%s l2=%d%d%d snake=%d smem=%zu",
              plan.swap ? "swapped" : "normal", p.bp, p.bn, p.bk, p.pair ? 256 : 128, p.bn,
              p.fp8 ? 32 : 16, p.mx ? "mxf8f6f4" : (p.fp8 ? "f8f6f4" : "f16"), p.stages,
              p.epi_bufs, p.epi_groups,
              p.producers, p.dep_early, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p,
              p.tiles_q, plan.grid, p.full_units, p.num_super - p.full_units, p.tail_split, p.sk,
-             scratch, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k",
+             scratch, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k", p.l2_p, p.l2_q, p.l2_cd, p.snake,
              tpg::tc_smem_bytes(p.stages, p.p_bytes + p.q_bytes + p.sf_bytes, p.epi_bufs));
 }
 
@@ -839,10 +896,12 @@ struct MxArgs {
 };
 
 // Workspace of tpgemm_gemm_mx: the packed scales of A, then (256-byte aligned)
-// those of B.
-size_t mx_ws_b_offset(int64_t M, int64_t K) { return (tpg::mx_packed_bytes(M, K) + 255) / 256 * 256; }
+// those of B, each sized for any tile height a plan may use.
+size_t mx_ws_b_offset(int64_t M, int64_t K) {
+    return (tpg::mx_packed_bytes_bound(M, K) + 255) / 256 * 256;
+}
 size_t mx_ws_bytes(int64_t M, int64_t N, int64_t K) {
-    return mx_ws_b_offset(M, K) + tpg::mx_packed_bytes(N, K);
+    return mx_ws_b_offset(M, K) + tpg::mx_packed_bytes_bound(N, K);
 }
 
 // Per-device epoch counter of the static scratch (all its calls share it).
@@ -1014,16 +1073,24 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     }
     if (mx) {
         // Pack both scale matrices into the workspace (ordered before the GEMM
-        // on the same stream); P's scales are A's in the normal orientation.
+        // on the same stream): P's in 128-row tiles, Q's in tiles of bn rows.
+        // P's scales are A's in the normal orientation.
         uint32_t* wa = static_cast<uint32_t*>(mx->ws);
         uint32_t* wb = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(mx->ws) +
                                                    mx_ws_b_offset(M, K));
-        cudaError_t e = tpg::launch_mx_pack_scales(mx->SFA, M, K, wa, st);
-        if (e == cudaSuccess) e = tpg::launch_mx_pack_scales(mx->SFB, N, K, wb, st);
+        const int rows_a = plan.swap ? p.bn : 128, rows_b = plan.swap ? 128 : p.bn;
+        cudaError_t e = tpg::launch_mx_pack_scales(mx->SFA, M, K, rows_a, wa, st);
+        if (e == cudaSuccess) e = tpg::launch_mx_pack_scales(mx->SFB, N, K, rows_b, wb, st);
         if (e != cudaSuccess)
             return fail(TPGEMM_ERR_LAUNCH, "scale packing launch: %s", cudaGetErrorString(e));
-        plan.tc.sf_p = plan.swap ? wb : wa;
-        plan.tc.sf_q = plan.swap ? wa : wb;
+        const uint32_t* sp = plan.swap ? wb : wa;
+        const uint32_t* sq = plan.swap ? wa : wb;
+        const uint64_t chunk_rows_p = tpg::mx_packed_bytes(p.Mp, K, 128) / 512;
+        const uint64_t chunk_rows_q = tpg::mx_packed_bytes(p.Nq, K, p.bn) / 512;
+        s = encode_u32_rows(enc, &maps.SP, sp, chunk_rows_p, 1, "P scales");
+        if (s != TPGEMM_OK) return s;
+        s = encode_u32_rows(enc, &maps.SQ, sq, chunk_rows_q, uint32_t(p.sf_q_chunks), "Q scales");
+        if (s != TPGEMM_OK) return s;
     }
     cudaError_t e = tpg::launch_tc(maps, p, plan.grid, st);
     if (e != cudaSuccess)
@@ -1324,6 +1391,7 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
         apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code1(dtype));
         choose_epi_groups(plan.tc, plan.grid);
         choose_producers(plan.tc, plan.grid);
+        choose_l2_policies(plan.tc, plan.grid);
     }
     char text[640];
     format_plan(plan, M, N, K, plan.tc.sk ? "allocated" : "none", text, sizeof(text));

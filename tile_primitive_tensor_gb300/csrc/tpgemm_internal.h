@@ -59,6 +59,7 @@ struct TcParams {
     int p_mn, q_mn;         // operand stored MN-contiguous (1) or K-contiguous (0)
     int beta;               // 0 or 1
     int group;              // tiles along P per raster group (L2 reuse)
+    int snake;              // 1: odd raster groups sweep Q backwards
     uint32_t idesc;         // tcgen05 instruction descriptor
     uint32_t p_bytes;       // shared bytes of one P stage tile
     uint32_t q_bytes;       // shared bytes of one Q stage tile
@@ -106,22 +107,28 @@ struct TcParams {
     uint32_t sk_epoch;      // value of a flag once its slot holds this launch's data
     int sk_slot_rows;       // rows of one slot in mapW's frame (128, or bn rounded to 32)
     // Block-scaled fp8 (kind::mxf8f6f4, one E8M0 scale per 32 K). The scales
-    // are packed by mx_pack_scales per (128-row tile, 128-element K stage) into
-    // 512 bytes: word 4 r + c holds the 4 scales of row 32 c + r of the tile for
-    // the stage's 4 K blocks (byte b for block b). That is the source layout a
-    // tcgen05.cp.32x128b.warpx4 copy spreads so that row m's word sits in
-    // tensor-memory column m / 32 of lane m (every lane quadrant gets the 32
-    // rows' 16 bytes). Each stage's words are bulk-loaded beside its operand
-    // tiles; the MMA thread copies them into the stage's scale slot in tensor
-    // memory (columns sf_col0 + stage * sf_cols: 4 for P, then 4 per 128 Q
-    // rows) and issues the four K = 32 MMAs with scale-factor IDs 0..3.
-    int mx;                 // 0 / 1 (single-CTA plans only)
-    const uint32_t* sf_p;   // packed scales of P: [ceil(Mp / 128)][k_blocks][128] words
-    const uint32_t* sf_q;   // packed scales of Q: [ceil(Nq / 128)][k_blocks][128] words
+    // are packed by mx_pack_scales per (tile, 128-element K stage, 128-row
+    // chunk of the tile) into 512 bytes: word 4 r + c holds the 4 scales of row
+    // 32 c + r of the chunk for the stage's 4 K blocks (byte b for block b).
+    // That is the source layout a tcgen05.cp.32x128b.warpx4 copy spreads so
+    // that row m's word sits in tensor-memory column m / 32 of lane m (every
+    // lane quadrant gets the 32 rows' 16 bytes). P tiles are 128 rows (one
+    // chunk), Q tiles bn rows (sf_q_chunks chunks). Each stage's chunks are
+    // TMA-loaded (mapSP, mapSQ) beside its operand tiles; the MMA thread copies
+    // them into the stage's scale slot in tensor memory (4 columns for P, then
+    // 4 per Q chunk) and issues the four K = 32 MMAs with scale-factor IDs
+    // 0..3. In a CTA pair each CTA holds its own P chunk and all Q chunks.
+    // Slot i lies in accumulator half i / sf_spr, at column sf_col0 + (i %
+    // sf_spr) sf_cols past that half's start (past its tile's columns).
+    int mx;                 // 0 / 1
+    int l2_p, l2_q;         // L2 policies of the P and Q loads: 0 normal, 1 evict_first,
+                            // 2 evict_last (ptx.cuh l2_policy)
+    int l2_cd;              // L2 policy of the C loads and D stores (read / written once)
     int sf_q_chunks;        // 128-row chunks of a Q tile's scales (1 or 2)
     uint32_t sf_bytes;      // shared bytes of a stage's scale area (0 without MX)
-    int sf_col0;            // first tensor-memory column of the scale slots
+    int sf_col0;            // first scale column in each accumulator half
     int sf_cols;            // tensor-memory columns of one stage's slot
+    int sf_spr;             // scale slots per accumulator half
 };
 
 struct TcMaps {
@@ -130,6 +137,8 @@ struct TcMaps {
     CUtensorMap Ch, Dh;     // C / D with a half-quadrant box (16 tensor-memory lanes)
     CUtensorMap Qt;         // Q with the (narrower) box of a tail unit
     CUtensorMap W;          // stream-K scratch slots, laid out like D tiles
+    CUtensorMap SP, SQ;     // packed scales of P / Q (block-scaled plans): 128 words x
+                            // one chunk per row; boxes of 1 / sf_q_chunks chunks
 };
 
 
@@ -156,12 +165,16 @@ constexpr int kMaxStaticScratchDevices = 64;
 cudaError_t tc_static_scratch(void** ptr);
 
 // ---- block-scaled fp8: scale packing pre-pass (mx_scales.cu) ----
-// sf [rows][kb] E8M0 bytes -> out [ceil(rows / 128)][ksteps][128] words in the
-// layout TcParams describes; rows or blocks past the ends read as 127 (scale 1).
+// sf [rows][kb] E8M0 bytes -> out [ceil(rows / tile_rows)][ksteps][chunks][128]
+// words (chunks = ceil(tile_rows / 128)) in the layout TcParams describes;
+// rows or blocks past the ends read as 127 (scale 1).
 constexpr int kMxBlock = 32;                 // K elements per scale
-size_t mx_packed_bytes(int64_t rows, int64_t K);
-cudaError_t launch_mx_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint32_t* out,
-                                  cudaStream_t stream);
+size_t mx_packed_bytes(int64_t rows, int64_t K, int tile_rows);
+// An upper bound of mx_packed_bytes over every tile height a plan uses (128,
+// or up to 192 for the Q operand).
+size_t mx_packed_bytes_bound(int64_t rows, int64_t K);
+cudaError_t launch_mx_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows,
+                                  uint32_t* out, cudaStream_t stream);
 
 
 }  // namespace tpg
