@@ -304,8 +304,8 @@ def oracle_sample_mx(w, A, B, C, seconds: float):
     import oracle
     oracle.build()
     SFA, SFB = wl.make_scales(w)
-    Bb, sfb = wl.bits(B), SFB.numpy()
-    Ab, sfa = wl.bits(A).reshape(w.M, w.K), SFA.numpy()
+    Bb, sfb = wl.operand_bits(w, B), SFB.numpy()
+    Ab, sfa = wl.operand_bits(w, A).reshape(w.M, w.K), SFA.numpy()
     Cn = None if C is None else C.numpy()
 
     def run(rows):
@@ -490,8 +490,9 @@ def roofline_of(w, launch_ms: float, peaks: dict, src: str) -> dict:
     """Achieved rate of one launch against the bound of its workload: tensor
     peak above the ridge point, HBM bandwidth below it."""
     # fp8 runs at twice the dense bf16 rate (nominal 4.5 / 2.25 PFLOP/s): its
-    # peak is the measured bf16 one times that ratio.
-    ratio = 2.0 if w.dtype in (wl.E4M3, wl.E5M2) else 1.0
+    # peak is the measured bf16 one times that ratio. fp4 runs on the same
+    # kind::f8f6f4 MMA at the fp8 rate.
+    ratio = 2.0 if w.dtype in (wl.E4M3, wl.E5M2, wl.E2M1) else 1.0
     t_peak = peaks["bf16_tflops"] * ratio
     t_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
     ridge = t_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
@@ -500,7 +501,8 @@ def roofline_of(w, launch_ms: float, peaks: dict, src: str) -> dict:
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(t_peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / t_peak, 4),
                 "peak_kind": f"{src} bf16 dense burst" + (
-                    " x 2 (nominal fp8 : bf16 ratio)" if ratio != 1.0 else ""),
+                    " x 2 (nominal fp8 : bf16 ratio; fp4 runs at the fp8 rate)"
+                    if ratio != 1.0 else ""),
                 "frac_of_sustained": round(achieved / t_sust, 4)}
     achieved = w.algorithmic_bytes / (launch_ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
@@ -533,7 +535,8 @@ def measure_configs(args, tp, dev, stream, scrub, peaks, src) -> dict:
     for name, modes in (("gemm_4096_f16", ("warm",)),
                         ("skinny_144x16392x4104_f16_beta1", ("cold", "cold_alone", "warm")),
                         ("gemm_8192_e4m3_transB_beta1", ("warm",)),
-                        ("mx_8192_e4m3_transB_beta1", ("warm",))):
+                        ("mx_8192_e4m3_transB_beta1", ("warm",)),
+                        ("mxfp4_8192_transB_beta1", ("warm",))):
         w = wl.BY_NAME[name]
         pr = Problem(tp, w, dev, stream)
         for _ in range(5):
@@ -671,7 +674,8 @@ def finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
-            {wl.F16: "f16", wl.BF16: "bf16", wl.E4M3: "e4m3", wl.E5M2: "e5m2"}[w.dtype],
+            {wl.F16: "f16", wl.BF16: "bf16", wl.E4M3: "e4m3", wl.E5M2: "e5m2",
+             wl.E2M1: "e2m1"}[w.dtype],
         "data": "synthetic (seeded, workloads.py)",
         "config": {**w.describe(), "l2": "flushed before every step (512 MB write + read)" if
                    args.flush_l2 else ("inputs larger than L2, no flush" if

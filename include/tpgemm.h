@@ -42,17 +42,21 @@
 extern "C" {
 #endif
 
-/* Element type of A and B (both the same). The fp8 types run on the tcgen05
- * kernel only (tcgen05.mma kind::f8f6f4, the fp8 gemm_async the pages mention
- * beside the f16 one) with A stored [M,K] (transA = 0) and B stored [N,K]
- * (transB = 1), both K-contiguous, and K % 16 == 0; other orientations return
- * TPGEMM_ERR_PATH. There is no per-block scale: D = A.B + beta.C exactly as for
- * f16, with the fp8 values as they are. */
+/* Element type of A and B (both the same). The fp8 and fp4 types run on the
+ * tcgen05 kernel only (tcgen05.mma kind::f8f6f4, the fp8 / fp4 gemm_async the
+ * pages mention beside the f16 one) with A stored [M,K] (transA = 0) and B
+ * stored [N,K] (transB = 1), both K-contiguous, and K % 16 == 0 (fp4: K % 128
+ * == 0); other orientations return TPGEMM_ERR_PATH. tpgemm_gemm applies no
+ * per-block scale: D = A.B + beta.C exactly as for f16, with the narrow values
+ * as they are (tpgemm_gemm_mx is the block-scaled form). */
 typedef enum {
     TPGEMM_F16 = 0,  /* IEEE binary16 */
     TPGEMM_BF16 = 1, /* bfloat16 */
     TPGEMM_E4M3 = 2, /* fp8 e4m3 (1 sign, 4 exponent bits, bias 7, 3 mantissa bits; no inf) */
-    TPGEMM_E5M2 = 3  /* fp8 e5m2 (1 sign, 5 exponent bits, bias 15, 2 mantissa bits) */
+    TPGEMM_E5M2 = 3, /* fp8 e5m2 (1 sign, 5 exponent bits, bias 15, 2 mantissa bits) */
+    TPGEMM_E2M1 = 4  /* fp4 e2m1 (1 sign, 2 exponent bits, bias 1, 1 mantissa bit; no inf or
+                        NaN), stored packed: element 2i in the low 4 bits of byte i and 2i + 1
+                        in the high 4 bits along K; A and B 32-byte aligned, K % 128 == 0 */
 } tpgemm_dtype;
 
 typedef enum {

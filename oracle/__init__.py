@@ -80,6 +80,8 @@ def _load():
         lib.oracle_gemm_entries.restype = ci
         lib.oracle_gemm_rows.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, ci, ci, ci, ci]
         lib.oracle_gemm_rows.restype = ci
+        lib.oracle_decode_e2m1.argtypes = [ctypes.c_uint16]
+        lib.oracle_decode_e2m1.restype = ctypes.c_double
         lib.oracle_decode_e8m0.argtypes = [ctypes.c_uint8]
         lib.oracle_decode_e8m0.restype = ctypes.c_double
         lib.oracle_gemm_mx.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, ci, ci, ci, ci, i64]

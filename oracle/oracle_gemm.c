@@ -30,6 +30,10 @@
  * Alongside D it can return S[i,j] = sum_k |a(i,k) * b(k,j)| in double, the
  * scale of the elementwise acceptance bound |D - D_ref| <= 2^-10 * S + 1e-6.
  *
+ * fp4 e2m1 (dtype 4) follows the same rules as fp8: patterns widened to 16
+ * bits, one element per entry (the callers unpack the two 4-bit codes of each
+ * stored byte).
+ *
  * Block-scaled fp8 (oracle_gemm_mx): the same page lists block scaling (SFA,
  * SFB) among the operand forms of gemm_async (section 七) without defining
  * it. The reading taken is the OCP Microscaling (MX) one: every run of
@@ -54,6 +58,7 @@
 #define ORACLE_BF16 1
 #define ORACLE_E4M3 2
 #define ORACLE_E5M2 3
+#define ORACLE_E2M1 4
 
 /* IEEE-754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
  * Exponent field 0 encodes zero and subnormals (fraction * 2^-24); 31 encodes
@@ -128,8 +133,21 @@ double oracle_decode_e5m2(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* fp4 e2m1 (OCP Microscaling): 1 sign bit, 2 exponent bits (bias 1), 1
+ * fraction bit, in the low 4 bits. Exponent 0 encodes zero and the subnormal
+ * 0.5; there is no infinity and no NaN: the magnitudes are 0, 0.5, 1, 1.5, 2,
+ * 3, 4 and 6. */
+double oracle_decode_e2m1(uint16_t h) {
+    int sign = (h >> 3) & 1;
+    int e = (h >> 1) & 0x3;
+    int m = h & 0x1;
+    double v = (e == 0) ? ldexp((double)m, -1) : ldexp((double)(2 + m), e - 2);
+    return sign ? -v : v;
+}
+
 static double decode(uint16_t h, int dtype) {
     switch (dtype) {
+        case ORACLE_E2M1: return oracle_decode_e2m1(h);
         case ORACLE_BF16: return oracle_decode_bf16(h);
         case ORACLE_E4M3: return oracle_decode_e4m3(h);
         case ORACLE_E5M2: return oracle_decode_e5m2(h);
@@ -164,7 +182,7 @@ int oracle_num_threads(void) {
 int oracle_gemm(float* D, double* sumabs, const uint16_t* A, const uint16_t* B, const float* C,
                 int64_t M, int64_t N, int64_t K, int transA, int transB, int dtype, int beta) {
     if (M <= 0 || N <= 0 || K <= 0 || !D || !A || !B || (beta && !C)) return -2;
-    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2) return -2;
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E2M1) return -2;
     /* Decode once into the normalised orientation: a[i*K+k] = a(i,k) and
      * bt[j*K+k] = b(k,j), so the sum over k walks both rows contiguously. */
     double* a = (double*)malloc(sizeof(double) * (size_t)(M * K));
@@ -210,7 +228,7 @@ int oracle_gemm_entries(float* D_out, double* sumabs_out, const int64_t* rows, c
                         int64_t M, int64_t N, int64_t K, int transA, int transB, int dtype,
                         int beta) {
     if (M <= 0 || N <= 0 || K <= 0 || !D_out || !A || !B || (beta && !C) || count < 0) return -2;
-    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2) return -2;
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E2M1) return -2;
     for (int64_t t = 0; t < count; ++t)
         if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -2;
 #pragma omp parallel for schedule(dynamic, 4)
@@ -238,7 +256,7 @@ int oracle_gemm_rows(float* D_rows, const uint16_t* A, const uint16_t* B, const 
                      int transA, int transB, int dtype, int beta) {
     if (M <= 0 || N <= 0 || K <= 0 || !D_rows || !A || !B || (beta && !C)) return -2;
     if (row_begin < 0 || row_end > M || row_begin >= row_end) return -2;
-    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2) return -2;
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E2M1) return -2;
     int64_t R = row_end - row_begin;
     double* a = (double*)malloc(sizeof(double) * (size_t)(R * K));
     double* bt = (double*)malloc(sizeof(double) * (size_t)(N * K));
@@ -285,7 +303,7 @@ int oracle_gemm_mx(float* D, double* sumabs, const uint16_t* A, const uint16_t* 
     if (M <= 0 || N <= 0 || K <= 0 || block <= 0 || !D || !A || !B || !SFA || !SFB ||
         (beta && !C))
         return -2;
-    if (dtype != ORACLE_E4M3 && dtype != ORACLE_E5M2) return -2;
+    if (dtype != ORACLE_E4M3 && dtype != ORACLE_E5M2 && dtype != ORACLE_E2M1) return -2;
     const int64_t KB = (K + block - 1) / block;
     double* a = (double*)malloc(sizeof(double) * (size_t)(M * K));
     double* bt = (double*)malloc(sizeof(double) * (size_t)(N * K));

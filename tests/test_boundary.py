@@ -66,10 +66,10 @@ def test_rejects_shape(lib, M, N, K, frag):
     assert frag in why
 
 
-@pytest.mark.parametrize("dtype", [4, 5, -1, 7])
+@pytest.mark.parametrize("dtype", [5, 6, -1, 7])
 def test_rejects_dtype(lib, dtype):
     # f16 accumulators, tf32, int8 and mixed types have no enumerator: any
-    # code other than F16 / BF16 / E4M3 / E5M2 is refused.
+    # code other than F16 / BF16 / E4M3 / E5M2 / E2M1 is refused.
     st, why = call(dtype=dtype)
     assert st == tp.TPGEMM_ERR_DTYPE and "dtype" in why
 
@@ -281,3 +281,17 @@ def test_mx_rejections(lib, kw, status, frag):
     st, why = call_mx(**kw)
     assert st == status, why
     assert frag in why
+
+
+
+def test_fp4_boundary_rules(lib):
+    # fp4: K a multiple of 128 (unpacked by the TMA 128 elements at a time),
+    # A and B 32-byte aligned, no host-buffer path.
+    st, why = call(M=256, N=256, K=192, tA=0, tB=1, dtype=tp.TPGEMM_E2M1, beta=0.0)
+    assert st == tp.TPGEMM_ERR_SHAPE and "multiple of 128" in why
+    st, why = call(M=256, N=256, K=256, A=BASE + 64 * MB + 16, tA=0, tB=1, dtype=tp.TPGEMM_E2M1,
+                   beta=0.0)
+    assert st == tp.TPGEMM_ERR_ALIGN and "32-byte" in why
+    st, why = call_mx(K=192, dtype=tp.TPGEMM_E2M1)
+    assert st == tp.TPGEMM_ERR_SHAPE and "multiple of 128" in why
+    assert tp.tpgemm_gemm_host_workspace_bytes(256, 256, 256, tp.TPGEMM_E2M1, 0.0) == 0

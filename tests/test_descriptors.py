@@ -75,6 +75,8 @@ IDESC_CASES = [
      "f16 MN/MN 128x16: 1 << 4, 1 << 15, 1 << 16, 2 << 17, 8 << 24"),
     (tp.TPGEMM_E4M3, 0, 0, 256, 256, 0x10400010,
      "e4m3 K/K 256x256: 1 << 4, 32 << 17, 16 << 24"),
+    (tp.TPGEMM_E2M1, 0, 0, 128, 128, 0x08201690,
+     "e2m1 K/K 128x128: 1 << 4, 5 << 7, 5 << 10, 16 << 17, 8 << 24"),
 ]
 
 
@@ -127,6 +129,8 @@ IDESC_MX_CASES = [
      "e5m2 128x144 ids 3/2: 2 << 4, 1 << 7, 1 << 10, 18 << 17, 1 << 23, 8 << 24, 3 << 29"),
     (tp.TPGEMM_E4M3, 128, 16, 1, 1, 0x28840010,
      "e4m3 128x16 ids 1/1: 1 << 4, 2 << 17, 1 << 23, 8 << 24, 1 << 29"),
+    (tp.TPGEMM_E2M1, 256, 192, 0, 0, 0x10B01680,
+     "e2m1 256x192 ids 0/0: 5 << 7, 5 << 10, 24 << 17, 1 << 23, 16 << 24"),
 ]
 
 

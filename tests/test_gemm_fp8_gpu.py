@@ -139,3 +139,28 @@ def test_fp8_workload_full_size(name):
                                          (16, 8, 16, wl.E4M3), (2048, 2056, 16, wl.E5M2)])
 def test_fp8_extreme_shapes(M, N, K, dtype):
     check(case(M, N, K, dtype, 1.0, seed=M + N + K))
+
+
+
+# fp4 e2m1 without block scales (kind::f8f6f4, format 5): A [M, K/2] and B
+# [N, K/2] packed two codes per byte, unpacked by the TMA into the 16-byte
+# padded groups the MMA reads.
+@pytest.mark.parametrize("M,N,K,beta", [(128, 128, 128, 0.0), (784, 1320, 512, 1.0),
+                                        (144, 4104, 1024, 1.0), (2048, 2048, 2048, 0.0)])
+def test_fp4_plain(M, N, K, beta):
+    w = dataclasses.replace(wl.BY_NAME["mxfp4_4096_int_transB"], name=f"fp4_{M}x{N}x{K}",
+                            M=M, N=N, K=K, beta=beta,
+                            c_dist=("normal", 0.0, 1.0) if beta else None, seed=300 + M + K)
+    w = wl.Workload(**{f.name: getattr(w, f.name) for f in dataclasses.fields(wl.Workload)})
+    A, B, C = wl.make_inputs(w)
+    D = torch.empty(M, N, device="cuda")
+    st = tp.tpgemm_gemm(D, A.cuda(), B.cuda(), None if C is None else C.cuda(), M, N, K, 0, 1,
+                        wl.E2M1, beta)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    Dref, S = oracle.gemm(wl.operand_bits(w, A), wl.operand_bits(w, B),
+                          None if C is None else C.numpy(), M, N, K, False, True, wl.E2M1, beta)
+    # fp4 values are multiples of 1/2 up to 6: every partial sum below K = 4096
+    # is a multiple of 1/4 under 2^18, exact in float32
+    ok, msg = oracle.compare(D.cpu().numpy(), Dref, S, exact=C is None)
+    assert ok, msg

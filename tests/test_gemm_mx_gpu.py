@@ -68,9 +68,9 @@ def run_mx(w):
 def check(w):
     D, plan, (A, B, C, SFA, SFB) = run_mx(w)
     assert "kind=mxf8f6f4" in plan, plan
-    Dref, S = oracle.gemm_mx(wl.bits(A), wl.bits(B), None if C is None else C.numpy(),
-                             SFA.numpy(), SFB.numpy(), w.M, w.N, w.K, w.transA, w.transB,
-                             w.dtype, w.beta)
+    Dref, S = oracle.gemm_mx(wl.operand_bits(w, A), wl.operand_bits(w, B),
+                             None if C is None else C.numpy(), SFA.numpy(), SFB.numpy(), w.M, w.N,
+                             w.K, w.transA, w.transB, w.dtype, w.beta)
     ok, msg = oracle.compare(D, Dref, S, exact=w.integer_valued)
     assert ok, f"{w.name} [{plan}]: {msg}"
     return plan
@@ -152,9 +152,9 @@ def test_mx_back_to_back_calls_share_nothing():
         outs.append((w, D, keep, (A, B, C, SFA, SFB)))
     torch.cuda.synchronize()
     for w, D, _, (A, B, C, SFA, SFB) in outs:
-        Dref, S = oracle.gemm_mx(wl.bits(A), wl.bits(B), None if C is None else C.numpy(),
-                                 SFA.numpy(), SFB.numpy(), w.M, w.N, w.K, False, True, w.dtype,
-                                 w.beta)
+        Dref, S = oracle.gemm_mx(wl.operand_bits(w, A), wl.operand_bits(w, B),
+                                 None if C is None else C.numpy(), SFA.numpy(), SFB.numpy(), w.M,
+                                 w.N, w.K, False, True, w.dtype, w.beta)
         ok, msg = oracle.compare(D.cpu().numpy(), Dref, S)
         assert ok, msg
 
@@ -193,3 +193,28 @@ def test_mx_8192_plan_is_a_pair():
     A, B, C = wl.make_inputs(w.with_shape(512, 512, 256))
     plan = check(w.with_shape(512, 512, 256, seed=104))
     assert "pair=1" in plan, plan
+
+
+
+# ------------------------------------------------------------ fp4 (MXFP4)
+FP4 = ("codes", 0, 15)
+
+
+def test_mxfp4_one_tile_exact():
+    # One 128 x 128 tile, one 128-element stage; every fp4 value is a multiple
+    # of 1/2, so with scales in {1/2, 1, 2} the sums are exact.
+    check(case(128, 128, 128, wl.E2M1, 0.0, dist=FP4, sf=(126, 128), seed=201))
+
+
+@pytest.mark.parametrize("M,N,K,beta", [
+    (784, 1320, 512, 1.0),   # CTA pairs, 192-wide tiles
+    (144, 4104, 1024, 1.0),  # swapped small M
+    (128, 64, 384, 0.0),     # one P tile, single CTA
+    (1024, 1024, 4096, 0.0),
+])
+def test_mxfp4_shapes(M, N, K, beta):
+    check(case(M, N, K, wl.E2M1, beta, dist=FP4, sf=(120, 134), seed=210 + M + K))
+
+
+def test_mxfp4_integer_exact_large():
+    check(case(1024, 1536, 2048, wl.E2M1, 0.0, dist=FP4, sf=(126, 128), seed=220))

@@ -254,3 +254,54 @@ def test_planted_mx_mistake_is_caught(oracle_lib, mutant):
         if not ok:
             failures.append(pin.__name__)
     assert failures, f"{mutant.__name__} passed every pin"
+
+
+# ------------------------------------------------------------------- fp4 e2m1
+E2M1 = 4
+# The OCP Microscaling E2M1 table: codes 0..7 are +0, 0.5, 1, 1.5, 2, 3, 4, 6
+# and codes 8..15 the same magnitudes negative.
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decode_matches_the_ocp_table(oracle_lib):
+    codes = np.arange(16, dtype=np.uint16)
+    got = oracle_lib.decode(codes, E2M1)
+    want = np.array(E2M1_TABLE + [-v for v in E2M1_TABLE])
+    assert np.array_equal(got, want)
+    assert np.signbit(got[8]) and not np.signbit(got[0])
+
+
+def test_fp4_block_scaled_exact_rational(oracle_lib):
+    # Random codes and scales on ragged tiny shapes against exact fractions
+    # built from the table above.
+    rng = np.random.default_rng(11)
+    for (M, N, K, block, beta) in ((2, 3, 40, 32, 1.0), (3, 2, 70, 32, 0.0), (2, 2, 9, 4, 1.0)):
+        a = rng.integers(0, 16, (M, K)).astype(np.uint16)
+        b = rng.integers(0, 16, (N, K)).astype(np.uint16)  # stored [N, K]
+        kb = -(-K // block)
+        SFA = rng.integers(120, 135, (M, kb)).astype(np.uint8)
+        SFB = rng.integers(120, 135, (N, kb)).astype(np.uint8)
+        C = rng.standard_normal((M, N)).astype(np.float32)
+        D, _ = oracle_lib.gemm_mx(a, b, C if beta else None, SFA, SFB, M, N, K, False, True,
+                                  E2M1, beta, block)
+        val = lambda c: (-1 if c >= 8 else 1) * Fraction(E2M1_TABLE[c & 7])  # noqa: E731
+        for i in range(M):
+            for j in range(N):
+                s = Fraction(0)
+                for k in range(K):
+                    s += (val(int(a[i, k])) * Fraction(2) ** (int(SFA[i, k // block]) - 127) *
+                          val(int(b[j, k])) * Fraction(2) ** (int(SFB[j, k // block]) - 127))
+                if beta:
+                    s += Fraction(float(C[i, j]))
+                assert D[i, j] == f32_rne(s), (M, N, K, i, j)
+
+
+def test_fp4_pack_and_unpack_are_inverse():
+    import torch
+
+    import workloads as wl
+    codes = torch.randint(0, 16, (5, 12), generator=torch.Generator().manual_seed(3))
+    packed = wl.pack_fp4(codes)
+    assert packed.shape == (5, 6) and packed.dtype == torch.uint8
+    assert int(packed[0, 0]) == int(codes[0, 0]) | (int(codes[0, 1]) << 4)
+    assert torch.equal(wl.unpack_fp4(packed), codes)

@@ -25,6 +25,7 @@ TPGEMM_F16 = 0
 TPGEMM_BF16 = 1
 TPGEMM_E4M3 = 2
 TPGEMM_E5M2 = 3
+TPGEMM_E2M1 = 4  # fp4, packed two per byte (element 2i in the low nibble of byte i)
 # tpgemm_status
 TPGEMM_OK = 0
 TPGEMM_ERR_SHAPE = 1
@@ -396,25 +397,30 @@ def dtype_code(torch_dtype) -> int:
                     f"got {torch_dtype}")
 
 
-def gemm_mx(A, B, SFA, SFB, C=None, *, beta=None, out=None, workspace=None, stream=None):
-    """Block-scaled fp8 D = (A.SA)(B.SB)^T + beta.C on CUDA tensors.
+def gemm_mx(A, B, SFA, SFB, C=None, *, beta=None, out=None, workspace=None, stream=None,
+            dtype=None):
+    """Block-scaled fp8 / fp4 D = (A.SA)(B.SB)^T + beta.C on CUDA tensors.
 
-    A is fp8 [M, K], B fp8 [N, K] (same dtype), SFA uint8 [M, ceil(K/32)] and
-    SFB uint8 [N, ceil(K/32)] E8M0 scales, C float32 [M, N]. The scale-packing
-    workspace is allocated here with torch unless given."""
+    A is fp8 [M, K], B fp8 [N, K] (same dtype), or both fp4 as uint8 [M, K/2]
+    and [N, K/2] (two codes per byte) with dtype=TPGEMM_E2M1; SFA uint8
+    [M, ceil(K/32)] and SFB uint8 [N, ceil(K/32)] E8M0 scales, C float32 [M, N].
+    The scale-packing workspace is allocated here with torch unless given."""
     import torch
     if beta is None:
         beta = 0.0 if C is None else 1.0
     M, K = A.shape
     N = B.shape[0]
-    if B.shape[1] != K or A.dtype != B.dtype:
-        raise ValueError("A must be [M, K] and B [N, K] of the same fp8 dtype")
+    if dtype == TPGEMM_E2M1:
+        K *= 2
+    code = dtype if dtype is not None else dtype_code(A.dtype)
+    if B.shape[1] != A.shape[1] or A.dtype != B.dtype:
+        raise ValueError("A must be [M, K] and B [N, K] of the same fp8 / fp4 dtype")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     wsb = tpgemm_gemm_mx_workspace_bytes(M, N, K)
     if workspace is None:
         workspace = torch.empty(wsb, dtype=torch.uint8, device=A.device)
-    check(tpgemm_gemm_mx(out, A, B, C, SFA, SFB, M, N, K, dtype_code(A.dtype), beta, workspace,
+    check(tpgemm_gemm_mx(out, A, B, C, SFA, SFB, M, N, K, code, beta, workspace,
                          workspace.numel() * workspace.element_size(), stream))
     return out
 

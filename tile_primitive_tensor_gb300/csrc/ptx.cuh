@@ -535,9 +535,9 @@ __host__ __device__ constexpr uint64_t smem_desc_with_addr(uint64_t tmpl, uint32
 // 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3, 1 = e5m2), 15 / 16 A / B
 // major-ness (0 = K-major, 1 = MN-major), 17-22 N >> 3, 24-28 M >> 4. Dense,
 // no negation, no saturation.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(bool bf16, bool a_mn_major, bool b_mn_major,
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t fmt, bool a_mn_major, bool b_mn_major,
                                                      int m, int n) {
-    return (1u << 4) | (uint32_t(bf16) << 7) | (uint32_t(bf16) << 10) |
+    return (1u << 4) | ((fmt & 7u) << 7) | ((fmt & 7u) << 10) |
            (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
            (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
@@ -545,12 +545,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(bool bf16, bool a_mn_major,
 // Instruction descriptor for the block-scaled kind::mxf8f6f4 (the PTX ISA's
 // instruction-descriptor table for the block-scaled kinds; the accumulator is
 // always f32): bits 4-5 B scale-factor ID, 7-9 A format and 10-12 B format
-// (0 = e4m3, 1 = e5m2), 15 / 16 A / B major-ness (0 = K-major), 17-22 N >> 3,
+// (0 = e4m3, 1 = e5m2, 5 = e2m1), 15 / 16 A / B major-ness (0 = K-major), 17-22 N >> 3,
 // 23 scale type (1 = E8M0), 24-28 M >> 4, 29-30 A scale-factor ID. Dense, no
 // negation. A scale-factor ID selects the byte of each 32-bit scale cell.
-__host__ __device__ constexpr uint32_t idesc_mx_f32(bool e5m2, int m, int n, uint32_t a_sf_id,
+__host__ __device__ constexpr uint32_t idesc_mx_f32(uint32_t fmt, int m, int n, uint32_t a_sf_id,
                                                     uint32_t b_sf_id) {
-    return ((b_sf_id & 3u) << 4) | (uint32_t(e5m2) << 7) | (uint32_t(e5m2) << 10) |
+    return ((b_sf_id & 3u) << 4) | ((fmt & 7u) << 7) | ((fmt & 7u) << 10) |
            (uint32_t(n >> 3) << 17) | (1u << 23) | (uint32_t(m >> 4) << 24) |
            ((a_sf_id & 3u) << 29);
 }

@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const CUtensorMap* mq = u.width == p.bn ? &mapQ : &mapQt;
                 const uint32_t tx = p.p_tx +
                                     (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
-                                            : uint32_t(q_rows) * 128u) +
+                                            : uint32_t(q_rows) * p.row_tx) +
                                     (MX ? 512u * uint32_t(1 + p.sf_q_chunks) : 0u);
                 const int nk = u.kb1 - u.kb0;
                 int kb = nk == p.k_blocks ? first_k_block(u.T, p) : u.kb0;

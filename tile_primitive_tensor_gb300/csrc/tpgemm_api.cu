@@ -151,14 +151,23 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-bool is_fp8(tpgemm_dtype d) { return d == TPGEMM_E4M3 || d == TPGEMM_E5M2; }
+// The narrow types run as tcgen05.mma kind::f8f6f4 (or its block-scaled form).
+bool is_f8f6f4(tpgemm_dtype d) {
+    return d == TPGEMM_E4M3 || d == TPGEMM_E5M2 || d == TPGEMM_E2M1;
+}
 
-// Bytes of one element of A and B.
-int elem_bytes(tpgemm_dtype d) { return is_fp8(d) ? 1 : 2; }
+// Bits of one element of A and B (fp4 is stored two per byte).
+int elem_bits(tpgemm_dtype d) { return d == TPGEMM_E2M1 ? 4 : (is_f8f6f4(d) ? 8 : 16); }
+
+size_t operand_bytes(tpgemm_dtype d, int64_t elems) {
+    return size_t(elems) * size_t(elem_bits(d)) / 8;
+}
 
 // The format code the instruction descriptor carries for A and B: kind::f16
-// f16 = 0 / bf16 = 1; kind::f8f6f4 e4m3 = 0 / e5m2 = 1.
-bool format_code1(tpgemm_dtype d) { return d == TPGEMM_BF16 || d == TPGEMM_E5M2; }
+// f16 = 0 / bf16 = 1; kind::f8f6f4 e4m3 = 0 / e5m2 = 1 / e2m1 = 5.
+uint32_t format_code(tpgemm_dtype d) {
+    return d == TPGEMM_E2M1 ? 5u : ((d == TPGEMM_BF16 || d == TPGEMM_E5M2) ? 1u : 0u);
+}
 
 tpgemm_status check_shape(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype, float beta) {
     if (M <= 0 || N <= 0 || K <= 0)
@@ -178,12 +187,17 @@ tpgemm_status check_shape(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype, f
                     "M=%lld N=%lld K=%lld: an operand exceeds one GPU's memory (at most 2^36 "
                     "elements of C / D and 2^37 of A or B)",
                     (long long)M, (long long)N, (long long)K);
-    if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16 && !is_fp8(dtype))
+    if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16 && !is_f8f6f4(dtype))
         return fail(TPGEMM_ERR_DTYPE,
-                    "dtype %d is not TPGEMM_F16 (0), TPGEMM_BF16 (1), TPGEMM_E4M3 (2) or "
-                    "TPGEMM_E5M2 (3)",
+                    "dtype %d is not TPGEMM_F16 (0), TPGEMM_BF16 (1), TPGEMM_E4M3 (2), "
+                    "TPGEMM_E5M2 (3) or TPGEMM_E2M1 (4)",
                     int(dtype));
-    if (is_fp8(dtype) && K % 16)
+    if (dtype == TPGEMM_E2M1 && K % 128)
+        return fail(TPGEMM_ERR_SHAPE,
+                    "K=%lld is not a multiple of 128 (fp4 rows are loaded and unpacked 128 "
+                    "elements at a time)",
+                    (long long)K);
+    if (is_f8f6f4(dtype) && K % 16)
         return fail(TPGEMM_ERR_SHAPE,
                     "K=%lld is not a multiple of 16 (fp8 rows must be whole 16-byte units)",
                     (long long)K);
@@ -193,7 +207,7 @@ tpgemm_status check_shape(int64_t M, int64_t N, int64_t K, tpgemm_dtype dtype, f
 }
 
 tpgemm_status check_pointers(float* D, const void* A, const void* B, const float* C, int64_t M,
-                             int64_t N, int64_t K, float beta, int eb) {
+                             int64_t N, int64_t K, float beta, tpgemm_dtype dtype) {
     if (!D) return fail(TPGEMM_ERR_NULL, "D is NULL");
     if (!A) return fail(TPGEMM_ERR_NULL, "A is NULL");
     if (!B) return fail(TPGEMM_ERR_NULL, "B is NULL");
@@ -202,12 +216,18 @@ tpgemm_status check_pointers(float* D, const void* A, const void* B, const float
     if (misaligned(D)) return fail(TPGEMM_ERR_ALIGN, "D=%p is not 16-byte aligned", (void*)D);
     if (misaligned(A)) return fail(TPGEMM_ERR_ALIGN, "A=%p is not 16-byte aligned", A);
     if (misaligned(B)) return fail(TPGEMM_ERR_ALIGN, "B=%p is not 16-byte aligned", B);
+    // The TMA unpacks fp4 from 32-byte aligned rows.
+    auto misaligned32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) != 0; };
+    if (dtype == TPGEMM_E2M1 && misaligned32(A))
+        return fail(TPGEMM_ERR_ALIGN, "A=%p is not 32-byte aligned (fp4)", A);
+    if (dtype == TPGEMM_E2M1 && misaligned32(B))
+        return fail(TPGEMM_ERR_ALIGN, "B=%p is not 32-byte aligned (fp4)", B);
     if (beta == 1.0f && misaligned(C))
         return fail(TPGEMM_ERR_ALIGN, "C=%p is not 16-byte aligned", (const void*)C);
     const size_t dn = size_t(M) * size_t(N) * 4;
-    if (overlaps(D, dn, A, size_t(M) * size_t(K) * size_t(eb)))
+    if (overlaps(D, dn, A, operand_bytes(dtype, M * K)))
         return fail(TPGEMM_ERR_ALIAS, "D overlaps A");
-    if (overlaps(D, dn, B, size_t(K) * size_t(N) * size_t(eb)))
+    if (overlaps(D, dn, B, operand_bytes(dtype, K * N)))
         return fail(TPGEMM_ERR_ALIAS, "D overlaps B");
     if (beta == 1.0f && static_cast<const void*>(C) != static_cast<const void*>(D) &&
         overlaps(D, dn, C, dn))
@@ -270,7 +290,7 @@ int pick_bn(int64_t M, int64_t N, int sms, bool pair) {
 
 tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
                       tpgemm_dtype dtype, float beta, int sms, Plan* out, bool mx = false) {
-    const bool fp8 = is_fp8(dtype);
+    const bool fp8 = is_f8f6f4(dtype);
     tpg::TcParams p{};
     // Small M: swap operands so N runs along the 128 tensor-memory lanes and
     // all of M fits one accumulator (UMMA N = M <= 256, a multiple of 16).
@@ -334,8 +354,8 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     p.pair = pair_ok ? 1 : 0;
     if (tuning().pair >= 0) p.pair = (tuning().pair != 0 && pair_ok) ? 1 : 0;
     const int q_rows = p.pair ? bn / 2 : bn;  // Q rows this CTA loads per stage
-    p.idesc = mx ? tpg::idesc_mx_f32(format_code1(dtype), p.pair ? 256 : 128, bn, 0, 0)
-                 : tpg::idesc_f16_f32(format_code1(dtype), p_mn, q_mn, p.pair ? 256 : 128, bn);
+    p.idesc = mx ? tpg::idesc_mx_f32(format_code(dtype), p.pair ? 256 : 128, bn, 0, 0)
+                 : tpg::idesc_f16_f32(format_code(dtype), p_mn, q_mn, p.pair ? 256 : 128, bn);
     p.mx = mx ? 1 : 0;
     if (mx) {
         // Scale slots: one per ring stage, in each accumulator half's columns
@@ -349,7 +369,8 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         if (p.sf_spr < 1) return fail(TPGEMM_ERR_PATH, "internal: no room for scale slots");
     }
     p.p_bytes = stage_tile_bytes(128, p_mn);
-    p.p_tx = 128u * 128u;
+    p.row_tx = dtype == TPGEMM_E2M1 ? 64u : 128u;
+    p.p_tx = 128u * p.row_tx;
     p.q_bytes = stage_tile_bytes(q_rows, q_mn);
     p.tx_bytes = p.p_bytes + p.q_bytes;
     p.timeout_ns = wait_timeout_ns();
@@ -573,7 +594,7 @@ void choose_p_rows(tpg::TcParams& p, int* grid, int max_grid, bool sk_requested)
     }
     if (bp == 128) return;
     p.bp = bp;
-    p.p_tx = uint32_t(bp) * 128u;
+    p.p_tx = uint32_t(bp) * p.row_tx;
     p.tx_bytes = p.p_tx + p.q_bytes;
     p.tiles_p = int((int64_t(p.Mp) + bp - 1) / bp);
     p.num_tiles = p.tiles_p * p.tiles_q;
@@ -721,7 +742,7 @@ tpgemm_status fit_grid(Plan* plan) {
 
 tpgemm_status make_plan(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
                         tpgemm_dtype dtype, float beta, tpgemm_path path, int sms, Plan* out) {
-    if (is_fp8(dtype)) {
+    if (is_f8f6f4(dtype)) {
         // fp8 runs on the tcgen05 kernel only (kind::f8f6f4).
         if (path == TPGEMM_PATH_MMA_SYNC)
             return fail(TPGEMM_ERR_PATH, "the mma.sync kernel takes f16 / bf16 only");
@@ -749,10 +770,10 @@ tpgemm_status make_plan(int64_t M, int64_t N, int64_t K, bool transA, bool trans
 
 // ---------------------------------------------------------- tensor maps
 tpgemm_status encode_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* base,
-                        CUtensorMapDataType type, int elem_bytes, uint64_t inner, uint64_t outer,
+                        CUtensorMapDataType type, int elem_bits, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer, const char* what) {
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * uint64_t(elem_bytes)};
+    cuuint64_t strides[1] = {inner * uint64_t(elem_bits) / 8};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -784,8 +805,13 @@ tpgemm_status encode_u32_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap
 
 // Map of a K x rows operand: K-contiguous -> dims {K, rows}, box {64, box_rows};
 // MN-contiguous -> dims {rows, K}, box {64, 64}.
+// fp4 is loaded with the TMA's 4-bit type that writes each 16-element group
+// (8 packed bytes) into 16 bytes of shared memory, the 8 bytes of padding the
+// kind::f8f6f4 MMA expects for 4-bit operands: a 128-element box fills one
+// 128-byte swizzle row, as 128 fp8 elements do.
 CUtensorMapDataType operand_type(tpgemm_dtype dtype) {
-    return is_fp8(dtype)          ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+    return dtype == TPGEMM_E2M1   ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
+           : is_f8f6f4(dtype)     ? CU_TENSOR_MAP_DATA_TYPE_UINT8
            : dtype == TPGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
@@ -798,12 +824,13 @@ tpgemm_status encode_operand(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap*
                              const void* base, tpgemm_dtype dtype, int64_t rows, int64_t K, bool mn,
                              int box_rows, const char* what, int mn_box = 0) {
     const CUtensorMapDataType t = operand_type(dtype);
-    const int eb = elem_bytes(dtype);
-    const uint32_t row_elems = uint32_t(128 / eb);  // one 128-byte swizzle row
+    const int bits = elem_bits(dtype);
+    // Elements of one 128-byte swizzle row of shared memory (fp4 unpacked).
+    const uint32_t row_elems = dtype == TPGEMM_E2M1 ? 128u : uint32_t(1024 / bits);
     if (mn)
-        return encode_2d(enc, map, base, t, eb, uint64_t(rows), uint64_t(K),
+        return encode_2d(enc, map, base, t, bits, uint64_t(rows), uint64_t(K),
                          mn_box > 0 ? uint32_t(mn_box) : row_elems, 64, what);
-    return encode_2d(enc, map, base, t, eb, uint64_t(K), uint64_t(rows), row_elems,
+    return encode_2d(enc, map, base, t, bits, uint64_t(K), uint64_t(rows), row_elems,
                      uint32_t(box_rows), what);
 }
 
@@ -818,7 +845,7 @@ tpgemm_status finish_tc_plan(Plan* plan, tpgemm_dtype dtype, SkMode sk_mode) {
     tpgemm_status s = fit_grid(plan);
     if (s != TPGEMM_OK) return s;
     choose_p_rows(plan->tc, &plan->grid, plan->max_grid, stream_k_requested(sk_mode));
-    apply_tail_split(plan->tc, &plan->grid, plan->max_grid, format_code1(dtype), sk_mode);
+    apply_tail_split(plan->tc, &plan->grid, plan->max_grid, format_code(dtype), sk_mode);
     choose_epi_groups(plan->tc, plan->grid);
     choose_producers(plan->tc, plan->grid);
     choose_l2_policies(plan->tc, plan->grid);
@@ -915,10 +942,10 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     g_detail.clear();
     tpgemm_status s = check_shape(M, N, K, dtype, beta);
     if (s != TPGEMM_OK) return s;
-    s = check_pointers(D, A, B, C, M, N, K, beta, elem_bytes(dtype));
+    s = check_pointers(D, A, B, C, M, N, K, beta, dtype);
     if (s != TPGEMM_OK) return s;
     if (mx) {
-        if (!is_fp8(dtype))
+        if (!is_f8f6f4(dtype))
             return fail(TPGEMM_ERR_DTYPE,
                         "block-scaled A and B must be TPGEMM_E4M3 or TPGEMM_E5M2 (dtype %d)",
                         int(dtype));
@@ -936,7 +963,7 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
             overlaps(D, dn, mx->SFB, size_t(N) * size_t(kb)))
             return fail(TPGEMM_ERR_ALIAS, "D overlaps a scale matrix");
         const void* ops[5] = {D, A, B, mx->SFA, mx->SFB};
-        const size_t lens[5] = {dn, size_t(M) * size_t(K), size_t(K) * size_t(N),
+        const size_t lens[5] = {dn, operand_bytes(dtype, M * K), operand_bytes(dtype, K * N),
                                 size_t(M) * size_t(kb), size_t(N) * size_t(kb)};
         for (int i = 0; i < 5; ++i)
             if (overlaps(mx->ws, need, ops[i], lens[i]))
@@ -1044,15 +1071,15 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
         const uint64_t bn32 = uint64_t(32 * ((p.bn + 31) / 32));
         const uint64_t cols = p.swap ? 128 : bn32;
         const uint64_t rows = uint64_t(plan.grid) * uint64_t(p.sk_slot_rows);
-        s = encode_2d(enc, &maps.W, p.sk_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, cols, rows, 32, 32,
+        s = encode_2d(enc, &maps.W, p.sk_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, cols, rows, 32, 32,
                       "stream-K scratch");
         if (s != TPGEMM_OK) return s;
     }
-    s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M), 32,
+    s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, uint64_t(N), uint64_t(M), 32,
                   32, "D");
     if (s != TPGEMM_OK) return s;
     if (p.beta) {
-        s = encode_2d(enc, &maps.C, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N), uint64_t(M),
+        s = encode_2d(enc, &maps.C, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, uint64_t(N), uint64_t(M),
                       32, 32, "C");
         if (s != TPGEMM_OK) return s;
     }
@@ -1062,11 +1089,11 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     maps.Ch = maps.C;
     if (p.bp % 32) {
         const uint32_t hx = plan.swap ? 16 : 32, hy = plan.swap ? 32 : 16;
-        s = encode_2d(enc, &maps.Dh, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N),
+        s = encode_2d(enc, &maps.Dh, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, uint64_t(N),
                       uint64_t(M), hx, hy, "D (half-quadrant box)");
         if (s != TPGEMM_OK) return s;
         if (p.beta) {
-            s = encode_2d(enc, &maps.Ch, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, uint64_t(N),
+            s = encode_2d(enc, &maps.Ch, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, uint64_t(N),
                           uint64_t(M), hx, hy, "C (half-quadrant box)");
             if (s != TPGEMM_OK) return s;
         }
@@ -1160,8 +1187,10 @@ tpgemm_status run_host(float* Dh, const void* Ah, const void* Bh, const float* C
     if (!ws) return fail(TPGEMM_ERR_NULL, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(ws) % kWsAlign)
         return fail(TPGEMM_ERR_ALIGN, "workspace is not 256-byte aligned");
+    if (dtype == TPGEMM_E2M1)
+        return fail(TPGEMM_ERR_DTYPE, "the host-buffer path takes f16, bf16 and fp8 operands");
     const bool use_c = beta == 1.0f;
-    const size_t eb = size_t(elem_bytes(dtype));
+    const size_t eb = size_t(elem_bits(dtype) / 8);
     const HostWsLayout L = host_ws_layout(M, N, K, use_c, int(eb));
     if (ws_bytes < L.total)
         return fail(TPGEMM_ERR_NULL, "workspace of %zu bytes; %zu needed", ws_bytes, L.total);
@@ -1270,7 +1299,8 @@ size_t tpgemm_gemm_host_workspace_bytes(int64_t M, int64_t N, int64_t K, tpgemm_
     const bool ok = check_shape(M, N, K, dtype, beta) == TPGEMM_OK;
     g_detail = keep;
     if (!ok) return 0;
-    return host_ws_layout(M, N, K, beta == 1.0f, elem_bytes(dtype)).total;
+    if (dtype == TPGEMM_E2M1) return 0;
+    return host_ws_layout(M, N, K, beta == 1.0f, elem_bits(dtype) / 8).total;
 }
 
 tpgemm_status tpgemm_gemm_host(float* D_host, const void* A_host, const void* B_host,
@@ -1388,7 +1418,7 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
         // As tpgemm_gemm plans it, except that the grid is one CTA (pair) per
         // SM without the device's cluster-occupancy query.
         choose_p_rows(plan.tc, &plan.grid, plan.max_grid, stream_k_requested(SkMode::Env));
-        apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code1(dtype));
+        apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code(dtype));
         choose_epi_groups(plan.tc, plan.grid);
         choose_producers(plan.tc, plan.grid);
         choose_l2_policies(plan.tc, plan.grid);
@@ -1424,13 +1454,13 @@ uint64_t tpgemm_encode_smem_desc(uint32_t start_addr, uint32_t lbo_bytes, uint32
 }
 
 uint32_t tpgemm_encode_idesc_mx(tpgemm_dtype dtype, int m, int n, int a_sf_id, int b_sf_id) {
-    if (!is_fp8(dtype)) return 0;
-    return tpg::idesc_mx_f32(format_code1(dtype), m, n, uint32_t(a_sf_id), uint32_t(b_sf_id));
+    if (!is_f8f6f4(dtype)) return 0;
+    return tpg::idesc_mx_f32(format_code(dtype), m, n, uint32_t(a_sf_id), uint32_t(b_sf_id));
 }
 
 uint32_t tpgemm_encode_idesc(tpgemm_dtype dtype, int a_mn_major, int b_mn_major, int m, int n) {
-    if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16 && !is_fp8(dtype)) return 0;
-    return tpg::idesc_f16_f32(format_code1(dtype), a_mn_major != 0, b_mn_major != 0, m, n);
+    if (dtype != TPGEMM_F16 && dtype != TPGEMM_BF16 && !is_f8f6f4(dtype)) return 0;
+    return tpg::idesc_f16_f32(format_code(dtype), a_mn_major != 0, b_mn_major != 0, m, n);
 }
 
 const char* tpgemm_version(void) { return "0.1.0"; }

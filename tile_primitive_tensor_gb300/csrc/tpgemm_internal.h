@@ -51,7 +51,10 @@ struct TcParams {
     // quadrant holding row bp - 16 (when bp % 32 == 16) stores through the
     // half-width C / D maps.
     int bp;
-    uint32_t p_tx;          // bytes the P boxes deliver per stage (bp rows of 128 bytes)
+    uint32_t p_tx;          // bytes the P boxes deliver per stage (bp rows of row_tx bytes)
+    uint32_t row_tx;        // bytes a K-contiguous box row counts on its mbarrier: 128
+                            // (one swizzle row), 64 for fp4 (the packed bytes read; the
+                            // TMA writes them as 128 bytes of shared memory)
     int num_tiles;
     int k_blocks;           // ceil(K / 64)
     int bn;                 // accumulator columns per tile = UMMA N (16..256, %16)

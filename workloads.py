@@ -28,13 +28,14 @@ F16 = 0
 BF16 = 1
 E4M3 = 2
 E5M2 = 3
+E2M1 = 4  # fp4: stored packed, two codes per byte (element 2i in the low nibble of byte i)
 _TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, E4M3: torch.float8_e4m3fn,
                 E5M2: torch.float8_e5m2}
-_DTYPE_NAME = {F16: "f16", BF16: "bf16", E4M3: "e4m3", E5M2: "e5m2"}
+_DTYPE_NAME = {F16: "f16", BF16: "bf16", E4M3: "e4m3", E5M2: "e5m2", E2M1: "e2m1"}
 
 
-def elem_bytes(dtype: int) -> int:
-    return 1 if dtype in (E4M3, E5M2) else 2
+def elem_bytes(dtype: int) -> float:
+    return {E4M3: 1, E5M2: 1, E2M1: 0.5}.get(dtype, 2)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -45,7 +46,7 @@ class Workload:
     M: int
     N: int
     K: int
-    dtype: int            # F16, BF16, E4M3 or E5M2
+    dtype: int            # F16, BF16, E4M3, E5M2 or E2M1
     a_dist: tuple         # ("int", lo, hi) | ("uniform", lo, hi) | ("normal", mean, std)
     b_dist: tuple
     c_dist: Optional[tuple]  # None when beta == 0
@@ -62,7 +63,7 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """Each operand read once, D written once; C only when beta = 1."""
         e = elem_bytes(self.dtype)
-        b = e * (self.M * self.K + self.K * self.N) + 4 * self.M * self.N
+        b = int(e * (self.M * self.K + self.K * self.N)) + 4 * self.M * self.N
         if self.beta != 0.0:
             b += 4 * self.M * self.N
         return b
@@ -139,10 +140,13 @@ class MxWorkload(Workload):
 
     @property
     def integer_valued(self) -> bool:
-        # integer operands and scales within [126, 128] keep every partial sum
-        # a multiple of 1/4 below 2^22: exact in float32
+        # integer operands (fp8) or any fp4 codes (multiples of 1/2 up to 6),
+        # with scales within [126, 128] and K <= 4096, keep every partial sum a
+        # multiple of 1/16 below 2^20: exact in float32
         lo, hi = self.sf_dist
-        return super().integer_valued and lo >= 126 and hi <= 128
+        ops = self.dtype == E2M1 and self.K <= 4096 or super().integer_valued
+        return ops and lo >= 126 and hi <= 128 and (self.c_dist is None or
+                                                    self.c_dist[0] == "int")
 
     def describe(self) -> dict:
         return {**super().describe(), "block_scale": f"E8M0 per {MX_BLOCK} K",
@@ -163,6 +167,16 @@ MX_WORKLOADS = [
                True, 1054),
 ]
 
+# Block-scaled fp4 (MXFP4): every E2M1 code equally likely. Values are
+# multiples of 1/2 up to 6, so with scales in [1/2, 2] every partial sum below
+# K = 4096 is a multiple of 1/16 under 2^20: exact in float32.
+MX_WORKLOADS += [
+    MxWorkload("mxfp4_8192_transB_beta1", 8192, 8192, 8192, E2M1, ("codes", 0, 15),
+               ("codes", 0, 15), ("normal", 0.0, 1.0), 1.0, False, True, 1060),
+    MxWorkload("mxfp4_4096_int_transB", 4096, 4096, 4096, E2M1, ("codes", 0, 15),
+               ("codes", 0, 15), None, 0.0, False, True, 1061, sf_dist=(126, 128)),
+]
+
 BY_NAME = {w.name: w for w in WORKLOADS + [WORKLOAD_4096_INT] + FP8_WORKLOADS + MX_WORKLOADS}
 
 
@@ -177,7 +191,23 @@ def _draw(shape, dist, gen: torch.Generator) -> torch.Tensor:
     if kind == "normal":
         mean, std = dist[1], dist[2]
         return torch.randn(shape, generator=gen, dtype=torch.float32) * std + mean
+    if kind == "codes":  # fp4: 4-bit codes drawn uniformly from [lo, hi]
+        lo, hi = dist[1], dist[2]
+        return torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int32)
     raise ValueError(f"unknown distribution {dist!r}")
+
+
+def pack_fp4(codes: torch.Tensor) -> torch.Tensor:
+    """Two 4-bit codes per byte along the last dimension: element 2i in the low
+    nibble of byte i, element 2i + 1 in the high nibble."""
+    c = codes.to(torch.uint8) & 0xF
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).contiguous()
+
+
+def unpack_fp4(packed: torch.Tensor) -> torch.Tensor:
+    p = packed.to(torch.int32)
+    out = torch.stack([p & 0xF, (p >> 4) & 0xF], dim=-1)
+    return out.reshape(*packed.shape[:-1], packed.shape[-1] * 2)
 
 
 def stored_shapes(w: Workload):
@@ -195,9 +225,13 @@ def make_inputs(w: Workload, c_fill: Optional[float] = None):
     """
     gen = torch.Generator("cpu").manual_seed(w.seed)
     sa, sb, sc = stored_shapes(w)
-    td = _TORCH_DTYPE[w.dtype]
-    A = _draw(sa, w.a_dist, gen).to(td)
-    B = _draw(sb, w.b_dist, gen).to(td)
+    if w.dtype == E2M1:
+        A = pack_fp4(_draw(sa, w.a_dist, gen))
+        B = pack_fp4(_draw(sb, w.b_dist, gen))
+    else:
+        td = _TORCH_DTYPE[w.dtype]
+        A = _draw(sa, w.a_dist, gen).to(td)
+        B = _draw(sb, w.b_dist, gen).to(td)
     C = None
     if w.c_dist is not None:
         C = _draw(sc, w.c_dist, gen)
@@ -224,6 +258,14 @@ def bits(t: torch.Tensor):
         return t.contiguous().view(torch.uint8).numpy().astype("uint16")
     assert t.dtype in (torch.float16, torch.bfloat16)
     return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def operand_bits(w: Workload, t: torch.Tensor):
+    """The element codes of an operand of workload w as numpy uint16, one per
+    element (fp4 unpacked from its two-per-byte storage)."""
+    if w.dtype == E2M1:
+        return unpack_fp4(t).numpy().astype("uint16")
+    return bits(t)
 
 
 def torch_dtype(dtype: int):
