@@ -70,7 +70,9 @@ typedef enum {
     TPGEMM_ERR_ARCH = 7,    /* current device is not compute capability 10.3 (sm_103) */
     TPGEMM_ERR_LAUNCH = 8,  /* a CUDA call failed while enqueueing (detail has the CUDA error) */
     TPGEMM_ERR_TIMEOUT = 9, /* a kernel's bounded wait expired (see tpgemm_last_device_error) */
-    TPGEMM_ERR_PATH = 10    /* the forced kernel path cannot run this problem */
+    TPGEMM_ERR_PATH = 10,   /* the forced kernel path cannot run this problem */
+    TPGEMM_ERR_BOUNDS = 11  /* (debug builds, libtpgemm_debug.so) a device-side bounds check
+                               failed; the access was skipped (see tpgemm_last_device_error) */
 } tpgemm_status;
 
 /* Kernel path selection, for tests and measurement. AUTO is the default plan. */
@@ -476,8 +478,12 @@ const char* tpgemm_status_string(tpgemm_status s);
 const char* tpgemm_last_error_detail(void);
 
 /* Device-side status of the kernels launched so far on the current device:
- * TPGEMM_ERR_TIMEOUT if any bounded wait inside a kernel expired, else
- * TPGEMM_OK. Synchronises the device first. Reading it resets it to OK. */
+ * TPGEMM_ERR_TIMEOUT if any bounded wait inside a kernel expired, in a debug
+ * build (TPGEMM_DEBUG, libtpgemm_debug.so) TPGEMM_ERR_BOUNDS if a device-side
+ * bounds check on a computed tensor-memory column, TMA coordinate or stream-K
+ * flag index failed (the detail names the site; the access was skipped, the
+ * result is undefined), else TPGEMM_OK. Synchronises the device first.
+ * Reading it resets it to OK. */
 tpgemm_status tpgemm_last_device_error(void);
 
 /* The plan tpgemm_gemm would use for this problem, written as text into buf

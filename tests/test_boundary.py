@@ -47,7 +47,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_status_strings(lib):
-    for s in range(0, 11):
+    for s in range(0, 12):
         assert tp.tpgemm_status_string(s) not in ("", "unknown status")
     assert tp.tpgemm_status_string(99) == "unknown status"
     assert tp.tpgemm_version().count(".") == 2
@@ -295,3 +295,16 @@ def test_fp4_boundary_rules(lib):
     st, why = call_mx(K=192, dtype=tp.TPGEMM_E2M1)
     assert st == tp.TPGEMM_ERR_SHAPE and "multiple of 128" in why
     assert tp.tpgemm_gemm_host_workspace_bytes(256, 256, 256, tp.TPGEMM_E2M1, 0.0) == 0
+
+
+
+def test_debug_build_compiles_and_exports_the_same_abi():
+    # The TPGEMM_DEBUG build (device-side bounds checks) is a second library
+    # with the same C ABI; it builds here (nvcc cross-compiles) and loads
+    # without a GPU.
+    path = tpbuild.build(debug=True)
+    assert path.endswith("libtpgemm_debug.so")
+    dbg = tp.debug_library()
+    assert dbg.tpgemm_version().decode().endswith("-debug")
+    for n in tp.header_functions():
+        assert hasattr(dbg, n), n

@@ -18,6 +18,8 @@ import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libtpgemm.so")
+# Debug build (device-side bounds checks; built on request by build(debug=True)).
+LIB_PATH_DEBUG = os.path.join(_HERE, "_lib", "libtpgemm_debug.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "tpgemm.h")
 
 # tpgemm_dtype
@@ -38,6 +40,7 @@ TPGEMM_ERR_ARCH = 7
 TPGEMM_ERR_LAUNCH = 8
 TPGEMM_ERR_TIMEOUT = 9
 TPGEMM_ERR_PATH = 10
+TPGEMM_ERR_BOUNDS = 11
 # tpgemm_path
 TPGEMM_PATH_AUTO = 0
 TPGEMM_PATH_TCGEN05 = 1
@@ -88,77 +91,94 @@ _lib = None
 _lock = threading.Lock()
 
 
+def _open(path):
+    """A ctypes handle of a libtpgemm build with every declared signature set."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is not built; run tile_primitive_tensor_gb300.build.build() "
+            "(nvcc for sm_103a). There is no CPU fallback.")
+    lib = ctypes.CDLL(path)
+    vp, i64, ci, cf = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    gemm_args = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, cf, vp]
+    lib.tpgemm_gemm.argtypes = gemm_args
+    lib.tpgemm_gemm.restype = ci
+    lib.tpgemm_gemm_path.argtypes = gemm_args + [ci]
+    lib.tpgemm_gemm_path.restype = ci
+    lib.tpgemm_gemm_noalloc.argtypes = gemm_args
+    lib.tpgemm_gemm_noalloc.restype = ci
+    lib.tpgemm_test_gemm_withhold_fill.argtypes = gemm_args
+    lib.tpgemm_test_gemm_withhold_fill.restype = ci
+    lib.tpgemm_reload_tuning.argtypes = []
+    lib.tpgemm_reload_tuning.restype = None
+    lib.tpgemm_gemm_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, cf, vp,
+                                     ctypes.c_size_t, vp]
+    lib.tpgemm_gemm_host.restype = ci
+    lib.tpgemm_gemm_host_workspace_bytes.argtypes = [i64, i64, i64, ci, cf]
+    lib.tpgemm_gemm_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.tpgemm_status_string.argtypes = [ci]
+    lib.tpgemm_status_string.restype = ctypes.c_char_p
+    lib.tpgemm_last_error_detail.argtypes = []
+    lib.tpgemm_last_error_detail.restype = ctypes.c_char_p
+    lib.tpgemm_last_device_error.argtypes = []
+    lib.tpgemm_last_device_error.restype = ci
+    lib.tpgemm_describe_plan.argtypes = [i64, i64, i64, ci, ci, ci, cf, ci, ctypes.c_char_p, ci]
+    lib.tpgemm_describe_plan.restype = ci
+    lib.tpgemm_last_plan.argtypes = [ctypes.c_char_p, ci]
+    lib.tpgemm_last_plan.restype = ci
+    u32 = ctypes.c_uint32
+    lib.tpgemm_encode_smem_desc.argtypes = [u32, u32, u32, ci]
+    lib.tpgemm_encode_smem_desc.restype = ctypes.c_uint64
+    lib.tpgemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
+    lib.tpgemm_encode_idesc.restype = u32
+    lib.tpgemm_encode_idesc_mx.argtypes = [ci, ci, ci, ci, ci]
+    lib.tpgemm_encode_idesc_mx.restype = u32
+    sz = ctypes.c_size_t
+    lib.tpgemm_gemm_mx.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, cf, vp, sz, vp]
+    lib.tpgemm_gemm_mx.restype = ci
+    lib.tpgemm_gemm_mx_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.tpgemm_gemm_mx_workspace_bytes.restype = sz
+    lib.tpgemm_version.argtypes = []
+    lib.tpgemm_version.restype = ctypes.c_char_p
+    lib.tpgemm_cp_parse_shape.argtypes = [ctypes.c_char_p, ctypes.POINTER(ci)]
+    lib.tpgemm_cp_parse_shape.restype = ci
+    lib.tpgemm_cp_plan.argtypes = [ctypes.POINTER(CpDesc), ctypes.c_char_p, ci]
+    lib.tpgemm_cp_plan.restype = ci
+    lib.tpgemm_cp_roundtrip.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
+                                        ctypes.c_uint32, ci, vp]
+    lib.tpgemm_cp_roundtrip.restype = ci
+    lib.tpgemm_cp_roundtrip_repeat.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
+                                               ctypes.c_uint32, ci, ci, ci, ci, vp]
+    lib.tpgemm_cp_roundtrip_repeat.restype = ci
+    lib.tpgemm_tmem_ldst_roundtrip.argtypes = [vp, vp, vp, ci, ci, ci, ci, ctypes.c_uint32,
+                                               vp]
+    lib.tpgemm_tmem_ldst_roundtrip.restype = ci
+    lib.tpgemm_vcopy_plan.argtypes = [ctypes.POINTER(VcopyDesc), ctypes.c_char_p, ci]
+    lib.tpgemm_vcopy_plan.restype = ci
+    lib.tpgemm_vcopy_roundtrip.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(VcopyDesc),
+                                           ci, i64, vp, vp]
+    lib.tpgemm_vcopy_roundtrip.restype = ci
+    return lib
+
+
+_lib_debug = None
+
+
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is not built; run tile_primitive_tensor_gb300.build.build() "
-                "(nvcc for sm_103a). There is no CPU fallback.")
-        lib = ctypes.CDLL(LIB_PATH)
-        vp, i64, ci, cf = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
-        gemm_args = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, cf, vp]
-        lib.tpgemm_gemm.argtypes = gemm_args
-        lib.tpgemm_gemm.restype = ci
-        lib.tpgemm_gemm_path.argtypes = gemm_args + [ci]
-        lib.tpgemm_gemm_path.restype = ci
-        lib.tpgemm_gemm_noalloc.argtypes = gemm_args
-        lib.tpgemm_gemm_noalloc.restype = ci
-        lib.tpgemm_test_gemm_withhold_fill.argtypes = gemm_args
-        lib.tpgemm_test_gemm_withhold_fill.restype = ci
-        lib.tpgemm_reload_tuning.argtypes = []
-        lib.tpgemm_reload_tuning.restype = None
-        lib.tpgemm_gemm_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, cf, vp,
-                                         ctypes.c_size_t, vp]
-        lib.tpgemm_gemm_host.restype = ci
-        lib.tpgemm_gemm_host_workspace_bytes.argtypes = [i64, i64, i64, ci, cf]
-        lib.tpgemm_gemm_host_workspace_bytes.restype = ctypes.c_size_t
-        lib.tpgemm_status_string.argtypes = [ci]
-        lib.tpgemm_status_string.restype = ctypes.c_char_p
-        lib.tpgemm_last_error_detail.argtypes = []
-        lib.tpgemm_last_error_detail.restype = ctypes.c_char_p
-        lib.tpgemm_last_device_error.argtypes = []
-        lib.tpgemm_last_device_error.restype = ci
-        lib.tpgemm_describe_plan.argtypes = [i64, i64, i64, ci, ci, ci, cf, ci, ctypes.c_char_p, ci]
-        lib.tpgemm_describe_plan.restype = ci
-        lib.tpgemm_last_plan.argtypes = [ctypes.c_char_p, ci]
-        lib.tpgemm_last_plan.restype = ci
-        u32 = ctypes.c_uint32
-        lib.tpgemm_encode_smem_desc.argtypes = [u32, u32, u32, ci]
-        lib.tpgemm_encode_smem_desc.restype = ctypes.c_uint64
-        lib.tpgemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
-        lib.tpgemm_encode_idesc.restype = u32
-        lib.tpgemm_encode_idesc_mx.argtypes = [ci, ci, ci, ci, ci]
-        lib.tpgemm_encode_idesc_mx.restype = u32
-        sz = ctypes.c_size_t
-        lib.tpgemm_gemm_mx.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, cf, vp, sz, vp]
-        lib.tpgemm_gemm_mx.restype = ci
-        lib.tpgemm_gemm_mx_workspace_bytes.argtypes = [i64, i64, i64]
-        lib.tpgemm_gemm_mx_workspace_bytes.restype = sz
-        lib.tpgemm_version.argtypes = []
-        lib.tpgemm_version.restype = ctypes.c_char_p
-        lib.tpgemm_cp_parse_shape.argtypes = [ctypes.c_char_p, ctypes.POINTER(ci)]
-        lib.tpgemm_cp_parse_shape.restype = ci
-        lib.tpgemm_cp_plan.argtypes = [ctypes.POINTER(CpDesc), ctypes.c_char_p, ci]
-        lib.tpgemm_cp_plan.restype = ci
-        lib.tpgemm_cp_roundtrip.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
-                                            ctypes.c_uint32, ci, vp]
-        lib.tpgemm_cp_roundtrip.restype = ci
-        lib.tpgemm_cp_roundtrip_repeat.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(CpDesc),
-                                                   ctypes.c_uint32, ci, ci, ci, ci, vp]
-        lib.tpgemm_cp_roundtrip_repeat.restype = ci
-        lib.tpgemm_tmem_ldst_roundtrip.argtypes = [vp, vp, vp, ci, ci, ci, ci, ctypes.c_uint32,
-                                                   vp]
-        lib.tpgemm_tmem_ldst_roundtrip.restype = ci
-        lib.tpgemm_vcopy_plan.argtypes = [ctypes.POINTER(VcopyDesc), ctypes.c_char_p, ci]
-        lib.tpgemm_vcopy_plan.restype = ci
-        lib.tpgemm_vcopy_roundtrip.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(VcopyDesc),
-                                               ci, i64, vp, vp]
-        lib.tpgemm_vcopy_roundtrip.restype = ci
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _open(LIB_PATH)
+        return _lib
+
+
+def debug_library():
+    """The ctypes handle of libtpgemm_debug.so (same C ABI, device-side bounds
+    checks that report TPGEMM_ERR_BOUNDS); build it with build(debug=True)."""
+    global _lib_debug
+    with _lock:
+        if _lib_debug is None:
+            _lib_debug = _open(LIB_PATH_DEBUG)
+        return _lib_debug
 
 
 def library():

@@ -20,6 +20,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtpgemm.so")
+# The debug build (-DTPGEMM_DEBUG): device-side bounds checks that report
+# TPGEMM_ERR_BOUNDS and skip the access. Built on request only.
+BUILD_DIR_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_PATH_DEBUG = os.path.join(LIB_DIR, "libtpgemm_debug.so")
 SOURCES = ["tpgemm_api.cu", "tc_gemm.cu", "mma_sync_gemm.cu", "tmem_copy.cu", "vec_copy.cu",
            "mx_scales.cu"]
 HEADERS = ["ptx.cuh", "tpgemm_internal.h"]
@@ -40,20 +44,26 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile and link the library if any source changed; return its path."""
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          debug: bool = False) -> str:
+    """Compile and link the library (or, with debug, libtpgemm_debug.so) if any
+    source changed; return its path."""
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = BUILD_DIR_DEBUG if debug else BUILD_DIR
+    lib_path = LIB_PATH_DEBUG if debug else LIB_PATH
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "tpgemm.h")]
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                     "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
+    if debug:
+        flags += ["-DTPGEMM_DEBUG"]
     if ptxas_verbose:
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         if force or ptxas_verbose or _stale(o, [s] + headers):
             cmd = [nvcc] + flags + ["-c", s, "-o", o]
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -65,16 +75,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if force or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
+    if force or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
-                ptxas_verbose="--ptxas-verbose" in sys.argv))
+                ptxas_verbose="--ptxas-verbose" in sys.argv, debug="--debug" in sys.argv))

@@ -36,6 +36,35 @@
 namespace tpg {
 
 __device__ int g_tc_status;  // 0 = ok, kStatusTimeout after an expired wait
+__device__ int g_tc_bounds_site;  // debug builds: the site of the last failed bounds check
+
+// Sites of the debug bounds checks (reported with TPGEMM_ERR_BOUNDS).
+enum BoundsSite : int {
+    kSiteEpilogueLoad = 1,   // a tcgen05.ld column past the accumulator's buffer
+    kSiteMmaAccumulator = 2, // an accumulator buffer past the tensor-memory allocation
+    kSiteScaleSlot = 3,      // a block-scale slot past the allocation
+    kSiteStore = 4,          // a TMA store coordinate negative or not 16-byte aligned
+    kSiteLoadC = 5,          // a TMA load coordinate of C or a partial tile not aligned
+    kSiteFlag = 6,           // a stream-K flag index past the flag area
+};
+
+// Debug builds (-DTPGEMM_DEBUG): a computed tensor-memory column, TMA
+// coordinate or stream-K flag index outside its range records kStatusBounds
+// and the site (read by tpgemm_last_device_error) and the caller skips the
+// access: nothing traps. Release builds compile every check away.
+__device__ __forceinline__ bool in_bounds(bool ok, int site) {
+#ifdef TPGEMM_DEBUG
+    if (!ok) {
+        atomicExch(&g_tc_status, kStatusBounds);
+        atomicExch(&g_tc_bounds_site, site);
+    }
+    return ok;
+#else
+    (void)ok;
+    (void)site;
+    return true;
+#endif
+}
 
 // Stream-K scratch of tpgemm_gemm_noalloc: partial-tile slots, then the epoch
 // flags in its last kStaticScratchFlagBytes. Every GPU that loads the library
@@ -498,6 +527,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!wait_phase(&s.acc_empty[b], acc_phase ^ 1u, s.abort, tmo)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem + uint32_t(b * acc_stride);
+                if (!in_bounds(b * acc_stride + 32 * ((p.bn + 31) / 32) <= p.tmem_cols,
+                               kSiteMmaAccumulator)) {
+                    ok = false;
+                    break;
+                }
                 for (int i = 0; i < nk; ++i) {
                     if (!wait_phase(&s.full[stage], phase, s.abort, tmo)) {
                         ok = false;
@@ -517,6 +551,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int hs = stage / sf_spr;
                         const uint32_t slot = sf_slot0 + uint32_t(hs) * half_cols +
                                               uint32_t(stage - hs * sf_spr) * sf_cols;
+                        if (!in_bounds((slot - tmem) + sf_cols <= uint32_t(p.tmem_cols),
+                                       kSiteScaleSlot)) {
+                            ok = false;
+                            break;
+                        }
                         tc_cp<CG>(6, slot, smem_desc_with_addr(dSF, sfs));
                         for (int j = 0; j < sf_q_chunks; ++j)
                             tc_cp<CG>(6, slot + 4u * uint32_t(1 + j),
@@ -660,7 +699,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (from_slot && my_chunks > 0) {
                 bool fok = true;
                 if (lane == 0) {
-                    fok = wait_flag(&p.sk_flags[src_slot * kEpiWarps + ew], p.sk_epoch, s.abort, tmo);
+                    fok = in_bounds(src_slot * kEpiWarps + ew < kTcMaxFlagSlots * kEpiWarps,
+                                    kSiteFlag) &&
+                          wait_flag(&p.sk_flags[src_slot * kEpiWarps + ew], p.sk_epoch, s.abort, tmo);
                     fence_proxy_async_global();
                 }
                 fok = __shfl_sync(0xffffffffu, fok ? 1 : 0, 0) != 0;
@@ -671,7 +712,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (add_src) {
                 for (int j = 0; j < nbw && j < my_chunks; ++j) {
                     const int c = ng * j + half;
-                    if (lane == 0) {
+                    if (lane == 0 && in_bounds(src_x(c) % 4 == 0, kSiteLoadC)) {
                         mbar_arrive_expect_tx(&cb[j], src_bytes);
                         tma_load_2d_hint(bufs + j * kEpiBufFloats, src_map, &cb[j], src_x(c),
                                          src_y(c), from_slot ? l2_policy(0) : pol_cd);
@@ -696,7 +737,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int bi = j % nbw;
                 float* buf = bufs + bi * kEpiBufFloats;
                 tmem_ld_wait(cur);
-                if (j + 1 < my_chunks)
+                if (j + 1 < my_chunks &&
+                    in_bounds(acc_col + uint32_t(32 * (c + ng)) + 32u <=
+                                  acc_col + uint32_t(acc_stride),
+                              kSiteEpilogueLoad))
                     tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * (c + ng)), nxt);
                 if (add_src) {
                     bool cok = wait_phase(&cb[bi], (cphase >> bi) & 1u, s.abort, tmo);
@@ -746,7 +790,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
+                if (lane == 0 && in_bounds(dst_x(c) >= 0 && dst_y(c) >= 0 && dst_x(c) % 4 == 0,
+                                           kSiteStore)) {
                     tma_store_2d_hint(dst_map, buf, dst_x(c), dst_y(c),
                                       to_slot ? l2_policy(0) : pol_cd);
                     bulk_commit_group();
@@ -763,8 +808,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 return true;
             };
             uint32_t ra[32], rb[32];
-            if (my_chunks > 0)
-                tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * half), ra);
+            uint32_t first_col = acc_col + uint32_t(32 * half);
+#ifdef TPGEMM_DEBUG
+            if (p.debug_plant) first_col += uint32_t(p.tmem_cols);  // caught below
+#endif
+            if (my_chunks > 0 &&
+                in_bounds(first_col + 32u <= acc_col + uint32_t(acc_stride), kSiteEpilogueLoad))
+                tmem_ld_32x32b_x32(tmem + lane_base + first_col, ra);
             for (int j = 0; j < my_chunks && ok; j += 2) {
                 ok = chunk(j, ra, rb);
                 if (ok && j + 1 < my_chunks) ok = chunk(j + 1, rb, ra);
@@ -781,7 +831,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // A partial written to this CTA's slot is published once its bulk
             // stores have completed (not just read their shared source).
-            if (ok && to_slot && lane == 0) {
+            if (ok && to_slot && lane == 0 &&
+                in_bounds(dst_slot * kEpiWarps + ew < kTcMaxFlagSlots * kEpiWarps, kSiteFlag)) {
                 bulk_wait_group<0>();
                 fence_proxy_async_global();
                 st_release_gpu(&p.sk_flags[dst_slot * kEpiWarps + ew], p.sk_epoch);
@@ -946,11 +997,14 @@ cudaError_t tc_static_scratch(void** ptr) {
     return cudaSuccess;
 }
 
-cudaError_t tc_read_and_clear_device_status(int* status) {
+cudaError_t tc_read_and_clear_device_status(int* status, int* bounds_site) {
     cudaError_t e = cudaMemcpyFromSymbol(status, g_tc_status, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(bounds_site, g_tc_bounds_site, sizeof(int));
     if (e != cudaSuccess) return e;
     const int zero = 0;
-    return cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(int));
+    e = cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_tc_bounds_site, &zero, sizeof(int));
 }
 
 }  // namespace tpg

@@ -93,6 +93,7 @@ struct Tuning {
     int bn = -1, bp = -1, dep_early = -1, epi_bufs = -1, epi_groups = -1, group = -1;
     int krotate = -1, max_clusters = -1, pair = -1, producers = -1, sk = -1, stages = -1;
     int tail = -1, host_blocks = -1, l2_p = -1, l2_q = -1, l2_cd = -1, snake = -1;
+    int debug_plant = -1;  // debug builds only
     int orient = 0;  // 1 "swap", 2 "normal"
     long long wait_ms = -1;
 };
@@ -125,6 +126,9 @@ Tuning read_tuning() {
         if (!strcmp(f, "normal")) t.orient = 2;
     }
     if (const char* f = getenv("TPGEMM_WAIT_TIMEOUT_MS")) t.wait_ms = atoll(f);
+#ifdef TPGEMM_DEBUG
+    geti("TPGEMM_DEBUG_PLANT", &t.debug_plant);
+#endif
     return t;
 }
 
@@ -477,7 +481,7 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
 // Stream-K scratch: one partial-tile slot per CTA (128 x bn fp32, bn rounded
 // up to 32) and one epoch flag per epilogue warp of each CTA. Sized for the
 // largest plan.
-constexpr int kSkMaxGrid = 256;
+constexpr int kSkMaxGrid = tpg::kTcMaxFlagSlots;
 constexpr size_t kSkSlotFloats = size_t(128) * 256;
 constexpr size_t kSkSlotBytes = kSkMaxGrid * kSkSlotFloats * sizeof(float);
 constexpr size_t kSkFlagBytes = kSkMaxGrid * tpg::kTcEpiWarps * sizeof(uint32_t);
@@ -1015,6 +1019,9 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
         if (s != TPGEMM_OK) return s;
     }
     plan.tc.test_stall = withhold_fill ? 1 : 0;
+#ifdef TPGEMM_DEBUG
+    plan.tc.debug_plant = tuning().debug_plant > 0 ? 1 : 0;
+#endif
     // P / Q operands: normal P = A (rows M), Q = B^T (rows N); swapped P = B^T, Q = A.
     const void* pp = plan.swap ? B : A;
     const void* qq = plan.swap ? A : B;
@@ -1374,6 +1381,7 @@ const char* tpgemm_status_string(tpgemm_status s) {
         case TPGEMM_ERR_LAUNCH: return "launch failed";
         case TPGEMM_ERR_TIMEOUT: return "device wait timed out";
         case TPGEMM_ERR_PATH: return "kernel path cannot run this problem";
+        case TPGEMM_ERR_BOUNDS: return "debug bounds check failed";
     }
     return "unknown status";
 }
@@ -1385,13 +1393,21 @@ tpgemm_status tpgemm_last_device_error(void) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
         return fail(TPGEMM_ERR_LAUNCH, "device synchronize: %s", cudaGetErrorString(e));
-    int st = 0, st_cp = 0;
-    e = tpg::tc_read_and_clear_device_status(&st);
+    int st = 0, st_cp = 0, site = 0;
+    e = tpg::tc_read_and_clear_device_status(&st, &site);
     if (e == cudaSuccess) e = tpg::cp_read_and_clear_device_status(&st_cp);
     if (e != cudaSuccess)
         return fail(TPGEMM_ERR_LAUNCH, "reading device status: %s", cudaGetErrorString(e));
     if (st == tpg::kStatusTimeout)
         return fail(TPGEMM_ERR_TIMEOUT, "a tcgen05 kernel wait exceeded its bound");
+    if (st == tpg::kStatusBounds) {
+        static const char* kSites[] = {"?", "epilogue tensor-memory load", "MMA accumulator",
+                                       "block-scale slot", "TMA store coordinate",
+                                       "TMA load coordinate", "stream-K flag index"};
+        return fail(TPGEMM_ERR_BOUNDS,
+                    "a debug bounds check failed at site %d (%s); the access was skipped", site,
+                    kSites[site >= 0 && site <= 6 ? site : 0]);
+    }
     if (st_cp == tpg::kStatusTimeout)
         return fail(TPGEMM_ERR_TIMEOUT, "a tensor-memory copy kernel wait exceeded its bound");
     return TPGEMM_OK;
@@ -1463,6 +1479,12 @@ uint32_t tpgemm_encode_idesc(tpgemm_dtype dtype, int a_mn_major, int b_mn_major,
     return tpg::idesc_f16_f32(format_code(dtype), a_mn_major != 0, b_mn_major != 0, m, n);
 }
 
-const char* tpgemm_version(void) { return "0.1.0"; }
+const char* tpgemm_version(void) {
+#ifdef TPGEMM_DEBUG
+    return "0.2.0-debug";
+#else
+    return "0.2.0";
+#endif
+}
 
 }  // extern "C"

@@ -9,6 +9,7 @@
 namespace tpg {
 
 constexpr int kStatusTimeout = 9;  // matches TPGEMM_ERR_TIMEOUT
+constexpr int kStatusBounds = 11;  // matches TPGEMM_ERR_BOUNDS (debug builds only)
 
 // The calling thread's reason for its last non-OK status, as returned by
 // tpgemm_last_error_detail (empty after a success).
@@ -19,8 +20,10 @@ void set_error_detail(const char* text);
 uint64_t wait_timeout_ns();
 
 // Device status words of the GEMM kernel and of the tensor-memory copy kernel
-// (0, or kStatusTimeout after an expired bounded wait); reading clears them.
-cudaError_t tc_read_and_clear_device_status(int* status);
+// (0, or kStatusTimeout after an expired bounded wait, or in a debug build
+// kStatusBounds after a failed bounds check, with the check's site);
+// reading clears them.
+cudaError_t tc_read_and_clear_device_status(int* status, int* bounds_site);
 cudaError_t cp_read_and_clear_device_status(int* status);
 
 // ---- warp-level mma.sync kernel (small problems) ----
@@ -123,6 +126,9 @@ struct TcParams {
     // 0..3. In a CTA pair each CTA holds its own P chunk and all Q chunks.
     // Slot i lies in accumulator half i / sf_spr, at column sf_col0 + (i %
     // sf_spr) sf_cols past that half's start (past its tile's columns).
+    int debug_plant;        // debug builds only: 1 offsets the epilogue's first
+                            // tensor-memory load past the allocation, which the bounds
+                            // check must catch (and skip)
     int mx;                 // 0 / 1
     int l2_p, l2_q;         // L2 policies of the P and Q loads: 0 normal, 1 evict_first,
                             // 2 evict_last (ptx.cuh l2_policy)
@@ -163,7 +169,8 @@ cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters);
 // Static stream-K scratch (no allocation): its size, the flag area at its end,
 // and its device address on the current device (taken on first use there).
 constexpr size_t kStaticScratchBytes = size_t(20) << 20;
-constexpr size_t kStaticScratchFlagBytes = size_t(256) * kTcEpiWarps * sizeof(uint32_t);
+constexpr int kTcMaxFlagSlots = 256;  // CTAs a stream-K flag area (allocated or static) covers
+constexpr size_t kStaticScratchFlagBytes = size_t(kTcMaxFlagSlots) * kTcEpiWarps * sizeof(uint32_t);
 constexpr int kMaxStaticScratchDevices = 64;
 cudaError_t tc_static_scratch(void** ptr);
 
