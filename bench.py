@@ -683,7 +683,7 @@ def finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src
                    "parallelism": "single GPU"},
         "clocks": clocks,
         # block-scaled steps launch the two scale-packing kernels before the GEMM
-        "gpu_launches": args.steps * (3 if isinstance(w, wl.MxWorkload) else 1),
+        "gpu_launches": args.steps * (2 if isinstance(w, wl.MxWorkload) else 1),
         "roofline": roof,
         "e2e": e2e,
     }

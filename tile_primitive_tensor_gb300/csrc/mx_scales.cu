@@ -19,6 +19,12 @@
 // and blocks past K read as 127 (a scale of 1; the operands there are
 // zero-filled by the TMA anyway). A stage's chunks of one tile are adjacent,
 // so one TMA box loads them all.
+//
+// One launch packs both operands. A block takes one 128-row chunk of one
+// tile and kPackSteps consecutive K stages: it reads the chunk's rows along
+// their scale bytes (consecutive threads on consecutive bytes of a row, so
+// the reads coalesce), transposes them in shared memory, and writes each
+// stage's 128 words as one contiguous run.
 #include <cstdint>
 
 #include "tpgemm_internal.h"
@@ -27,29 +33,70 @@ namespace tpg {
 
 namespace {
 
-__global__ void __launch_bounds__(256)
-    mx_pack_scales_kernel(const uint8_t* __restrict__ sf, int64_t rows, int kb, int ksteps,
-                          int tile_rows, int chunks, int64_t words, uint32_t* __restrict__ out) {
-    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t w = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; w < words; w += stride) {
-        const int idx = int(w & 127);
-        int64_t rest = w >> 7;  // ((tile * ksteps + step) * chunks + j)
-        const int j = int(rest % chunks);
-        rest /= chunks;
-        const int step = int(rest % ksteps);
-        const int64_t tile = rest / ksteps;
-        const int in_tile = 128 * j + 32 * (idx & 3) + (idx >> 2);
-        const int64_t row = tile * tile_rows + in_tile;
-        const bool live = in_tile < tile_rows && row < rows;
-        uint32_t v = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int blk = 4 * step + b;
-            const uint32_t e = (live && blk < kb) ? uint32_t(sf[row * kb + blk]) : 127u;
-            v |= e << (8 * b);
-        }
-        out[w] = v;
+constexpr int kPackSteps = 16;  // K stages per block: 64 scale bytes of each row
+
+struct PackJob {
+    const uint8_t* sf;
+    uint32_t* out;
+    int64_t rows;
+    int kb, ksteps, tile_rows, chunks, groups;
+    int64_t blocks;  // tiles * chunks * groups
+};
+
+__device__ __forceinline__ void pack_block(const PackJob& jb, int64_t b, uint32_t (*w)[kPackSteps + 1]) {
+    const int g = int(b % jb.groups);
+    const int64_t tj = b / jb.groups;  // tile * chunks + j
+    const int j = int(tj % jb.chunks);
+    const int64_t tile = tj / jb.chunks;
+    const int s0 = g * kPackSteps;
+    const int nsteps = min(kPackSteps, jb.ksteps - s0);
+    constexpr int kRowBytes = 4 * kPackSteps;
+    // w[4 r + c][s] holds chunk row 32 c + r, stage s0 + s: the output order,
+    // so the write-out below reads consecutive rows of w (no bank conflicts).
+    uint8_t* wb = reinterpret_cast<uint8_t*>(w);
+#pragma unroll 8
+    for (int e = threadIdx.x; e < 128 * kRowBytes; e += blockDim.x) {
+        const int r = e / kRowBytes;
+        const int byte = e % kRowBytes;
+        const int in_tile = 128 * j + r;
+        const int64_t row = tile * jb.tile_rows + in_tile;
+        const int blk = 4 * s0 + byte;
+        const bool live = in_tile < jb.tile_rows && row < jb.rows && blk < jb.kb;
+        const uint8_t v = live ? jb.sf[row * jb.kb + blk] : uint8_t(127);
+        const int idx = 4 * (r & 31) + (r >> 5);
+        wb[(idx * (kPackSteps + 1) + (byte >> 2)) * 4 + (byte & 3)] = v;
     }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nsteps * 128; e += blockDim.x) {
+        const int st = e >> 7;
+        const int idx = e & 127;
+        jb.out[((tile * jb.ksteps + s0 + st) * jb.chunks + j) * 128 + idx] = w[idx][st];
+    }
+}
+
+__global__ void __launch_bounds__(256) mx_pack_scales_kernel(PackJob a, PackJob b) {
+    __shared__ uint32_t w[128][kPackSteps + 1];
+    const int64_t blk = blockIdx.x;
+    if (blk < a.blocks)
+        pack_block(a, blk, w);
+    else
+        pack_block(b, blk - a.blocks, w);
+}
+
+bool make_job(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint32_t* out,
+              PackJob& jb) {
+    if (tile_rows < 16 || tile_rows > 256) return false;
+    jb.sf = sf;
+    jb.out = out;
+    jb.rows = rows;
+    jb.kb = int((K + kMxBlock - 1) / kMxBlock);
+    jb.ksteps = int((K + 127) / 128);
+    jb.tile_rows = tile_rows;
+    jb.chunks = (tile_rows + 127) / 128;
+    jb.groups = (jb.ksteps + kPackSteps - 1) / kPackSteps;
+    const int64_t tiles = (rows + tile_rows - 1) / tile_rows;
+    jb.blocks = tiles * jb.chunks * jb.groups;
+    return true;
 }
 
 }  // namespace
@@ -69,17 +116,17 @@ size_t mx_packed_bytes_bound(int64_t rows, int64_t K) {
     return size_t(2 * ((rows + 127) / 128) + 2) * size_t(ksteps) * 512;
 }
 
-cudaError_t launch_mx_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows,
-                                  uint32_t* out, cudaStream_t stream) {
-    if (tile_rows < 16 || tile_rows > 256) return cudaErrorInvalidValue;
-    const int kb = int((K + kMxBlock - 1) / kMxBlock);
-    const int ksteps = int((K + 127) / 128);
-    const int chunks = (tile_rows + 127) / 128;
-    const int64_t words = int64_t(mx_packed_bytes(rows, K, tile_rows) / 4);
-    const int64_t want = (words + 255) / 256;
-    const int blocks = int(want < 4096 ? want : 4096);
-    mx_pack_scales_kernel<<<blocks, 256, 0, stream>>>(sf, rows, kb, ksteps, tile_rows, chunks,
-                                                      words, out);
+cudaError_t launch_mx_pack_scales(const uint8_t* sfa, int64_t rows_a, int tile_rows_a,
+                                  uint32_t* out_a, const uint8_t* sfb, int64_t rows_b,
+                                  int tile_rows_b, uint32_t* out_b, int64_t K,
+                                  cudaStream_t stream) {
+    PackJob a, b;
+    if (!make_job(sfa, rows_a, K, tile_rows_a, out_a, a) ||
+        !make_job(sfb, rows_b, K, tile_rows_b, out_b, b))
+        return cudaErrorInvalidValue;
+    const int64_t blocks = a.blocks + b.blocks;
+    if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    mx_pack_scales_kernel<<<unsigned(blocks), 256, 0, stream>>>(a, b);
     return cudaGetLastError();
 }
 

@@ -325,8 +325,11 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
     // Block-scaled tiles are at most 192 wide: each accumulator half keeps the
     // columns past its tile for the scale slots (at 192, five 12-column slots
     // per half).
+    const int mx_bn = (tuning().bn >= 32 && tuning().bn <= 192 && tuning().bn % 32 == 0)
+                          ? tuning().bn
+                          : 192;
     const int bn = swap_small ? int(Nq)
-                   : mx       ? (Nq <= 192 ? int(((Nq + 15) / 16) * 16) : 192)
+                   : mx       ? (Nq <= mx_bn ? int(((Nq + 15) / 16) * 16) : mx_bn)
                               : pick_bn(Mp, Nq, sms, pair_wanted);
     p.Mp = int(Mp);
     p.Nq = int(Nq);
@@ -1113,8 +1116,8 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
         uint32_t* wb = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(mx->ws) +
                                                    mx_ws_b_offset(M, K));
         const int rows_a = plan.swap ? p.bn : 128, rows_b = plan.swap ? 128 : p.bn;
-        cudaError_t e = tpg::launch_mx_pack_scales(mx->SFA, M, K, rows_a, wa, st);
-        if (e == cudaSuccess) e = tpg::launch_mx_pack_scales(mx->SFB, N, K, rows_b, wb, st);
+        cudaError_t e =
+            tpg::launch_mx_pack_scales(mx->SFA, M, rows_a, wa, mx->SFB, N, rows_b, wb, K, st);
         if (e != cudaSuccess)
             return fail(TPGEMM_ERR_LAUNCH, "scale packing launch: %s", cudaGetErrorString(e));
         const uint32_t* sp = plan.swap ? wb : wa;

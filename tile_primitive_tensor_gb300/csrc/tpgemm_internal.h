@@ -183,8 +183,12 @@ size_t mx_packed_bytes(int64_t rows, int64_t K, int tile_rows);
 // An upper bound of mx_packed_bytes over every tile height a plan uses (128,
 // or up to 192 for the Q operand).
 size_t mx_packed_bytes_bound(int64_t rows, int64_t K);
-cudaError_t launch_mx_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows,
-                                  uint32_t* out, cudaStream_t stream);
+// Packs both operands' scales in one launch (A's rows_a rows in tiles of
+// tile_rows_a, B's likewise).
+cudaError_t launch_mx_pack_scales(const uint8_t* sfa, int64_t rows_a, int tile_rows_a,
+                                  uint32_t* out_a, const uint8_t* sfb, int64_t rows_b,
+                                  int tile_rows_b, uint32_t* out_b, int64_t K,
+                                  cudaStream_t stream);
 
 
 }  // namespace tpg
