@@ -196,8 +196,11 @@ tpgemm_status tpgemm_gemm_mx(float* D, const void* A, const void* B, const float
                              int64_t K, tpgemm_dtype dtype, float beta, void* workspace,
                              size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace tpgemm_gemm_mx needs: the packed scales, 512 bytes per
- * (128 rows, 128 K) of A and of B. 0 for non-positive or oversized shapes. */
+/* Bytes of workspace tpgemm_gemm_mx needs: the packed scales of A and of B,
+ * 512 bytes per (128 rows, 128 K) of an operand tile, four times over for
+ * tiles of more than 128 rows, sized for the largest tiling a plan can choose
+ * (about 0.8 MB per 1024 rows per 1024 K of the larger operand). 0 for
+ * non-positive or oversized shapes. */
 size_t tpgemm_gemm_mx_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Host copy of the block-scaled instruction descriptor encoder (test aid, as

@@ -257,12 +257,15 @@ def call_mx(M=256, N=256, K=256, D=BASE, A=BASE + 64 * MB, B=BASE + 128 * MB, C=
 
 
 def test_mx_workspace_size(lib):
-    # 512 bytes per 128-row chunk and 128-element K stage, sized for any tile
-    # height (2 ceil(rows / 128) + 2 chunks per stage), A's then B's from a
-    # 256-byte boundary: 256 x 256 x 256 is 6 x 2 chunks each; 144 x 16392 x
-    # 4112 (33 stages) is 6 x 33 and 260 x 33.
-    assert tp.tpgemm_gemm_mx_workspace_bytes(256, 256, 256) == 2 * 6 * 2 * 512
-    assert tp.tpgemm_gemm_mx_workspace_bytes(144, 16392, 4112) == (6 * 33 + 260 * 33) * 512
+    # 512 bytes per 128-row chunk and 128-element K stage, each chunk stored 4
+    # times for tiles of more than 128 rows; sized for the largest of the tile
+    # heights a plan can use (multiples of 32 up to 192, or all rows when they
+    # fit one tile), A's then B's from a 256-byte boundary. 256 x 256 x 256:
+    # 160- or 192-row tiles, 2 tiles x 2 chunks x 4 copies x 2 stages each.
+    # 144 x 16392 x 4112 (33 stages): A as one 144-row tile (8 chunk copies),
+    # B in 103 tiles of 160 rows (824).
+    assert tp.tpgemm_gemm_mx_workspace_bytes(256, 256, 256) == 2 * 16 * 2 * 512
+    assert tp.tpgemm_gemm_mx_workspace_bytes(144, 16392, 4112) == (8 + 824) * 33 * 512
     assert tp.tpgemm_gemm_mx_workspace_bytes(0, 8, 16) == 0
 
 
@@ -272,7 +275,7 @@ def test_mx_workspace_size(lib):
     ({"SFA": None}, tp.TPGEMM_ERR_NULL, "SFA is NULL"),
     ({"SFB": None}, tp.TPGEMM_ERR_NULL, "SFB is NULL"),
     ({"ws": None}, tp.TPGEMM_ERR_NULL, "workspace is NULL"),
-    ({"ws_bytes": 12287}, tp.TPGEMM_ERR_NULL, "12288 needed"),
+    ({"ws_bytes": 32767}, tp.TPGEMM_ERR_NULL, "32768 needed"),
     ({"ws": BASE + 320 * MB + 16}, tp.TPGEMM_ERR_ALIGN, "256-byte aligned"),
     ({"ws": BASE}, tp.TPGEMM_ERR_ALIAS, "workspace overlaps"),
     ({"SFA": BASE + 16}, tp.TPGEMM_ERR_ALIAS, "scale matrix"),

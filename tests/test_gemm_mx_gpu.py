@@ -165,13 +165,23 @@ def test_mx_workload_full_size(name):
     check(wl.BY_NAME[name])
 
 
-def test_mx_pair_and_192_wide_tiles():
+def test_mx_pair_and_224_wide_tiles():
     # The default for large problems: CTA pairs (cta_group::2 block-scaled MMA,
     # each CTA holding its own A scales and all of the tile's B scales) on
-    # 192-wide tiles, so Q tiles start at multiples of 192 and their scales
-    # span two 128-row chunks.
+    # 224-wide tiles, so Q tiles start at multiples of 224 and their scales
+    # span two 128-row chunks (one replicated 128x256b copy), two scale slots
+    # per accumulator half.
     plan = check(case(784, 1320, 528, wl.E4M3, 1.0, seed=101))
-    assert "pair=1" in plan and "tile=128x192x128" in plan, plan
+    assert "pair=1" in plan and "tile=128x224x128" in plan, plan
+
+
+@pytest.mark.parametrize("bn", [192, 160, 128, 96])
+def test_mx_tile_widths(bn, tune):
+    # Narrower tiles: five 12-column slots per half at 192, eight at 160, and
+    # one warpx4 Q copy (no replication) at 128 and below.
+    tune.setenv("TPGEMM_TC_BN", str(bn))
+    plan = check(case(784, 1320, 528, wl.E4M3, 1.0, seed=110 + bn))
+    assert f"tile=128x{bn}x128" in plan, plan
 
 
 def test_mx_single_cta_when_one_p_tile():
@@ -207,7 +217,7 @@ def test_mxfp4_one_tile_exact():
 
 
 @pytest.mark.parametrize("M,N,K,beta", [
-    (784, 1320, 512, 1.0),   # CTA pairs, 192-wide tiles
+    (784, 1320, 512, 1.0),   # CTA pairs, 224-wide tiles
     (144, 4104, 1024, 1.0),  # swapped small M
     (128, 64, 384, 0.0),     # one P tile, single CTA
     (1024, 1024, 4096, 0.0),

@@ -13,18 +13,23 @@
 //
 // This pre-pass writes exactly that, per tile of tile_rows rows (128 for the
 // kernel's P operand, the tile width for Q) split into 128-row chunks:
-// out[((tile * ksteps + s) * chunks + j) * 128 + 4 r + c] = the four scales of
-// row tile_rows tile + 128 j + 32 c + r for blocks 4 s .. 4 s + 3
-// (little-endian, byte b = block 4 s + b). Rows past the tile or the matrix
-// and blocks past K read as 127 (a scale of 1; the operands there are
-// zero-filled by the TMA anyway). A stage's chunks of one tile are adjacent,
-// so one TMA box loads them all.
+// out[(((tile * ksteps + s) * chunks + j) * reps + i) * 128 + 4 r + c] = the
+// four scales of row tile_rows tile + 128 j + 32 c + r for blocks 4 s .. 4 s +
+// 3 (little-endian, byte b = block 4 s + b), for every replica i < reps. A
+// tile of more than 128 rows has reps = 4: its stage's 4 KB are then the
+// 128-row, 32-byte-wide source of one tcgen05.cp.128x256b (row 32 i + r of
+// chunk j's image is 16-byte unit j of source row 32 i + r), which puts the
+// same words in every lane quadrant as a warpx4 copy of each chunk. Rows
+// past the tile or the matrix and blocks past K read as 127 (a scale of 1;
+// the operands there are zero-filled by the TMA anyway). A stage's chunks of
+// one tile are adjacent, so one TMA box loads them all.
 //
 // One launch packs both operands. A block takes one 128-row chunk of one
 // tile and kPackSteps consecutive K stages: it reads the chunk's rows along
 // their scale bytes (consecutive threads on consecutive bytes of a row, so
 // the reads coalesce), transposes them in shared memory, and writes each
 // stage's 128 words as one contiguous run.
+#include <algorithm>
 #include <cstdint>
 
 #include "tpgemm_internal.h"
@@ -39,7 +44,7 @@ struct PackJob {
     const uint8_t* sf;
     uint32_t* out;
     int64_t rows;
-    int kb, ksteps, tile_rows, chunks, groups;
+    int kb, ksteps, tile_rows, chunks, reps, groups;
     int64_t blocks;  // tiles * chunks * groups
 };
 
@@ -70,7 +75,9 @@ __device__ __forceinline__ void pack_block(const PackJob& jb, int64_t b, uint32_
     for (int e = threadIdx.x; e < nsteps * 128; e += blockDim.x) {
         const int st = e >> 7;
         const int idx = e & 127;
-        jb.out[((tile * jb.ksteps + s0 + st) * jb.chunks + j) * 128 + idx] = w[idx][st];
+        const uint32_t v = w[idx][st];
+        uint32_t* o = jb.out + (((tile * jb.ksteps + s0 + st) * jb.chunks + j) * jb.reps) * 128 + idx;
+        for (int i = 0; i < jb.reps; ++i) o[i * 128] = v;
     }
 }
 
@@ -93,6 +100,7 @@ bool make_job(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint32_
     jb.ksteps = int((K + 127) / 128);
     jb.tile_rows = tile_rows;
     jb.chunks = (tile_rows + 127) / 128;
+    jb.reps = mx_reps(tile_rows);
     jb.groups = (jb.ksteps + kPackSteps - 1) / kPackSteps;
     const int64_t tiles = (rows + tile_rows - 1) / tile_rows;
     jb.blocks = tiles * jb.chunks * jb.groups;
@@ -105,15 +113,16 @@ size_t mx_packed_bytes(int64_t rows, int64_t K, int tile_rows) {
     const int64_t tiles = (rows + tile_rows - 1) / tile_rows;
     const int64_t chunks = (tile_rows + 127) / 128;
     const int64_t ksteps = (K + 127) / 128;
-    return size_t(tiles) * size_t(chunks) * size_t(ksteps) * 512;
+    return size_t(tiles) * size_t(chunks) * size_t(mx_reps(tile_rows)) * size_t(ksteps) * 512;
 }
 
-// Tile heights are 128, at most 192 when an operand has more rows than one
-// tile, or all of the operand's rows (at most 192) when it fits one tile:
-// at most 2 ceil(rows / 128) + 2 chunks per K stage.
+// Tile heights a plan uses: 128 (P), a multiple of 32 up to 192 (Q over
+// several tiles), or all rows rounded up to 16 when they fit one Q tile.
 size_t mx_packed_bytes_bound(int64_t rows, int64_t K) {
-    const int64_t ksteps = (K + 127) / 128;
-    return size_t(2 * ((rows + 127) / 128) + 2) * size_t(ksteps) * 512;
+    size_t b = 0;
+    for (int t = 32; t <= 192; t += 32) b = std::max(b, mx_packed_bytes(rows, K, t));
+    if (rows <= 192) b = std::max(b, mx_packed_bytes(rows, K, int((rows + 15) / 16 * 16)));
+    return b;
 }
 
 cudaError_t launch_mx_pack_scales(const uint8_t* sfa, int64_t rows_a, int tile_rows_a,

@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t tx = p.p_tx +
                                     (p.q_mn ? uint32_t(q_atoms) * kAtomBytes
                                             : uint32_t(q_rows) * p.row_tx) +
-                                    (MX ? 512u * uint32_t(1 + p.sf_q_chunks) : 0u);
+                                    (MX ? 512u * uint32_t(1 + p.sf_q_rows) : 0u);
                 const int nk = u.kb1 - u.kb0;
                 int kb = nk == p.k_blocks ? first_k_block(u.T, p) : u.kb0;
                 if constexpr (EARLY) {
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             uint8_t* sf = sq + p.q_bytes;
                             tma_load_2d_pair(sf, &mapSP, fb, 0, (p0 / 128) * p.k_blocks + kb);
                             tma_load_2d_pair(sf + 512, &mapSQ, fb, 0,
-                                             (tq * p.k_blocks + kb) * p.sf_q_chunks);
+                                             (tq * p.k_blocks + kb) * p.sf_q_rows);
                         }
                         issued_any |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         uint8_t* sf = sq + p.q_bytes;
                         tma_load_2d(sf, &mapSP, &s.full[stage], 0, (p0 / 128) * p.k_blocks + kb);
                         tma_load_2d(sf + 512, &mapSQ, &s.full[stage], 0,
-                                    (tq * p.k_blocks + kb) * p.sf_q_chunks);
+                                    (tq * p.k_blocks + kb) * p.sf_q_rows);
                     }
                     issued_any |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -500,9 +500,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t stage_bytes = p.p_bytes + p.q_bytes + p.sf_bytes;
             const uint32_t pq_bytes = p.p_bytes + p.q_bytes;
             // Scale slots (MX): a no-swizzle K-major source of 16-byte rows, 8-row
-            // groups 128 bytes apart; each stage has its own slot in tensor memory.
+            // groups 128 bytes apart (a second 16-byte unit of each row 2 KB on,
+            // for the replicated Q image); each stage has its own slot in
+            // tensor memory.
             const uint64_t dSF = smem_desc_template(512, 128, kDescLayoutNone);
-            const int sf_q_chunks = p.sf_q_chunks;
+            const uint64_t dSF2 = smem_desc_template(2048, 128, kDescLayoutNone);
+            const bool sf_q_wide = p.sf_q_rows == 8;
             const uint32_t sf_slot0 = tmem + uint32_t(p.sf_col0);
             const uint32_t sf_cols = uint32_t(p.sf_cols);
             const int sf_spr = p.sf_spr > 0 ? p.sf_spr : 1;
@@ -557,9 +560,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             break;
                         }
                         tc_cp<CG>(6, slot, smem_desc_with_addr(dSF, sfs));
-                        for (int j = 0; j < sf_q_chunks; ++j)
-                            tc_cp<CG>(6, slot + 4u * uint32_t(1 + j),
-                                      smem_desc_with_addr(dSF, sfs + 512u * uint32_t(1 + j)));
+                        if (sf_q_wide)  // both Q chunks, replicated: 128x256b
+                            tc_cp<CG>(1, slot + 4u, smem_desc_with_addr(dSF2, sfs + 512u));
+                        else
+                            tc_cp<CG>(6, slot + 4u, smem_desc_with_addr(dSF, sfs + 512u));
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint64_t adesc = smem_desc_with_addr(dP, ap + kk * 32);
@@ -919,9 +923,10 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
     // past the tile's columns, 1024-aligned stages.
     if (p.mx && (p.bp != 128 || p.tail_split != 1 || p.sk || p.tmem_cols != 512 ||
                  !(p.sf_q_chunks == 1 || p.sf_q_chunks == 2) ||
+                 p.sf_q_rows != (p.sf_q_chunks == 2 ? 8 : 1) ||
                  p.sf_cols != 4 + 4 * p.sf_q_chunks || p.sf_col0 < 32 * ((p.bn + 31) / 32) ||
                  p.sf_spr < 1 || p.sf_col0 + p.sf_spr * p.sf_cols > 256 ||
-                 p.stages > 2 * p.sf_spr || p.sf_bytes < 512u * uint32_t(1 + p.sf_q_chunks) ||
+                 p.stages > 2 * p.sf_spr || p.sf_bytes < 512u * uint32_t(1 + p.sf_q_rows) ||
                  (p.p_bytes + p.q_bytes + p.sf_bytes) % 1024 != 0))
         return cudaErrorInvalidValue;
     if (!p.mx && p.sf_bytes != 0) return cudaErrorInvalidValue;

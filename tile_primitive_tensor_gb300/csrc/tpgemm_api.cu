@@ -322,12 +322,16 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
                     "stored [N,K] (transB = 1)");
     // The CTA-pair MMA needs at least two 128-row P tiles.
     const bool pair_wanted = Mp > 128;
-    // Block-scaled tiles are at most 192 wide: each accumulator half keeps the
-    // columns past its tile for the scale slots (at 192, five 12-column slots
-    // per half).
-    const int mx_bn = (tuning().bn >= 32 && tuning().bn <= 192 && tuning().bn % 32 == 0)
+    // Block-scaled tiles are at most 224 wide: each accumulator half keeps the
+    // columns past its tile for the scale slots (two 12-column slots per half
+    // at 224, so a 4-deep ring; five at 192). Measured on GB300, 8192^3 e4m3:
+    // 224 wide 491 us, 192 wide 570 us, 160 wide 654 us (4096^3 e5m2: 80 vs
+    // 94 us at 192): the operand bytes per flop fall with the width and the
+    // kernel is bound by operand delivery. TPGEMM_TC_BN (32..224, a multiple
+    // of 32) overrides.
+    const int mx_bn = (tuning().bn >= 32 && tuning().bn <= 224 && tuning().bn % 32 == 0)
                           ? tuning().bn
-                          : 192;
+                          : 224;
     const int bn = swap_small ? int(Nq)
                    : mx       ? (Nq <= mx_bn ? int(((Nq + 15) / 16) * 16) : mx_bn)
                               : pick_bn(Mp, Nq, sms, pair_wanted);
@@ -369,10 +373,11 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
         // past its tile ([bn rounded to 32, 256) of the half).
         p.tmem_cols = 512;
         p.sf_q_chunks = (bn + 127) / 128;
+        p.sf_q_rows = p.sf_q_chunks * tpg::mx_reps(bn);
         p.sf_cols = 4 + 4 * p.sf_q_chunks;
         p.sf_col0 = 32 * ((bn + 31) / 32);
         p.sf_spr = (256 - p.sf_col0) / p.sf_cols;
-        p.sf_bytes = uint32_t(((512 * (1 + p.sf_q_chunks)) + 1023) / 1024 * 1024);
+        p.sf_bytes = uint32_t(((512 * (1 + p.sf_q_rows)) + 1023) / 1024 * 1024);
         if (p.sf_spr < 1) return fail(TPGEMM_ERR_PATH, "internal: no room for scale slots");
     }
     p.p_bytes = stage_tile_bytes(128, p_mn);
@@ -1126,7 +1131,7 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
         const uint64_t chunk_rows_q = tpg::mx_packed_bytes(p.Nq, K, p.bn) / 512;
         s = encode_u32_rows(enc, &maps.SP, sp, chunk_rows_p, 1, "P scales");
         if (s != TPGEMM_OK) return s;
-        s = encode_u32_rows(enc, &maps.SQ, sq, chunk_rows_q, uint32_t(p.sf_q_chunks), "Q scales");
+        s = encode_u32_rows(enc, &maps.SQ, sq, chunk_rows_q, uint32_t(p.sf_q_rows), "Q scales");
         if (s != TPGEMM_OK) return s;
     }
     cudaError_t e = tpg::launch_tc(maps, p, plan.grid, st);

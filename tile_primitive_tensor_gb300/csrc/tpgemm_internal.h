@@ -119,11 +119,16 @@ struct TcParams {
     // That is the source layout a tcgen05.cp.32x128b.warpx4 copy spreads so
     // that row m's word sits in tensor-memory column m / 32 of lane m (every
     // lane quadrant gets the 32 rows' 16 bytes). P tiles are 128 rows (one
-    // chunk), Q tiles bn rows (sf_q_chunks chunks). Each stage's chunks are
-    // TMA-loaded (mapSP, mapSQ) beside its operand tiles; the MMA thread copies
-    // them into the stage's scale slot in tensor memory (4 columns for P, then
-    // 4 per Q chunk) and issues the four K = 32 MMAs with scale-factor IDs
-    // 0..3. In a CTA pair each CTA holds its own P chunk and all Q chunks.
+    // chunk), Q tiles bn rows (sf_q_chunks chunks). A tile of more than 128
+    // rows stores each chunk 4 times (mx_reps): rows 32 q + r of that 128-row
+    // image are the chunk's row r, so one tcgen05.cp.128x256b writes both
+    // chunks to every lane quadrant (each copy holds the tensor pipe about as
+    // long as the MMAs of a 64-wide stage, whatever its size, so two copies per
+    // stage cost less than three). Each stage's chunks are TMA-loaded (mapSP,
+    // mapSQ) beside its operand tiles; the MMA thread copies them into the
+    // stage's scale slot in tensor memory (4 columns for P, then 4 per Q chunk)
+    // and issues the four K = 32 MMAs with scale-factor IDs 0..3. In a CTA pair
+    // each CTA holds its own P chunk and all Q chunks.
     // Slot i lies in accumulator half i / sf_spr, at column sf_col0 + (i %
     // sf_spr) sf_cols past that half's start (past its tile's columns).
     int debug_plant;        // debug builds only: 1 offsets the epilogue's first
@@ -134,6 +139,7 @@ struct TcParams {
                             // 2 evict_last (ptx.cuh l2_policy)
     int l2_cd;              // L2 policy of the C loads and D stores (read / written once)
     int sf_q_chunks;        // 128-row chunks of a Q tile's scales (1 or 2)
+    int sf_q_rows;          // 512-byte rows of a Q stage's packed scales (chunks x reps)
     uint32_t sf_bytes;      // shared bytes of a stage's scale area (0 without MX)
     int sf_col0;            // first scale column in each accumulator half
     int sf_cols;            // tensor-memory columns of one stage's slot
@@ -147,7 +153,7 @@ struct TcMaps {
     CUtensorMap Qt;         // Q with the (narrower) box of a tail unit
     CUtensorMap W;          // stream-K scratch slots, laid out like D tiles
     CUtensorMap SP, SQ;     // packed scales of P / Q (block-scaled plans): 128 words x
-                            // one chunk per row; boxes of 1 / sf_q_chunks chunks
+                            // one chunk per row; boxes of 1 / sf_q_rows rows
 };
 
 
@@ -175,13 +181,13 @@ constexpr int kMaxStaticScratchDevices = 64;
 cudaError_t tc_static_scratch(void** ptr);
 
 // ---- block-scaled fp8: scale packing pre-pass (mx_scales.cu) ----
-// sf [rows][kb] E8M0 bytes -> out [ceil(rows / tile_rows)][ksteps][chunks][128]
-// words (chunks = ceil(tile_rows / 128)) in the layout TcParams describes;
-// rows or blocks past the ends read as 127 (scale 1).
+// sf [rows][kb] E8M0 bytes -> out [ceil(rows / tile_rows)][ksteps][chunks][reps][128]
+// words (chunks = ceil(tile_rows / 128), reps = mx_reps(tile_rows)) in the
+// layout TcParams describes; rows or blocks past the ends read as 127 (scale 1).
 constexpr int kMxBlock = 32;                 // K elements per scale
+__host__ __device__ constexpr int mx_reps(int tile_rows) { return tile_rows > 128 ? 4 : 1; }
 size_t mx_packed_bytes(int64_t rows, int64_t K, int tile_rows);
-// An upper bound of mx_packed_bytes over every tile height a plan uses (128,
-// or up to 192 for the Q operand).
+// An upper bound of mx_packed_bytes over every tile height a plan can use.
 size_t mx_packed_bytes_bound(int64_t rows, int64_t K);
 // Packs both operands' scales in one launch (A's rows_a rows in tiles of
 // tile_rows_a, B's likewise).
