@@ -108,6 +108,17 @@ def test_mx_small_m_swapped(M):
     assert "orientation=swapped" in plan, plan
 
 
+@pytest.mark.parametrize("bp", [64, 80, 96, 112])
+@pytest.mark.parametrize("shape", [(144, 4104, 1040), (2064, 200, 528)])
+def test_mx_p_rows(bp, shape, tune):
+    # All of Q in one tile: each CTA streams bp < 128 rows of P, whose scales
+    # are packed in tiles of bp rows (the copy's rows past bp read as 1).
+    # Swapped small M, and the normal orientation with a narrow N.
+    tune.setenv("TPGEMM_TC_BP", str(bp))
+    plan = check(case(*shape, wl.E4M3, 1.0, seed=120 + bp + shape[0]))
+    assert f"tile={bp}x" in plan, plan
+
+
 def test_mx_m176_stays_normal():
     plan = check(case(176, 2048, 512, wl.E4M3, 0.0, seed=61))
     assert "orientation=normal" in plan, plan

@@ -26,8 +26,9 @@
 //
 // One launch packs both operands. A block takes one 128-row chunk of one
 // tile and kPackSteps consecutive K stages: it reads the chunk's rows along
-// their scale bytes (consecutive threads on consecutive bytes of a row, so
-// the reads coalesce), transposes them in shared memory, and writes each
+// their scale bytes (two 16-byte loads per thread when the rows are 16-byte
+// aligned, else consecutive threads on consecutive bytes of a row, so the
+// reads coalesce), transposes them in shared memory, and writes each
 // stage's 128 words as one contiguous run.
 #include <algorithm>
 #include <cstdint>
@@ -39,12 +40,14 @@ namespace tpg {
 namespace {
 
 constexpr int kPackSteps = 16;  // K stages per block: 64 scale bytes of each row
+static_assert(kPackSteps == 16, "a block's 256 threads read 128 rows x 2 x 32 bytes");
 
 struct PackJob {
     const uint8_t* sf;
     uint32_t* out;
     int64_t rows;
     int kb, ksteps, tile_rows, chunks, reps, groups;
+    int vec;         // rows start 16-byte aligned: vector loads
     int64_t blocks;  // tiles * chunks * groups
 };
 
@@ -55,29 +58,63 @@ __device__ __forceinline__ void pack_block(const PackJob& jb, int64_t b, uint32_
     const int64_t tile = tj / jb.chunks;
     const int s0 = g * kPackSteps;
     const int nsteps = min(kPackSteps, jb.ksteps - s0);
-    constexpr int kRowBytes = 4 * kPackSteps;
-    // w[4 r + c][s] holds chunk row 32 c + r, stage s0 + s: the output order,
-    // so the write-out below reads consecutive rows of w (no bank conflicts).
-    uint8_t* wb = reinterpret_cast<uint8_t*>(w);
-#pragma unroll 8
-    for (int e = threadIdx.x; e < 128 * kRowBytes; e += blockDim.x) {
-        const int r = e / kRowBytes;
-        const int byte = e % kRowBytes;
+    if (jb.vec && 4 * s0 + 4 * kPackSteps <= jb.kb) {
+        // 16-byte aligned rows, the block's 64 bytes of each inside it: thread
+        // t reads 32 bytes (stages s0 + 8 h .. + 7) of chunk row r = t / 2,
+        // h = t % 2, with two vector loads in flight at once.
+        const int r = int(threadIdx.x) >> 1;
+        const int h = int(threadIdx.x) & 1;
         const int in_tile = 128 * j + r;
         const int64_t row = tile * jb.tile_rows + in_tile;
-        const int blk = 4 * s0 + byte;
-        const bool live = in_tile < jb.tile_rows && row < jb.rows && blk < jb.kb;
-        const uint8_t v = live ? jb.sf[row * jb.kb + blk] : uint8_t(127);
+        uint32_t v[8];
+        if (in_tile < jb.tile_rows && row < jb.rows) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(jb.sf + row * jb.kb + 4 * s0 + 32 * h);
+            const uint4 x = src[0], y = src[1];
+            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = 0x7f7f7f7fu;
+        }
+        // w[4 r' + c][s] holds chunk row 32 c + r', stage s0 + s: the output
+        // order, so the write-out below reads consecutive rows of w.
         const int idx = 4 * (r & 31) + (r >> 5);
-        wb[(idx * (kPackSteps + 1) + (byte >> 2)) * 4 + (byte & 3)] = v;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[idx][8 * h + q] = v[q];
+    } else {
+        // Any alignment: consecutive threads read consecutive bytes of a row
+        // (a warp covers 32 bytes of one row), all 32 loads issued before
+        // any store.
+        constexpr int kRowBytes = 4 * kPackSteps;
+        uint8_t v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const int e = int(threadIdx.x) + 256 * k;
+            const int in_tile = 128 * j + e / kRowBytes;
+            const int64_t row = tile * jb.tile_rows + in_tile;
+            const int blk = 4 * s0 + e % kRowBytes;
+            v[k] = (in_tile < jb.tile_rows && row < jb.rows && blk < jb.kb)
+                       ? jb.sf[row * jb.kb + blk]
+                       : uint8_t(127);
+        }
+        uint8_t* wb = reinterpret_cast<uint8_t*>(w);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const int e = int(threadIdx.x) + 256 * k;
+            const int r = e / kRowBytes;
+            const int byte = e % kRowBytes;
+            const int idx = 4 * (r & 31) + (r >> 5);
+            wb[(idx * (kPackSteps + 1) + (byte >> 2)) * 4 + (byte & 3)] = v[k];
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e < nsteps * 128; e += blockDim.x) {
         const int st = e >> 7;
-        const int idx = e & 127;
-        const uint32_t v = w[idx][st];
-        uint32_t* o = jb.out + (((tile * jb.ksteps + s0 + st) * jb.chunks + j) * jb.reps) * 128 + idx;
-        for (int i = 0; i < jb.reps; ++i) o[i * 128] = v;
+        const int i = e & 127;
+        const uint32_t x = w[i][st];
+        uint32_t* o = jb.out + (((tile * jb.ksteps + s0 + st) * jb.chunks + j) * jb.reps) * 128 + i;
+        for (int k = 0; k < jb.reps; ++k) o[k * 128] = x;
     }
 }
 
@@ -101,6 +138,7 @@ bool make_job(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint32_
     jb.tile_rows = tile_rows;
     jb.chunks = (tile_rows + 127) / 128;
     jb.reps = mx_reps(tile_rows);
+    jb.vec = (reinterpret_cast<uintptr_t>(sf) % 16 == 0 && jb.kb % 16 == 0) ? 1 : 0;
     jb.groups = (jb.ksteps + kPackSteps - 1) / kPackSteps;
     const int64_t tiles = (rows + tile_rows - 1) / tile_rows;
     jb.blocks = tiles * jb.chunks * jb.groups;

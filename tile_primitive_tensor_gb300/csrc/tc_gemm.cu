@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if constexpr (MX) {
                             // This CTA's P chunk and all of the tile's Q chunks.
                             uint8_t* sf = sq + p.q_bytes;
-                            tma_load_2d_pair(sf, &mapSP, fb, 0, (p0 / 128) * p.k_blocks + kb);
+                            tma_load_2d_pair(sf, &mapSP, fb, 0, (p0 / p.bp) * p.k_blocks + kb);
                             tma_load_2d_pair(sf + 512, &mapSQ, fb, 0,
                                              (tq * p.k_blocks + kb) * p.sf_q_rows);
                         }
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // This stage's packed scales: the P tile's chunk, then
                         // the Q tile's chunks.
                         uint8_t* sf = sq + p.q_bytes;
-                        tma_load_2d(sf, &mapSP, &s.full[stage], 0, (p0 / 128) * p.k_blocks + kb);
+                        tma_load_2d(sf, &mapSP, &s.full[stage], 0, (p0 / p.bp) * p.k_blocks + kb);
                         tma_load_2d(sf + 512, &mapSQ, &s.full[stage], 0,
                                     (tq * p.k_blocks + kb) * p.sf_q_rows);
                     }
@@ -919,9 +919,9 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
         !(p.tmem_cols == 64 || p.tmem_cols == 128 || p.tmem_cols == 256 || p.tmem_cols == 512) ||
         p.tmem_cols / 2 < 32 * ((p.bn + 31) / 32))
         return cudaErrorInvalidValue;
-    // MX: 128-row P tiles, one scale slot per stage in the accumulator halves
-    // past the tile's columns, 1024-aligned stages.
-    if (p.mx && (p.bp != 128 || p.tail_split != 1 || p.sk || p.tmem_cols != 512 ||
+    // MX: one scale slot per stage in the accumulator halves past the tile's
+    // columns, 1024-aligned stages (P tiles of bp rows, packed as such).
+    if (p.mx && (p.tail_split != 1 || p.sk || p.tmem_cols != 512 ||
                  !(p.sf_q_chunks == 1 || p.sf_q_chunks == 2) ||
                  p.sf_q_rows != (p.sf_q_chunks == 2 ? 8 : 1) ||
                  p.sf_cols != 4 + 4 * p.sf_q_chunks || p.sf_col0 < 32 * ((p.bn + 31) / 32) ||

@@ -583,7 +583,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
 // Stream-K plans keep 128 rows (their scratch slots are whole tiles).
 // TPGEMM_TC_BP (64 .. 128, a multiple of 16) overrides where it fits one wave.
 void choose_p_rows(tpg::TcParams& p, int* grid, int max_grid, bool sk_requested) {
-    if (sk_requested || p.mx || p.tiles_q != 1 || p.bp != 128) return;
+    if (sk_requested || p.tiles_q != 1 || p.bp != 128) return;
     const int avail = std::max(1, max_grid / p.mc);
     if (p.num_super > avail) return;
     auto supers = [&](int bp) {
@@ -1115,19 +1115,20 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     }
     if (mx) {
         // Pack both scale matrices into the workspace (ordered before the GEMM
-        // on the same stream): P's in 128-row tiles, Q's in tiles of bn rows.
+        // on the same stream): P's in tiles of bp rows (one chunk, rows past bp
+        // padded), Q's in tiles of bn rows.
         // P's scales are A's in the normal orientation.
         uint32_t* wa = static_cast<uint32_t*>(mx->ws);
         uint32_t* wb = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(mx->ws) +
                                                    mx_ws_b_offset(M, K));
-        const int rows_a = plan.swap ? p.bn : 128, rows_b = plan.swap ? 128 : p.bn;
+        const int rows_a = plan.swap ? p.bn : p.bp, rows_b = plan.swap ? p.bp : p.bn;
         cudaError_t e =
             tpg::launch_mx_pack_scales(mx->SFA, M, rows_a, wa, mx->SFB, N, rows_b, wb, K, st);
         if (e != cudaSuccess)
             return fail(TPGEMM_ERR_LAUNCH, "scale packing launch: %s", cudaGetErrorString(e));
         const uint32_t* sp = plan.swap ? wb : wa;
         const uint32_t* sq = plan.swap ? wa : wb;
-        const uint64_t chunk_rows_p = tpg::mx_packed_bytes(p.Mp, K, 128) / 512;
+        const uint64_t chunk_rows_p = tpg::mx_packed_bytes(p.Mp, K, p.bp) / 512;
         const uint64_t chunk_rows_q = tpg::mx_packed_bytes(p.Nq, K, p.bn) / 512;
         s = encode_u32_rows(enc, &maps.SP, sp, chunk_rows_p, 1, "P scales");
         if (s != TPGEMM_OK) return s;

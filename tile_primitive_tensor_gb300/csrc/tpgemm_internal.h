@@ -118,8 +118,8 @@ struct TcParams {
     // 32 c + r of the chunk for the stage's 4 K blocks (byte b for block b).
     // That is the source layout a tcgen05.cp.32x128b.warpx4 copy spreads so
     // that row m's word sits in tensor-memory column m / 32 of lane m (every
-    // lane quadrant gets the 32 rows' 16 bytes). P tiles are 128 rows (one
-    // chunk), Q tiles bn rows (sf_q_chunks chunks). A tile of more than 128
+    // lane quadrant gets the 32 rows' 16 bytes). P tiles are bp <= 128 rows
+    // (one chunk, rows past bp padded), Q tiles bn rows (sf_q_chunks chunks). A tile of more than 128
     // rows stores each chunk 4 times (mx_reps): rows 32 q + r of that 128-row
     // image are the chunk's row r, so one tcgen05.cp.128x256b writes both
     // chunks to every lane quadrant (each copy holds the tensor pipe about as
