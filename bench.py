@@ -571,6 +571,48 @@ def measure_configs(args, tp, dev, stream, scrub, peaks, src) -> dict:
     return out
 
 
+# Side-by-side (not a target): the same multiplies through torch's cuBLAS GEMM.
+CUBLAS_WORKLOADS = ("gemm_8192_bf16_transB_beta1", "gemm_4096_f16",
+                    "skinny_144x16392x4104_f16_beta1")
+
+
+def measure_cublas(args, dev, stream, peaks, src) -> dict:
+    """Each workload's D = A.B (+ C) through torch.addmm / torch.mm with an f32
+    output (cuBLAS, f16/bf16 in, f32 accumulate), or with a 16-bit output where
+    this torch has no f32-output form; back to back, warm L2."""
+    import torch
+    out = {}
+    n = max(3, args.config_steps)
+    for name in CUBLAS_WORKLOADS:
+        w = wl.BY_NAME[name]
+        A, B, C = (None if t is None else t.to(dev) for t in wl.make_inputs(w))
+        a = A.t() if w.transA else A
+        b = B.t() if w.transB else B
+        form = "f32 out"
+
+        def f32_call():
+            if w.beta:
+                return torch.addmm(C, a, b, out_dtype=torch.float32)
+            return torch.mm(a, b, out_dtype=torch.float32)
+
+        try:
+            f32_call()
+            call = f32_call
+        except (RuntimeError, TypeError):
+            form = "16-bit out, no C (no f32-output form in this torch)"
+            call = lambda: torch.mm(a, b)  # noqa: E731
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        ms = time_back_to_back(call, stream, n) / n
+        e = config_entry(w, ms, peaks, src, f"mean of {n} calls back to back, no L2 flush")
+        e["form"] = f"torch {'addmm' if (w.beta and form == 'f32 out') else 'mm'}, {form}"
+        out[name] = e
+        del A, B, C, a, b
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -619,6 +661,7 @@ def run_ours(args):
     peaks, src = load_peaks()
     configs = None if args.no_configs else measure_configs(args, tp, dev, stream, scrub, peaks,
                                                             src)
+    cublas = None if args.no_configs else measure_cublas(args, dev, stream, peaks, src)
     del scrub
     torch.cuda.empty_cache()
 
@@ -628,7 +671,7 @@ def run_ours(args):
     # multiply has no host-buffer entry point.)
     if isinstance(w, wl.MxWorkload):
         return finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src,
-                           configs, A, B, C, None)
+                           configs, A, B, C, None, cublas)
     lib = tp.library()
     sh = int(stream.cuda_stream)
     pin = lambda t: t.pin_memory()  # noqa: E731
@@ -658,11 +701,11 @@ def run_ours(args):
     e2e = {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
     return finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src, configs,
-                       A, B, C, e2e)
+                       A, B, C, e2e, cublas)
 
 
 def finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src, configs,
-                A, B, C, e2e):
+                A, B, C, e2e, cublas=None):
     """The JSON line: roofline of the (single) kernel of a step, configs, CPU baseline."""
     # ---- roofline of the (single) kernel of a step
     roof = roofline_of(w, launch_ms, peaks, src)
@@ -682,13 +725,15 @@ def finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src
                                        w.algorithmic_bytes > 129e6 else "warm L2 (inputs fit)"),
                    "parallelism": "single GPU"},
         "clocks": clocks,
-        # block-scaled steps launch the two scale-packing kernels before the GEMM
+        # block-scaled steps launch the scale-packing kernel before the GEMM
         "gpu_launches": args.steps * (2 if isinstance(w, wl.MxWorkload) else 1),
         "roofline": roof,
         "e2e": e2e,
     }
     if configs is not None:
         out["configs"] = configs
+    if cublas is not None:
+        out["cublas_side_by_side"] = cublas
     if not args.no_cpu_baseline:
         v, n, el, cores = oracle_sample(w, A, B, C, args.cpu_seconds)
         full = {}

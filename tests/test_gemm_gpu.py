@@ -14,6 +14,7 @@ guard bands around D, and the five workloads at their full sizes (every
 element against the oracle's whole output).
 """
 import dataclasses
+import re
 import itertools
 import os
 import sys
@@ -280,17 +281,26 @@ def test_normal_orientation_mn_contiguous_q(pair, tune):
     ("swapped_large", 1024, 1024, 2048, False, False, 1.0, "1"),
     ("one_cta", 1024, 1024, 2048, False, True, 1.0, "0"),
 ], ids=lambda c: c[0])
-def test_stream_k(case, tune):
-    # Leftover work items split along K across all clusters: partial tiles go
-    # through the scratch slots (chains of several segments per tile here).
+@pytest.mark.parametrize("mode", ["1", "2"])
+def test_stream_k(case, mode, tune):
+    # Leftover work items split along K: partial tiles go through the scratch
+    # slots. Mode 1 spreads their K blocks over all clusters (chains of
+    # several segments per tile here); mode 2 gives each leftover tile two K
+    # halves on two clusters (one hand-off per tile).
     name, M, N, K, tA, tB, beta, pair = case
     tune.setenv("TPGEMM_TC_PAIR", pair)
-    tune.setenv("TPGEMM_TC_SK", "1")
+    tune.setenv("TPGEMM_TC_SK", mode)
     base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
     w = dataclasses.replace(base.with_shape(M, N, K, seed=6370 + M + K), transA=tA, transB=tB,
                             beta=beta, c_dist=("normal", 0.0, 1.0) if beta else None)
     st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
     assert "stream_k=1" in text, text
+    units = re.search(r"units=(\d+)\+(\d+)x", text)
+    grid = int(re.search(r" grid=(\d+)", text).group(1))
+    ncl = grid // (2 if " pair=1" in text else 1)
+    sk_ncl = int(re.search(r"sk_clusters=(\d+)", text).group(1))
+    rem = int(units.group(2))
+    assert sk_ncl == (2 * rem if mode == "2" and 2 * rem <= ncl else ncl), text
     D1 = check_full(w, TC)
     # Deterministic: a second launch (next epoch) gives the same bits.
     (A, B, C), (Ad, Bd, Cd) = device_inputs(w)

@@ -202,8 +202,10 @@ struct Seg {
     int T, q_off, width, kb0, kb1, owner, has_next;
 };
 
-__device__ __forceinline__ int sk_begin(int c, int ncl, const TcParams& p) {
-    return int((int64_t(p.sk_total) * c) / ncl);
+// First stream-K K block of cluster c: the first p.sk_ncl clusters share them
+// evenly; the others get none.
+__device__ __forceinline__ int sk_begin(int c, const TcParams& p) {
+    return c >= p.sk_ncl ? p.sk_total : int((int64_t(p.sk_total) * c) / p.sk_ncl);
 }
 
 // This cluster's segments in order: its whole work units first (U = cid,
@@ -211,7 +213,7 @@ __device__ __forceinline__ int sk_begin(int c, int ncl, const TcParams& p) {
 struct SegIter {
     int U, u, ub;
     __device__ __forceinline__ SegIter(int cid, int ncl, const TcParams& p)
-        : U(cid), u(p.sk ? sk_begin(cid, ncl, p) : 0), ub(p.sk ? sk_begin(cid + 1, ncl, p) : 0) {}
+        : U(cid), u(p.sk ? sk_begin(cid, p) : 0), ub(p.sk ? sk_begin(cid + 1, p) : 0) {}
     __device__ __forceinline__ bool next(int ncl, const TcParams& p, Seg& s) {
         if (U < p.num_units) {
             const Unit un = unit_of(U, p);
@@ -930,6 +932,8 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
                  (p.p_bytes + p.q_bytes + p.sf_bytes) % 1024 != 0))
         return cudaErrorInvalidValue;
     if (!p.mx && p.sf_bytes != 0) return cudaErrorInvalidValue;
+    // Every stream-K K block must belong to a cluster of the grid.
+    if (p.sk && (p.sk_ncl < 1 || p.sk_ncl > grid / p.mc)) return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes(p.stages, p.p_bytes + p.q_bytes + p.sf_bytes, p.epi_bufs);
     if (smem > size_t(kTcMaxSmem)) return cudaErrorInvalidConfiguration;
     auto kernel = pick_kernel(p);

@@ -505,7 +505,10 @@ constexpr size_t kSkWorkspaceBytes = kSkSlotBytes + kSkFlagBytes;
 // us), 8192^3 (696 vs 688 us) and the 144 x 16392 x 4104 shape (37.7 vs
 // 34.2 us), whose K loop already streams at ~91 % of the HBM copy rate; the
 // chained partials lengthen the epilogue and a full grid leaves no idle SMs
-// for the next launch's early start.
+// for the next launch's early start. TPGEMM_TC_SK=2 gives each leftover tile
+// exactly two K halves on two clusters (one partial hand-off per tile): 4096^3
+// 92.3 us against 104.6 with TPGEMM_TC_SK=1 and 90.4 with the tail split
+// (one box, interleaved), so it stays off by default too.
 // *grid is the persistent grid (at most one cluster per work item); max_grid
 // is every cluster the device holds at once. Stream-K runs on max_grid.
 // Whether a plan may use stream-K: as TPGEMM_TC_SK says (default off), always
@@ -522,6 +525,7 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
                       SkMode sk_mode = SkMode::Env) {
     p.sk = 0;
     p.sk_total = 0;
+    p.sk_ncl = 1;
     // Block-scaled plans keep whole 128-wide units (their Q tiles start on the
     // packed scales' 128-row boundaries) and use no stream-K.
     if (p.mx) {
@@ -542,6 +546,9 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
             p.full_units = full;
             p.sk = 1;
             p.sk_total = rem * p.k_blocks;
+            // TPGEMM_TC_SK=2: each leftover tile in exactly two K halves (one
+            // partial hand-off per tile) on 2 rem clusters, where they fit.
+            p.sk_ncl = (tuning().sk == 2 && 2 * rem <= ncl && p.k_blocks >= 2) ? 2 * rem : ncl;
             p.k_rotate = 0;
             p.tail_split = 1;
             p.num_units = p.full_units;
@@ -908,14 +915,15 @@ void format_plan(const Plan& plan, int64_t M, int64_t N, int64_t K, const char* 
              "path=tcgen05 orientation=%s tile=%dx%dx%d umma=%dx%dx%d kind=%s stages=%d "
              "epi_bufs=%d epi_groups=%d producers=%d dep_early=%d k_rotate=%d cluster=%d pair=%d "
              "tmem=%d tiles=%dx%d grid=%d units=%d+%dx%d stream_k=%d scratch=%s p_major=%s "
-             "q_major=%s l2=%d%d%d snake=%d smem=%zu",
+             "q_major=%s l2=%d%d%d snake=%d smem=%zu sk_clusters=%d",
              plan.swap ? "swapped" : "normal", p.bp, p.bn, p.bk, p.pair ? 256 : 128, p.bn,
              p.fp8 ? 32 : 16, p.mx ? "mxf8f6f4" : (p.fp8 ? "f8f6f4" : "f16"), p.stages,
              p.epi_bufs, p.epi_groups,
              p.producers, p.dep_early, p.k_rotate, p.mc, p.pair, p.tmem_cols, p.tiles_p,
              p.tiles_q, plan.grid, p.full_units, p.num_super - p.full_units, p.tail_split, p.sk,
              scratch, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k", p.l2_p, p.l2_q, p.l2_cd, p.snake,
-             tpg::tc_smem_bytes(p.stages, p.p_bytes + p.q_bytes + p.sf_bytes, p.epi_bufs));
+             tpg::tc_smem_bytes(p.stages, p.p_bytes + p.q_bytes + p.sf_bytes, p.epi_bufs),
+             p.sk ? p.sk_ncl : 0);
 }
 
 void copy_text(const char* text, char* buf, int buflen) {

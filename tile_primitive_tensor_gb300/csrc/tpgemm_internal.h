@@ -101,13 +101,16 @@ struct TcParams {
                             // first stage, so the bounded waits expire and the kernel
                             // reports a timeout
     // Stream-K: work items [full_units, num_super) are not given whole to one
-    // cluster; their K blocks (sk_total of them) are divided evenly among all
-    // clusters. A tile's segment holding its last K blocks adds C and writes a
+    // cluster; their K blocks (sk_total of them) are divided evenly among the
+    // first sk_ncl clusters (all of them, or two per leftover tile so that
+    // each is split into two K halves). A tile's segment holding its last K
+    // blocks adds C and writes a
     // partial tile to its CTA's scratch slot; each earlier segment adds the
     // next segment's partial to its accumulator; the segment holding K block 0
     // writes D. Slots are published with per-quadrant epoch flags.
     int sk;                 // 0 / 1
     int sk_total;
+    int sk_ncl;             // clusters sharing the stream-K K blocks (<= the grid's)
     float* sk_ws;           // partial tiles: slot = blockIdx.x (written through mapW)
     uint32_t* sk_flags;     // [gridDim.x][kTcEpiWarps] epoch flags, one per epilogue warp
     uint32_t sk_epoch;      // value of a flag once its slot holds this launch's data
