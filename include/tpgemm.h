@@ -23,10 +23,12 @@
  *   D: [M,N] float32 (written).
  * For tpgemm_gemm all four are device pointers owned by the caller (for
  * tpgemm_gemm_host they are host pointers). The library keeps no pointer to
- * them after a call is enqueued. Its default plans allocate no device memory;
- * the opt-in stream-K mode (environment TPGEMM_TC_SK=1) takes one scratch
- * buffer per (device, stream) with cudaMalloc on first use and keeps it until
- * exit, and tpgemm_gemm_noalloc runs that mode on a static array instead.
+ * them after a call is enqueued. No call allocates device memory for itself,
+ * with one exception: a plan whose last wave is split by K across clusters
+ * (stream-K, on by default where it applies; environment TPGEMM_TC_SK=0 turns
+ * it off) needs an 8 KB array of flags, taken once per (device, stream) with
+ * cudaMalloc on the first such call and kept until exit, so make that call
+ * outside stream capture. tpgemm_gemm_noalloc uses a static array instead.
  *
  * Errors: every function returns a status. Argument errors are detected on the
  * host before anything is enqueued, and a readable reason is available from
@@ -119,28 +121,28 @@ tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const flo
  * (a long-running service that reserves everything at start-up), code inside
  * another allocator's out-of-memory or reclaim path, or a process whose device
  * memory is all held by another framework's pool. Such callers cannot use the
- * stream-K scratch that the library would otherwise cudaMalloc per stream.
+ * stream-K flags that the library would otherwise cudaMalloc per stream.
  *
  * Same arguments, layouts and results as tpgemm_gemm (within the same
  * tolerance; the K-summation order differs). The tcgen05 kernel runs in its
- * stream-K mode whenever the plan has a partial last wave, with its scratch
- * (partial tiles and flags) in one file-scope static device array of
- * TPGEMM_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds
- * until exit. When a problem's stream-K scratch would not fit that array, the
- * call runs the plan that needs no scratch (the last wave split along N, as
- * tpgemm_gemm does by default) instead of failing. tpgemm_last_plan() tells
- * which plan ran ("stream_k=1 scratch=static" for the static array). It calls
- * no cudaMalloc, cudaFree or other allocating routine.
+ * stream-K mode whenever the plan has a partial last wave that fits it (each
+ * leftover tile split into two K halves on two clusters, twice the leftover
+ * tiles at most the grid's clusters), with its flags in one file-scope static
+ * device array of TPGEMM_NOALLOC_SCRATCH_BYTES bytes that every GPU loading
+ * the library holds until exit; otherwise it runs the plan that needs none
+ * (the last wave split along N). tpgemm_last_plan() tells which plan ran
+ * ("stream_k=1 scratch=static" for the static array). It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
  *
  * The first call on a device takes the array's device address
- * (cudaGetSymbolAddress) and zeroes its flag area, synchronising the device;
+ * (cudaGetSymbolAddress) and zeroes it, synchronising the device;
  * make that first call before any stream capture. All calls on a device
  * share the array and it keeps the last call's contents: calls that overlap
  * on the GPU (e.g. on two streams at once) race, so serialise them.
  *
  * Returns as tpgemm_gemm.
  */
-#define TPGEMM_NOALLOC_SCRATCH_BYTES (20u << 20)
+#define TPGEMM_NOALLOC_SCRATCH_BYTES 8192u
 tpgemm_status tpgemm_gemm_noalloc(float* D, const void* A, const void* B, const float* C,
                                   int64_t M, int64_t N, int64_t K, int transA, int transB,
                                   tpgemm_dtype dtype, float beta, void* stream);

@@ -241,9 +241,22 @@ def test_last_plan_before_any_gemm_reports_none():
     assert st == tp.TPGEMM_ERR_NULL and text == ""
 
 
-def test_describe_plan_names_its_scratch(lib):
+def test_describe_plan_names_its_scratch(lib, tune):
+    # 8192^3: 1024 pair tiles on 76 pairs leave 36 for the last wave, each
+    # split into two K halves (stream-K, its flags allocated per stream);
+    # TPGEMM_TC_SK=0 splits them along N instead and needs no scratch.
+    st, text = tp.tpgemm_describe_plan(8192, 8192, 8192, 0, 1, tp.TPGEMM_BF16, 1.0)
+    assert st == tp.TPGEMM_OK and " stream_k=1 scratch=allocated " in text, text
+    assert "units=988+36x1 " in text and "sk_clusters=72" in text, text
+    tune.setenv("TPGEMM_TC_SK", "0")
     st, text = tp.tpgemm_describe_plan(8192, 8192, 8192, 0, 1, tp.TPGEMM_BF16, 1.0)
     assert st == tp.TPGEMM_OK and " stream_k=0 scratch=none " in text, text
+    assert "units=988+36x2 " in text and "sk_clusters=0" in text, text
+    # A short K loop keeps the tail split by default (256^3: 4 K blocks).
+    tune.delenv("TPGEMM_TC_SK")
+    st, text = tp.tpgemm_describe_plan(256, 256, 256, 0, 1, tp.TPGEMM_BF16, 1.0,
+                                       tp.TPGEMM_PATH_TCGEN05)
+    assert st == tp.TPGEMM_OK and " stream_k=0 " in text, text
 
 
 # ------------------------------------------------ block-scaled fp8 (MX) boundary

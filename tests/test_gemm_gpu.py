@@ -237,6 +237,7 @@ def test_tail_wave_split(M, N, pair, tB, tune):
     # N into 2 or 4 narrower units (the plan text shows "units=full+rem x split").
     tune.setenv("TPGEMM_TC_PAIR", pair)
     tune.setenv("TPGEMM_TC_BN", "256")
+    tune.setenv("TPGEMM_TC_SK", "0")  # the tail split, not stream-K
     base = wl.BY_NAME["gemm_8192_bf16_transB_beta1"]
     w = dataclasses.replace(base.with_shape(M, N, 136, seed=6330 + M), transB=tB)
     st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
@@ -281,26 +282,20 @@ def test_normal_orientation_mn_contiguous_q(pair, tune):
     ("swapped_large", 1024, 1024, 2048, False, False, 1.0, "1"),
     ("one_cta", 1024, 1024, 2048, False, True, 1.0, "0"),
 ], ids=lambda c: c[0])
-@pytest.mark.parametrize("mode", ["1", "2"])
-def test_stream_k(case, mode, tune):
-    # Leftover work items split along K: partial tiles go through the scratch
-    # slots. Mode 1 spreads their K blocks over all clusters (chains of
-    # several segments per tile here); mode 2 gives each leftover tile two K
-    # halves on two clusters (one hand-off per tile).
+def test_stream_k(case, tune):
+    # Each leftover work item split into two K halves on two clusters: the
+    # first zeroes the tile's D region at kernel start, both add into it with
+    # TMA reductions (the first with beta.C).
     name, M, N, K, tA, tB, beta, pair = case
     tune.setenv("TPGEMM_TC_PAIR", pair)
-    tune.setenv("TPGEMM_TC_SK", mode)
+    tune.setenv("TPGEMM_TC_SK", "1")
     base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
     w = dataclasses.replace(base.with_shape(M, N, K, seed=6370 + M + K), transA=tA, transB=tB,
                             beta=beta, c_dist=("normal", 0.0, 1.0) if beta else None)
     st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
     assert "stream_k=1" in text, text
-    units = re.search(r"units=(\d+)\+(\d+)x", text)
-    grid = int(re.search(r" grid=(\d+)", text).group(1))
-    ncl = grid // (2 if " pair=1" in text else 1)
-    sk_ncl = int(re.search(r"sk_clusters=(\d+)", text).group(1))
-    rem = int(units.group(2))
-    assert sk_ncl == (2 * rem if mode == "2" and 2 * rem <= ncl else ncl), text
+    rem = int(re.search(r"units=(\d+)\+(\d+)x", text).group(2))
+    assert f"sk_clusters={2 * rem}" in text, text
     D1 = check_full(w, TC)
     # Deterministic: a second launch (next epoch) gives the same bits.
     (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
@@ -314,7 +309,7 @@ def test_stream_k(case, mode, tune):
     ("normal_beta0_one_buf", 1024, 1024, 520, True, True, 0.0, {}),
     ("swapped_beta0", 784, 1320, 264, False, False, 0.0, {"TPGEMM_TC_ORIENT": "swap"}),
     ("odd_bufs_reload", 1024, 1024, 264, False, True, 1.0, {"TPGEMM_TC_EPI_BUFS": "3"}),
-    ("tail_split", 2048, 2560, 136, False, True, 1.0, {"TPGEMM_TC_BN": "256"}),
+    ("tail_split", 2048, 2560, 136, False, True, 1.0, {"TPGEMM_TC_BN": "256", "TPGEMM_TC_SK": "0"}),
     ("stream_k", 1024, 1024, 2048, False, True, 1.0, {"TPGEMM_TC_SK": "1"}),
     ("one_cta", 784, 1320, 264, False, True, 1.0, {"TPGEMM_TC_PAIR": "0"}),
 ], ids=lambda c: c[0])
@@ -580,7 +575,8 @@ def test_p_rows_default_skinny_plan():
 # groups (warps 6..8 produce, then run their epilogue), no CTA pair, stream-K,
 # fp8 and a two-stage ring (P capped at the ring depth).
 @pytest.mark.parametrize("case", [
-    ("multi_wave_tail", "gemm_256_bf16_transB_beta1", 2048, 2560, 264, {"TPGEMM_TC_BN": "256"}),
+    ("multi_wave_tail", "gemm_256_bf16_transB_beta1", 2048, 2560, 264,
+     {"TPGEMM_TC_BN": "256", "TPGEMM_TC_SK": "0"}),
     ("single_wave_two_groups", "skinny_144x16392x4104_f16_beta1", 144, 4104, 520, {}),
     ("no_pair", "gemm_4096_f16", 784, 1320, 264, {"TPGEMM_TC_PAIR": "0"}),
     ("stream_k", "gemm_256_bf16_transB_beta1", 1024, 1024, 2048, {"TPGEMM_TC_SK": "1"}),

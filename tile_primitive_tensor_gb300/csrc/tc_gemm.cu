@@ -66,9 +66,9 @@ __device__ __forceinline__ bool in_bounds(bool ok, int site) {
 #endif
 }
 
-// Stream-K scratch of tpgemm_gemm_noalloc: partial-tile slots, then the epoch
-// flags in its last kStaticScratchFlagBytes. Every GPU that loads the library
-// holds it until exit; all calls of that entry point on a device share it.
+// Stream-K flags of tpgemm_gemm_noalloc (one epoch flag per epilogue warp of
+// each CTA). Every GPU that loads the library holds it until exit; all calls
+// of that entry point on a device share it.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 namespace {
@@ -233,7 +233,17 @@ struct SegIter {
     }
 };
 
-// Bounded wait for a stream-K slot flag to reach this launch's epoch.
+// The cluster whose stream-K share holds K block 0 of leftover tile t (the
+// tile's first segment).
+__device__ __forceinline__ int sk_owner_cluster(int t, const TcParams& p) {
+    const int u0 = t * p.k_blocks;
+    int c = int((int64_t(u0) * p.sk_ncl) / max(1, p.sk_total));
+    while (c + 1 < p.sk_ncl && sk_begin(c + 1, p) <= u0) ++c;
+    while (c > 0 && sk_begin(c, p) > u0) --c;
+    return c;
+}
+
+// Bounded wait for a stream-K flag to reach this launch's epoch.
 __device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t v, volatile int* abort,
                                           uint64_t timeout_ns) {
     if (ld_acquire_gpu(f) == v) return true;
@@ -253,7 +263,7 @@ template <bool SWAP, bool PAIR, bool EARLY, bool MX>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapP, const __grid_constant__ CUtensorMap mapQ,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapD,
-                   const __grid_constant__ CUtensorMap mapQt, const __grid_constant__ CUtensorMap mapW,
+                   const __grid_constant__ CUtensorMap mapQt,
                    const __grid_constant__ CUtensorMap mapPh, const __grid_constant__ CUtensorMap mapCh,
                    const __grid_constant__ CUtensorMap mapDh, const __grid_constant__ CUtensorMap mapSP,
                    const __grid_constant__ CUtensorMap mapSQ, const TcParams p) {
@@ -279,7 +289,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (p.p_mn) prefetch_tensormap(&mapPh);
         prefetch_tensormap(&mapQ);
         if (p.tail_split > 1) prefetch_tensormap(&mapQt);
-        if (p.sk) prefetch_tensormap(&mapW);
         if (MX) {
             prefetch_tensormap(&mapSP);
             prefetch_tensormap(&mapSQ);
@@ -655,6 +664,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Output extents in the kernel's (P, Q) frame, for skipping empty chunks.
         const int lim_p = p.Mp;
         const int lim_q = p.Nq;
+        if (p.sk) {
+            // Stream-K: the leftover tile whose first K blocks this cluster
+            // holds (at most one) gets this warp's part of its D region zeroed
+            // now, under the MMAs of the whole units, and a flag published
+            // once the zeros are written; every segment of the tile then adds
+            // its accumulator into D with a TMA reduction.
+            SegIter pre(cid, ncl, p);
+            Seg v;
+            while (pre.next(ncl, p, v)) {
+                if (!(v.owner && v.has_next)) continue;
+                int tps, tq;
+                tile_coords(v.T, p, tps, tq);
+                const int pw = (tps * MC + rank) * p.bp + quad * 32;
+                const int q0 = tq * p.bn + v.q_off;
+                const int q_lanes = min(32, p.bp - quad * 32);
+                const int live = (pw < lim_p && q_lanes > 0)
+                                     ? min((v.width + 31) / 32, (lim_q - q0 + 31) / 32)
+                                     : 0;
+                const int my_chunks = live > half ? (live - half + ng - 1) / ng : 0;
+                if (my_chunks == 0) break;
+                const CUtensorMap* dmap = q_lanes == 16 ? &mapDh : &mapD;
+                float4* z = reinterpret_cast<float4*>(bufs);
+                for (int k = lane; k < kEpiBufFloats / 4; k += 32)
+                    z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int j = 0; j < my_chunks; ++j) {
+                        const int c = ng * j + half;
+                        const int x = SWAP ? pw : q0 + 32 * c;
+                        const int y = SWAP ? q0 + 32 * c : pw;
+                        if (in_bounds(x >= 0 && y >= 0 && x % 4 == 0, kSiteStore))
+                            tma_store_2d(dmap, bufs, x, y);
+                    }
+                    bulk_commit_group();
+                    bulk_wait_group<0>();  // written, not just read
+                    fence_proxy_async_global();
+                    if (in_bounds(int(blockIdx.x) * kEpiWarps + ew < kTcMaxFlagSlots * kEpiWarps,
+                                  kSiteFlag))
+                        st_release_gpu(&p.sk_flags[blockIdx.x * kEpiWarps + ew], p.sk_epoch);
+                }
+                __syncwarp();
+                break;
+            }
+        }
         int it = 0;
         SegIter iter(cid, ncl, p);
         Seg u;
@@ -674,54 +728,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (warp_live) live_chunks = min(nchunks, (lim_q - q0 + 31) / 32);
             // This warp's chunks: c = ng j + half for j < my_chunks.
             const int my_chunks = live_chunks > half ? (live_chunks - half + ng - 1) / ng : 0;
-            // Where chunk c's 32 x 32 box comes from (C, or the next stream-K
-            // segment's scratch slot) and goes to (D, or this CTA's slot).
-            // D / C boxes: (x = column, y = row) of D; slot boxes: the same
-            // tile layout, rows offset by the slot index.
-            const bool to_slot = !u.owner;
-            const bool from_slot = u.has_next;
-            const bool add_src = from_slot || p.beta;
-            const int src_slot = (cid + 1) * MC + rank;
-            const int dst_slot = int(blockIdx.x);
-            const int qw = quad * 32;
+            // Stream-K: a tile split into K segments gets its D region zeroed
+            // by its first segment (the owner, which also adds C), and every
+            // segment adds its accumulator into D with a TMA reduction; two
+            // or more f32 addends onto zero, so the order of the reductions
+            // does not matter when there are two. The owner publishes a flag
+            // once its zeros are written; the others wait for it before their
+            // first reduction.
+            const bool split = !(u.owner && !u.has_next);
+            const bool add_src = p.beta && u.owner;
+            const int owner_block =
+                (u.owner ? cid : sk_owner_cluster(u.T - p.full_units, p)) * MC + rank;
             auto box_x = [&](int c) { return SWAP ? pw : q0 + 32 * c; };
             auto box_y = [&](int c) { return SWAP ? q0 + 32 * c : pw; };
-            auto slot_x = [&](int c) { return SWAP ? qw : 32 * c; };
-            auto slot_y = [&](int slot, int c) {
-                return slot * p.sk_slot_rows + (SWAP ? 32 * c : qw);
-            };
-            // Stream-K plans keep bp = 128, so a half quadrant never uses a slot.
-            const CUtensorMap* src_map = from_slot ? &mapW : (half_q ? &mapCh : &mapC);
-            const CUtensorMap* dst_map = to_slot ? &mapW : (half_q ? &mapDh : &mapD);
+            // D / C boxes: (x = column, y = row) of D.
+            const CUtensorMap* src_map = half_q ? &mapCh : &mapC;
+            const CUtensorMap* dst_map = half_q ? &mapDh : &mapD;
             const uint32_t src_bytes = half_q ? kEpiBufFloats * 2 : kEpiBufFloats * 4;
-            auto src_x = [&](int c) { return from_slot ? slot_x(c) : box_x(c); };
-            auto src_y = [&](int c) { return from_slot ? slot_y(src_slot, c) : box_y(c); };
-            auto dst_x = [&](int c) { return to_slot ? slot_x(c) : box_x(c); };
-            auto dst_y = [&](int c) { return to_slot ? slot_y(dst_slot, c) : box_y(c); };
+            auto src_x = [&](int c) { return box_x(c); };
+            auto src_y = [&](int c) { return box_y(c); };
+            auto dst_x = [&](int c) { return box_x(c); };
+            auto dst_y = [&](int c) { return box_y(c); };
 
             // All staging buffers free: every earlier store has read its source.
             if (lane == 0) bulk_wait_group_read<0>();
-            // The next segment's partial must be published before it is read.
-            if (from_slot && my_chunks > 0) {
-                bool fok = true;
-                if (lane == 0) {
-                    fok = in_bounds(src_slot * kEpiWarps + ew < kTcMaxFlagSlots * kEpiWarps,
-                                    kSiteFlag) &&
-                          wait_flag(&p.sk_flags[src_slot * kEpiWarps + ew], p.sk_epoch, s.abort, tmo);
-                    fence_proxy_async_global();
-                }
-                fok = __shfl_sync(0xffffffffu, fok ? 1 : 0, 0) != 0;
-                if (!fok) break;
-            }
-            // Prefetch the source (C or the partial) for the first chunks (all
-            // of them when they fit the staging buffers) while the MMAs run.
+            // Prefetch C for the first chunks (all of them when they fit the
+            // staging buffers) while the MMAs run.
             if (add_src) {
                 for (int j = 0; j < nbw && j < my_chunks; ++j) {
                     const int c = ng * j + half;
                     if (lane == 0 && in_bounds(src_x(c) % 4 == 0, kSiteLoadC)) {
                         mbar_arrive_expect_tx(&cb[j], src_bytes);
                         tma_load_2d_hint(bufs + j * kEpiBufFloats, src_map, &cb[j], src_x(c),
-                                         src_y(c), from_slot ? l2_policy(0) : pol_cd);
+                                         src_y(c), pol_cd);
                     }
                     cpend |= 1u << j;
                 }
@@ -732,6 +771,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = wait_phase(&s.acc_full[b], acc_phase, s.abort, tmo);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
+            if (split && !u.owner && my_chunks > 0) {
+                // The owner's zeros are in D before this segment adds to it.
+                bool fok = true;
+                if (lane == 0) {
+                    fok = in_bounds(owner_block * kEpiWarps + ew < kTcMaxFlagSlots * kEpiWarps,
+                                    kSiteFlag) &&
+                          wait_flag(&p.sk_flags[owner_block * kEpiWarps + ew], p.sk_epoch, s.abort,
+                                    tmo);
+                    fence_proxy_async_global();
+                }
+                ok = __shfl_sync(0xffffffffu, fok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+            }
             tc_fence_after_sync();
             const uint32_t acc_col = uint32_t(b * acc_stride);
             // This warp's j-th chunk (column chunk c = ng j + half): its
@@ -798,15 +850,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __syncwarp();
                 if (lane == 0 && in_bounds(dst_x(c) >= 0 && dst_y(c) >= 0 && dst_x(c) % 4 == 0,
                                            kSiteStore)) {
-                    tma_store_2d_hint(dst_map, buf, dst_x(c), dst_y(c),
-                                      to_slot ? l2_policy(0) : pol_cd);
+                    if (split)
+                        tma_reduce_add_2d(dst_map, buf, dst_x(c), dst_y(c));
+                    else
+                        tma_store_2d_hint(dst_map, buf, dst_x(c), dst_y(c), pol_cd);
                     bulk_commit_group();
                     if (add_src && j + nbw < my_chunks) {
                         const int cn = c + ng * nbw;  // this warp's chunk j + nbw
                         bulk_wait_group_read<0>();  // the store just issued has read buf
                         mbar_arrive_expect_tx(&cb[bi], src_bytes);
-                        tma_load_2d_hint(buf, src_map, &cb[bi], src_x(cn), src_y(cn),
-                                         from_slot ? l2_policy(0) : pol_cd);
+                        tma_load_2d_hint(buf, src_map, &cb[bi], src_x(cn), src_y(cn), pol_cd);
                     }
                 }
                 if (add_src && j + nbw < my_chunks) cpend |= 1u << bi;
@@ -834,14 +887,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive_cluster(mapa_shared(smem_u32(&s.acc_empty[b]), 0));
                 else
                     mbar_arrive(&s.acc_empty[b]);
-            }
-            // A partial written to this CTA's slot is published once its bulk
-            // stores have completed (not just read their shared source).
-            if (ok && to_slot && lane == 0 &&
-                in_bounds(dst_slot * kEpiWarps + ew < kTcMaxFlagSlots * kEpiWarps, kSiteFlag)) {
-                bulk_wait_group<0>();
-                fence_proxy_async_global();
-                st_release_gpu(&p.sk_flags[dst_slot * kEpiWarps + ew], p.sk_epoch);
             }
             if (!ok) break;
         }
@@ -882,7 +927,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                             CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
-                            CUtensorMap, TcParams);
+                            TcParams);
 
 template <bool EARLY>
 TcKernelFn pick_kernel_dep(const TcParams& p) {
@@ -957,7 +1002,7 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.mc > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, maps.Qt, maps.W, maps.Ph,
+    return cudaLaunchKernelEx(&cfg, kernel, maps.P, maps.Q, maps.C, maps.D, maps.Qt, maps.Ph,
                               maps.Ch, maps.Dh, maps.SP, maps.SQ, p);
 }
 
@@ -995,8 +1040,7 @@ cudaError_t tc_static_scratch(void** ptr) {
         void* a = nullptr;
         e = cudaGetSymbolAddress(&a, g_static_scratch);
         if (e != cudaSuccess) return e;
-        e = cudaMemset(static_cast<unsigned char*>(a) + kStaticScratchBytes - kStaticScratchFlagBytes,
-                       0, kStaticScratchFlagBytes);
+        e = cudaMemset(a, 0, kStaticScratchBytes);
         if (e != cudaSuccess) return e;
         e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return e;

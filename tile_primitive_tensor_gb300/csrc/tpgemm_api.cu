@@ -486,40 +486,38 @@ tpgemm_status plan_tc(int64_t M, int64_t N, int64_t K, bool transA, bool transB,
 // 4 narrower units (as many as still fit one wave), so the wave takes half or
 // a quarter of the time. A unit stays a whole number of 32-column chunks and
 // each CTA's share of it whole 8-row groups (K-contiguous Q) or 16-row steps.
-// Stream-K scratch: one partial-tile slot per CTA (128 x bn fp32, bn rounded
-// up to 32) and one epoch flag per epilogue warp of each CTA. Sized for the
-// largest plan.
+// Stream-K flags: one epoch flag per epilogue warp of each CTA, sized for the
+// largest grid.
 constexpr int kSkMaxGrid = tpg::kTcMaxFlagSlots;
-constexpr size_t kSkSlotFloats = size_t(128) * 256;
-constexpr size_t kSkSlotBytes = kSkMaxGrid * kSkSlotFloats * sizeof(float);
 constexpr size_t kSkFlagBytes = kSkMaxGrid * tpg::kTcEpiWarps * sizeof(uint32_t);
-constexpr size_t kSkWorkspaceBytes = kSkSlotBytes + kSkFlagBytes;
 
-// Balance the last, partial wave of the persistent grid by splitting the
-// leftover tiles along Q into 2 or 4 narrower units (as many as still fit one
-// wave). A unit stays a whole number of 32-column chunks and each CTA's share
-// of it whole 8-row groups (K-contiguous Q) or 16-row steps.
-// Stream-K (TPGEMM_TC_SK=1) instead divides the leftover work items' K blocks
-// evenly among all clusters when each gets at least 4. It is correct and
-// tested but off by default: measured slower on GB300 for 4096^3 (108 vs 98
-// us), 8192^3 (696 vs 688 us) and the 144 x 16392 x 4104 shape (37.7 vs
-// 34.2 us), whose K loop already streams at ~91 % of the HBM copy rate; the
-// chained partials lengthen the epilogue and a full grid leaves no idle SMs
-// for the next launch's early start. TPGEMM_TC_SK=2 gives each leftover tile
-// exactly two K halves on two clusters (one partial hand-off per tile): 4096^3
-// 92.3 us against 104.6 with TPGEMM_TC_SK=1 and 90.4 with the tail split
-// (one box, interleaved), so it stays off by default too.
+// Balance the last, partial wave of the persistent grid. Stream-K: each
+// leftover tile is split into two K halves on two clusters (when twice the
+// leftover tiles fit the grid), the halves adding their accumulators into D
+// with TMA reductions onto zeros written at kernel start. Measured on GB300,
+// 4096^3 f16: 84.2 us against 88.5 with the tail split below (one box,
+// interleaved). The tail split instead divides the leftover tiles along Q
+// into 2 or 4 narrower units (as many as still fit one wave); a narrower MMA
+// takes about as long per instruction, so a half-width unit takes about as
+// long as a whole one (0.94 of it at 4096^3). A unit stays a whole number of
+// 32-column chunks and each CTA's share of it whole 8-row groups (K-contiguous
+// Q) or 16-row steps.
 // *grid is the persistent grid (at most one cluster per work item); max_grid
 // is every cluster the device holds at once. Stream-K runs on max_grid.
-// Whether a plan may use stream-K: as TPGEMM_TC_SK says (default off), always
-// (the static scratch of tpgemm_gemm_noalloc), or never (its fallback when the
-// stream-K scratch would not fit that array).
+// Whether a plan may use stream-K: by default (TPGEMM_TC_SK=0 turns it off),
+// always (the static flags of tpgemm_gemm_noalloc), or never.
 enum class SkMode { Env, Force, Off };
 
 bool stream_k_requested(SkMode m) {
     if (m != SkMode::Env) return m == SkMode::Force;
-    return tuning().sk > 0;
+    return tuning().sk != 0;  // on unless TPGEMM_TC_SK=0
 }
+
+// Fewest K blocks per tile for the default stream-K plans: the first half's
+// zero-fill, the flag and the reductions cost a few microseconds, which a
+// short K loop would not win back. TPGEMM_TC_SK=1 and the static flags of
+// tpgemm_gemm_noalloc take any split (two blocks at least).
+constexpr int kSkMinKBlocks = 16;
 
 void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
                       SkMode sk_mode = SkMode::Env) {
@@ -540,21 +538,19 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
         const int ncl = std::max(1, max_grid / p.mc);
         const int full = (p.num_super / ncl) * ncl;
         const int rem = p.num_super - full;
-        if (sk_on && rem > 0 && max_grid <= kSkMaxGrid &&
-            int64_t(rem) * p.k_blocks >= int64_t(4) * ncl) {
+        const int min_kb = (sk_mode == SkMode::Env && tuning().sk < 0) ? kSkMinKBlocks : 2;
+        if (sk_on && rem > 0 && 2 * rem <= ncl && max_grid <= kSkMaxGrid &&
+            p.k_blocks >= min_kb) {
             *grid = ncl * p.mc;
             p.full_units = full;
             p.sk = 1;
             p.sk_total = rem * p.k_blocks;
-            // TPGEMM_TC_SK=2: each leftover tile in exactly two K halves (one
-            // partial hand-off per tile) on 2 rem clusters, where they fit.
-            p.sk_ncl = (tuning().sk == 2 && 2 * rem <= ncl && p.k_blocks >= 2) ? 2 * rem : ncl;
+            p.sk_ncl = 2 * rem;
             p.k_rotate = 0;
             p.tail_split = 1;
             p.num_units = p.full_units;
             p.idesc_tail = p.idesc;
             p.q_box_rows = p.pair ? p.bn / 2 : p.bn;
-            p.sk_slot_rows = p.swap ? 32 * ((p.bn + 31) / 32) : 128;
             return;
         }
     }
@@ -587,10 +583,9 @@ void apply_tail_split(tpg::TcParams& p, int* grid, int max_grid, bool code1,
 // 128 -> 152 SMs streaming the same bytes each took 33.9 -> 35.8 us for 19 %
 // more data), so it gives each CTA fewer P rows and uses more SMs: the
 // smallest bp of 64 .. 112 (steps of 16) whose tiles still fit one wave.
-// Stream-K plans keep 128 rows (their scratch slots are whole tiles).
 // TPGEMM_TC_BP (64 .. 128, a multiple of 16) overrides where it fits one wave.
-void choose_p_rows(tpg::TcParams& p, int* grid, int max_grid, bool sk_requested) {
-    if (sk_requested || p.tiles_q != 1 || p.bp != 128) return;
+void choose_p_rows(tpg::TcParams& p, int* grid, int max_grid) {
+    if (p.tiles_q != 1 || p.bp != 128) return;
     const int avail = std::max(1, max_grid / p.mc);
     if (p.num_super > avail) return;
     auto supers = [&](int bp) {
@@ -701,24 +696,22 @@ struct SkWorkspace {
 std::mutex g_sk_mutex;
 std::map<std::pair<int, cudaStream_t>, SkWorkspace> g_sk;
 
-tpgemm_status stream_k_workspace(cudaStream_t st, float** slots, uint32_t** flags,
-                                 uint32_t* epoch) {
+tpgemm_status stream_k_workspace(cudaStream_t st, uint32_t** flags, uint32_t* epoch) {
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(g_sk_mutex);
     SkWorkspace& w = g_sk[std::make_pair(dev, st)];
     if (!w.base) {
         void* b = nullptr;
-        cudaError_t e = cudaMalloc(&b, kSkWorkspaceBytes);
+        cudaError_t e = cudaMalloc(&b, kSkFlagBytes);
         if (e != cudaSuccess)
-            return fail(TPGEMM_ERR_LAUNCH, "stream-K scratch allocation: %s", cudaGetErrorString(e));
-        e = cudaMemset(static_cast<uint8_t*>(b) + kSkSlotBytes, 0, kSkFlagBytes);
+            return fail(TPGEMM_ERR_LAUNCH, "stream-K flag allocation: %s", cudaGetErrorString(e));
+        e = cudaMemset(b, 0, kSkFlagBytes);
         if (e != cudaSuccess)
-            return fail(TPGEMM_ERR_LAUNCH, "stream-K scratch init: %s", cudaGetErrorString(e));
+            return fail(TPGEMM_ERR_LAUNCH, "stream-K flag init: %s", cudaGetErrorString(e));
         w.base = b;
     }
-    *slots = static_cast<float*>(w.base);
-    *flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(w.base) + kSkSlotBytes);
+    *flags = static_cast<uint32_t*>(w.base);
     *epoch = ++w.epoch;
     if (w.epoch == 0) *epoch = ++w.epoch;  // 0 is the flags' initial value
     return TPGEMM_OK;
@@ -863,7 +856,7 @@ tpgemm_status finish_tc_plan(Plan* plan, tpgemm_dtype dtype, SkMode sk_mode) {
     if (plan->kernel != Kernel::Tc) return TPGEMM_OK;
     tpgemm_status s = fit_grid(plan);
     if (s != TPGEMM_OK) return s;
-    choose_p_rows(plan->tc, &plan->grid, plan->max_grid, stream_k_requested(sk_mode));
+    choose_p_rows(plan->tc, &plan->grid, plan->max_grid);
     apply_tail_split(plan->tc, &plan->grid, plan->max_grid, format_code(dtype), sk_mode);
     choose_epi_groups(plan->tc, plan->grid);
     choose_producers(plan->tc, plan->grid);
@@ -871,16 +864,11 @@ tpgemm_status finish_tc_plan(Plan* plan, tpgemm_dtype dtype, SkMode sk_mode) {
     return TPGEMM_OK;
 }
 
-// Bytes of the static array a stream-K plan uses: one partial-tile slot per
-// CTA (laid out like a D tile, 32-column chunks) and the flag area at its end.
-// Plans with more CTAs than the flag area has rows for never fit.
+// Bytes of the static array a stream-K plan uses: one flag per epilogue warp
+// of each CTA. Plans with more CTAs than the array has rows for never fit.
 size_t static_scratch_need(const Plan& plan) {
-    const tpg::TcParams& p = plan.tc;
-    if (plan.grid > int(tpg::kStaticScratchFlagBytes / (tpg::kTcEpiWarps * sizeof(uint32_t))))
-        return ~size_t(0);
-    return size_t(plan.grid) * size_t(p.sk_slot_rows) *
-               size_t(p.swap ? 128 : 32 * ((p.bn + 31) / 32)) * sizeof(float) +
-           tpg::kStaticScratchFlagBytes;
+    if (plan.grid > tpg::kTcMaxFlagSlots) return ~size_t(0);
+    return size_t(plan.grid) * tpg::kTcEpiWarps * sizeof(uint32_t);
 }
 
 // The calling thread's last launched plan (tpgemm_last_plan).
@@ -1060,16 +1048,15 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
         if (s != TPGEMM_OK) return s;
     }
     if (p.sk) {
-        // Slots laid out like D tiles: [128 rows][bn32 cols] (normal) or
-        // [bn32 rows][128 cols] (swapped), one per CTA, stacked along rows.
+        // The epoch flags of the first segments' zero-fills.
         if (scratch == Scratch::Static) {
-            // No allocation: slots at the start of the static array, flags at
-            // its end; the plan must fit, else the call is refused.
+            // No allocation: the static flag array; the plan must fit, else
+            // the call is refused.
             const size_t need = static_scratch_need(plan);
             if (need > tpg::kStaticScratchBytes)
                 return fail(TPGEMM_ERR_SHAPE,
-                            "internal: stream-K scratch for this plan needs %zu bytes; the static "
-                            "scratch holds %zu",
+                            "internal: stream-K flags for this plan need %zu bytes; the static "
+                            "array holds %zu",
                             need, tpg::kStaticScratchBytes);
             void* base = nullptr;
             cudaError_t e = tpg::tc_static_scratch(&base);
@@ -1083,20 +1070,12 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
                 epoch = ++g_static_epoch[dev];
                 if (epoch == 0) epoch = ++g_static_epoch[dev];
             }
-            plan.tc.sk_ws = static_cast<float*>(base);
-            plan.tc.sk_flags = reinterpret_cast<uint32_t*>(
-                static_cast<uint8_t*>(base) + tpg::kStaticScratchBytes - tpg::kStaticScratchFlagBytes);
+            plan.tc.sk_flags = static_cast<uint32_t*>(base);
             plan.tc.sk_epoch = epoch;
         } else {
-            s = stream_k_workspace(st, &plan.tc.sk_ws, &plan.tc.sk_flags, &plan.tc.sk_epoch);
+            s = stream_k_workspace(st, &plan.tc.sk_flags, &plan.tc.sk_epoch);
             if (s != TPGEMM_OK) return s;
         }
-        const uint64_t bn32 = uint64_t(32 * ((p.bn + 31) / 32));
-        const uint64_t cols = p.swap ? 128 : bn32;
-        const uint64_t rows = uint64_t(plan.grid) * uint64_t(p.sk_slot_rows);
-        s = encode_2d(enc, &maps.W, p.sk_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, cols, rows, 32, 32,
-                      "stream-K scratch");
-        if (s != TPGEMM_OK) return s;
     }
     s = encode_2d(enc, &maps.D, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, uint64_t(N), uint64_t(M), 32,
                   32, "D");
@@ -1450,7 +1429,7 @@ tpgemm_status tpgemm_describe_plan(int64_t M, int64_t N, int64_t K, int transA, 
     if (plan.kernel == Kernel::Tc) {
         // As tpgemm_gemm plans it, except that the grid is one CTA (pair) per
         // SM without the device's cluster-occupancy query.
-        choose_p_rows(plan.tc, &plan.grid, plan.max_grid, stream_k_requested(SkMode::Env));
+        choose_p_rows(plan.tc, &plan.grid, plan.max_grid);
         apply_tail_split(plan.tc, &plan.grid, plan.max_grid, format_code(dtype));
         choose_epi_groups(plan.tc, plan.grid);
         choose_producers(plan.tc, plan.grid);

@@ -101,20 +101,17 @@ struct TcParams {
                             // first stage, so the bounded waits expire and the kernel
                             // reports a timeout
     // Stream-K: work items [full_units, num_super) are not given whole to one
-    // cluster; their K blocks (sk_total of them) are divided evenly among the
-    // first sk_ncl clusters (all of them, or two per leftover tile so that
-    // each is split into two K halves). A tile's segment holding its last K
-    // blocks adds C and writes a
-    // partial tile to its CTA's scratch slot; each earlier segment adds the
-    // next segment's partial to its accumulator; the segment holding K block 0
-    // writes D. Slots are published with per-quadrant epoch flags.
+    // cluster; each is split into two K halves (their K blocks, sk_total of
+    // them, divided evenly among the first sk_ncl = 2 x leftover clusters).
+    // The first half's cluster zeroes the tile's D region at kernel start and
+    // publishes per-warp epoch flags; both halves then add their accumulators
+    // (the first with beta.C) into D with TMA reductions, after the flag. Two
+    // f32 addends onto zero give the same bits in either order.
     int sk;                 // 0 / 1
     int sk_total;
     int sk_ncl;             // clusters sharing the stream-K K blocks (<= the grid's)
-    float* sk_ws;           // partial tiles: slot = blockIdx.x (written through mapW)
     uint32_t* sk_flags;     // [gridDim.x][kTcEpiWarps] epoch flags, one per epilogue warp
-    uint32_t sk_epoch;      // value of a flag once its slot holds this launch's data
-    int sk_slot_rows;       // rows of one slot in mapW's frame (128, or bn rounded to 32)
+    uint32_t sk_epoch;      // value of a flag once its zeros are written in this launch
     // Block-scaled fp8 (kind::mxf8f6f4, one E8M0 scale per 32 K). The scales
     // are packed by mx_pack_scales per (tile, 128-element K stage, 128-row
     // chunk of the tile) into 512 bytes: word 4 r + c holds the 4 scales of row
@@ -154,7 +151,6 @@ struct TcMaps {
     CUtensorMap Ph;         // MN-contiguous P: box of P rows 64 .. bp - 1 of a tile
     CUtensorMap Ch, Dh;     // C / D with a half-quadrant box (16 tensor-memory lanes)
     CUtensorMap Qt;         // Q with the (narrower) box of a tail unit
-    CUtensorMap W;          // stream-K scratch slots, laid out like D tiles
     CUtensorMap SP, SQ;     // packed scales of P / Q (block-scaled plans): 128 words x
                             // one chunk per row; boxes of 1 / sf_q_rows rows
 };
@@ -175,11 +171,11 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
 // persistent grid is this many clusters at most).
 cudaError_t tc_max_active_clusters(const TcParams& p, int* clusters);
 
-// Static stream-K scratch (no allocation): its size, the flag area at its end,
-// and its device address on the current device (taken on first use there).
-constexpr size_t kStaticScratchBytes = size_t(20) << 20;
+// Static stream-K flags (no allocation): one epoch flag per epilogue warp of
+// up to kTcMaxFlagSlots CTAs, and its device address on the current device
+// (taken on first use there).
 constexpr int kTcMaxFlagSlots = 256;  // CTAs a stream-K flag area (allocated or static) covers
-constexpr size_t kStaticScratchFlagBytes = size_t(kTcMaxFlagSlots) * kTcEpiWarps * sizeof(uint32_t);
+constexpr size_t kStaticScratchBytes = size_t(kTcMaxFlagSlots) * kTcEpiWarps * sizeof(uint32_t);
 constexpr int kMaxStaticScratchDevices = 64;
 cudaError_t tc_static_scratch(void** ptr);
 
