@@ -231,6 +231,10 @@ struct SegIter {
         }
         return false;
     }
+    // Whether a later call of next() would return a segment.
+    __device__ __forceinline__ bool more(const TcParams& p) const {
+        return U < p.num_units || u < ub;
+    }
 };
 
 // The cluster whose stream-K share holds K block 0 of leftover tile t (the
@@ -790,9 +794,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // accumulator registers `cur` were loaded by the previous step; the
             // next chunk's tcgen05.ld is issued into `nxt` before this one's
             // shared-memory work so the two overlap.
+            // This CTA's last unit, with no source to load: once its MMAs are
+            // done (acc_full, which in a pair also covers the leader's reads
+            // of this CTA's half) no fill or MMA touches the TMA ring again,
+            // so D is staged through the ring, one buffer per chunk, and no
+            // chunk waits for an earlier store to have read its buffer.
+            int snbw = nbw;
+            if (!add_src && !iter.more(p)) {
+                const int per_warp =
+                    int((uint32_t(p.stages) * (p.p_bytes + p.q_bytes + p.sf_bytes)) /
+                        (uint32_t(kEpiQuads * ng) * uint32_t(kEpiBufFloats * sizeof(float))));
+                if (per_warp >= my_chunks && my_chunks > nbw) {
+                    snbw = my_chunks;
+                    bufs = reinterpret_cast<float*>(s.stages) + ew * per_warp * kEpiBufFloats;
+                }
+            }
             auto chunk = [&](int j, uint32_t (&cur)[32], uint32_t (&nxt)[32]) -> bool {
                 const int c = ng * j + half;
-                const int bi = j % nbw;
+                const int bi = j % snbw;
                 float* buf = bufs + bi * kEpiBufFloats;
                 tmem_ld_wait(cur);
                 if (j + 1 < my_chunks &&
@@ -809,10 +828,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     cphase ^= 1u << bi;
                     cpend &= ~(1u << bi);
-                } else {
+                } else if (j >= snbw) {
                     // The store that last used buf (this warp's chunk j - nbw) has read it.
                     if (lane == 0) {
-                        if (nbw == 1)
+                        if (snbw == 1)
                             bulk_wait_group_read<0>();
                         else
                             bulk_wait_group_read<1>();
