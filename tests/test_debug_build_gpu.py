@@ -92,6 +92,39 @@ def test_debug_build_stream_k(dbg, monkeypatch):
         dbg.tpgemm_reload_tuning()
 
 
+def test_debug_build_stream_k_default_swapped(dbg):
+    # The default two-half split of a single partial wave in the swapped
+    # orientation with beta = 0 (the layout of the 4096^3 workload): the
+    # kernel-start zero-fill, the flag waits, the TMA reductions and the
+    # ring-staged last epilogue, every index checked.
+    w = wl.BY_NAME["gemm_4096_f16"].with_shape(1024, 1024, 2048, seed=955)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+    assert "orientation=swapped" in text and "stream_k=1" in text, text
+    check(dbg, w)
+
+
+def test_debug_build_block_scaled(dbg):
+    w = wl.BY_NAME["mx_8192_e4m3_transB_beta1"].with_shape(784, 1320, 528, seed=958)
+    A, B, C = wl.make_inputs(w)
+    SFA, SFB = wl.make_scales(w)
+    t = [x.cuda() for x in (A, B, C, SFA, SFB)]
+    D = torch.full((w.M, w.N), float("nan"), device="cuda")
+    wsb = int(dbg.tpgemm_gemm_mx_workspace_bytes(w.M, w.N, w.K))
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    st = dbg.tpgemm_gemm_mx(D.data_ptr(), t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(),
+                            t[3].data_ptr(), t[4].data_ptr(), w.M, w.N, w.K, w.dtype,
+                            float(w.beta), ws.data_ptr(), wsb, None)
+    assert st == tp.TPGEMM_OK, dbg.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    st, why = status(dbg)
+    assert st == tp.TPGEMM_OK, why
+    Dref, S = oracle.gemm_mx(wl.operand_bits(w, A), wl.operand_bits(w, B), C.numpy(),
+                             SFA.numpy(), SFB.numpy(), w.M, w.N, w.K, w.transA, w.transB,
+                             w.dtype, w.beta)
+    ok, msg = oracle.compare(D.cpu().numpy(), Dref, S)
+    assert ok, msg
+
+
 def test_planted_bad_column_is_caught_and_skipped(dbg, monkeypatch):
     # The plant moves the epilogue's first tensor-memory load past the
     # allocation; the check reports it and the load is skipped.
