@@ -383,6 +383,24 @@ def test_in_place_d_equals_c(path):
     assert ok, msg
 
 
+def test_in_place_takes_the_n_split_not_stream_k():
+    # 1024^2 x 2048 (16 pair tiles, one partial wave) would split each tile
+    # into two K halves whose first zeroes D at kernel start; in place (D ==
+    # C) that would erase C, so the call takes the split along N and the
+    # result still matches the oracle. The same shape out of place runs
+    # stream-K.
+    w = wl.BY_NAME["gemm_256_bf16_transB_beta1"].with_shape(1024, 1024, 2048, seed=6510)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert "stream_k=1" in text, text
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+    D = run_gpu(w, Ad, Bd, Cd, TC, D=Cd)
+    st, plan = tp.tpgemm_last_plan()
+    assert "stream_k=0" in plan, plan
+    Dref, S = oracle_full(w, A, B, C)
+    ok, msg = oracle.compare(D, Dref, S)
+    assert ok, msg
+
+
 @pytest.mark.parametrize("path", [MMA, TC])
 def test_identity_bit_exact_real_data(path):
     # A = I  =>  D = fp32(B) exactly, for any real B (the oracle pin, now on the GPU).

@@ -661,8 +661,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint64_t* cb = es.cb;
         const uint32_t lane_base = uint32_t(quad * 32) << 16;
         // C is read once and D written once: their lines should not push the
-        // operand panels that later tiles reuse out of L2. Stream-K partial
-        // tiles are re-read, so they keep the normal policy.
+        // operand panels that later tiles reuse out of L2. (A stream-K tile's
+        // zeros, which its reductions read back, keep the normal policy.)
         const uint64_t pol_cd = l2_policy(p.l2_cd);
 
         // Output extents in the kernel's (P, Q) frame, for skipping empty chunks.

@@ -1011,7 +1011,12 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     const tpg::TcParams& p = plan.tc;
     tpg::TcMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    const SkMode sk_mode = scratch == Scratch::Static ? SkMode::Force : SkMode::Env;
+    // In place (D == C with beta = 1): stream-K's first half zeroes its tile
+    // of D at kernel start, which here would erase C before it is read, so
+    // those calls take the split along N.
+    const bool in_place = beta == 1.0f && static_cast<const void*>(D) == static_cast<const void*>(C);
+    const SkMode sk_mode =
+        in_place ? SkMode::Off : (scratch == Scratch::Static ? SkMode::Force : SkMode::Env);
     s = finish_tc_plan(&plan, dtype, sk_mode);
     if (s != TPGEMM_OK) return s;
     if (scratch == Scratch::Static && plan.tc.sk && static_scratch_need(plan) > tpg::kStaticScratchBytes) {
