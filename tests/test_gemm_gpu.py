@@ -281,6 +281,8 @@ def test_normal_orientation_mn_contiguous_q(pair, tune):
     ("normal_chain_beta0", 1024, 1024, 2048, True, True, 0.0, "1"),
     ("swapped_large", 1024, 1024, 2048, False, False, 1.0, "1"),
     ("one_cta", 1024, 1024, 2048, False, True, 1.0, "0"),
+    ("ragged_odd_k", 1040, 1000, 2056, False, True, 1.0, "1"),  # partial edge tiles, 33 K blocks
+    ("ragged_nn_beta0", 1008, 1304, 1096, False, False, 0.0, "1"),
 ], ids=lambda c: c[0])
 def test_stream_k(case, tune):
     # Each leftover work item split into two K halves on two clusters: the
@@ -381,6 +383,19 @@ def test_in_place_d_equals_c(path):
     Dref, S = oracle_full(w, A, B, C)
     ok, msg = oracle.compare(D, Dref, S)
     assert ok, msg
+
+
+@pytest.mark.parametrize("bp", ["112", "80"])
+def test_stream_k_half_quadrant(bp, tune):
+    # P tiles of 112 or 80 rows: one lane quadrant holds 16 of the tile's rows
+    # and reduces (and zero-fills) through the half-width D map.
+    tune.setenv("TPGEMM_TC_BP", bp)
+    tune.setenv("TPGEMM_TC_SK", "1")
+    base = wl.BY_NAME["skinny_144x16392x4104_f16_beta1"]
+    w = base.with_shape(144, 4104, 1160, seed=6380 + int(bp))
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert f"tile={bp}x" in text and "stream_k=1" in text, text
+    check_full(w, TC)
 
 
 def test_in_place_takes_the_n_split_not_stream_k():
