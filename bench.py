@@ -39,9 +39,12 @@ import workloads as wl  # noqa: E402
 METRIC = "GEMM TFLOP/s (fp16/bf16->fp32) at 4096^3/8192^3; % of tensor peak or HBM roof"
 DEFAULT_WORKLOAD = "gemm_8192_bf16_transB_beta1"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The device code of the tcgen05 kernel. What the planner chooses for a
+# workload (tile, ring, grid, orientation, last-wave split, L2 policies) is in
+# its plan string, recorded beside each traffic figure.
 KERNEL_SOURCES = ["tile_primitive_tensor_gb300/csrc/tc_gemm.cu",
                   "tile_primitive_tensor_gb300/csrc/ptx.cuh",
-                  "tile_primitive_tensor_gb300/csrc/tpgemm_api.cu"]
+                  "tile_primitive_tensor_gb300/csrc/tpgemm_internal.h"]
 
 
 def log(*a):
@@ -113,8 +116,9 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def load_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches this kernel."""
+def load_traffic(workload: str, plan=None):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken of
+    this kernel (same device-code hash) running this plan (when one is given)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -122,6 +126,8 @@ def load_traffic(workload: str):
         d = json.load(f)
     e = d.get(workload)
     if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    if plan is not None and e.get("plan") != plan:
         return None
     return e.get("traffic_bytes_per_launch")
 
@@ -709,7 +715,7 @@ def finish_line(args, w, value, ms_per_step, launch_ms, clocks, plan, peaks, src
     """The JSON line: roofline of the (single) kernel of a step, configs, CPU baseline."""
     # ---- roofline of the (single) kernel of a step
     roof = roofline_of(w, launch_ms, peaks, src)
-    roof["traffic"] = load_traffic(w.name)
+    roof["traffic"] = load_traffic(w.name, plan)
     roof["algorithmic"] = w.flops if roof["bound"] == "tensor" else w.algorithmic_bytes
     roof["kernel"] = plan
 

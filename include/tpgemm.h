@@ -25,10 +25,13 @@
  * tpgemm_gemm_host they are host pointers). The library keeps no pointer to
  * them after a call is enqueued. No call allocates device memory for itself,
  * with one exception: a plan whose last wave is split by K across clusters
- * (stream-K, on by default where it applies, never in place; environment
- * TPGEMM_TC_SK=0 turns it off) needs an 8 KB array of flags, taken once per (device, stream) with
- * cudaMalloc on the first such call and kept until exit, so make that call
- * outside stream capture. tpgemm_gemm_noalloc uses a static array instead.
+ * (stream-K, on by default where it applies; environment TPGEMM_TC_SK=0
+ * turns it off) needs an 8 KB array of flags, taken once per (device, stream)
+ * with cudaMalloc on the first such call and kept until exit;
+ * tpgemm_gemm_noalloc uses a static array instead. Calls in place (D == C)
+ * and calls on a stream being captured into a CUDA graph never use that mode
+ * (a graph replay would reuse the captured flag epoch): they split the last
+ * wave along N, which needs nothing.
  *
  * Errors: every function returns a status. Argument errors are detected on the
  * host before anything is enqueued, and a readable reason is available from
@@ -127,8 +130,9 @@ tpgemm_status tpgemm_gemm_path(float* D, const void* A, const void* B, const flo
  * tolerance; the K-summation order differs). The tcgen05 kernel runs in its
  * stream-K mode whenever the plan has a partial last wave that fits it (each
  * leftover tile split into two K halves on two clusters, twice the leftover
- * tiles at most the grid's clusters) and the call is not in place (D == C,
- * which takes the split along N), with its flags in one file-scope static
+ * tiles at most the grid's clusters) and the call is neither in place (D ==
+ * C) nor on a capturing stream (those take the split along N), with its flags
+ * in one file-scope static
  * device array of TPGEMM_NOALLOC_SCRATCH_BYTES bytes that every GPU loading
  * the library holds until exit; otherwise it runs the plan that needs none
  * (the last wave split along N). tpgemm_last_plan() tells which plan ran

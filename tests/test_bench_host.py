@@ -34,8 +34,26 @@ def test_traffic_table_is_keyed_by_a_current_hash_or_reads_null():
         got = bench.load_traffic(workload)
         if row["kernel_hash"] == h:
             assert got == row["traffic_bytes_per_launch"]
+            # Only for the plan it was taken of.
+            assert bench.load_traffic(workload, row["plan"]) == got
+            assert bench.load_traffic(workload, row["plan"] + " other") is None
         else:
             assert got is None
+
+
+def test_recorded_plans_are_the_planners_plans():
+    # The traffic table's plans are what the planner gives these workloads on
+    # a 152-SM GB300 (the plan string carries no device name; the grid does).
+    import tile_primitive_tensor_gb300 as tp
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        table = json.load(f)
+    for workload, row in table.items():
+        w = bench.wl.BY_NAME[workload]
+        if isinstance(w, bench.wl.MxWorkload):
+            continue  # block-scaled plans are made inside tpgemm_gemm_mx
+        st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta)
+        assert st == tp.TPGEMM_OK
+        assert text == row["plan"], (workload, text, row["plan"])
 
 
 def _sample(t, sm, **reasons):

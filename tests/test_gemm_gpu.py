@@ -398,6 +398,37 @@ def test_stream_k_half_quadrant(bp, tune):
     check_full(w, TC)
 
 
+def test_graph_capture_replays_take_no_stream_k():
+    # A launch captured into a CUDA graph keeps its stream-K flag epoch, and a
+    # replay would find the flags already at that value; so a call on a
+    # capturing stream plans the split along N. Outside the capture the same
+    # shape runs stream-K. Three replays each match the oracle.
+    w = wl.BY_NAME["gemm_256_bf16_transB_beta1"].with_shape(1024, 1024, 2048, seed=6520)
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+    D = torch.empty(w.M, w.N, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        st = tp.tpgemm_gemm_path(D, Ad, Bd, Cd, w.M, w.N, w.K, w.transA, w.transB, w.dtype,
+                                 w.beta, None, TC)
+        assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    torch.cuda.synchronize()
+    assert "stream_k=1" in tp.tpgemm_last_plan()[1]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        st = tp.tpgemm_gemm_path(D, Ad, Bd, Cd, w.M, w.N, w.K, w.transA, w.transB, w.dtype,
+                                 w.beta, None, TC)
+    assert st == tp.TPGEMM_OK, tp.tpgemm_last_error_detail()
+    assert "stream_k=0" in tp.tpgemm_last_plan()[1], tp.tpgemm_last_plan()[1]
+    Dref, S = oracle_full(w, A, B, C)
+    for _ in range(3):
+        D.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ok, msg = oracle.compare(D.cpu().numpy(), Dref, S)
+        assert ok, msg
+    assert tp.tpgemm_last_device_error() == tp.TPGEMM_OK
+
+
 def test_in_place_takes_the_n_split_not_stream_k():
     # 1024^2 x 2048 (16 pair tiles, one partial wave) would split each tile
     # into two K halves whose first zeroes D at kernel start; in place (D ==

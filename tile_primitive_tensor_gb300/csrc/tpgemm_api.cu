@@ -1013,10 +1013,20 @@ tpgemm_status run(float* D, const void* A, const void* B, const float* C, int64_
     std::memset(&maps, 0, sizeof(maps));
     // In place (D == C with beta = 1): stream-K's first half zeroes its tile
     // of D at kernel start, which here would erase C before it is read, so
-    // those calls take the split along N.
+    // those calls take the split along N. So do calls on a stream being
+    // captured into a graph: a captured launch keeps its flag epoch, and a
+    // replay would find the flags already at that value (and the first
+    // stream-K call on a stream allocates its flags).
     const bool in_place = beta == 1.0f && static_cast<const void*>(D) == static_cast<const void*>(C);
-    const SkMode sk_mode =
-        in_place ? SkMode::Off : (scratch == Scratch::Static ? SkMode::Force : SkMode::Env);
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capture) != cudaSuccess) {
+        (void)cudaGetLastError();
+        capture = cudaStreamCaptureStatusActive;  // unknown: plan as if captured
+    }
+    const bool capturing = capture != cudaStreamCaptureStatusNone;
+    const SkMode sk_mode = (in_place || capturing)
+                               ? SkMode::Off
+                               : (scratch == Scratch::Static ? SkMode::Force : SkMode::Env);
     s = finish_tc_plan(&plan, dtype, sk_mode);
     if (s != TPGEMM_OK) return s;
     if (scratch == Scratch::Static && plan.tc.sk && static_scratch_need(plan) > tpg::kStaticScratchBytes) {
