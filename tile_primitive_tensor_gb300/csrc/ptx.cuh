@@ -130,6 +130,15 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const 
         : "memory");
 }
 
+// Prefetch one tensor-map box into L2 (no shared-memory destination, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Shared -> global tile reduction: each element of the box is added (f32, in
 // L2) to the global element it maps to, as one bulk-group operation.
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src,

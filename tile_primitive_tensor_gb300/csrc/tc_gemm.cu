@@ -396,7 +396,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int nk = u.kb1 - u.kb0;
                 int kb = nk == p.k_blocks ? first_k_block(u.T, p) : u.kb0;
                 if constexpr (EARLY) {
-                    if (first_seg) grid_dependency_wait();
+                    if (first_seg) {
+                        // Before waiting for the previous grid, ask L2 for the
+                        // operand boxes of this producer's first ring of fills.
+                        // L2 is where the previous grid's writes land, so a line
+                        // prefetched early is never stale; the fills themselves
+                        // still come after the wait.
+                        for (int i = prod_r; i < nk && i < p.stages; i += nprod) {
+                            const int k0 = ((kb + i) % p.k_blocks) * p.bk;
+                            if (p.p_mn) {
+                                tma_prefetch_2d(&mapP, p0, k0);
+                                if (p.bp > 64) tma_prefetch_2d(&mapPh, p0 + 64, k0);
+                            } else {
+                                tma_prefetch_2d(&mapP, k0, p0);
+                            }
+                            const int qh = q0 + (PAIR ? rank * q_rows : 0);
+                            if (p.q_mn) {
+                                for (int a = 0; a < q_atoms; ++a)
+                                    tma_prefetch_2d(&mapQ, qh + 64 * a, k0);
+                            } else {
+                                tma_prefetch_2d(mq, k0, qh);
+                            }
+                        }
+                        grid_dependency_wait();
+                    }
                 }
                 for (int i = 0; i < nk;
                      ++i, turn = (turn + 1 == nprod) ? 0 : turn + 1,
