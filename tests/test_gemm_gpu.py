@@ -306,6 +306,59 @@ def test_stream_k(case, tune):
 
 
 @pytest.mark.parametrize("case", [
+    # name, workload, M, N, K, tA, tB, beta, pair, extra overrides
+    ("pair_kmajor_ragged_k", "gemm_4096_f16_int", 1024, 1024, 1032, False, True, 1.0, "1", {}),
+    ("pair_swapped_beta0", "gemm_4096_f16_int", 1024, 1040, 2056, False, False, 0.0, "1", {}),
+    ("one_cta_rotated", "gemm_4096_f16_int", 1024, 1024, 1096, False, True, 1.0, "0",
+     {"TPGEMM_TC_KROTATE": "3", "TPGEMM_TC_SK": "0"}),
+    ("pair_n_split_tail", "gemm_4096_f16_int", 1040, 1000, 1032, True, True, 1.0, "1",
+     {"TPGEMM_TC_SK": "0"}),
+    ("pair_fp8", "gemm_4096_e4m3_int_transB", 1024, 1280, 1040, False, True, 0.0, "1", {}),
+    ("pair_random_bf16", "gemm_256_bf16_transB_beta1", 1024, 1024, 1032, False, True, 1.0, "1", {}),
+], ids=lambda c: c[0])
+@pytest.mark.parametrize("krev", ["0", "1"])
+def test_k_direction(case, krev, tune):
+    # With k_reverse a cluster's second, fourth, ... unit walks its K blocks
+    # backwards. Six clusters give each one several units, so both directions
+    # run in one launch. Integer-valued inputs make every order of the sum give
+    # the same value, so those results must equal the oracle's exactly.
+    name, base_name, M, N, K, tA, tB, beta, pair, extra = case
+    tune.setenv("TPGEMM_TC_PAIR", pair)
+    tune.setenv("TPGEMM_TC_MAX_CLUSTERS", "6")
+    tune.setenv("TPGEMM_TC_KREV", krev)
+    for k, v in extra.items():
+        tune.setenv(k, v)
+    base = wl.BY_NAME[base_name]
+    w = dataclasses.replace(base.with_shape(M, N, K, seed=6410 + M + K), transA=tA, transB=tB,
+                            beta=beta,
+                            c_dist=(("int", -3, 3) if base.integer_valued else
+                                    ("normal", 0.0, 1.0)) if beta else None)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert f"k_reverse={krev}" in text, text
+    if "TPGEMM_TC_KROTATE" in extra:
+        assert f"k_rotate={extra['TPGEMM_TC_KROTATE']}" in text, text
+    units = re.search(r"units=(\d+)\+(\d+)x(\d+)", text)
+    whole = int(units.group(1))
+    grid = int(re.search(r"grid=(\d+)", text).group(1))
+    assert whole >= 2 * (grid // (2 if pair == "1" else 1)), text  # a second wave exists
+    check_full(w, TC)
+
+
+def test_k_reverse_default_plans():
+    # On by default only for 16-bit plans of eight or more waves.
+    cases = [
+        (8192, 8192, 8192, False, True, wl.BF16, 1.0, 1),
+        (4096, 4096, 4096, False, False, wl.F16, 0.0, 0),
+        (8192, 8192, 8192, False, True, wl.E4M3, 1.0, 0),
+        (144, 16392, 4104, False, False, wl.F16, 1.0, 0),
+    ]
+    for M, N, K, tA, tB, dtype, beta, want in cases:
+        st, text = tp.tpgemm_describe_plan(M, N, K, tA, tB, dtype, beta, TC)
+        assert st == tp.TPGEMM_OK
+        assert f"k_reverse={want}" in text, (M, N, K, dtype, text)
+
+
+@pytest.mark.parametrize("case", [
     ("skinny_swap_pair", 144, 2072, 520, False, False, 1.0, {"TPGEMM_TC_PAIR": "1"}),
     ("normal_beta1_one_buf", 1024, 1024, 2048, False, True, 1.0, {}),
     ("normal_beta0_one_buf", 1024, 1024, 520, True, True, 0.0, {}),

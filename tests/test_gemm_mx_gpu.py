@@ -129,6 +129,16 @@ def test_mx_integer_bit_exact_large():
     check(case(512, 768, 2048, wl.E5M2, 0.0, dist=("int", -3, 3), sf=(126, 128), seed=72))
 
 
+@pytest.mark.parametrize("krev", ["0", "1"])
+def test_mx_k_direction(krev, tune):
+    # Each stage's scales are loaded for the K block its operands come from,
+    # whichever way the unit walks K; six clusters give each one several units.
+    tune.setenv("TPGEMM_TC_MAX_CLUSTERS", "6")
+    tune.setenv("TPGEMM_TC_KREV", krev)
+    plan = check(case(1024, 1344, 1024, wl.E4M3, 1.0, dist=("int", -3, 3), sf=(126, 128), seed=91))
+    assert f"k_reverse={krev}" in plan, plan
+
+
 def test_mx_unit_scales_equal_plain_fp8():
     # With every scale 1 the block-scaled multiply is the plain fp8 one, and the
     # library's two paths agree within the bound (the oracle agrees bit for bit).

@@ -197,9 +197,10 @@ __device__ __forceinline__ Unit unit_of(int U, const TcParams& p) {
 // its Q tile) over K blocks [kb0, kb1). Whole tiles have owner = 1 and
 // has_next = 0. Stream-K segments: owner = the segment holds K block 0 (it
 // writes D); has_next = a later segment of the same tile exists, in the next
-// cluster, whose partial this segment adds.
+// cluster, whose partial this segment adds. rev: the producer walks the K
+// blocks backwards.
 struct Seg {
-    int T, q_off, width, kb0, kb1, owner, has_next;
+    int T, q_off, width, kb0, kb1, owner, has_next, rev;
 };
 
 // First stream-K K block of cluster c: the first p.sk_ncl clusters share them
@@ -211,21 +212,22 @@ __device__ __forceinline__ int sk_begin(int c, const TcParams& p) {
 // This cluster's segments in order: its whole work units first (U = cid,
 // cid + ncl, ...), then its contiguous share of the stream-K K blocks.
 struct SegIter {
-    int U, u, ub;
+    int U, u, ub, odd;
     __device__ __forceinline__ SegIter(int cid, int ncl, const TcParams& p)
-        : U(cid), u(p.sk ? sk_begin(cid, p) : 0), ub(p.sk ? sk_begin(cid + 1, p) : 0) {}
+        : U(cid), u(p.sk ? sk_begin(cid, p) : 0), ub(p.sk ? sk_begin(cid + 1, p) : 0), odd(0) {}
     __device__ __forceinline__ bool next(int ncl, const TcParams& p, Seg& s) {
         if (U < p.num_units) {
             const Unit un = unit_of(U, p);
-            s = {un.T, un.q_off, un.width, 0, p.k_blocks, 1, 0};
+            s = {un.T, un.q_off, un.width, 0, p.k_blocks, 1, 0, odd & p.k_reverse};
             U += ncl;
+            odd ^= 1;
             return true;
         }
         if (u < ub) {
             const int t = u / p.k_blocks;
             const int k0 = u - t * p.k_blocks;
             const int k1 = min(p.k_blocks, k0 + (ub - u));
-            s = {p.full_units + t, 0, p.bn, k0, k1, k0 == 0, k1 < p.k_blocks};
+            s = {p.full_units + t, 0, p.bn, k0, k1, k0 == 0, k1 < p.k_blocks, 0};
             u += k1 - k0;
             return true;
         }
@@ -395,6 +397,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     (MX ? 512u * uint32_t(1 + p.sf_q_rows) : 0u);
                 const int nk = u.kb1 - u.kb0;
                 int kb = nk == p.k_blocks ? first_k_block(u.T, p) : u.kb0;
+                // Backwards: the same blocks in the opposite order, ending on
+                // the block a forward walk starts on.
+                if (u.rev) kb = (kb == 0 ? p.k_blocks : kb) - 1;
                 if constexpr (EARLY) {
                     if (first_seg) {
                         // Before waiting for the previous grid, ask L2 for the
@@ -423,7 +428,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 for (int i = 0; i < nk;
                      ++i, turn = (turn + 1 == nprod) ? 0 : turn + 1,
-                     kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
+                     kb = u.rev ? (kb == 0 ? p.k_blocks : kb) - 1
+                                : (kb + 1 == p.k_blocks ? 0 : kb + 1)) {
                     if (turn != prod_r) {  // another producer's fill
                         if (++stage == p.stages) {
                             stage = 0;

@@ -79,6 +79,9 @@ struct TcParams {
     int epi_groups;         // active epilogue warpgroups (1 or 2); warp 2 + 4 g + i
                             // reads lane quadrant (i + 2) % 4, chunks c % groups == g
     int k_rotate;           // 0, or tiles per group sharing a rotated first K block
+    int k_reverse;          // 1: a cluster's second, fourth, ... whole unit (the odd waves of
+                            // the persistent grid) walks its K blocks backwards, so it starts
+                            // on the slices the previous wave read last
     int dep_early;          // 1: only threads touching global memory wait for the previous
                             // grid, each just before its first access; 0: all wait after set-up
     int producers;          // TMA-issuing threads (1..4, at most the ring depth): warp 0,
