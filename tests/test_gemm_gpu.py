@@ -344,6 +344,60 @@ def test_k_direction(case, krev, tune):
     check_full(w, TC)
 
 
+@pytest.mark.parametrize("case", [
+    # name, workload, M, N, K, tA, tB, beta, extra overrides
+    ("whole_units_beta1", "gemm_4096_f16_int", 1024, 1024, 1032, False, True, 1.0,
+     {"TPGEMM_TC_MAX_CLUSTERS": "6"}),
+    ("swapped_beta0", "gemm_4096_f16_int", 1024, 1040, 2056, False, False, 0.0,
+     {"TPGEMM_TC_MAX_CLUSTERS": "6"}),
+    ("stream_k_halves_beta1", "gemm_4096_f16_int", 1040, 1000, 2056, False, True, 1.0,
+     {"TPGEMM_TC_SK": "1"}),
+    ("stream_k_halves_beta0", "gemm_4096_f16_int", 1008, 1304, 1096, False, False, 0.0,
+     {"TPGEMM_TC_SK": "1"}),
+    ("n_split_tail_ragged", "gemm_4096_f16_int", 1040, 1000, 1032, True, True, 1.0,
+     {"TPGEMM_TC_SK": "0", "TPGEMM_TC_MAX_CLUSTERS": "6"}),
+    ("odd_chunks_one_cta", "gemm_4096_f16_int", 1024, 1000, 1032, False, True, 1.0,
+     {"TPGEMM_TC_PAIR": "0", "TPGEMM_TC_BN": "224", "TPGEMM_TC_MAX_CLUSTERS": "6"}),
+    ("fp8", "gemm_4096_e4m3_int_transB", 1024, 1280, 1040, False, True, 1.0,
+     {"TPGEMM_TC_MAX_CLUSTERS": "6"}),
+], ids=lambda c: c[0])
+@pytest.mark.parametrize("help_", ["0", "1"])
+def test_last_segment_helpers(case, help_, tune):
+    # In a one-group plan warps 6..9 take the odd 32-column chunks of each
+    # CTA's last segment, staged through the TMA ring; with C they load it
+    # there themselves. Integer-valued inputs: the result must equal the
+    # oracle's exactly, with the helpers and without.
+    name, base_name, M, N, K, tA, tB, beta, extra = case
+    for k, v in extra.items():
+        tune.setenv(k, v)
+    tune.setenv("TPGEMM_TC_EPI_HELP", help_)
+    base = wl.BY_NAME[base_name]
+    w = dataclasses.replace(base.with_shape(M, N, K, seed=6470 + M + K), transA=tA, transB=tB,
+                            beta=beta, c_dist=("int", -3, 3) if beta else None)
+    st, text = tp.tpgemm_describe_plan(w.M, w.N, w.K, w.transA, w.transB, w.dtype, w.beta, TC)
+    assert "epi_groups=1" in text and f"epi_help={help_}" in text, text
+    if extra.get("TPGEMM_TC_SK") == "1":
+        assert "stream_k=1" in text, text
+    D1 = check_full(w, TC)
+    assert f"epi_help={help_}" in tp.tpgemm_last_plan()[1]
+    # A second launch (stream-K: the next flag epoch) gives the same bits.
+    (A, B, C), (Ad, Bd, Cd) = device_inputs(w)
+    D2 = run_gpu(w, Ad, Bd, Cd, TC)
+    assert np.array_equal(D1.view(np.uint32), D2.view(np.uint32))
+
+
+def test_last_segment_helpers_default_plans():
+    # On for one-group plans whose ring holds a helper's chunks; the single-wave
+    # plans that run two epilogue groups have no helpers.
+    for M, N, K, tA, tB, dtype, beta, want in [
+        (8192, 8192, 8192, False, True, wl.BF16, 1.0, "epi_groups=1 epi_help=1"),
+        (4096, 4096, 4096, False, False, wl.F16, 0.0, "epi_groups=1 epi_help=1"),
+        (144, 16392, 4104, False, False, wl.F16, 1.0, "epi_groups=2 epi_help=0"),
+    ]:
+        st, text = tp.tpgemm_describe_plan(M, N, K, tA, tB, dtype, beta, TC)
+        assert st == tp.TPGEMM_OK and want in text, text
+
+
 def test_k_reverse_default_plans():
     # On by default only for 16-bit plans of eight or more waves.
     cases = [

@@ -139,6 +139,16 @@ def test_mx_k_direction(krev, tune):
     assert f"k_reverse={krev}" in plan, plan
 
 
+@pytest.mark.parametrize("help_", ["0", "1"])
+def test_mx_last_segment_helpers(help_, tune):
+    # The helpers' share of a block-scaled tile's last segment (224 columns:
+    # 7 chunks, 3 of them the helpers'), with C.
+    tune.setenv("TPGEMM_TC_MAX_CLUSTERS", "6")
+    tune.setenv("TPGEMM_TC_EPI_HELP", help_)
+    plan = check(case(1024, 1344, 1024, wl.E4M3, 1.0, dist=("int", -3, 3), sf=(126, 128), seed=93))
+    assert f"epi_help={help_}" in plan, plan
+
+
 def test_mx_unit_scales_equal_plain_fp8():
     # With every scale 1 the block-scaled multiply is the plain fp8 one, and the
     # library's two paths agree within the bound (the oracle agrees bit for bit).

@@ -46,6 +46,7 @@ enum BoundsSite : int {
     kSiteStore = 4,          // a TMA store coordinate negative or not 16-byte aligned
     kSiteLoadC = 5,          // a TMA load coordinate of C or a partial tile not aligned
     kSiteFlag = 6,           // a stream-K flag index past the flag area
+    kSiteHelperStaging = 7,  // a helper warp's chunks do not fit its share of the TMA ring
 };
 
 // Debug builds (-DTPGEMM_DEBUG): a computed tensor-memory column, TMA
@@ -89,6 +90,8 @@ struct Smem {
     uint64_t* acc_empty;   // [2]
     uint64_t* cbar;        // [4 quadrants][kTcMaxEpiBufs]
     uint64_t* drain;       // [1]
+    uint64_t* last_full;   // [1] the CTA's last accumulator is complete (epi_help)
+    uint64_t* hbar;        // [4 quadrants] C fills of the last segment's helper warps
     uint32_t* tmem_base;
     volatile int* abort;
 };
@@ -108,7 +111,9 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const TcParams& p) {
     s.acc_empty = s.acc_full + 2;
     s.cbar = s.acc_empty + 2;
     s.drain = s.cbar + kTcMaxEpiBufs * kEpiQuads;
-    s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.last_full = s.drain + 1;
+    s.hbar = s.last_full + 1;
+    s.tmem_base = reinterpret_cast<uint32_t*>(s.hbar + kEpiQuads);
     s.abort = reinterpret_cast<volatile int*>(s.tmem_base + 1);
     return s;
 }
@@ -319,6 +324,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < kTcMaxEpiBufs * kEpiQuads; ++i) mbar_init(&s.cbar[i], 1);
         mbar_init(s.drain, 1);
+        mbar_init(s.last_full, 1);
+        for (int i = 0; i < kEpiQuads; ++i) mbar_init(&s.hbar[i], 1);
         *s.abort = 0;
         fence_mbarrier_init();
     }
@@ -353,6 +360,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t issued_any = 0;     // producer: bit i = stage i was ever filled
     uint32_t cphase = 0;         // epilogue: bit i = parity of the next C fill of buffer i
     uint32_t cpend = 0;          // epilogue: bit i = a C fill into staging buffer i in flight
+    bool hpend = false;          // helper warp: its C fill of the last segment is in flight
 
     // ---------------------------------------------------------- TMA producers
     // Lane 0 of warp 0 and, with p.producers > 1, of warps 6, 7, 8 (the second
@@ -663,6 +671,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_commit_pair_multicast(&s.acc_full[b], pair_mask);
                 else
                     tc_commit(&s.acc_full[b]);
+                // The last one also for the helper warps (a barrier of its own,
+                // which completes once per launch).
+                if (p.epi_help && !iter.more(p)) {
+                    if (PAIR)
+                        tc_commit_pair_multicast(s.last_full, pair_mask);
+                    else
+                        tc_commit(s.last_full);
+                }
             }
             };
             if (p.fp8)
@@ -676,15 +692,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_commit(s.drain);
             wait_phase(s.drain, 0, s.abort, tmo, true);
         }
-    } else if (warp >= 2 && warp < 2 + kEpiQuads * p.epi_groups) {
+    } else if (warp >= 2 && (warp < 2 + kEpiQuads * p.epi_groups || p.epi_help)) {
         // (A producing warp of the second group has issued its fills first.)
         // --------------------------------------------------------- epilogue
         if constexpr (EARLY) grid_dependency_wait();
-        const int ew = warp - 2;           // 0 .. 4 epi_groups - 1
+        const int ew = warp - 2;           // 0 .. 4 epi_groups - 1, or 4 .. 7 for a helper
         const int quad = warp & 3;         // tensor-memory lane quadrant of this warp
-        const EpiShare es = epi_share(s, p, ew);
-        const int ng = p.epi_groups;
-        const int half = es.g;
+        // A helper (warps 6..9 of a one-group plan with epi_help) works on the
+        // CTA's last segment only, and has no staging tiles of its own: by
+        // then the TMA ring is idle and holds its chunks.
+        const bool helper = ew >= kEpiQuads * p.epi_groups;
+        const EpiShare es = helper ? EpiShare{1, 0, nullptr, nullptr} : epi_share(s, p, ew);
         const int nbw = es.nbw;
         float* bufs = es.bufs;
         uint64_t* cb = es.cb;
@@ -697,7 +715,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Output extents in the kernel's (P, Q) frame, for skipping empty chunks.
         const int lim_p = p.Mp;
         const int lim_q = p.Nq;
-        if (p.sk) {
+        if (p.sk && !helper) {
+            const int ng = p.epi_groups;
+            const int half = es.g;
             // Stream-K: the leftover tile whose first K blocks this cluster
             // holds (at most one) gets this warp's part of its D region zeroed
             // now, under the MMAs of the whole units, and a flag published
@@ -735,8 +755,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     bulk_wait_group<0>();  // written, not just read
                     fence_proxy_async_global();
                     if (in_bounds(int(blockIdx.x) * kEpiWarps + ew < kTcMaxFlagSlots * kEpiWarps,
-                                  kSiteFlag))
+                                  kSiteFlag)) {
                         st_release_gpu(&p.sk_flags[blockIdx.x * kEpiWarps + ew], p.sk_epoch);
+                        // This warp zeroed every chunk of its quadrant, so the
+                        // quadrant's helper may add into them too.
+                        if (p.epi_help)
+                            st_release_gpu(&p.sk_flags[blockIdx.x * kEpiWarps + ew + kEpiQuads],
+                                           p.sk_epoch);
+                    }
                 }
                 __syncwarp();
                 break;
@@ -746,6 +772,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         SegIter iter(cid, ncl, p);
         Seg u;
         for (; iter.next(ncl, p, u); ++it) {
+            const bool last = !iter.more(p);
+            if (helper && !last) continue;
+            // The last segment of an epi_help plan: the quadrant's first warp
+            // takes the even chunks, its helper the odd ones.
+            const bool shared_last = p.epi_help && last;
+            const int ng = shared_last ? 2 : p.epi_groups;
+            const int half = shared_last ? (helper ? 1 : 0) : es.g;
             int tps, tq;
             tile_coords(u.T, p, tps, tq);
             const int tp = tps * MC + rank;
@@ -799,12 +832,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             __syncwarp();
+            if (helper && my_chunks == 0) break;
             const int b = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
-            bool ok = wait_phase(&s.acc_full[b], acc_phase, s.abort, tmo);
+            // (A helper may wait from kernel start: its bound covers each of
+            // the cluster's segments, as the other waits cover one.)
+            bool ok = helper ? wait_phase(s.last_full, 0, s.abort, tmo * uint64_t(it + 1))
+                             : wait_phase(&s.acc_full[b], acc_phase, s.abort, tmo);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            if (split && !u.owner && my_chunks > 0) {
+            // A helper of the tile's owner waits for the zeros as well: the
+            // owner's first warps wrote them.
+            if (split && (!u.owner || helper) && my_chunks > 0) {
                 // The owner's zeros are in D before this segment adds to it.
                 bool fok = true;
                 if (lane == 0) {
@@ -828,14 +867,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // of this CTA's half) no fill or MMA touches the TMA ring again,
             // so D is staged through the ring, one buffer per chunk, and no
             // chunk waits for an earlier store to have read its buffer.
+            // A helper always stages this way (the plan checks that its chunks
+            // fit), and loads the segment's C, if any, once the ring is idle.
             int snbw = nbw;
-            if (!add_src && !iter.more(p)) {
+            if ((helper || !add_src) && last) {
                 const int per_warp =
                     int((uint32_t(p.stages) * (p.p_bytes + p.q_bytes + p.sf_bytes)) /
                         (uint32_t(kEpiQuads * ng) * uint32_t(kEpiBufFloats * sizeof(float))));
-                if (per_warp >= my_chunks && my_chunks > nbw) {
+                if (per_warp >= my_chunks && (helper || my_chunks > nbw)) {
                     snbw = my_chunks;
                     bufs = reinterpret_cast<float*>(s.stages) + ew * per_warp * kEpiBufFloats;
+                }
+            }
+            if (helper) {
+                if (!in_bounds(snbw == my_chunks, kSiteHelperStaging)) break;
+                if (add_src) {
+                    if (lane == 0) {
+                        uint32_t bytes = 0;
+                        for (int j = 0; j < my_chunks; ++j)
+                            if (in_bounds(src_x(ng * j + half) % 4 == 0, kSiteLoadC))
+                                bytes += src_bytes;
+                        mbar_arrive_expect_tx(&s.hbar[quad], bytes);
+                        for (int j = 0; j < my_chunks; ++j) {
+                            const int c = ng * j + half;
+                            if (in_bounds(src_x(c) % 4 == 0, kSiteLoadC))
+                                tma_load_2d_hint(bufs + j * kEpiBufFloats, src_map, &s.hbar[quad],
+                                                 src_x(c), src_y(c), pol_cd);
+                        }
+                    }
+                    hpend = true;
+                    bool cok = wait_phase(&s.hbar[quad], 0, s.abort, tmo);
+                    ok = __all_sync(0xffffffffu, cok);
+                    if (!ok) break;
+                    hpend = false;
                 }
             }
             auto chunk = [&](int j, uint32_t (&cur)[32], uint32_t (&nxt)[32]) -> bool {
@@ -848,7 +912,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                   acc_col + uint32_t(acc_stride),
                               kSiteEpilogueLoad))
                     tmem_ld_32x32b_x32(tmem + lane_base + acc_col + uint32_t(32 * (c + ng)), nxt);
-                if (add_src) {
+                if (add_src && !helper) {
                     bool cok = wait_phase(&cb[bi], (cphase >> bi) & 1u, s.abort, tmo);
                     cok = __all_sync(0xffffffffu, cok);
                     if (!cok) {
@@ -903,14 +967,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     else
                         tma_store_2d_hint(dst_map, buf, dst_x(c), dst_y(c), pol_cd);
                     bulk_commit_group();
-                    if (add_src && j + nbw < my_chunks) {
+                    if (add_src && !helper && j + nbw < my_chunks) {
                         const int cn = c + ng * nbw;  // this warp's chunk j + nbw
                         bulk_wait_group_read<0>();  // the store just issued has read buf
                         mbar_arrive_expect_tx(&cb[bi], src_bytes);
                         tma_load_2d_hint(buf, src_map, &cb[bi], src_x(cn), src_y(cn), pol_cd);
                     }
                 }
-                if (add_src && j + nbw < my_chunks) cpend |= 1u << bi;
+                if (add_src && !helper && j + nbw < my_chunks) cpend |= 1u << bi;
                 __syncwarp();
                 return true;
             };
@@ -930,7 +994,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // (issued by the pair's leader in pair mode).
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) {
+            if (lane == 0 && !helper) {
                 if (PAIR)
                     mbar_arrive_cluster(mapa_shared(smem_u32(&s.acc_empty[b]), 0));
                 else
@@ -960,6 +1024,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (cpend & (1u << i))
                     wait_phase(&es.cb[i], (cphase >> i) & 1u, s.abort, tmo, true);
         }
+        if (hpend) wait_phase(&s.hbar[warp & 3], 0, s.abort, tmo, true);
         __syncthreads();
     }
     // No CTA of a pair leaves while its peer may still arrive on its barriers.
@@ -1003,7 +1068,15 @@ TcKernelFn pick_kernel(const TcParams& p) {
 size_t tc_smem_bytes(int stages, uint32_t stage_bytes, int epi_bufs) {
     return 1024 + size_t(stages) * stage_bytes +
            size_t(kEpiQuads) * epi_bufs * kEpiBufFloats * sizeof(float) +
-           sizeof(uint64_t) * (2 * size_t(stages) + 4 + kTcMaxEpiBufs * kEpiQuads + 1) + 16;
+           sizeof(uint64_t) * (2 * size_t(stages) + 4 + kTcMaxEpiBufs * kEpiQuads + 2 + kEpiQuads) +
+           16;
+}
+
+bool tc_epi_help_fits(const TcParams& p) {
+    const uint32_t ring = uint32_t(p.stages) * (p.p_bytes + p.q_bytes + p.sf_bytes);
+    const uint32_t per_warp = ring / (uint32_t(2 * kEpiQuads) * kEpiBufFloats * sizeof(float));
+    const int chunks = (p.bn + 31) / 32;
+    return per_warp >= uint32_t((chunks + 1) / 2);
 }
 
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
@@ -1025,6 +1098,8 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStrea
                  (p.p_bytes + p.q_bytes + p.sf_bytes) % 1024 != 0))
         return cudaErrorInvalidValue;
     if (!p.mx && p.sf_bytes != 0) return cudaErrorInvalidValue;
+    // Helper warps: one-group plans whose ring holds a helper's share of a tile.
+    if (p.epi_help && (p.epi_groups != 1 || !tc_epi_help_fits(p))) return cudaErrorInvalidValue;
     // Every stream-K K block must belong to a cluster of the grid.
     if (p.sk && (p.sk_ncl < 1 || p.sk_ncl > grid / p.mc)) return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes(p.stages, p.p_bytes + p.q_bytes + p.sf_bytes, p.epi_bufs);

@@ -93,6 +93,7 @@ struct Tuning {
     int bn = -1, bp = -1, dep_early = -1, epi_bufs = -1, epi_groups = -1, group = -1;
     int krotate = -1, max_clusters = -1, pair = -1, producers = -1, sk = -1, stages = -1;
     int tail = -1, host_blocks = -1, l2_p = -1, l2_q = -1, l2_cd = -1, snake = -1, krev = -1;
+    int epi_help = -1;
     int debug_plant = -1;  // debug builds only
     int orient = 0;  // 1 "swap", 2 "normal"
     long long wait_ms = -1;
@@ -108,6 +109,7 @@ Tuning read_tuning() {
     geti("TPGEMM_TC_DEP_EARLY", &t.dep_early);
     geti("TPGEMM_TC_EPI_BUFS", &t.epi_bufs);
     geti("TPGEMM_TC_EPI_GROUPS", &t.epi_groups);
+    geti("TPGEMM_TC_EPI_HELP", &t.epi_help);
     geti("TPGEMM_TC_GROUP", &t.group);
     geti("TPGEMM_TC_KROTATE", &t.krotate);
     geti("TPGEMM_TC_KREV", &t.krev);
@@ -632,6 +634,11 @@ void choose_epi_groups(tpg::TcParams& p, int grid) {
         const int v = tuning().epi_groups;
         if (v == 1 || v == 2) p.epi_groups = v;
     }
+    // One-group plans: the second warpgroup's warps (TMA issuers or idle
+    // until then) share the epilogue of each CTA's last segment, which no
+    // later MMA hides, staging through the idle TMA ring.
+    p.epi_help = (p.epi_groups == 1 && tpg::tc_epi_help_fits(p)) ? 1 : 0;
+    if (tuning().epi_help == 0) p.epi_help = 0;
 }
 
 // TMA-issuing threads: warp 0, and with more than one producer warps 6, 7, 8,
@@ -915,12 +922,12 @@ void format_plan(const Plan& plan, int64_t M, int64_t N, int64_t K, const char* 
     const tpg::TcParams& p = plan.tc;
     snprintf(text, len,
              "path=tcgen05 orientation=%s tile=%dx%dx%d umma=%dx%dx%d kind=%s stages=%d "
-             "epi_bufs=%d epi_groups=%d producers=%d dep_early=%d k_rotate=%d k_reverse=%d cluster=%d pair=%d "
+             "epi_bufs=%d epi_groups=%d epi_help=%d producers=%d dep_early=%d k_rotate=%d k_reverse=%d cluster=%d pair=%d "
              "tmem=%d tiles=%dx%d grid=%d units=%d+%dx%d stream_k=%d scratch=%s p_major=%s "
              "q_major=%s l2=%d%d%d snake=%d smem=%zu sk_clusters=%d",
              plan.swap ? "swapped" : "normal", p.bp, p.bn, p.bk, p.pair ? 256 : 128, p.bn,
              p.fp8 ? 32 : 16, p.mx ? "mxf8f6f4" : (p.fp8 ? "f8f6f4" : "f16"), p.stages,
-             p.epi_bufs, p.epi_groups,
+             p.epi_bufs, p.epi_groups, p.epi_help,
              p.producers, p.dep_early, p.k_rotate, p.k_reverse, p.mc, p.pair, p.tmem_cols, p.tiles_p,
              p.tiles_q, plan.grid, p.full_units, p.num_super - p.full_units, p.tail_split, p.sk,
              scratch, p.p_mn ? "mn" : "k", p.q_mn ? "mn" : "k", p.l2_p, p.l2_q, p.l2_cd, p.snake,
@@ -1428,10 +1435,11 @@ tpgemm_status tpgemm_last_device_error(void) {
     if (st == tpg::kStatusBounds) {
         static const char* kSites[] = {"?", "epilogue tensor-memory load", "MMA accumulator",
                                        "block-scale slot", "TMA store coordinate",
-                                       "TMA load coordinate", "stream-K flag index"};
+                                       "TMA load coordinate", "stream-K flag index",
+                                       "helper staging"};
         return fail(TPGEMM_ERR_BOUNDS,
                     "a debug bounds check failed at site %d (%s); the access was skipped", site,
-                    kSites[site >= 0 && site <= 6 ? site : 0]);
+                    kSites[site >= 0 && site <= 7 ? site : 0]);
     }
     if (st_cp == tpg::kStatusTimeout)
         return fail(TPGEMM_ERR_TIMEOUT, "a tensor-memory copy kernel wait exceeded its bound");

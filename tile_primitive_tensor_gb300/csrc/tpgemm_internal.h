@@ -78,6 +78,9 @@ struct TcParams {
     int fp8;                // operands are e4m3 / e5m2: kind::f8f6f4 MMAs
     int epi_groups;         // active epilogue warpgroups (1 or 2); warp 2 + 4 g + i
                             // reads lane quadrant (i + 2) % 4, chunks c % groups == g
+    int epi_help;           // one-group plans: 1 = warps 6..9 join the epilogue of the CTA's
+                            // last segment (after any fills they issue), taking its odd
+                            // chunks and staging them through the then idle TMA ring
     int k_rotate;           // 0, or tiles per group sharing a rotated first K block
     int k_reverse;          // 1: a cluster's second, fourth, ... whole unit (the odd waves of
                             // the persistent grid) walks its K blocks backwards, so it starts
@@ -169,6 +172,9 @@ constexpr int kTcEpiWarps = 8;
 constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);
 constexpr int kTcMaxSmem = 232448;  // 227 KB opt-in per block on sm_100-class parts
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream);
+// Whether the TMA ring holds the chunks of a last-segment helper warp (half of
+// a tile's 32-column chunks per lane quadrant, one 4 KB staging tile each).
+bool tc_epi_help_fits(const TcParams& p);
 
 // Clusters of p.mc CTAs of this kernel that fit the device at once (the
 // persistent grid is this many clusters at most).
