@@ -645,9 +645,10 @@ void choose_epi_groups(tpg::TcParams& p, int grid) {
 // fill g going to producer g % producers. One issuing thread puts its own
 // wake-up and issue latency on the path of every fill; two halve that and
 // issue the first ring fill twice as fast. Measured on GB300 against one
-// producer: 144 x 16392 x 4104 32.9 -> 32.7 us, 4096^3 105 -> 98.8 us; on
-// 8192^3 (power-capped, 14 work units per cluster) a second producer cost
-// 0.4 % and four 1 %, so plans with 8 or more units per cluster keep one.
+// producer: 144 x 16392 x 4104 32.9 -> 32.7 us, 4096^3 105 -> 98.8 us, and,
+// interleaved on one box with the current kernel, 8192^3 bf16 589 -> 584 us,
+// e4m3 320 -> 317 us, block-scaled e4m3 499 -> 485 us (a third producer gained
+// nothing at 4096^3).
 // Warps 6, 7, 8 belong to the second epilogue warpgroup; when that group is
 // active they issue their fills before their epilogue work, which is only
 // safe when the cluster has a single work unit (with more, the MMA of a third
@@ -655,8 +656,7 @@ void choose_epi_groups(tpg::TcParams& p, int grid) {
 // TPGEMM_TC_PRODUCERS (1..4) overrides within those limits.
 void choose_producers(tpg::TcParams& p, int grid) {
     const int ncl = std::max(1, grid / p.mc);
-    const int units_per_cluster = (p.num_units + ncl - 1) / ncl;
-    int n = std::min(units_per_cluster >= 8 ? 1 : 2, p.stages);
+    int n = std::min(2, p.stages);
     {
         const int v = tuning().producers;
         if (v >= 1 && v <= 4) n = std::min(v, p.stages);
