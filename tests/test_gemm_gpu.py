@@ -386,32 +386,6 @@ def test_last_segment_helpers(case, help_, tune):
     assert np.array_equal(D1.view(np.uint32), D2.view(np.uint32))
 
 
-def test_last_segment_helpers_default_plans():
-    # On for one-group plans whose ring holds a helper's chunks; the single-wave
-    # plans that run two epilogue groups have no helpers.
-    for M, N, K, tA, tB, dtype, beta, want in [
-        (8192, 8192, 8192, False, True, wl.BF16, 1.0, "epi_groups=1 epi_help=1"),
-        (4096, 4096, 4096, False, False, wl.F16, 0.0, "epi_groups=1 epi_help=1"),
-        (144, 16392, 4104, False, False, wl.F16, 1.0, "epi_groups=2 epi_help=0"),
-    ]:
-        st, text = tp.tpgemm_describe_plan(M, N, K, tA, tB, dtype, beta, TC)
-        assert st == tp.TPGEMM_OK and want in text, text
-
-
-def test_k_reverse_default_plans():
-    # On by default only for 16-bit plans of eight or more waves.
-    cases = [
-        (8192, 8192, 8192, False, True, wl.BF16, 1.0, 1),
-        (4096, 4096, 4096, False, False, wl.F16, 0.0, 0),
-        (8192, 8192, 8192, False, True, wl.E4M3, 1.0, 0),
-        (144, 16392, 4104, False, False, wl.F16, 1.0, 0),
-    ]
-    for M, N, K, tA, tB, dtype, beta, want in cases:
-        st, text = tp.tpgemm_describe_plan(M, N, K, tA, tB, dtype, beta, TC)
-        assert st == tp.TPGEMM_OK
-        assert f"k_reverse={want}" in text, (M, N, K, dtype, text)
-
-
 @pytest.mark.parametrize("case", [
     ("skinny_swap_pair", 144, 2072, 520, False, False, 1.0, {"TPGEMM_TC_PAIR": "1"}),
     ("normal_beta1_one_buf", 1024, 1024, 2048, False, True, 1.0, {}),
