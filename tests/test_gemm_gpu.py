@@ -576,10 +576,25 @@ def test_workload_full_size(name):
 @pytest.mark.parametrize("M,N,K,tA,tB,beta", [
     (16, 8, 16, False, False, 0.0),       # one block, mma.sync
     (528, 392, 200, True, False, 1.0),    # 4 blocks of 144 (last 96), A column blocks
-    (2320, 1000, 264, False, True, 1.0),  # 10 blocks of 256 (last 16), tcgen05 per block
-    (4096, 520, 136, True, True, 0.0),    # 8 blocks of 512, A column blocks
+    (2320, 1000, 264, False, True, 1.0),  # edges of 512, 5 blocks of 256 and one of 16 between
+    (4096, 520, 136, True, True, 0.0),    # edges of 512, 6 blocks of 512, A column blocks
 ])
 def test_gemm_host_buffers(M, N, K, tA, tB, beta):
+    check_host_buffers(M, N, K, tA, tB, beta)
+
+
+@pytest.mark.parametrize("edge", ["0", "256"])
+@pytest.mark.parametrize("M,N,K,tA,tB,beta", [
+    (2320, 1000, 264, False, True, 1.0),
+    (4096, 520, 136, True, True, 0.0),
+])
+def test_gemm_host_buffers_edge_blocks(M, N, K, tA, tB, beta, edge, tune):
+    # Equal row blocks (no edge blocks), and edges of 256 rows.
+    tune.setenv("TPGEMM_HOST_EDGE", edge)
+    check_host_buffers(M, N, K, tA, tB, beta)
+
+
+def check_host_buffers(M, N, K, tA, tB, beta):
     base = wl.BY_NAME["gemm_256_bf16_transB_beta1"]
     w = dataclasses.replace(base.with_shape(M, N, K, seed=6400 + M), transA=tA, transB=tB,
                             beta=beta, c_dist=("normal", 0.0, 1.0) if beta else None)
