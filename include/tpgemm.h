@@ -155,9 +155,11 @@ tpgemm_status tpgemm_gemm_noalloc(float* D, const void* A, const void* B, const 
 /*
  * Planner overrides (not on the pages; for measurement and tests). The
  * environment variables TPGEMM_TC_* (tile width, P rows, ring depth, staging
- * tiles, epilogue groups, producers, raster group, K rotation, CTA pair,
- * orientation, tail split, stream-K, cluster cap), TPGEMM_HOST_BLOCKS and
- * TPGEMM_WAIT_TIMEOUT_MS (the bound of every in-kernel wait, default 2000 ms)
+ * tiles, epilogue groups and last-segment helper warps, producers, raster
+ * group, K rotation and direction, CTA pair, orientation, tail split,
+ * stream-K, cluster cap, L2 priorities), TPGEMM_HOST_BLOCKS and
+ * TPGEMM_HOST_EDGE (row blocks of tpgemm_gemm_host) and TPGEMM_WAIT_TIMEOUT_MS
+ * (the bound of every in-kernel wait, default 2000 ms)
  * are read once per process, at the first call that plans a GEMM. This call
  * reads them again; calls already running keep the values they started with.
  */
@@ -228,7 +230,8 @@ size_t tpgemm_gemm_host_workspace_bytes(int64_t M, int64_t N, int64_t K, tpgemm_
  * overlap; pageable memory works but serialises them.
  *
  * The call enqueues, ordered after the work already on `stream`: the copy of B
- * to the device, then for each row block of M the copy-in of its A rows (and C
+ * to the device, then for each row block of M (about 12 for large M, the first
+ * and last of them shorter) the copy-in of its A rows (and C
  * rows), the multiply of that block by the tcgen05 / mma.sync kernels, and the
  * copy-out of its D rows. Copies run on two library-owned helper streams so
  * that block i+1's copy-in and block i-1's copy-out overlap block i's multiply;
